@@ -1,0 +1,419 @@
+// chain.cu -- the whole decoder as one device-resident chain.
+//
+// cortiq-engine "Module vae": VaeChainArgs lists the decoder in execution
+// order (conv_in -> mid_res1 -> mid_attn -> mid_res2 -> ups[..] ->
+// norm_out+SiLU -> conv_out) and carries a stable key so a backend uploads
+// the weights once; VaeDecoder adds the latent de-normalisation
+// z / scaling_factor + shift_factor. "VAE decode -> GPU handoff", step 3:
+// activations stay on the device and only the RGB image comes back.
+//
+// vae_chain_prepare packs every weight once into GEMM layout (TF32-rounded;
+// each resnet's 1x1 shortcut appended to conv2's reduction with the summed
+// bias) and returns the handle that plays the role of that key.
+// vae_decode_chain then walks the chain on the caller's stream with no host
+// synchronisation, ping-ponging NHWC activations through the workspace:
+//   X, Y  the residual stream (a resnet without a shortcut updates it in
+//         place: conv2's epilogue adds the skip element by element)
+//   T     GroupNorm+SiLU output (TF32-rounded: it is the next conv's operand)
+//   H     conv1 output
+// plus the latent staging buffer and the attention scratch.
+#include <cmath>
+#include <vector>
+
+#include "common.cuh"
+#include "ops.cuh"
+
+namespace vae {
+
+namespace {
+
+constexpr uint32_t kMagic = 0x56414543u;  // "VAEC"
+
+struct ConvW {
+  float *w = nullptr, *b = nullptr;
+  int cin = 0, cout = 0, k = 0, ldb = 0, sc_cin = 0;
+};
+struct NormW {
+  float *g = nullptr, *b = nullptr;
+  int c = 0;
+};
+struct ResW {
+  NormW n1, n2;
+  ConvW c1, c2;  // c2 carries the shortcut (sc_cin > 0) when present
+};
+struct AttnW {
+  NormW n;
+  float *wqkv = nullptr, *bqkv = nullptr, *wo = nullptr, *bo = nullptr;
+  int c = 0;
+};
+struct UpW {
+  std::vector<ResW> res;
+  bool has_up = false;
+  ConvW up;
+};
+
+struct Chain {
+  uint32_t magic = kMagic;
+  int device = 0;
+  int latent_c = 0, groups = 32;
+  float eps = 1e-6f, sf = 1.f, sh = 0.f;
+  ConvW conv_in, conv_out;
+  ResW mid1, mid2;
+  AttnW attn;
+  std::vector<UpW> ups;
+  NormW norm_out;
+  std::vector<void *> allocs;
+};
+
+struct Builder {
+  Chain *ch;
+  cudaStream_t s;
+  std::vector<void *> temps;
+  int status = VAE_OK;
+
+  template <class T>
+  T *dev(size_t count) {
+    void *p = nullptr;
+    if (status != VAE_OK) return nullptr;
+    if (cudaMalloc(&p, std::max<size_t>(count, 1) * sizeof(T)) != cudaSuccess) {
+      status = VAE_ENOMEM;
+      return nullptr;
+    }
+    ch->allocs.push_back(p);
+    return static_cast<T *>(p);
+  }
+  const float *upload_tmp(const float *src, size_t count) {
+    void *p = nullptr;
+    if (status != VAE_OK) return nullptr;
+    if (!src) {
+      status = VAE_EINVAL;
+      return nullptr;
+    }
+    if (cudaMalloc(&p, count * sizeof(float)) != cudaSuccess) {
+      status = VAE_ENOMEM;
+      return nullptr;
+    }
+    temps.push_back(p);
+    if (cudaMemcpyAsync(p, src, count * sizeof(float), cudaMemcpyDefault, s) != cudaSuccess)
+      status = VAE_ECUDA;
+    return static_cast<const float *>(p);
+  }
+  float *upload(const float *src, size_t count) {
+    float *p = dev<float>(count);
+    if (status != VAE_OK) return nullptr;
+    if (!src) {
+      status = VAE_EINVAL;
+      return nullptr;
+    }
+    if (cudaMemcpyAsync(p, src, count * sizeof(float), cudaMemcpyDefault, s) != cudaSuccess)
+      status = VAE_ECUDA;
+    return p;
+  }
+  void fail(int st) {
+    if (status == VAE_OK) status = st;
+  }
+
+  NormW norm(const vae_norm_ref &r, int c) {
+    NormW n;
+    if (r.c != c || c % ch->groups) fail(VAE_EINVAL);
+    n.c = c;
+    n.g = upload(r.weight, c);
+    n.b = upload(r.bias, c);
+    return n;
+  }
+  // Conv (optionally with the 1x1 shortcut appended to its reduction).
+  ConvW conv(const vae_conv_ref &r, int cin, int cout, const vae_conv_ref *sc = nullptr) {
+    ConvW c;
+    if (r.cin != cin || r.cout != cout || !(r.k == 1 || r.k == 3)) fail(VAE_EINVAL);
+    const bool has_sc = sc && sc->weight;
+    if (has_sc && (sc->k != 1 || sc->cout != cout)) fail(VAE_EINVAL);
+    if (status != VAE_OK) return c;
+    c.cin = cin;
+    c.cout = cout;
+    c.k = r.k;
+    c.sc_cin = has_sc ? sc->cin : 0;
+    c.ldb = packed_ldb(cin, r.k * r.k, c.sc_cin);
+    const float *wt = upload_tmp(r.weight, static_cast<size_t>(cout) * cin * r.k * r.k);
+    const float *wsc = has_sc ? upload_tmp(sc->weight, static_cast<size_t>(cout) * c.sc_cin)
+                              : nullptr;
+    c.w = dev<float>(static_cast<size_t>(cout) * c.ldb);
+    if (status != VAE_OK) return c;
+    fail(pack_conv_weights(wt, cout, cin, r.k * r.k, wsc, c.sc_cin, c.w, cout, c.ldb, s));
+    if (has_sc) {
+      const float *b1 = r.bias ? upload_tmp(r.bias, cout) : nullptr;
+      const float *b2 = sc->bias ? upload_tmp(sc->bias, cout) : nullptr;
+      c.b = dev<float>(cout);
+      if (status == VAE_OK) fail(add_bias(c.b, b1, b2, cout, s));
+    } else if (r.bias) {
+      c.b = upload(r.bias, cout);
+    }
+    return c;
+  }
+  ResW resnet(const vae_resnet_ref &r, int cin, int cout) {
+    ResW w;
+    if ((cin != cout) != (r.shortcut.weight != nullptr)) fail(VAE_EINVAL);
+    w.n1 = norm(r.norm1, cin);
+    w.c1 = conv(r.conv1, cin, cout);
+    w.n2 = norm(r.norm2, cout);
+    w.c2 = conv(r.conv2, cout, cout, &r.shortcut);
+    if (w.c2.sc_cin && w.c2.sc_cin != cin) fail(VAE_EINVAL);
+    if (w.c1.k != 3 || w.c2.k != 3) fail(VAE_EINVAL);
+    return w;
+  }
+  AttnW attention(const vae_attn_ref &r, int c) {
+    AttnW a;
+    a.c = c;
+    if (c % 32) fail(VAE_EUNSUPPORTED);
+    a.n = norm(r.norm, c);
+    const vae_conv_ref *p[3] = {&r.q, &r.k, &r.v};
+    a.wqkv = dev<float>(3ull * c * c);
+    a.bqkv = dev<float>(3ull * c);
+    for (int i = 0; i < 3 && status == VAE_OK; ++i) {
+      if (p[i]->cin != c || p[i]->cout != c || p[i]->k != 1) fail(VAE_EINVAL);
+      const float *wt = upload_tmp(p[i]->weight, static_cast<size_t>(c) * c);
+      if (status != VAE_OK) break;
+      fail(pack_conv_weights(wt, c, c, 1, nullptr, 0, a.wqkv + static_cast<size_t>(i) * c * c,
+                             c, c, s));
+      if (!p[i]->bias) fail(VAE_EINVAL);
+      if (status == VAE_OK &&
+          cudaMemcpyAsync(a.bqkv + i * c, p[i]->bias, c * 4, cudaMemcpyDefault, s) != cudaSuccess)
+        fail(VAE_ECUDA);
+    }
+    if (r.out.cin != c || r.out.cout != c || r.out.k != 1) fail(VAE_EINVAL);
+    const float *wo = upload_tmp(r.out.weight, static_cast<size_t>(c) * c);
+    a.wo = dev<float>(static_cast<size_t>(c) * c);
+    if (status == VAE_OK) fail(pack_conv_weights(wo, c, c, 1, nullptr, 0, a.wo, c, c, s));
+    a.bo = upload(r.out.bias, c);
+    return a;
+  }
+};
+
+// Sizes of the ping-pong buffers for one decode.
+struct Plan {
+  size_t max_elems = 0;  // largest activation (n * H * W * C) of the chain
+  int max_c = 0;
+  int attn_c = 0, attn_l = 0;
+};
+
+Plan make_plan(const Chain &ch, int n, int h, int w) {
+  Plan p;
+  auto see = [&](long long hh, long long ww, int c) {
+    p.max_elems = std::max(p.max_elems, static_cast<size_t>(n * hh * ww * c));
+    p.max_c = std::max(p.max_c, c);
+  };
+  long long hh = h, ww = w;
+  see(hh, ww, ch.conv_in.cout);
+  p.attn_c = ch.attn.c;
+  p.attn_l = static_cast<int>(hh * ww);
+  for (const UpW &u : ch.ups) {
+    for (const ResW &r : u.res) {
+      see(hh, ww, r.c1.cin);
+      see(hh, ww, r.c1.cout);
+    }
+    if (u.has_up) {
+      hh *= 2;
+      ww *= 2;
+      see(hh, ww, u.up.cout);
+    }
+  }
+  return p;
+}
+
+struct DecodeWs {
+  float *lat, *X, *Y, *T, *H;
+  AttnScratch attn;
+  void *gn;
+};
+
+DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, int w) {
+  DecodeWs d{};
+  d.lat = cv.take<float>(static_cast<size_t>(n) * h * w * round_up32(ch.latent_c));
+  d.X = cv.take<float>(p.max_elems);
+  d.Y = cv.take<float>(p.max_elems);
+  d.T = cv.take<float>(p.max_elems);
+  d.H = cv.take<float>(p.max_elems);
+  const size_t nl = static_cast<size_t>(n) * p.attn_l;
+  const size_t lp = static_cast<size_t>(round_up32(p.attn_l));
+  const int c = p.attn_c;
+  d.attn.t = cv.take<float>(nl * c);
+  d.attn.qkv = cv.take<float>(nl * 3 * c);
+  d.attn.vt = cv.take<float>(static_cast<size_t>(c) * lp);
+  d.attn.s = cv.take<float>(static_cast<size_t>(p.attn_l) * lp);
+  d.attn.o = cv.take<float>(nl * c);
+  d.gn = cv.take<char>(groupnorm_ws_bytes(n, p.max_c, 1, ch.groups));
+  d.attn.gn = d.gn;
+  return d;
+}
+
+int run_conv(const ConvW &c, const float *in, int n, int h, int w, const float *sc_in,
+             const float *residual, float *out, int round_out, cudaStream_t s,
+             bool upsample = false, bool nchw_out = false) {
+  IgemmDesc d;
+  d.mode = upsample ? AMode::Upsample : AMode::Conv;
+  d.a = in;
+  d.imgs = n;
+  d.hin = h;
+  d.win = w;
+  d.a_c = round_up32(c.cin);
+  d.k = c.k;
+  d.sc = c.sc_cin ? sc_in : nullptr;
+  d.sc_c = c.sc_cin ? round_up32(c.sc_cin) : 0;
+  d.b = c.w;
+  d.ldb = c.ldb;
+  d.cout = c.cout;
+  d.out = out;
+  d.ldo = c.cout;
+  d.out_nchw = nchw_out;
+  d.bias = c.b;
+  d.residual = residual;
+  d.round_out = round_out;
+  return igemm_launch(d, s);
+}
+
+// One resnet on NHWC data: `in` [n,h,w,cin] -> `out` [n,h,w,cout]; out == in
+// is allowed when there is no shortcut.
+int run_resnet(const Chain &ch, const ResW &r, const float *in, float *out, const DecodeWs &ws,
+               int n, int h, int w, int round_out, cudaStream_t s) {
+  const long long sp = static_cast<long long>(h) * w;
+  VAE_TRY(groupnorm_silu(in, n, r.c1.cin, sp, 1, ch.groups, ch.eps, r.n1.g, r.n1.b, 1, 1, ws.T,
+                         ws.gn, s));
+  VAE_TRY(run_conv(r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s));
+  VAE_TRY(groupnorm_silu(ws.H, n, r.c1.cout, sp, 1, ch.groups, ch.eps, r.n2.g, r.n2.b, 1, 1,
+                         ws.T, ws.gn, s));
+  if (r.c2.sc_cin) return run_conv(r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s);
+  return run_conv(r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s);
+}
+
+}  // namespace
+
+}  // namespace vae
+
+using namespace vae;
+
+extern "C" {
+
+int vae_chain_prepare(const vae_chain_args *a, void **handle, vae_stream_t stream) {
+  if (!a || !handle) return VAE_EINVAL;
+  *handle = nullptr;
+  if (a->latent_channels <= 0 || a->groups <= 0 || a->n_ups < 0 || (a->n_ups && !a->ups) ||
+      a->scaling_factor == 0.f)
+    return VAE_EINVAL;
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  Chain *ch = new Chain();
+  cudaGetDevice(&ch->device);
+  ch->latent_c = a->latent_channels;
+  ch->groups = a->groups;
+  ch->eps = a->eps;
+  ch->sf = a->scaling_factor;
+  ch->sh = a->shift_factor;
+  Builder b{ch, s};
+  const int c0 = a->conv_in.cout;
+  ch->conv_in = b.conv(a->conv_in, a->latent_channels, c0);
+  if (ch->conv_in.k != 3) b.fail(VAE_EINVAL);
+  ch->mid1 = b.resnet(a->mid_res1, c0, c0);
+  ch->attn = b.attention(a->mid_attn, c0);
+  ch->mid2 = b.resnet(a->mid_res2, c0, c0);
+  int c = c0;
+  for (int i = 0; i < a->n_ups && b.status == VAE_OK; ++i) {
+    const vae_up_ref &u = a->ups[i];
+    UpW uw;
+    if (u.n_resnets <= 0 || !u.resnets) b.fail(VAE_EINVAL);
+    for (int j = 0; j < u.n_resnets && b.status == VAE_OK; ++j) {
+      const int cout = u.resnets[j].conv1.cout;
+      uw.res.push_back(b.resnet(u.resnets[j], c, cout));
+      c = cout;
+    }
+    uw.has_up = u.upsample_conv.weight != nullptr;
+    if (uw.has_up) {
+      uw.up = b.conv(u.upsample_conv, c, u.upsample_conv.cout);
+      if (uw.up.k != 3) b.fail(VAE_EINVAL);
+      c = u.upsample_conv.cout;
+    }
+    ch->ups.push_back(std::move(uw));
+  }
+  ch->norm_out = b.norm(a->norm_out, c);
+  ch->conv_out = b.conv(a->conv_out, c, a->conv_out.cout);
+  if (ch->conv_out.k != 3 && b.status == VAE_OK) b.fail(VAE_EINVAL);
+  if (b.status == VAE_OK && cudaStreamSynchronize(s) != cudaSuccess) b.fail(VAE_ECUDA);
+  cudaStreamSynchronize(s);
+  for (void *p : b.temps) cudaFree(p);
+  if (b.status != VAE_OK) {
+    for (void *p : ch->allocs) cudaFree(p);
+    ch->magic = 0;
+    delete ch;
+    return b.status;
+  }
+  *handle = ch;
+  return VAE_OK;
+}
+
+size_t vae_chain_workspace_size(const void *handle, int n, int h, int w) {
+  const Chain *ch = static_cast<const Chain *>(handle);
+  if (!ch || ch->magic != kMagic || n <= 0 || h <= 0 || w <= 0) return 0;
+  const Plan p = make_plan(*ch, n, h, w);
+  Carver cv(nullptr, 0);
+  carve_decode(cv, *ch, p, n, h, w);
+  return cv.used;
+}
+
+int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *rgb, void *ws,
+                     size_t ws_bytes, vae_stream_t stream) {
+  Chain *ch = static_cast<Chain *>(handle);
+  if (!ch || ch->magic != kMagic) return VAE_ENOTPREPARED;
+  if (!z || !rgb || !ws || n <= 0 || h <= 0 || w <= 0) return VAE_EINVAL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != ch->device) return VAE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(z) | reinterpret_cast<uintptr_t>(rgb)) & 15) return VAE_EINVAL;
+  const long long L = static_cast<long long>(h) * w;
+  if (L > 65536 || static_cast<long long>(n) * L > 0x7fffffffll) return VAE_EUNSUPPORTED;
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  const Plan p = make_plan(*ch, n, h, w);
+  Carver cv(ws, ws_bytes);
+  DecodeWs d = carve_decode(cv, *ch, p, n, h, w);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+
+  // z / scaling_factor + shift_factor, NCHW -> NHWC (channels padded to 32).
+  const float *lat = nullptr;
+  VAE_TRY(stage_nhwc(z, n, ch->latent_c, L, VAE_NCHW, d.lat, round_up32(ch->latent_c),
+                     1.0f / ch->sf, ch->sh, 1, &lat, s));
+  float *cur = d.X, *other = d.Y;
+  int hh = h, ww = w;
+  VAE_TRY(run_conv(ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s));
+  VAE_TRY(run_resnet(*ch, ch->mid1, cur, cur, d, n, hh, ww, 0, s));
+  VAE_TRY(attention_nhwc(cur, n, ch->attn.c, static_cast<int>(L), ch->groups, ch->eps,
+                         ch->attn.n.g, ch->attn.n.b, ch->attn.wqkv, ch->attn.bqkv, ch->attn.wo,
+                         ch->attn.bo, cur, d.attn, s));
+  VAE_TRY(run_resnet(*ch, ch->mid2, cur, cur, d, n, hh, ww, 0, s));
+  for (const UpW &u : ch->ups) {
+    for (size_t j = 0; j < u.res.size(); ++j) {
+      const ResW &r = u.res[j];
+      // The block's last resnet output is only read by the upsample conv as
+      // an MMA operand, so it is stored TF32-rounded.
+      const int round = (u.has_up && j + 1 == u.res.size()) ? 1 : 0;
+      float *dst = r.c2.sc_cin ? other : cur;
+      VAE_TRY(run_resnet(*ch, r, cur, dst, d, n, hh, ww, round, s));
+      if (dst != cur) std::swap(cur, other);
+    }
+    if (u.has_up) {
+      // Output rounded: the next resnet may read it through its shortcut MMA.
+      VAE_TRY(run_conv(u.up, cur, n, hh, ww, nullptr, nullptr, other, 1, s, true));
+      std::swap(cur, other);
+      hh *= 2;
+      ww *= 2;
+    }
+  }
+  VAE_TRY(groupnorm_silu(cur, n, ch->norm_out.c, static_cast<long long>(hh) * ww, 1, ch->groups,
+                         ch->eps, ch->norm_out.g, ch->norm_out.b, 1, 1, d.T, d.gn, s));
+  return run_conv(ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, rgb, 0, s, false, true);
+}
+
+int vae_chain_destroy(void *handle) {
+  Chain *ch = static_cast<Chain *>(handle);
+  if (!ch || ch->magic != kMagic) return VAE_ENOTPREPARED;
+  for (void *p : ch->allocs) cudaFree(p);
+  ch->magic = 0;
+  delete ch;
+  return VAE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+// common.cuh -- internal host/device helpers shared by the kernels' launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/vae.h"
+
+namespace vae {
+
+#define VAE_CUDA_TRY(expr)                              \
+  do {                                                  \
+    cudaError_t e__ = (expr);                           \
+    if (e__ != cudaSuccess) return VAE_ECUDA;           \
+  } while (0)
+
+#define VAE_TRY(expr)                                   \
+  do {                                                  \
+    int s__ = (expr);                                   \
+    if (s__ != VAE_OK) return s__;                      \
+  } while (0)
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+inline int round_up32(int c) { return (c + 31) / 32 * 32; }
+
+// Bump allocator over a caller-provided workspace. Every carve is 256-byte
+// aligned. With base == nullptr it only measures.
+struct Carver {
+  char *base;
+  size_t cap;
+  size_t used = 0;
+  Carver(void *b, size_t c) : base(static_cast<char *>(b)), cap(c) {}
+  template <class T>
+  T *take(size_t count) {
+    size_t off = align_up(used, 256);
+    used = off + count * sizeof(T);
+    return base ? reinterpret_cast<T *>(base + off) : nullptr;
+  }
+  bool ok() const { return base == nullptr || used <= cap; }
+};
+
+// Device error word of the current device (int), via the library's
+// __device__ symbol; resolved once per device.
+int *device_error_word();
+int num_sms();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+int encode_tiled(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                 const uint64_t *strides_bytes /* rank-1 entries */, const uint32_t *box);
+
+// ------------------------------------------------------------------ kernels
+// Implicit-GEMM convolution / GEMM on tcgen05 (igemm.cu).
+enum class AMode : int { Conv = 0, Upsample = 1, Gemm = 2 };
+
+struct IgemmDesc {
+  AMode mode = AMode::Conv;
+  // --- A operand (activations, NHWC; channels padded to a multiple of 32)
+  const float *a = nullptr;  // Conv/Upsample: [imgs, Hin, Win, a_c]; Gemm: [M, lda]
+  int imgs = 1;              // images (n * t for 3-D)
+  int t = 1;                 // frames per sample (3-D); imgs = n * t
+  int hin = 1, win = 1;      // input spatial dims (Upsample: low-res)
+  int a_c = 32;              // channel count of `a` (multiple of 32)
+  int lda = 0;               // Gemm: row stride of A in floats
+  int M = 0;                 // Gemm: rows
+  int k = 3;                 // Conv: spatial kernel (1 or 3)
+  int kt = 1;                // Conv: temporal taps (1 or 3, causal)
+  // --- 1x1 shortcut operand (Conv only), same spatial dims as the output
+  const float *sc = nullptr;
+  int sc_c = 0;  // channels of sc (multiple of 32), 0 = none
+  // --- B operand: packed weights [rows >= cout][ldb] K-major, TF32-rounded
+  const float *b = nullptr;
+  int ldb = 0;   // floats per row (the packed K extent)
+  int kdim = 0;  // Gemm: K (multiple of 32)
+  int cout = 0;  // N extent
+  // --- epilogue
+  float *out = nullptr;
+  int ldo = 0;           // NHWC / Gemm: floats between consecutive rows
+  int out_nchw = 0;      // write [n, cout, t, h, w] instead of rows
+  const float *bias = nullptr;
+  int bias_per_row = 0;  // Gemm: bias indexed by row instead of column
+  const float *residual = nullptr;  // same layout / ld as out
+  float alpha = 1.0f;
+  int round_out = 0;  // store TF32-rounded values (output feeds another MMA)
+};
+size_t igemm_smem_bytes(int bn);
+int igemm_launch(const IgemmDesc &d, cudaStream_t stream);
+
+// Weight packing (layout.cu): w [cout][cin][taps] (+ shortcut [cout][sc_cin])
+// -> dst [cout_rows][ldb] with K index tap * cin_pad + c, TF32-rounded, zeros in
+// the padding.
+int pack_conv_weights(const float *w, int cout, int cin, int taps, const float *w_sc,
+                      int sc_cin, float *dst, int cout_rows, int ldb, cudaStream_t s);
+inline int packed_ldb(int cin, int taps, int sc_cin) {
+  return taps * round_up32(cin) + (sc_cin ? round_up32(sc_cin) : 0);
+}
+
+// Layout transforms (layout.cu). src [outer][rows][cols] (row stride src_ld)
+// -> dst [outer][cols][rows] (row stride dst_ld), dst = src * alpha + beta,
+// optionally TF32-rounded. Used for NCHW <-> NHWC and V^T.
+int transpose(const float *src, long long src_outer_stride, int src_ld, float *dst,
+              long long dst_outer_stride, int dst_ld, int outer, int rows, int cols,
+              float alpha, float beta, int round, cudaStream_t s);
+// Copy rows of `cols` floats into rows of `dst_cols` (zero padded).
+int pad_rows(const float *src, long long rows, int cols, float *dst, int dst_cols,
+             cudaStream_t s);
+int add_bias(float *dst, const float *a, const float *b, int n, cudaStream_t s);
+
+// GroupNorm (+SiLU) (groupnorm.cu). `x` NHWC [n][spatial][c] or NCHW.
+size_t groupnorm_ws_bytes(int n, int c, long long spatial, int groups);
+int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, int groups,
+                   float eps, const float *gamma, const float *beta, int silu, int round_out,
+                   float *y, void *ws, cudaStream_t s);
+
+// Row softmax in place: s[r][:L] <- softmax(scale * s[r][:L]), TF32-rounded.
+int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st);
+
+}  // namespace vae

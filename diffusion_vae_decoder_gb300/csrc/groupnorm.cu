@@ -1,0 +1,277 @@
+// groupnorm.cu -- two-pass GroupNorm (+ SiLU), HBM-bound.
+//
+// Definition: cortiq-engine "Module vae", structs GroupNorm / VaeNormRef
+// (eps 1e-6, affine); statistics as vae3d.rs struct GroupNorm::apply computes
+// them (mean, then the biased variance, 1/sqrt(var + eps), then gamma/beta);
+// SiLU as vae3d.rs fn silu.
+//
+// Pass 1 (stats): many CTAs per sample each reduce a contiguous slab of
+// pixels. Every thread owns a fixed float4 of channels and accumulates sums
+// of (x - first value it saw), which keeps f32 cancellation small; the
+// per-thread (count, mean, M2) triples are merged into per-(CTA, group)
+// partials with the parallel-variance (Chan et al.) combination in f64.
+// Finalize: one CTA per (sample, group) merges the partials and writes the
+// per-channel affine  y = x * scale[c] + shift[c].
+// Pass 2 (apply): one vectorised elementwise sweep, SiLU, optional TF32
+// rounding when the result feeds a tensor-core conv.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace vae {
+
+namespace {
+
+constexpr int kStatThreads = 256;
+constexpr int kMaxBlocksPerGroupSeg = 512;  // partial slots per (sample, group)
+
+struct Triple {
+  double n, mean, m2;
+};
+
+__device__ __forceinline__ Triple merge(Triple a, Triple b) {
+  if (a.n == 0) return b;
+  if (b.n == 0) return a;
+  const double n = a.n + b.n;
+  const double d = b.mean - a.mean;
+  return {n, a.mean + d * (b.n / n), a.m2 + b.m2 + d * d * (a.n * b.n / n)};
+}
+
+// NHWC: x[n][spatial][c]. grid = (nblk, n). Partials [n][groups][nblk].
+__global__ void __launch_bounds__(kStatThreads)
+    gn_stats_nhwc(const float *__restrict__ x, int c, long long spatial, int groups, int nblk,
+                  double *__restrict__ part) {
+  extern __shared__ float sm[];  // [ppi][c] x 3
+  const int n = blockIdx.y, blk = blockIdx.x;
+  const int tpp = c >> 2;
+  const int ppi = kStatThreads / tpp;
+  const int tid = threadIdx.x;
+  const int lc = tid % tpp, pl = tid / tpp;
+  const long long p0 = spatial * blk / nblk, p1 = spatial * (blk + 1) / nblk;
+  float k[4] = {0, 0, 0, 0}, s[4] = {0, 0, 0, 0}, ss[4] = {0, 0, 0, 0};
+  int cnt = 0;
+  if (pl < ppi) {
+    const float *base = x + (static_cast<long long>(n) * spatial) * c + 4 * lc;
+    for (long long pix = p0 + pl; pix < p1; pix += ppi) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(base + pix * c));
+      const float a[4] = {v.x, v.y, v.z, v.w};
+      if (cnt == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) k[j] = a[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float d = a[j] - k[j];
+        s[j] += d;
+        ss[j] = fmaf(d, d, ss[j]);
+      }
+      ++cnt;
+    }
+    float *e = sm + (static_cast<long long>(pl) * c + 4 * lc) * 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float mean_d = cnt ? s[j] / cnt : 0.f;
+      e[3 * j + 0] = static_cast<float>(cnt);
+      e[3 * j + 1] = k[j] + mean_d;
+      e[3 * j + 2] = cnt ? fmaxf(ss[j] - s[j] * mean_d, 0.f) : 0.f;
+    }
+  }
+  __syncthreads();
+  const int cg = c / groups;
+  for (int g = tid; g < groups; g += kStatThreads) {
+    Triple acc{0, 0, 0};
+    for (int l = 0; l < ppi; ++l)
+      for (int ch = g * cg; ch < (g + 1) * cg; ++ch) {
+        const float *e = sm + (static_cast<long long>(l) * c + ch) * 3;
+        acc = merge(acc, Triple{e[0], e[1], e[2]});
+      }
+    double *o = part + ((static_cast<long long>(n) * groups + g) * nblk + blk) * 3;
+    o[0] = acc.n;
+    o[1] = acc.mean;
+    o[2] = acc.m2;
+  }
+}
+
+// NCHW: group (n, g) is the contiguous segment of cg * spatial floats.
+// grid = (nblk, n * groups).
+__global__ void __launch_bounds__(kStatThreads)
+    gn_stats_nchw(const float *__restrict__ x, int c, long long spatial, int groups, int nblk,
+                  double *__restrict__ part) {
+  __shared__ double red[kStatThreads][3];
+  const int ng = blockIdx.y, blk = blockIdx.x;
+  const int cg = c / groups;
+  const long long seg = static_cast<long long>(cg) * spatial;
+  const float *base = x + static_cast<long long>(ng) * seg;
+  const long long e0 = seg * blk / nblk, e1 = seg * (blk + 1) / nblk;
+  float k = 0.f, s = 0.f, ss = 0.f;
+  int cnt = 0;
+  for (long long i = e0 + threadIdx.x; i < e1; i += kStatThreads) {
+    const float v = __ldg(base + i);
+    if (cnt == 0) k = v;
+    const float d = v - k;
+    s += d;
+    ss = fmaf(d, d, ss);
+    ++cnt;
+  }
+  const float md = cnt ? s / cnt : 0.f;
+  red[threadIdx.x][0] = cnt;
+  red[threadIdx.x][1] = k + md;
+  red[threadIdx.x][2] = cnt ? fmaxf(ss - s * md, 0.f) : 0.f;
+  __syncthreads();
+  for (int w = kStatThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      const Triple a{red[threadIdx.x][0], red[threadIdx.x][1], red[threadIdx.x][2]};
+      const Triple b{red[threadIdx.x + w][0], red[threadIdx.x + w][1], red[threadIdx.x + w][2]};
+      const Triple r = merge(a, b);
+      red[threadIdx.x][0] = r.n;
+      red[threadIdx.x][1] = r.mean;
+      red[threadIdx.x][2] = r.m2;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    double *o = part + (static_cast<long long>(ng) * nblk + blk) * 3;
+    o[0] = red[0][0];
+    o[1] = red[0][1];
+    o[2] = red[0][2];
+  }
+}
+
+// One CTA per (n, g): merge nblk partials, write scale/shift per channel.
+__global__ void gn_finalize(const double *__restrict__ part, int nblk, int c, int groups,
+                            float eps, const float *__restrict__ gamma,
+                            const float *__restrict__ beta, float *__restrict__ scale,
+                            float *__restrict__ shift) {
+  __shared__ double red[128][3];
+  const int ng = blockIdx.x;
+  const int n = ng / groups, g = ng % groups;
+  Triple acc{0, 0, 0};
+  for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+    const double *e = part + (static_cast<long long>(ng) * nblk + b) * 3;
+    acc = merge(acc, Triple{e[0], e[1], e[2]});
+  }
+  red[threadIdx.x][0] = acc.n;
+  red[threadIdx.x][1] = acc.mean;
+  red[threadIdx.x][2] = acc.m2;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      const Triple a{red[threadIdx.x][0], red[threadIdx.x][1], red[threadIdx.x][2]};
+      const Triple b{red[threadIdx.x + w][0], red[threadIdx.x + w][1], red[threadIdx.x + w][2]};
+      const Triple r = merge(a, b);
+      red[threadIdx.x][0] = r.n;
+      red[threadIdx.x][1] = r.mean;
+      red[threadIdx.x][2] = r.m2;
+    }
+    __syncthreads();
+  }
+  const int cg = c / groups;
+  if (threadIdx.x < cg) {
+    const double cntv = red[0][0];
+    const double mean = red[0][1];
+    const double var = cntv > 0 ? red[0][2] / cntv : 0.0;
+    const double rstd = 1.0 / sqrt(var + static_cast<double>(eps));
+    const int ch = g * cg + threadIdx.x;
+    const double a = rstd * gamma[ch];
+    scale[n * c + ch] = static_cast<float>(a);
+    shift[n * c + ch] = static_cast<float>(beta[ch] - mean * a);
+  }
+}
+
+__device__ __forceinline__ float finish(float v, int silu, int round) {
+  if (silu) v = v / (1.0f + expf(-v));
+  return round ? round_tf32(v) : v;
+}
+
+__global__ void gn_apply_nhwc(const float *__restrict__ x, long long total4, int c,
+                              long long per_sample, const float *__restrict__ scale,
+                              const float *__restrict__ shift, int silu, int round,
+                              float *__restrict__ y) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long e = 4 * i;
+    const int n = static_cast<int>(e / per_sample);
+    const int ch = static_cast<int>(e % c);
+    const float4 v = reinterpret_cast<const float4 *>(x)[i];
+    const float4 a = *reinterpret_cast<const float4 *>(scale + n * c + ch);
+    const float4 b = *reinterpret_cast<const float4 *>(shift + n * c + ch);
+    float4 o;
+    o.x = finish(fmaf(v.x, a.x, b.x), silu, round);
+    o.y = finish(fmaf(v.y, a.y, b.y), silu, round);
+    o.z = finish(fmaf(v.z, a.z, b.z), silu, round);
+    o.w = finish(fmaf(v.w, a.w, b.w), silu, round);
+    reinterpret_cast<float4 *>(y)[i] = o;
+  }
+}
+
+__global__ void gn_apply_nchw(const float *__restrict__ x, long long total, int c,
+                              long long spatial, const float *__restrict__ scale,
+                              const float *__restrict__ shift, int silu, int round,
+                              float *__restrict__ y) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long nc = i / spatial;  // n * c + ch
+    y[i] = finish(fmaf(x[i], scale[nc], shift[nc]), silu, round);
+  }
+}
+
+int nblk_for(long long elems_per_seg, int segs) {
+  long long want = elems_per_seg / (kStatThreads * 16);
+  const long long cap = std::max(1ll, 4ll * num_sms() / std::max(1, segs));
+  want = std::min(want, cap);
+  want = std::min<long long>(want, kMaxBlocksPerGroupSeg);
+  return static_cast<int>(std::max(1ll, want));
+}
+
+}  // namespace
+
+size_t groupnorm_ws_bytes(int n, int c, long long spatial, int groups) {
+  (void)spatial;
+  Carver cv(nullptr, 0);
+  cv.take<double>(static_cast<size_t>(n) * groups * kMaxBlocksPerGroupSeg * 3);
+  cv.take<float>(static_cast<size_t>(n) * c);
+  cv.take<float>(static_cast<size_t>(n) * c);
+  return cv.used;
+}
+
+int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, int groups,
+                   float eps, const float *gamma, const float *beta, int silu, int round_out,
+                   float *y, void *ws, cudaStream_t s) {
+  if (!x || !y || !gamma || !beta || !ws || n <= 0 || c <= 0 || spatial <= 0 || groups <= 0)
+    return VAE_EINVAL;
+  if (c % groups || c % 4 || c > 1024) return VAE_EUNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) return VAE_EINVAL;
+  Carver cv(ws, ~size_t(0));
+  double *part = cv.take<double>(static_cast<size_t>(n) * groups * kMaxBlocksPerGroupSeg * 3);
+  float *scale = cv.take<float>(static_cast<size_t>(n) * c);
+  float *shift = cv.take<float>(static_cast<size_t>(n) * c);
+  const int cg = c / groups;
+  int nblk;
+  if (nhwc) {
+    nblk = nblk_for(spatial * c, n);
+    const int tpp = c / 4, ppi = kStatThreads / tpp;
+    const size_t sm = static_cast<size_t>(ppi) * c * 3 * sizeof(float);
+    gn_stats_nhwc<<<dim3(nblk, n), kStatThreads, sm, s>>>(x, c, spatial, groups, nblk, part);
+  } else {
+    nblk = nblk_for(spatial * cg, n * groups);
+    gn_stats_nchw<<<dim3(nblk, n * groups), kStatThreads, 0, s>>>(x, c, spatial, groups, nblk,
+                                                                   part);
+  }
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  gn_finalize<<<n * groups, 128, 0, s>>>(part, nblk, c, groups, eps, gamma, beta, scale, shift);
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  const long long total = static_cast<long long>(n) * c * spatial;
+  const int threads = 256;
+  if (nhwc) {
+    const long long total4 = total / 4;
+    const long long g = std::min<long long>((total4 + threads - 1) / threads, 8ll * num_sms());
+    gn_apply_nhwc<<<static_cast<int>(g), threads, 0, s>>>(x, total4, c, spatial * c, scale,
+                                                          shift, silu, round_out, y);
+  } else {
+    const long long g = std::min<long long>((total + threads - 1) / threads, 8ll * num_sms());
+    gn_apply_nchw<<<static_cast<int>(g), threads, 0, s>>>(x, total, c, spatial, scale, shift,
+                                                          silu, round_out, y);
+  }
+  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+}
+
+}  // namespace vae

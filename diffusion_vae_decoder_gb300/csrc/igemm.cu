@@ -1,0 +1,555 @@
+// igemm.cu -- implicit-GEMM convolution and plain GEMM on the tcgen05 tensor
+// cores (TF32 operands, FP32 accumulation in TMEM), sm_103a.
+//
+// The convolution is the decoder's hot path ("VAE decode -> GPU handoff
+// (FLUX/LTX render services)", "The CPU VAE code": the late up-block convs at
+// full resolution dominate). That page plans an im2col buffer followed by an
+// SGEMM ("GPU plan -- im2col + cuBLAS SGEMM", steps 1-2); here the im2col
+// matrix is never stored. Output pixels are the GEMM rows, output channels the
+// columns, and (tap, input channel) the reduction index. Each reduction step
+// is one tap x 32 input channels: a TMA tiled copy of the NHWC activation
+// shifted by the tap offset (out-of-range coordinates read as zero, which is
+// exactly the zero padding), plus a TMA copy of the packed weights.
+//
+// CTA layout (192 threads, persistent over output tiles):
+//   warp 0     TMA producer (one thread) filling a STAGES-deep smem ring
+//   warp 1     TMEM allocator + MMA issuer (one thread)
+//   warps 2-5  epilogue: TMEM -> registers, bias / residual / scale, stores
+// The accumulator is double-buffered in TMEM so the epilogue of tile i
+// overlaps the MMAs of tile i+1.
+//
+// Operand tiles: 128 rows x 32 f32 (128 bytes per row) with the 128-byte
+// swizzle, i.e. the K-major SW128 canonical layout tcgen05 reads directly.
+//
+// A-operand modes
+//   Conv      NHWC input, k x k (x kt causal) taps; the 1x1 resnet shortcut is
+//             appended as extra reduction steps over its own input.
+//   Upsample  nearest-2x upsample folded into a 3x3 conv (cortiq-engine
+//             "Module vae", VaeUpRef). Output rows of a tile are ordered by
+//             output-pixel parity (py, px); for each parity and tap the needed
+//             low-resolution pixels form a plain R x P box offset by
+//             floor((p + k - 1) / 2), so four TMA boxes per step build the
+//             tile and the upsampled tensor is never materialised.
+//   Gemm      row-major A [M, K] (token-major activations for attention).
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace vae {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = kBM * 128;
+
+struct KParams {
+  int imgs, t, hin, win, hout, wout;
+  int bh, bw;  // Conv: tile rows/cols of output pixels; Upsample: R, P (low-res box)
+  int tiles_x, tiles_y;
+  int m_tiles, n_tiles, total_tiles;
+  int M;
+  int k, kt, taps;
+  int cin_chunks, sc_chunks, k_stages, cin_pad;
+  int cout;
+  float *out;
+  int ldo, out_nchw;
+  const float *bias;
+  int bias_per_row;
+  const float *residual;
+  float alpha;
+  int round_out;
+  int *err;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr uint32_t B_BYTES = BN * 128;
+  static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
+  static constexpr size_t SMEM =
+      1024 + STAGES * (kABytes + B_BYTES) + (2 * STAGES + 5) * sizeof(uint64_t) + 16;
+};
+
+__device__ __forceinline__ void raise_error(const KParams &p, volatile uint32_t *abort) {
+  *abort = 1u;
+  atomicCAS(p.err, 0, static_cast<int>(VAE_EDEVICE_TIMEOUT));
+}
+
+// Unbounded-by-abort wait used only while draining after an abort.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+  return true;
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    igemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmS, const KParams p) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  constexpr uint32_t STAGE_TX = kABytes + C::B_BYTES;
+  constexpr uint32_t IDESC = idesc_tf32(kBM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * kABytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *acc_full = empty + STAGES;
+  uint64_t *acc_empty = acc_full + 2;
+  uint64_t *drain = acc_empty + 2;  // used only after an abort
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile uint32_t *abort = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (MODE == 0 && p.sc_chunks > 0) prefetch_tmap(&tmS);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t pending = 0, pend_par = 0;  // stages with a copy issued, and its parity
+      bool failed = false;
+      for (int tile = blockIdx.x; tile < p.total_tiles && !failed; tile += gridDim.x) {
+        const int mt = tile / p.n_tiles;
+        const int n0 = (tile % p.n_tiles) * BN;
+        int img = 0, ty = 0, tx = 0;
+        if (MODE != 2) {
+          const int per_img = p.tiles_x * p.tiles_y;
+          img = mt / per_img;
+          const int rem = mt % per_img;
+          ty = rem / p.tiles_x;
+          tx = rem % p.tiles_x;
+        }
+        const int n_idx = img / p.t, t_idx = img % p.t;
+        for (int ks = 0; ks < p.k_stages; ++ks) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+            raise_error(p, abort);
+            failed = true;
+            break;
+          }
+          uint8_t *a_dst = sA + stage * kABytes;
+          uint8_t *b_dst = sB + stage * C::B_BYTES;
+          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+          if (MODE == 0) {
+            const int main_steps = p.taps * p.cin_chunks;
+            if (ks < main_steps) {
+              const int tap = ks / p.cin_chunks, cc = ks % p.cin_chunks;
+              const int kk = p.k * p.k;
+              const int ktap = tap / kk, sp = tap % kk;
+              const int dy = sp / p.k - p.k / 2, dx = sp % p.k - p.k / 2;
+              int ft = t_idx + ktap - (p.kt - 1);
+              ft = ft < 0 ? 0 : ft;  // causal padding repeats the first frame
+              tma_load_4d(a_dst, &tmA, &full[stage], cc * 32, tx * p.bw + dx, ty * p.bh + dy,
+                          n_idx * p.t + ft);
+              tma_load_2d(b_dst, &tmB, &full[stage], tap * p.cin_pad + cc * 32, n0);
+            } else {
+              const int cc = ks - main_steps;
+              tma_load_4d(a_dst, &tmS, &full[stage], cc * 32, tx * p.bw, ty * p.bh, img);
+              tma_load_2d(b_dst, &tmB, &full[stage], p.taps * p.cin_pad + cc * 32, n0);
+            }
+          } else if (MODE == 1) {
+            const int tap = ks / p.cin_chunks, cc = ks % p.cin_chunks;
+            const int ky = tap / 3, kx = tap % 3;
+#pragma unroll
+            for (int ph = 0; ph < 4; ++ph) {
+              const int oy = ((ph >> 1) + ky - 1) >> 1;  // floor((py + ky - 1) / 2)
+              const int ox = ((ph & 1) + kx - 1) >> 1;
+              tma_load_4d(a_dst + ph * 4096, &tmA, &full[stage], cc * 32, tx * p.bw + ox,
+                          ty * p.bh + oy, img);
+            }
+            tma_load_2d(b_dst, &tmB, &full[stage], tap * p.cin_pad + cc * 32, n0);
+          } else {
+            tma_load_2d(a_dst, &tmA, &full[stage], ks * 32, mt * kBM);
+            tma_load_2d(b_dst, &tmB, &full[stage], ks * 32, n0);
+          }
+          pending |= 1u << stage;
+          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort) {
+        // Let every copy this thread issued land before the CTA exits.
+        for (int s = 0; s < STAGES; ++s)
+          if (pending & (1u << s)) mbar_wait_drain(&full[s], (pend_par >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int local = 0;
+      bool failed = false, issued = false;
+      for (int tile = blockIdx.x; tile < p.total_tiles && !failed; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort)) {
+          raise_error(p, abort);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int ks = 0; ks < p.k_stages; ++ks) {
+          if (!mbar_wait(&full[stage], phase, abort)) {
+            raise_error(p, abort);
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + stage * kABytes));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)  // 4 x K=8 TF32 steps = 32 channels (128 bytes)
+            umma_tf32(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, (ks | k) != 0);
+          issued = true;
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!failed) umma_commit(&acc_full[buf]);
+      }
+      if (*abort && issued) {
+        // Wait for the MMAs still reading shared memory / writing TMEM before
+        // the CTA frees TMEM and exits.
+        umma_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int m = q * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      bool ok = mbar_wait(&acc_full[buf], aph, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) raise_error(p, abort);
+        break;
+      }
+      tc_fence_after();
+
+      const int mt = tile / p.n_tiles;
+      const int n0 = (tile % p.n_tiles) * BN;
+      bool valid;
+      long long row;     // NHWC / GEMM row index
+      long long nchw0 = 0;  // NCHW: offset of channel 0 for this pixel
+      long long cstride = 0;
+      if (MODE == 2) {
+        row = static_cast<long long>(mt) * kBM + m;
+        valid = row < p.M;
+      } else {
+        const int per_img = p.tiles_x * p.tiles_y;
+        const int img = mt / per_img;
+        const int rem = mt % per_img;
+        const int ty = rem / p.tiles_x, tx = rem % p.tiles_x;
+        int y, x;
+        if (MODE == 0) {
+          y = ty * p.bh + m / p.bw;
+          x = tx * p.bw + m % p.bw;
+          valid = y < p.hout && x < p.wout;
+        } else {
+          const int ph = m >> 5, r = m & 31;
+          const int yl = ty * p.bh + r / p.bw, xl = tx * p.bw + r % p.bw;
+          y = 2 * yl + (ph >> 1);
+          x = 2 * xl + (ph & 1);
+          valid = yl < p.hin && xl < p.win;
+        }
+        row = (static_cast<long long>(img) * p.hout + y) * p.wout + x;
+        const long long hw = static_cast<long long>(p.hout) * p.wout;
+        const int n_idx = img / p.t, t_idx = img % p.t;
+        cstride = hw * p.t;
+        nchw0 = static_cast<long long>(n_idx) * p.cout * cstride + t_idx * hw +
+                static_cast<long long>(y) * p.wout + x;
+      }
+      const float rbias = (MODE == 2 && p.bias_per_row && p.bias && valid) ? p.bias[row] : 0.f;
+
+#pragma unroll 1
+      for (int c = 0; c < BN / C::CH; ++c) {
+        float v[C::CH];
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(buf * BN + c * C::CH);
+        if (C::CH == 32)
+          tmem_ld_32cols(taddr, v);
+        else
+          tmem_ld_16cols(taddr, v);
+        const int col0 = n0 + c * C::CH;
+        if (col0 >= p.cout || !valid) continue;
+        const int ncols = min(C::CH, p.cout - col0);
+#pragma unroll
+        for (int i = 0; i < C::CH; ++i) {
+          float b = rbias;
+          if (!p.bias_per_row && p.bias && i < ncols) b = __ldg(p.bias + col0 + i);
+          v[i] = fmaf(v[i], p.alpha, b);
+        }
+        if (p.out_nchw) {
+          float *o = p.out + nchw0 + static_cast<long long>(col0) * cstride;
+          const float *r = p.residual ? p.residual + nchw0 + static_cast<long long>(col0) * cstride
+                                      : nullptr;
+#pragma unroll
+          for (int i = 0; i < C::CH; ++i) {
+            if (i < ncols) {
+              float val = v[i];
+              if (r) val += r[i * cstride];
+              if (p.round_out) val = round_tf32(val);
+              o[i * cstride] = val;
+            }
+          }
+        } else {
+          float *o = p.out + row * p.ldo + col0;
+          const float *r = p.residual ? p.residual + row * p.ldo + col0 : nullptr;
+          if (ncols == C::CH) {
+#pragma unroll
+            for (int i = 0; i < C::CH; i += 4) {
+              float4 val = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+              if (r) {
+                const float4 rv = *reinterpret_cast<const float4 *>(r + i);
+                val.x += rv.x;
+                val.y += rv.y;
+                val.z += rv.z;
+                val.w += rv.w;
+              }
+              if (p.round_out) {
+                val.x = round_tf32(val.x);
+                val.y = round_tf32(val.y);
+                val.z = round_tf32(val.z);
+                val.w = round_tf32(val.w);
+              }
+              *reinterpret_cast<float4 *>(o + i) = val;
+            }
+          } else {
+            for (int i = 0; i < ncols; ++i) {
+              float val = v[i];
+              if (r) val += r[i];
+              if (p.round_out) val = round_tf32(val);
+              o[i] = val;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+int pow2_at_least(int v) {
+  int r = 1;
+  while (r < v) r <<= 1;
+  return r;
+}
+
+template <int BN, int MODE>
+int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ts,
+                 const KParams &kp, cudaStream_t stream) {
+  using C = Cfg<BN>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(igemm_kernel<BN, MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(C::SMEM));
+  });
+  if (attr_err != cudaSuccess) return VAE_ECUDA;
+  const int grid = std::min(kp.total_tiles, num_sms());
+  igemm_kernel<BN, MODE><<<grid, kThreads, C::SMEM, stream>>>(ta, tb, ts, kp);
+  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+}
+
+template <int MODE>
+int launch_mode(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ts,
+                const KParams &kp, cudaStream_t s) {
+  switch (bn) {
+    case 256: return launch_typed<256, MODE>(ta, tb, ts, kp, s);
+    case 128: return launch_typed<128, MODE>(ta, tb, ts, kp, s);
+    case 64: return launch_typed<64, MODE>(ta, tb, ts, kp, s);
+    case 32: return launch_typed<32, MODE>(ta, tb, ts, kp, s);
+    default: return launch_typed<16, MODE>(ta, tb, ts, kp, s);
+  }
+}
+
+int pick_bn(int cout) {
+  if (cout > 128) return 256;
+  if (cout > 64) return 128;
+  if (cout > 32) return 64;
+  if (cout > 16) return 32;
+  return 16;
+}
+
+}  // namespace
+
+size_t igemm_smem_bytes(int bn) {
+  switch (bn) {
+    case 256: return Cfg<256>::SMEM;
+    case 128: return Cfg<128>::SMEM;
+    case 64: return Cfg<64>::SMEM;
+    case 32: return Cfg<32>::SMEM;
+    default: return Cfg<16>::SMEM;
+  }
+}
+
+int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
+  if (!d.a || !d.b || !d.out || d.cout <= 0) return VAE_EINVAL;
+  auto misaligned = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) != 0; };
+  if (misaligned(d.a) || misaligned(d.b) || (d.sc && misaligned(d.sc))) return VAE_EINVAL;
+
+  const int bn = pick_bn(d.cout);
+  KParams kp{};
+  kp.err = device_error_word();
+  if (!kp.err) return VAE_ECUDA;
+  kp.cout = d.cout;
+  kp.out = d.out;
+  kp.ldo = d.ldo;
+  kp.out_nchw = d.out_nchw;
+  kp.bias = d.bias;
+  kp.bias_per_row = d.bias_per_row;
+  kp.residual = d.residual;
+  kp.alpha = d.alpha;
+  kp.round_out = d.round_out;
+  kp.t = d.t > 0 ? d.t : 1;
+  kp.imgs = d.imgs;
+  kp.n_tiles = ceil_div(d.cout, bn);
+
+  CUtensorMap ta{}, tb{}, ts{};
+  int bkdim;
+  if (d.mode == AMode::Gemm) {
+    if (d.kdim <= 0 || d.kdim % 32 || d.M <= 0 || d.lda % 4) return VAE_EINVAL;
+    kp.M = d.M;
+    kp.m_tiles = ceil_div(d.M, kBM);
+    kp.taps = 1;
+    kp.cin_chunks = d.kdim / 32;
+    kp.cin_pad = d.kdim;
+    kp.k_stages = kp.cin_chunks;
+    const uint64_t dims[2] = {static_cast<uint64_t>(d.kdim), static_cast<uint64_t>(d.M)};
+    const uint64_t str[1] = {static_cast<uint64_t>(d.lda) * 4};
+    const uint32_t box[2] = {32, static_cast<uint32_t>(kBM)};
+    VAE_TRY(encode_tiled(&ta, d.a, 2, dims, str, box));
+    bkdim = d.kdim;
+  } else {
+    if (d.a_c <= 0 || d.a_c % 32 || d.hin <= 0 || d.win <= 0 || d.imgs <= 0) return VAE_EINVAL;
+    kp.hin = d.hin;
+    kp.win = d.win;
+    kp.cin_chunks = d.a_c / 32;
+    kp.cin_pad = d.a_c;
+    uint32_t box[4];
+    if (d.mode == AMode::Conv) {
+      if (!(d.k == 1 || d.k == 3) || !(d.kt == 1 || d.kt == 3)) return VAE_EUNSUPPORTED;
+      kp.k = d.k;
+      kp.kt = d.kt;
+      kp.taps = d.k * d.k * d.kt;
+      kp.hout = d.hin;
+      kp.wout = d.win;
+      kp.bw = std::min(128, pow2_at_least(d.win));
+      kp.bh = kBM / kp.bw;
+      kp.tiles_x = ceil_div(d.win, kp.bw);
+      kp.tiles_y = ceil_div(d.hin, kp.bh);
+      kp.sc_chunks = d.sc ? d.sc_c / 32 : 0;
+      if (d.sc && (d.sc_c <= 0 || d.sc_c % 32)) return VAE_EINVAL;
+      box[0] = 32;
+      box[1] = kp.bw;
+      box[2] = kp.bh;
+      box[3] = 1;
+    } else {
+      kp.taps = 9;
+      kp.hout = 2 * d.hin;
+      kp.wout = 2 * d.win;
+      kp.bw = std::min(32, pow2_at_least(d.win));  // P
+      kp.bh = 32 / kp.bw;                          // R
+      kp.tiles_x = ceil_div(d.win, kp.bw);
+      kp.tiles_y = ceil_div(d.hin, kp.bh);
+      box[0] = 32;
+      box[1] = kp.bw;
+      box[2] = kp.bh;
+      box[3] = 1;
+    }
+    kp.m_tiles = d.imgs * kp.tiles_x * kp.tiles_y;
+    kp.k_stages = kp.taps * kp.cin_chunks + kp.sc_chunks;
+    const uint64_t dims[4] = {static_cast<uint64_t>(d.a_c), static_cast<uint64_t>(d.win),
+                              static_cast<uint64_t>(d.hin), static_cast<uint64_t>(d.imgs)};
+    const uint64_t str[3] = {static_cast<uint64_t>(d.a_c) * 4,
+                             static_cast<uint64_t>(d.win) * d.a_c * 4,
+                             static_cast<uint64_t>(d.hin) * d.win * d.a_c * 4};
+    VAE_TRY(encode_tiled(&ta, d.a, 4, dims, str, box));
+    if (kp.sc_chunks) {
+      const uint64_t sdims[4] = {static_cast<uint64_t>(d.sc_c), static_cast<uint64_t>(kp.wout),
+                                 static_cast<uint64_t>(kp.hout), static_cast<uint64_t>(d.imgs)};
+      const uint64_t sstr[3] = {static_cast<uint64_t>(d.sc_c) * 4,
+                                static_cast<uint64_t>(kp.wout) * d.sc_c * 4,
+                                static_cast<uint64_t>(kp.hout) * kp.wout * d.sc_c * 4};
+      VAE_TRY(encode_tiled(&ts, d.sc, 4, sdims, sstr, box));
+    } else {
+      ts = ta;
+    }
+    bkdim = d.ldb;
+  }
+  if (d.ldb % 4 || bkdim <= 0) return VAE_EINVAL;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(bkdim), static_cast<uint64_t>(d.cout)};
+    const uint64_t str[1] = {static_cast<uint64_t>(d.ldb) * 4};
+    const uint32_t box[2] = {32, static_cast<uint32_t>(bn)};
+    VAE_TRY(encode_tiled(&tb, d.b, 2, dims, str, box));
+  }
+  const long long total = static_cast<long long>(kp.m_tiles) * kp.n_tiles;
+  if (total <= 0 || total > (1ll << 31) - 1) return VAE_EUNSUPPORTED;
+  kp.total_tiles = static_cast<int>(total);
+
+  switch (d.mode) {
+    case AMode::Conv: return launch_mode<0>(bn, ta, tb, ts, kp, stream);
+    case AMode::Upsample: return launch_mode<1>(bn, ta, tb, ts, kp, stream);
+    default: return launch_mode<2>(bn, ta, tb, ts, kp, stream);
+  }
+}
+
+}  // namespace vae

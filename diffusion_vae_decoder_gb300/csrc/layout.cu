@@ -1,0 +1,123 @@
+// layout.cu -- weight packing and layout transforms around the tensor-core
+// kernels: NCHW <-> NHWC at the chain boundary, the latent de-normalisation
+// (cortiq-engine "Module vae", VaeDecoder: z / scaling_factor + shift_factor)
+// fused into that transpose, and V^T for the attention's second product.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace vae {
+
+namespace {
+
+// dst[o][tap * cin_pad + c] = tf32(w[o][c][tap]); shortcut columns follow at
+// taps * cin_pad + c; zero in every padding slot and padding row.
+__global__ void pack_kernel(const float *__restrict__ w, int cout, int cin, int taps,
+                            const float *__restrict__ wsc, int sc_cin, float *__restrict__ dst,
+                            int rows, int ldb, int cin_pad) {
+  const long long total = static_cast<long long>(rows) * ldb;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int o = static_cast<int>(i / ldb);
+    const int kidx = static_cast<int>(i % ldb);
+    float v = 0.f;
+    if (o < cout) {
+      const int main = taps * cin_pad;
+      if (kidx < main) {
+        const int tap = kidx / cin_pad, c = kidx % cin_pad;
+        if (c < cin) v = w[(static_cast<long long>(o) * cin + c) * taps + tap];
+      } else {
+        const int c = kidx - main;
+        if (c < sc_cin) v = wsc[static_cast<long long>(o) * sc_cin + c];
+      }
+    }
+    dst[i] = round_tf32(v);
+  }
+}
+
+// 32x32 tile transpose through shared memory, with an affine map and optional
+// TF32 rounding on the way.
+__global__ void transpose_kernel(const float *__restrict__ src, long long so, int sld,
+                                 float *__restrict__ dst, long long dso, int dld, int rows,
+                                 int cols, float alpha, float beta, int round) {
+  __shared__ float tile[32][33];
+  const int b = blockIdx.y;
+  const int tiles_c = (cols + 31) / 32;
+  const int r0 = static_cast<int>(blockIdx.x / tiles_c) * 32;
+  const int c0 = static_cast<int>(blockIdx.x % tiles_c) * 32;
+  const float *s = src + b * so;
+  float *d = dst + b * dso;
+  for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+    const int r = r0 + dy, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[dy][threadIdx.x] = s[static_cast<long long>(r) * sld + c];
+  }
+  __syncthreads();
+  for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+    const int c = c0 + dy, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) {
+      float v = fmaf(tile[threadIdx.x][dy], alpha, beta);
+      if (round) v = round_tf32(v);
+      d[static_cast<long long>(c) * dld + r] = v;
+    }
+  }
+}
+
+__global__ void pad_rows_kernel(const float *__restrict__ src, long long rows, int cols,
+                                float *__restrict__ dst, int dcols) {
+  const long long total = rows * dcols;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / dcols;
+    const int c = static_cast<int>(i % dcols);
+    dst[i] = c < cols ? src[r * cols + c] : 0.f;
+  }
+}
+
+__global__ void add_kernel(float *dst, const float *a, const float *b, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    dst[i] = (a ? a[i] : 0.f) + (b ? b[i] : 0.f);
+}
+
+int grid_for(long long n, int threads) {
+  long long g = (n + threads - 1) / threads;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  return static_cast<int>(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+}  // namespace
+
+int pack_conv_weights(const float *w, int cout, int cin, int taps, const float *w_sc,
+                      int sc_cin, float *dst, int cout_rows, int ldb, cudaStream_t s) {
+  if (!w || !dst || cout <= 0 || cin <= 0 || cout_rows < cout) return VAE_EINVAL;
+  if (ldb != packed_ldb(cin, taps, w_sc ? sc_cin : 0)) return VAE_EINVAL;
+  const long long total = static_cast<long long>(cout_rows) * ldb;
+  pack_kernel<<<grid_for(total, 256), 256, 0, s>>>(w, cout, cin, taps, w_sc, w_sc ? sc_cin : 0,
+                                                   dst, cout_rows, ldb, round_up32(cin));
+  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+}
+
+int transpose(const float *src, long long src_outer_stride, int src_ld, float *dst,
+              long long dst_outer_stride, int dst_ld, int outer, int rows, int cols, float alpha,
+              float beta, int round, cudaStream_t s) {
+  if (outer <= 0 || rows <= 0 || cols <= 0) return VAE_EINVAL;
+  if (outer > 65535) return VAE_EUNSUPPORTED;
+  const long long tiles = static_cast<long long>(ceil_div(cols, 32)) * ceil_div(rows, 32);
+  if (tiles > 0x7fffffffll) return VAE_EUNSUPPORTED;
+  dim3 grid(static_cast<unsigned>(tiles), outer);
+  transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(src, src_outer_stride, src_ld, dst,
+                                                 dst_outer_stride, dst_ld, rows, cols, alpha,
+                                                 beta, round);
+  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+}
+
+int pad_rows(const float *src, long long rows, int cols, float *dst, int dst_cols,
+             cudaStream_t s) {
+  pad_rows_kernel<<<grid_for(rows * dst_cols, 256), 256, 0, s>>>(src, rows, cols, dst, dst_cols);
+  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+}
+
+int add_bias(float *dst, const float *a, const float *b, int n, cudaStream_t s) {
+  add_kernel<<<grid_for(n, 256), 256, 0, s>>>(dst, a, b, n);
+  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+}
+
+}  // namespace vae

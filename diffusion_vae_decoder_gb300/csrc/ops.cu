@@ -1,0 +1,417 @@
+// ops.cu -- the single-op C-ABI entry points: conv2d (with the fused resnet
+// skip), upsample+conv, GroupNorm+SiLU, mid-block attention and the 3-D
+// causal conv. Each one stages its operands into the NHWC, 32-channel-padded
+// layout the tensor-core kernel reads, packs its weights (TF32-rounded) into
+// the caller's workspace, and enqueues kernels on the caller's stream.
+#include <cmath>
+
+#include "common.cuh"
+#include "ops.cuh"
+
+namespace vae {
+
+int stage_nhwc(const float *x, int n, int c, long long spatial, int layout, float *staging,
+               int cpad, float alpha, float beta, int round, const float **out,
+               cudaStream_t s) {
+  const bool passthrough =
+      layout == VAE_NHWC && c == cpad && alpha == 1.0f && beta == 0.0f && !round;
+  if (passthrough) {
+    *out = x;
+    return VAE_OK;
+  }
+  if (!staging) return VAE_EINVAL;
+  if (spatial > 0x7fffffffll) return VAE_EUNSUPPORTED;
+  if (cpad != c)
+    VAE_CUDA_TRY(cudaMemsetAsync(staging, 0, static_cast<size_t>(n) * spatial * cpad * 4, s));
+  if (layout == VAE_NCHW) {
+    VAE_TRY(transpose(x, static_cast<long long>(c) * spatial, static_cast<int>(spatial), staging,
+                      spatial * cpad, cpad, n, c, static_cast<int>(spatial), alpha, beta, round,
+                      s));
+  } else {
+    if (alpha != 1.0f || beta != 0.0f || round) return VAE_EINVAL;
+    VAE_TRY(pad_rows(x, static_cast<long long>(n) * spatial, c, staging, cpad, s));
+  }
+  *out = staging;
+  return VAE_OK;
+}
+
+int unstage_nchw(const float *src_nhwc, int n, int c, long long spatial, float *dst_nchw,
+                 cudaStream_t s) {
+  if (spatial > 0x7fffffffll) return VAE_EUNSUPPORTED;
+  return transpose(src_nhwc, spatial * c, c, dst_nchw, static_cast<long long>(c) * spatial,
+                   static_cast<int>(spatial), n, static_cast<int>(spatial), c, 1.0f, 0.0f, 0, s);
+}
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool needs_stage(int layout, int c) { return layout == VAE_NCHW || c % 32 != 0; }
+
+// ---------------------------------------------------------------- conv2d
+struct ConvWs {
+  float *packed, *bias_sum, *xs, *scs;
+};
+
+ConvWs carve_conv(Carver &cv, int n, int cin, long long spatial, int layout, int cout, int taps,
+                  int sc_cin) {
+  ConvWs w{};
+  const int ldb = packed_ldb(cin, taps, sc_cin);
+  w.packed = cv.take<float>(static_cast<size_t>(cout) * ldb);
+  w.bias_sum = sc_cin ? cv.take<float>(cout) : nullptr;
+  w.xs = needs_stage(layout, cin)
+             ? cv.take<float>(static_cast<size_t>(n) * spatial * round_up32(cin))
+             : nullptr;
+  w.scs = (sc_cin && needs_stage(layout, sc_cin))
+              ? cv.take<float>(static_cast<size_t>(n) * spatial * round_up32(sc_cin))
+              : nullptr;
+  return w;
+}
+
+// ---------------------------------------------------------------- attention
+struct AttnWs {
+  float *xs, *t, *wqkv, *bqkv, *wo, *qkv, *vt, *s, *o, *y;
+  void *gn;
+};
+
+AttnWs carve_attn(Carver &cv, int n, int c, int L, int layout) {
+  AttnWs w{};
+  const size_t nl = static_cast<size_t>(n) * L;
+  const size_t lp = static_cast<size_t>(round_up32(L));
+  w.xs = layout == VAE_NCHW ? cv.take<float>(nl * c) : nullptr;
+  w.t = cv.take<float>(nl * c);
+  w.wqkv = cv.take<float>(3ull * c * c);
+  w.bqkv = cv.take<float>(3ull * c);
+  w.wo = cv.take<float>(static_cast<size_t>(c) * c);
+  w.qkv = cv.take<float>(nl * 3 * c);
+  w.vt = cv.take<float>(static_cast<size_t>(c) * lp);
+  w.s = cv.take<float>(static_cast<size_t>(L) * lp);
+  w.o = cv.take<float>(nl * c);
+  w.y = layout == VAE_NCHW ? cv.take<float>(nl * c) : nullptr;
+  w.gn = cv.take<char>(groupnorm_ws_bytes(n, c, L, c));  // groups <= c
+  return w;
+}
+
+}  // namespace
+
+size_t attn_ws_bytes(int n, int c, int L, int layout) {
+  Carver cv(nullptr, 0);
+  carve_attn(cv, n, c, L, layout);
+  return cv.used;
+}
+
+// Attention on NHWC data (token-major): x_nhwc [n][L][c] -> y_nhwc (may equal
+// x_nhwc). Weights are pre-packed: wqkv [3c][c], bqkv [3c], wo [c][c].
+int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
+                   const float *gn_w, const float *gn_b, const float *wqkv, const float *bqkv,
+                   const float *wo, const float *bo, float *y, const AttnScratch &sc,
+                   cudaStream_t s) {
+  const int lp = round_up32(L);
+  // t = GroupNorm(x), no SiLU; TF32-rounded because it is an MMA operand.
+  VAE_TRY(groupnorm_silu(x, n, c, L, 1, groups, eps, gn_w, gn_b, 0, 1, sc.t, sc.gn, s));
+  // [q | k | v] = t [Wq; Wk; Wv]^T + [bq; bk; bv], one GEMM for all images.
+  {
+    IgemmDesc d;
+    d.mode = AMode::Gemm;
+    d.a = sc.t;
+    d.lda = c;
+    d.M = n * L;
+    d.kdim = c;
+    d.b = wqkv;
+    d.ldb = c;
+    d.cout = 3 * c;
+    d.out = sc.qkv;
+    d.ldo = 3 * c;
+    d.bias = bqkv;
+    d.round_out = 1;
+    VAE_TRY(igemm_launch(d, s));
+  }
+  if (lp != L) VAE_CUDA_TRY(cudaMemsetAsync(sc.vt, 0, static_cast<size_t>(c) * lp * 4, s));
+  for (int b = 0; b < n; ++b) {
+    const float *qkv_b = sc.qkv + static_cast<size_t>(b) * L * 3 * c;
+    // V^T [c][L] (row stride lp): the K-major B operand of P.V.
+    VAE_TRY(transpose(qkv_b + 2 * c, 0, 3 * c, sc.vt, 0, lp, 1, L, c, 1.0f, 0.0f, 0, s));
+    // S = q k^T (scale applied inside the softmax).
+    {
+      IgemmDesc d;
+      d.mode = AMode::Gemm;
+      d.a = qkv_b;
+      d.lda = 3 * c;
+      d.M = L;
+      d.kdim = c;
+      d.b = qkv_b + c;
+      d.ldb = 3 * c;
+      d.cout = L;
+      d.out = sc.s;
+      d.ldo = lp;
+      VAE_TRY(igemm_launch(d, s));
+    }
+    VAE_TRY(softmax_rows(sc.s, L, L, lp, 1.0f / std::sqrt(static_cast<float>(c)), s));
+    // o = P V
+    {
+      IgemmDesc d;
+      d.mode = AMode::Gemm;
+      d.a = sc.s;
+      d.lda = lp;
+      d.M = L;
+      d.kdim = lp;
+      d.b = sc.vt;
+      d.ldb = lp;
+      d.cout = c;
+      d.out = sc.o + static_cast<size_t>(b) * L * c;
+      d.ldo = c;
+      d.round_out = 1;
+      VAE_TRY(igemm_launch(d, s));
+    }
+  }
+  // y = x + (o Wo^T + bo)
+  IgemmDesc d;
+  d.mode = AMode::Gemm;
+  d.a = sc.o;
+  d.lda = c;
+  d.M = n * L;
+  d.kdim = c;
+  d.b = wo;
+  d.ldb = c;
+  d.cout = c;
+  d.out = y;
+  d.ldo = c;
+  d.bias = bo;
+  d.residual = x;
+  return igemm_launch(d, s);
+}
+
+}  // namespace vae
+
+using namespace vae;
+
+extern "C" {
+
+// ------------------------------------------------------------------ conv2d
+size_t vae_conv2d_workspace_size(int n, int cin, int h, int w, int layout, int cout, int k,
+                                 int sc_cin) {
+  if (n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0 || k <= 0 || sc_cin < 0) return 0;
+  Carver cv(nullptr, 0);
+  carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout, k * k, sc_cin);
+  return cv.used;
+}
+
+int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout, const float *weight,
+               const float *bias, int cout, int k, const float *residual, const float *sc_x,
+               const float *sc_w, const float *sc_b, int sc_cin, float *y, void *ws,
+               size_t ws_bytes, vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !weight || !y || !ws || n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0)
+    return VAE_EINVAL;
+  if (layout != VAE_NCHW && layout != VAE_NHWC) return VAE_EINVAL;
+  if (k != 1 && k != 3) return VAE_EUNSUPPORTED;
+  const bool has_sc = sc_x != nullptr || sc_w != nullptr;
+  if (has_sc && (!sc_x || !sc_w || sc_cin <= 0)) return VAE_EINVAL;
+  if (cin > 4096 || cout > 4096 || sc_cin > 4096 || h > 65535 || w > 65535)
+    return VAE_EUNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) ||
+      (sc_x && !aligned16(sc_x)))
+    return VAE_EINVAL;
+  if (layout == VAE_NHWC && cout % 4) return VAE_EUNSUPPORTED;
+  const int scc = has_sc ? sc_cin : 0;
+  const long long spatial = static_cast<long long>(h) * w;
+  Carver cv(ws, ws_bytes);
+  ConvWs cw = carve_conv(cv, n, cin, spatial, layout, cout, k * k, scc);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+
+  const int ldb = packed_ldb(cin, k * k, scc);
+  VAE_TRY(pack_conv_weights(weight, cout, cin, k * k, sc_w, scc, cw.packed, cout, ldb, s));
+  const float *bsum = bias;
+  if (has_sc && (bias || sc_b)) {
+    VAE_TRY(add_bias(cw.bias_sum, bias, sc_b, cout, s));
+    bsum = cw.bias_sum;
+  }
+  const float *xa = nullptr, *sca = nullptr;
+  VAE_TRY(stage_nhwc(x, n, cin, spatial, layout, cw.xs, round_up32(cin), 1.f, 0.f, 0, &xa, s));
+  if (has_sc)
+    VAE_TRY(stage_nhwc(sc_x, n, scc, spatial, layout, cw.scs, round_up32(scc), 1.f, 0.f, 0,
+                       &sca, s));
+  IgemmDesc d;
+  d.mode = AMode::Conv;
+  d.a = xa;
+  d.imgs = n;
+  d.hin = h;
+  d.win = w;
+  d.a_c = round_up32(cin);
+  d.k = k;
+  d.sc = sca;
+  d.sc_c = has_sc ? round_up32(scc) : 0;
+  d.b = cw.packed;
+  d.ldb = ldb;
+  d.cout = cout;
+  d.out = y;
+  d.ldo = cout;
+  d.out_nchw = layout == VAE_NCHW;
+  d.bias = bsum;
+  d.residual = residual;
+  return igemm_launch(d, s);
+}
+
+// ------------------------------------------------------------------ upsample + conv
+size_t vae_upsample_conv_workspace_size(int n, int cin, int h, int w, int layout, int cout) {
+  if (n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0) return 0;
+  Carver cv(nullptr, 0);
+  carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout, 9, 0);
+  return cv.used;
+}
+
+int vae_upsample_conv(const float *x, int n, int cin, int h, int w, int layout,
+                      const float *weight, const float *bias, int cout, float *y, void *ws,
+                      size_t ws_bytes, vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !weight || !y || !ws || n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0)
+    return VAE_EINVAL;
+  if (layout != VAE_NCHW && layout != VAE_NHWC) return VAE_EINVAL;
+  if (cin > 4096 || cout > 4096 || h > 32767 || w > 32767) return VAE_EUNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y)) return VAE_EINVAL;
+  if (layout == VAE_NHWC && cout % 4) return VAE_EUNSUPPORTED;
+  const long long spatial = static_cast<long long>(h) * w;
+  Carver cv(ws, ws_bytes);
+  ConvWs cw = carve_conv(cv, n, cin, spatial, layout, cout, 9, 0);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  const int ldb = packed_ldb(cin, 9, 0);
+  VAE_TRY(pack_conv_weights(weight, cout, cin, 9, nullptr, 0, cw.packed, cout, ldb, s));
+  const float *xa = nullptr;
+  VAE_TRY(stage_nhwc(x, n, cin, spatial, layout, cw.xs, round_up32(cin), 1.f, 0.f, 0, &xa, s));
+  IgemmDesc d;
+  d.mode = AMode::Upsample;
+  d.a = xa;
+  d.imgs = n;
+  d.hin = h;
+  d.win = w;
+  d.a_c = round_up32(cin);
+  d.b = cw.packed;
+  d.ldb = ldb;
+  d.cout = cout;
+  d.out = y;
+  d.ldo = cout;
+  d.out_nchw = layout == VAE_NCHW;
+  d.bias = bias;
+  return igemm_launch(d, s);
+}
+
+// ------------------------------------------------------------------ GroupNorm + SiLU
+size_t vae_groupnorm_silu_workspace_size(int n, int c, long long spatial, int layout,
+                                         int groups) {
+  (void)layout;
+  if (n <= 0 || c <= 0 || spatial <= 0 || groups <= 0) return 0;
+  return groupnorm_ws_bytes(n, c, spatial, groups);
+}
+
+int vae_groupnorm_silu(const float *x, int n, int c, long long spatial, int layout, int groups,
+                       float eps, const float *gamma, const float *beta, int apply_silu,
+                       float *y, void *ws, size_t ws_bytes, vae_stream_t stream) {
+  if (layout != VAE_NCHW && layout != VAE_NHWC) return VAE_EINVAL;
+  if (n <= 0 || c <= 0 || spatial <= 0 || groups <= 0) return VAE_EINVAL;
+  if (ws_bytes < groupnorm_ws_bytes(n, c, spatial, groups)) return VAE_EWORKSPACE;
+  return groupnorm_silu(x, n, c, spatial, layout == VAE_NHWC, groups, eps, gamma, beta,
+                        apply_silu != 0, 0, y, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ mid attention
+size_t vae_mid_attn_workspace_size(int n, int c, int h, int w, int layout) {
+  if (n <= 0 || c <= 0 || h <= 0 || w <= 0) return 0;
+  Carver cv(nullptr, 0);
+  const size_t a = attn_ws_bytes(n, c, h * w, layout);
+  cv.take<char>(a);
+  return cv.used;
+}
+
+int vae_mid_attn(const float *x, int n, int c, int h, int w, int layout, int groups, float eps,
+                 const float *gn_w, const float *gn_b, const float *wq, const float *bq,
+                 const float *wk, const float *bk, const float *wv, const float *bv,
+                 const float *wo, const float *bo, float *y, void *ws, size_t ws_bytes,
+                 vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !y || !ws || !gn_w || !gn_b || !wq || !bq || !wk || !bk || !wv || !bv || !wo || !bo)
+    return VAE_EINVAL;
+  if (n <= 0 || c <= 0 || h <= 0 || w <= 0 || groups <= 0) return VAE_EINVAL;
+  if (layout != VAE_NCHW && layout != VAE_NHWC) return VAE_EINVAL;
+  if (c % 32 || c > 1024 || c % groups) return VAE_EUNSUPPORTED;
+  const long long Lll = static_cast<long long>(h) * w;
+  if (Lll > 65536) return VAE_EUNSUPPORTED;
+  const int L = static_cast<int>(Lll);
+  if (!aligned16(x) || !aligned16(y)) return VAE_EINVAL;
+  Carver cv(ws, ws_bytes);
+  AttnWs aw = carve_attn(cv, n, c, L, layout);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+
+  // Pack [Wq; Wk; Wv] and Wo (TF32-rounded, K-major rows) and [bq; bk; bv].
+  const size_t cc = static_cast<size_t>(c) * c;
+  VAE_TRY(pack_conv_weights(wq, c, c, 1, nullptr, 0, aw.wqkv, c, c, s));
+  VAE_TRY(pack_conv_weights(wk, c, c, 1, nullptr, 0, aw.wqkv + cc, c, c, s));
+  VAE_TRY(pack_conv_weights(wv, c, c, 1, nullptr, 0, aw.wqkv + 2 * cc, c, c, s));
+  VAE_TRY(pack_conv_weights(wo, c, c, 1, nullptr, 0, aw.wo, c, c, s));
+  VAE_CUDA_TRY(cudaMemcpyAsync(aw.bqkv, bq, c * 4, cudaMemcpyDeviceToDevice, s));
+  VAE_CUDA_TRY(cudaMemcpyAsync(aw.bqkv + c, bk, c * 4, cudaMemcpyDeviceToDevice, s));
+  VAE_CUDA_TRY(cudaMemcpyAsync(aw.bqkv + 2 * c, bv, c * 4, cudaMemcpyDeviceToDevice, s));
+
+  const float *xa = x;
+  float *ya = y;
+  if (layout == VAE_NCHW) {
+    VAE_TRY(stage_nhwc(x, n, c, L, layout, aw.xs, c, 1.f, 0.f, 0, &xa, s));
+    ya = aw.y;
+  }
+  AttnScratch sc{aw.t, aw.qkv, aw.vt, aw.s, aw.o, aw.gn};
+  VAE_TRY(attention_nhwc(xa, n, c, L, groups, eps, gn_w, gn_b, aw.wqkv, aw.bqkv, aw.wo, bo, ya,
+                         sc, s));
+  if (layout == VAE_NCHW) VAE_TRY(unstage_nchw(ya, n, c, L, y, s));
+  return VAE_OK;
+}
+
+// ------------------------------------------------------------------ 3-D causal conv
+size_t vae_conv3d_causal_workspace_size(int n, int cin, int t, int h, int w, int layout,
+                                        int cout) {
+  if (n <= 0 || cin <= 0 || t <= 0 || h <= 0 || w <= 0 || cout <= 0) return 0;
+  Carver cv(nullptr, 0);
+  carve_conv(cv, n, cin, static_cast<long long>(t) * h * w, layout, cout, 27, 0);
+  return cv.used;
+}
+
+int vae_conv3d_causal(const float *x, int n, int cin, int t, int h, int w, int layout,
+                      const float *weight, const float *bias, int cout, const float *residual,
+                      float *y, void *ws, size_t ws_bytes, vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !weight || !y || !ws || n <= 0 || cin <= 0 || t <= 0 || h <= 0 || w <= 0 ||
+      cout <= 0)
+    return VAE_EINVAL;
+  if (layout != VAE_NCHW && layout != VAE_NHWC) return VAE_EINVAL;
+  if (cin > 4096 || cout > 4096 || h > 65535 || w > 65535 || static_cast<long long>(n) * t > 65535)
+    return VAE_EUNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual))) return VAE_EINVAL;
+  if (layout == VAE_NHWC && cout % 4) return VAE_EUNSUPPORTED;
+  const long long spatial = static_cast<long long>(t) * h * w;
+  Carver cv(ws, ws_bytes);
+  ConvWs cw = carve_conv(cv, n, cin, spatial, layout, cout, 27, 0);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  const int ldb = packed_ldb(cin, 27, 0);
+  VAE_TRY(pack_conv_weights(weight, cout, cin, 27, nullptr, 0, cw.packed, cout, ldb, s));
+  const float *xa = nullptr;
+  VAE_TRY(stage_nhwc(x, n, cin, spatial, layout, cw.xs, round_up32(cin), 1.f, 0.f, 0, &xa, s));
+  IgemmDesc d;
+  d.mode = AMode::Conv;
+  d.a = xa;
+  d.imgs = n * t;
+  d.t = t;
+  d.hin = h;
+  d.win = w;
+  d.a_c = round_up32(cin);
+  d.k = 3;
+  d.kt = 3;
+  d.b = cw.packed;
+  d.ldb = ldb;
+  d.cout = cout;
+  d.out = y;
+  d.ldo = cout;
+  d.out_nchw = layout == VAE_NCHW;
+  d.bias = bias;
+  d.residual = residual;
+  return igemm_launch(d, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// runtime.cu -- per-device runtime state shared by every entry point: the
+// device error word kernels report into, the SM count persistent grids are
+// sized from, and TMA tensor-map encoding through the driver entry point.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace vae {
+
+namespace {
+__device__ int g_vae_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_err_addr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+int *device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_vae_error_word) != cudaSuccess) return nullptr;
+    g_err_addr[dev] = static_cast<int *>(p);
+  }
+  return g_err_addr[dev];
+}
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 1;
+    g_sms[dev] = v;
+  }
+  return g_sms[dev];
+}
+
+int encode_tiled(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box) {
+  auto fn = encode_fn();
+  if (!fn) return VAE_ECUDA;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<cuuint32_t>(rank),
+         const_cast<void *>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VAE_OK : VAE_EUNSUPPORTED;
+}
+
+}  // namespace vae
+
+extern "C" {
+
+const char *vae_status_string(int status) {
+  switch (status) {
+    case VAE_OK: return "ok";
+    case VAE_EINVAL: return "invalid argument";
+    case VAE_EUNSUPPORTED: return "unsupported shape";
+    case VAE_EWORKSPACE: return "workspace too small";
+    case VAE_ECUDA: return "CUDA call or launch failed";
+    case VAE_ENOTPREPARED: return "chain handle not prepared";
+    case VAE_EDEVICE_TIMEOUT: return "a device-side wait timed out";
+    case VAE_ENOMEM: return "out of device memory";
+    default: return "unknown status";
+  }
+}
+
+int vae_device_error(vae_stream_t stream, int *code) {
+  if (!code) return VAE_EINVAL;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VAE_ECUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, vae::g_vae_error_word, sizeof(int)) != cudaSuccess)
+    return VAE_ECUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(vae::g_vae_error_word, &zero, sizeof(int)) != cudaSuccess)
+    return VAE_ECUDA;
+  *code = v;
+  return VAE_OK;
+}
+
+int vae_num_sms(void) { return vae::num_sms(); }
+
+}  // extern "C"

@@ -1,0 +1,223 @@
+/*
+ * vae.h -- C ABI of the GB300 (sm_103a) FLUX-class AutoencoderKL latent decoder.
+ *
+ * The decoder is the one the cortiq-engine 0.7.7 "Module vae" page documents
+ * (structs VaeDecoder, VaeChainArgs, VaeConvRef, VaeNormRef, VaeResnetRef,
+ * VaeAttnRef, VaeUpRef): latent [B,16,h,w] -> RGB [B,3,8h,8w].
+ *
+ * Conventions shared by every entry point
+ *   - Tensor pointers (x, y, residual, z, rgb, weights of the single-op calls,
+ *     ws) are DEVICE pointers owned by the caller, float32, 16-byte aligned.
+ *     Weights given to vae_chain_prepare may be host or device pointers.
+ *   - layout: VAE_NCHW (NCDHW for the 3-D call) or VAE_NHWC (NDHWC).
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). No entry point allocates device memory (vae_chain_prepare is the
+ *     one exception) or synchronises; scratch comes from `ws`, `ws_bytes` long,
+ *     whose required size the matching *_workspace_size call returns.
+ *   - Return value: VAE_OK (0) or a negative vae_status. On a nonzero status
+ *     the contents of the outputs are unspecified. Argument and shape checks
+ *     run before any launch. There is no CPU fallback.
+ *   - Arithmetic: 3x3 / 1x1 / 3x3x3 convolutions, attention projections and
+ *     the attention products run on the tcgen05 tensor cores with TF32
+ *     operands and FP32 accumulation; weights are rounded to TF32
+ *     (round-to-nearest) when packed; normalisation, softmax and epilogues are
+ *     FP32.
+ *   - Outputs may not alias inputs, except y == residual (vae_conv2d,
+ *     vae_conv3d_causal) and y == x (vae_groupnorm_silu).
+ *   - Device-side waits are bounded: a kernel that gives up records
+ *     VAE_EDEVICE_TIMEOUT in a device error word that vae_device_error reads.
+ */
+#ifndef VAE_GB300_H
+#define VAE_GB300_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define VAE_API __attribute__((visibility("default")))
+#else
+#define VAE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *vae_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  VAE_OK = 0,
+  VAE_EINVAL = -1,          /* null pointer, non-positive size, bad layout  */
+  VAE_EUNSUPPORTED = -2,    /* shape outside what the kernels handle        */
+  VAE_EWORKSPACE = -3,      /* ws_bytes below the *_workspace_size value    */
+  VAE_ECUDA = -4,           /* a CUDA runtime/driver call or launch failed  */
+  VAE_ENOTPREPARED = -5,    /* null or destroyed chain handle               */
+  VAE_EDEVICE_TIMEOUT = -6, /* a bounded device-side wait expired           */
+  VAE_ENOMEM = -7           /* vae_chain_prepare could not allocate         */
+} vae_status;
+
+typedef enum { VAE_NCHW = 0, VAE_NHWC = 1 } vae_layout;
+
+/* ------------------------------------------------------------------------
+ * vae_conv2d -- 2-D convolution, stride 1, square kernel k in {1,3}, zero
+ * padding k/2 (cortiq-engine "Module vae", structs Conv2d and VaeConvRef):
+ *   y[n,o,i,j] = bias[o] + sum_{c,ky,kx} weight[o,c,ky,kx] x[n,c,i+ky-k/2,j+kx-k/2]
+ *              (+ residual[n,o,i,j])
+ *              (+ sum_c sc_w[o,c] sc_x[n,c,i,j] + sc_b[o])
+ * The residual and the 1x1 shortcut form the resnet skip of VaeResnetRef
+ * ("x + conv2(...)", "the skip through the 1x1 shortcut"); both are optional
+ * (NULL). The shortcut is fused as extra reduction steps into the same
+ * accumulator.
+ *   x        [n,cin,h,w] (layout)          weight [cout,cin,k,k] row-major
+ *   bias     [cout] or NULL                residual [n,cout,h,w] or NULL
+ *   sc_x     [n,sc_cin,h,w] or NULL        sc_w [cout,sc_cin], sc_b [cout] or NULL
+ *   y        [n,cout,h,w]
+ * Limits: cin, sc_cin <= 4096; cout <= 4096; h, w <= 65535.
+ */
+VAE_API size_t vae_conv2d_workspace_size(int n, int cin, int h, int w, int layout, int cout, int k,
+                                 int sc_cin);
+VAE_API int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout, const float *weight,
+               const float *bias, int cout, int k, const float *residual, const float *sc_x,
+               const float *sc_w, const float *sc_b, int sc_cin, float *y, void *ws,
+               size_t ws_bytes, vae_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * vae_upsample_conv -- nearest-2x upsample followed by a 3x3 stride-1 pad-1
+ * convolution (cortiq-engine "Module vae", struct VaeUpRef):
+ *   u[n,c,i,j] = x[n,c,i/2,j/2];  y = conv3x3(u) + bias
+ * The upsampled tensor is never stored: the convolution gathers its operand
+ * tiles straight from the low-resolution x.
+ *   x [n,cin,h,w]; weight [cout,cin,3,3]; bias [cout] or NULL; y [n,cout,2h,2w]
+ */
+VAE_API size_t vae_upsample_conv_workspace_size(int n, int cin, int h, int w, int layout, int cout);
+VAE_API int vae_upsample_conv(const float *x, int n, int cin, int h, int w, int layout,
+                      const float *weight, const float *bias, int cout, float *y, void *ws,
+                      size_t ws_bytes, vae_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * vae_groupnorm_silu -- GroupNorm (cortiq-engine "Module vae", structs
+ * GroupNorm and VaeNormRef; statistics as vae3d.rs GroupNorm::apply computes
+ * them): per (sample, group) over the group's c/groups channels and all
+ * `spatial` positions (H*W, or T*H*W for 5-D data),
+ *   mean, var = biased variance,  y = (x-mean)/sqrt(var+eps)*gamma[c] + beta[c]
+ * then, if apply_silu != 0, y = y / (1 + exp(-y)) (vae3d.rs fn silu).
+ *   x, y [n,c,spatial] (layout; y == x allowed); gamma, beta [c]
+ * Limits: c % groups == 0, c % 4 == 0, c <= 1024.
+ */
+VAE_API size_t vae_groupnorm_silu_workspace_size(int n, int c, long long spatial, int layout,
+                                         int groups);
+VAE_API int vae_groupnorm_silu(const float *x, int n, int c, long long spatial, int layout, int groups,
+                       float eps, const float *gamma, const float *beta, int apply_silu,
+                       float *y, void *ws, size_t ws_bytes, vae_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * vae_mid_attn -- mid-block single-head spatial attention (cortiq-engine
+ * "Module vae", struct VaeAttnRef): t = GroupNorm(x); tokens p = i*w + j;
+ * q,k,v = t W^T + b with W [c,c] row-major (out x in);
+ * o = softmax(q k^T / sqrt(c)) v (row softmax with max subtraction, vae3d.rs
+ * fn softmax_inplace); y = x + (o wo^T + bo).
+ *   x, y [n,c,h,w] (layout); gn_w, gn_b [c]; wq..wo [c,c]; bq..bo [c]
+ * Limits: c % 32 == 0, c <= 1024, h*w <= 65536.
+ */
+VAE_API size_t vae_mid_attn_workspace_size(int n, int c, int h, int w, int layout);
+VAE_API int vae_mid_attn(const float *x, int n, int c, int h, int w, int layout, int groups, float eps,
+                 const float *gn_w, const float *gn_b, const float *wq, const float *bq,
+                 const float *wk, const float *bk, const float *wv, const float *bv,
+                 const float *wo, const float *bo, float *y, void *ws, size_t ws_bytes,
+                 vae_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * vae_conv3d_causal -- 3-D convolution with causal time padding ("VAE decode
+ * -> GPU handoff (FLUX/LTX render services)", sections "The CPU VAE code"
+ * and "GPU plan" step 1): kernel 3x3x3, stride 1, spatial zero padding 1,
+ * time padded by prepending two copies of the first frame:
+ *   y[n,o,t,i,j] = bias[o] + sum w[o,c,kt,ky,kx] x[n,c,max(t+kt-2,0),i+ky-1,j+kx-1]
+ *                  (+ residual[n,o,t,i,j])
+ *   x [n,cin,t,h,w] (NCDHW or NDHWC); weight [cout,cin,3,3,3]; y [n,cout,t,h,w]
+ */
+VAE_API size_t vae_conv3d_causal_workspace_size(int n, int cin, int t, int h, int w, int layout,
+                                        int cout);
+VAE_API int vae_conv3d_causal(const float *x, int n, int cin, int t, int h, int w, int layout,
+                      const float *weight, const float *bias, int cout, const float *residual,
+                      float *y, void *ws, size_t ws_bytes, vae_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The whole decoder (cortiq-engine "Module vae", structs VaeChainArgs and
+ * VaeDecoder), in execution order: z/scaling_factor + shift_factor ->
+ * conv_in -> mid_res1 -> mid_attn -> mid_res2 -> ups[0..n_ups) ->
+ * GroupNorm+SiLU (norm_out) -> conv_out. Activations stay in device memory
+ * (NHWC inside the chain); only the RGB output is written to `rgb`.
+ * A conv_ref with weight == NULL is absent (shortcut, upsample conv).
+ * Attention projections are conv_refs with k = 1, cin = cout = c.
+ */
+typedef struct {
+  const float *weight; /* [cout, cin, k, k] row-major */
+  const float *bias;   /* [cout] */
+  int cout, cin, k;
+} vae_conv_ref;
+
+typedef struct {
+  const float *weight; /* gamma [c] */
+  const float *bias;   /* beta [c] */
+  int c;
+} vae_norm_ref;
+
+typedef struct {
+  vae_norm_ref norm1;
+  vae_conv_ref conv1;
+  vae_norm_ref norm2;
+  vae_conv_ref conv2;
+  vae_conv_ref shortcut; /* 1x1, weight NULL when cin == cout */
+} vae_resnet_ref;
+
+typedef struct {
+  vae_norm_ref norm;
+  vae_conv_ref q, k, v, out;
+} vae_attn_ref;
+
+typedef struct {
+  int n_resnets;
+  const vae_resnet_ref *resnets;
+  vae_conv_ref upsample_conv; /* weight NULL: no upsample */
+} vae_up_ref;
+
+typedef struct {
+  int latent_channels;
+  float scaling_factor, shift_factor;
+  int groups;
+  float eps;
+  vae_conv_ref conv_in;
+  vae_resnet_ref mid_res1;
+  vae_attn_ref mid_attn;
+  vae_resnet_ref mid_res2;
+  int n_ups;
+  const vae_up_ref *ups;
+  vae_norm_ref norm_out;
+  vae_conv_ref conv_out;
+} vae_chain_args;
+
+/* Packs every weight once (TF32-rounded, GEMM layout) into device memory owned
+ * by the returned handle, which the key-cached weight set of VaeChainArgs
+ * corresponds to. Allocates; enqueues copies on `stream` and synchronises it. */
+VAE_API int vae_chain_prepare(const vae_chain_args *args, void **handle, vae_stream_t stream);
+/* Workspace for one vae_decode_chain call on a [n,latent_channels,h,w] latent;
+ * 0 for a null handle. */
+VAE_API size_t vae_chain_workspace_size(const void *handle, int n, int h, int w);
+/*   z   [n,latent_channels,h,w] NCHW (not yet de-normalised)
+ *   rgb [n,3,8h,8w] NCHW (raw decoder output, not clamped) */
+VAE_API int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *rgb, void *ws,
+                     size_t ws_bytes, vae_stream_t stream);
+VAE_API int vae_chain_destroy(void *handle);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics. */
+VAE_API const char *vae_status_string(int status);
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device; *code receives 0 or the VAE_E* status a kernel recorded. */
+VAE_API int vae_device_error(vae_stream_t stream, int *code);
+/* Number of SMs the kernels size their persistent grids for (current device). */
+VAE_API int vae_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VAE_GB300_H */

@@ -1,0 +1,80 @@
+"""GPU parity of the whole decoder chain (vae_decode_chain) against the
+float64 CPU oracle, on the seeded synthetic latents and random-init weights
+of the decoder workloads: RGB cosine >= 0.99999 and max |err| <= 5e-3."""
+import numpy as np
+import pytest
+
+import oracle as O
+import vae_synth as S
+from tests._parity import COS_MIN, RGB_MAXABS, SENTINEL, assert_all_written, metrics
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import diffusion_vae_decoder_gb300 as pkg
+    pkg.load_library()
+    yield
+    assert pkg.vae_device_error() == 0
+
+
+def _decode(arch, latent_shape, seed, n_up=4):
+    import diffusion_vae_decoder_gb300 as pkg
+    w = S.make_decoder_weights(arch, seed)
+    z = S.make_latent(latent_shape, seed)
+    chain = pkg.VaeChain(w, n_up_blocks=n_up)
+    n, _, h, ww = latent_shape
+    out = torch.full((n, 3, 8 * h, 8 * ww), SENTINEL, dtype=torch.float32, device="cuda")
+    chain.decode(torch.from_numpy(z).cuda(), out=out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    chain.close()
+    return w, z, got
+
+
+def _check(got, ref, what):
+    assert_all_written(got, what)
+    m = metrics(got, ref)
+    print(what, m)
+    assert m["cos"] >= COS_MIN and m["max_abs"] <= RGB_MAXABS, (what, m)
+    return m
+
+
+def test_tiny_decoder_parity():
+    seed = S.seed_of("tiny_decoder")
+    w, z, got = _decode("tiny", (1, 16, 8, 8), seed)
+    ref = O.decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
+    _check(got, ref, "tiny [1,16,8,8]")
+
+
+def test_tiny_decoder_batch_and_ragged_latent():
+    """Batch of 2 on a latent whose sides are not powers of two."""
+    seed = 77
+    w, z, got = _decode("tiny", (2, 16, 5, 7), seed)
+    ref = O.decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
+    _check(got, ref, "tiny [2,16,5,7]")
+
+
+def test_decoder_256_parity():
+    seed = S.seed_of("decoder_256")
+    w, z, got = _decode("flux", (1, 16, 32, 32), seed)
+    ref = O.decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
+    _check(got, ref, "flux [1,16,32,32] -> 256^2")
+
+
+def test_chain_rejects_small_workspace():
+    import diffusion_vae_decoder_gb300 as pkg
+    w = S.make_decoder_weights("tiny", 5)
+    chain = pkg.VaeChain(w, n_up_blocks=4)
+    z = torch.zeros((1, 16, 8, 8), device="cuda")
+    need = chain.workspace_size(1, 8, 8)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkg.VaeError) as e:
+        chain.decode(z, ws=ws)
+    assert e.value.status == -3
+    chain.close()
