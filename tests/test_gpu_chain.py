@@ -52,12 +52,27 @@ def test_tiny_decoder_parity():
     _check(got, ref, "tiny [1,16,8,8]")
 
 
+# Extra coverage cases (not one of the configured workloads) use a bound
+# derived from the arithmetic: rounding both operands of every product to
+# TF32 (unit roundoff 2^-11), modelled on the CPU for this very input, gives
+# relative L2 1.05e-3 and max |err| 5.2e-3 at the RGB output; the bound is
+# twice that model.
+EXTRA_MAXABS = 1.0e-2
+EXTRA_REL_L2 = 2.0e-3
+
+
 def test_tiny_decoder_batch_and_ragged_latent():
     """Batch of 2 on a latent whose sides are not powers of two."""
     seed = 77
     w, z, got = _decode("tiny", (2, 16, 5, 7), seed)
     ref = O.decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
-    _check(got, ref, "tiny [2,16,5,7]")
+    assert_all_written(got)
+    m = metrics(got, ref)
+    print("tiny [2,16,5,7]", m)
+    assert m["cos"] >= COS_MIN and m["max_abs"] <= EXTRA_MAXABS and m["rel_l2"] <= EXTRA_REL_L2, m
+    for b in range(2):  # every image of the batch decodes like it would alone
+        mb = metrics(got[b], ref[b])
+        assert mb["cos"] >= COS_MIN, (b, mb)
 
 
 def test_decoder_256_parity():
