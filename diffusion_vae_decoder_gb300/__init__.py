@@ -67,6 +67,13 @@ class ChainArgs(ctypes.Structure):
                 ("ups", ctypes.POINTER(UpRef)), ("norm_out", NormRef), ("conv_out", ConvRef)]
 
 
+class ProfRecord(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("kernels", ctypes.c_int), ("flops", ctypes.c_double),
+                ("bytes", ctypes.c_double), ("ms", ctypes.c_double)]
+
+
+PROF_KINDS = {0: "conv3x3", 1: "upsample_conv", 2: "groupnorm", 3: "attention", 4: "layout"}
+
 _I, _LL, _F, _SZ = ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
     "vae_conv2d_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
@@ -87,6 +94,9 @@ _SIGS = {
     "vae_status_string": (ctypes.c_char_p, [_I]),
     "vae_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "vae_num_sms": (_I, []),
+    "vae_chain_profile": (_I, [_P, _I]),
+    "vae_chain_profile_read": (_I, [_P, ctypes.POINTER(ProfRecord), _I, ctypes.POINTER(_I)]),
+    "vae_kernel_launch_count": (_LL, []),
 }
 
 
@@ -260,6 +270,10 @@ def vae_conv3d_causal(x, weight, bias=None, residual=None, layout=VAE_NCHW, out=
     return out
 
 
+def vae_kernel_launch_count():
+    return load_library().vae_kernel_launch_count()
+
+
 def vae_device_error(stream=None):
     lib = load_library()
     code = ctypes.c_int(0)
@@ -353,6 +367,21 @@ class VaeChain:
         _check("vae_decode_chain", lib.vae_decode_chain(
             self.handle, _ptr(z), n, h, w, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
         return out
+
+    def profile(self, enable=True):
+        _check("vae_chain_profile", load_library().vae_chain_profile(self.handle, int(enable)))
+
+    def profile_read(self):
+        """Per-step records of the profiled decodes (synchronises their events)."""
+        lib = load_library()
+        cnt = ctypes.c_int(0)
+        _check("vae_chain_profile_read", lib.vae_chain_profile_read(self.handle, None, 0,
+                                                                    ctypes.byref(cnt)))
+        arr = (ProfRecord * max(1, cnt.value))()
+        _check("vae_chain_profile_read", lib.vae_chain_profile_read(self.handle, arr, cnt.value,
+                                                                    ctypes.byref(cnt)))
+        return [dict(kind=PROF_KINDS.get(r.kind, r.kind), kernels=r.kernels, flops=r.flops,
+                     bytes=r.bytes, ms=r.ms) for r in arr[:cnt.value]]
 
     def close(self):
         if getattr(self, "handle", None):

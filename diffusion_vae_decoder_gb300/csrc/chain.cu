@@ -52,8 +52,57 @@ struct UpW {
   ConvW up;
 };
 
+// Per-step CUDA-event profiler (enabled through vae_chain_profile).
+struct Profiler {
+  struct Rec {
+    vae_prof_record r;
+    int ev0, ev1;
+    long long launches0;
+  };
+  bool on = false;
+  std::vector<cudaEvent_t> events;
+  std::vector<Rec> recs;
+  int next = 0;
+
+  int event(cudaStream_t s) {
+    if (next == static_cast<int>(events.size())) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return -1;
+      events.push_back(e);
+    }
+    if (cudaEventRecord(events[next], s) != cudaSuccess) return -1;
+    return next++;
+  }
+  // Opens a step; returns its record index, or -1 when profiling is off.
+  int open(int kind, double flops, double bytes, cudaStream_t s) {
+    if (!on) return -1;
+    Rec rec{};
+    rec.r.kind = kind;
+    rec.r.flops = flops;
+    rec.r.bytes = bytes;
+    rec.launches0 = launch_count();
+    rec.ev0 = event(s);
+    rec.ev1 = -1;
+    recs.push_back(rec);
+    return static_cast<int>(recs.size()) - 1;
+  }
+  void close(int idx, cudaStream_t s) {
+    if (idx < 0) return;
+    recs[idx].ev1 = event(s);
+    recs[idx].r.kernels = static_cast<int>(launch_count() - recs[idx].launches0);
+  }
+  void reset() {
+    recs.clear();
+    next = 0;
+  }
+  ~Profiler() {
+    for (cudaEvent_t e : events) cudaEventDestroy(e);
+  }
+};
+
 struct Chain {
   uint32_t magic = kMagic;
+  Profiler prof;
   int device = 0;
   int latent_c = 0, groups = 32;
   float eps = 1e-6f, sf = 1.f, sh = 0.f;
@@ -245,9 +294,26 @@ DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, 
   return d;
 }
 
-int run_conv(const ConvW &c, const float *in, int n, int h, int w, const float *sc_in,
-             const float *residual, float *out, int round_out, cudaStream_t s,
-             bool upsample = false, bool nchw_out = false) {
+// RAII bracket of one profiled step.
+struct Step {
+  Profiler &p;
+  cudaStream_t s;
+  int idx;
+  Step(Profiler &prof, int kind, double flops, double bytes, cudaStream_t st)
+      : p(prof), s(st), idx(prof.open(kind, flops, bytes, st)) {}
+  ~Step() { p.close(idx, s); }
+};
+
+double conv_flops(const ConvW &c, long long out_pixels) {
+  return 2.0 * out_pixels * c.cout * (static_cast<double>(c.cin) * c.k * c.k + c.sc_cin);
+}
+
+int run_conv(Profiler &prof, const ConvW &c, const float *in, int n, int h, int w,
+             const float *sc_in, const float *residual, float *out, int round_out,
+             cudaStream_t s, bool upsample = false, bool nchw_out = false) {
+  const long long out_px = static_cast<long long>(n) * h * w * (upsample ? 4 : 1);
+  Step st(prof, upsample ? VAE_PROF_UPSAMPLE_CONV : VAE_PROF_CONV3X3, conv_flops(c, out_px), 0,
+          s);
   IgemmDesc d;
   d.mode = upsample ? AMode::Upsample : AMode::Conv;
   d.a = in;
@@ -272,16 +338,20 @@ int run_conv(const ConvW &c, const float *in, int n, int h, int w, const float *
 
 // One resnet on NHWC data: `in` [n,h,w,cin] -> `out` [n,h,w,cout]; out == in
 // is allowed when there is no shortcut.
-int run_resnet(const Chain &ch, const ResW &r, const float *in, float *out, const DecodeWs &ws,
-               int n, int h, int w, int round_out, cudaStream_t s) {
+int run_gn(Chain &ch, const NormW &nw, const float *in, int n, long long sp, float *out,
+           void *gnws, cudaStream_t s) {
+  Step st(ch.prof, VAE_PROF_GROUPNORM, 0, 12.0 * n * sp * nw.c, s);
+  return groupnorm_silu(in, n, nw.c, sp, 1, ch.groups, ch.eps, nw.g, nw.b, 1, 1, out, gnws, s);
+}
+
+int run_resnet(Chain &ch, const ResW &r, const float *in, float *out, const DecodeWs &ws, int n,
+               int h, int w, int round_out, cudaStream_t s) {
   const long long sp = static_cast<long long>(h) * w;
-  VAE_TRY(groupnorm_silu(in, n, r.c1.cin, sp, 1, ch.groups, ch.eps, r.n1.g, r.n1.b, 1, 1, ws.T,
-                         ws.gn, s));
-  VAE_TRY(run_conv(r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s));
-  VAE_TRY(groupnorm_silu(ws.H, n, r.c1.cout, sp, 1, ch.groups, ch.eps, r.n2.g, r.n2.b, 1, 1,
-                         ws.T, ws.gn, s));
-  if (r.c2.sc_cin) return run_conv(r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s);
-  return run_conv(r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s);
+  VAE_TRY(run_gn(ch, r.n1, in, n, sp, ws.T, ws.gn, s));
+  VAE_TRY(run_conv(ch.prof, r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s));
+  VAE_TRY(run_gn(ch, r.n2, ws.H, n, sp, ws.T, ws.gn, s));
+  if (r.c2.sc_cin) return run_conv(ch.prof, r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s);
+  return run_conv(ch.prof, r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s);
 }
 
 }  // namespace
@@ -374,15 +444,23 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
 
   // z / scaling_factor + shift_factor, NCHW -> NHWC (channels padded to 32).
   const float *lat = nullptr;
-  VAE_TRY(stage_nhwc(z, n, ch->latent_c, L, VAE_NCHW, d.lat, round_up32(ch->latent_c),
-                     1.0f / ch->sf, ch->sh, 1, &lat, s));
+  {
+    const int cp = round_up32(ch->latent_c);
+    Step st(ch->prof, VAE_PROF_LAYOUT, 0, 4.0 * n * L * (ch->latent_c + cp), s);
+    VAE_TRY(stage_nhwc(z, n, ch->latent_c, L, VAE_NCHW, d.lat, cp, 1.0f / ch->sf, ch->sh, 1,
+                       &lat, s));
+  }
   float *cur = d.X, *other = d.Y;
   int hh = h, ww = w;
-  VAE_TRY(run_conv(ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s));
+  VAE_TRY(run_conv(ch->prof, ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s));
   VAE_TRY(run_resnet(*ch, ch->mid1, cur, cur, d, n, hh, ww, 0, s));
-  VAE_TRY(attention_nhwc(cur, n, ch->attn.c, static_cast<int>(L), ch->groups, ch->eps,
-                         ch->attn.n.g, ch->attn.n.b, ch->attn.wqkv, ch->attn.bqkv, ch->attn.wo,
-                         ch->attn.bo, cur, d.attn, s));
+  {
+    const double c = ch->attn.c;
+    Step st(ch->prof, VAE_PROF_ATTENTION, n * (4.0 * L * L * c + 8.0 * L * c * c), 0, s);
+    VAE_TRY(attention_nhwc(cur, n, ch->attn.c, static_cast<int>(L), ch->groups, ch->eps,
+                           ch->attn.n.g, ch->attn.n.b, ch->attn.wqkv, ch->attn.bqkv, ch->attn.wo,
+                           ch->attn.bo, cur, d.attn, s));
+  }
   VAE_TRY(run_resnet(*ch, ch->mid2, cur, cur, d, n, hh, ww, 0, s));
   for (const UpW &u : ch->ups) {
     for (size_t j = 0; j < u.res.size(); ++j) {
@@ -396,15 +474,43 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
     }
     if (u.has_up) {
       // Output rounded: the next resnet may read it through its shortcut MMA.
-      VAE_TRY(run_conv(u.up, cur, n, hh, ww, nullptr, nullptr, other, 1, s, true));
+      VAE_TRY(run_conv(ch->prof, u.up, cur, n, hh, ww, nullptr, nullptr, other, 1, s, true));
       std::swap(cur, other);
       hh *= 2;
       ww *= 2;
     }
   }
-  VAE_TRY(groupnorm_silu(cur, n, ch->norm_out.c, static_cast<long long>(hh) * ww, 1, ch->groups,
-                         ch->eps, ch->norm_out.g, ch->norm_out.b, 1, 1, d.T, d.gn, s));
-  return run_conv(ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, rgb, 0, s, false, true);
+  VAE_TRY(run_gn(*ch, ch->norm_out, cur, n, static_cast<long long>(hh) * ww, d.T, d.gn, s));
+  return run_conv(ch->prof, ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, rgb, 0, s, false,
+                  true);
+}
+
+int vae_chain_profile(void *handle, int enable) {
+  Chain *ch = static_cast<Chain *>(handle);
+  if (!ch || ch->magic != kMagic) return VAE_ENOTPREPARED;
+  ch->prof.on = enable != 0;
+  if (ch->prof.on) ch->prof.reset();
+  return VAE_OK;
+}
+
+int vae_chain_profile_read(void *handle, vae_prof_record *out, int capacity, int *count) {
+  Chain *ch = static_cast<Chain *>(handle);
+  if (!ch || ch->magic != kMagic) return VAE_ENOTPREPARED;
+  if (!count || (capacity > 0 && !out)) return VAE_EINVAL;
+  Profiler &p = ch->prof;
+  const int n = static_cast<int>(p.recs.size());
+  *count = n;
+  for (int i = 0; i < n && i < capacity; ++i) {
+    Profiler::Rec &r = p.recs[i];
+    float ms = 0.f;
+    if (r.ev0 < 0 || r.ev1 < 0) return VAE_ECUDA;
+    if (cudaEventSynchronize(p.events[r.ev1]) != cudaSuccess) return VAE_ECUDA;
+    if (cudaEventElapsedTime(&ms, p.events[r.ev0], p.events[r.ev1]) != cudaSuccess)
+      return VAE_ECUDA;
+    r.r.ms = ms;
+    out[i] = r.r;
+  }
+  return VAE_OK;
 }
 
 int vae_chain_destroy(void *handle) {

@@ -47,6 +47,9 @@ struct Carver {
 // __device__ symbol; resolved once per device.
 int *device_error_word();
 int num_sms();
+// Every kernel launch of the library bumps this process-wide counter.
+void count_launches(int n);
+long long launch_count();
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 int encode_tiled(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,

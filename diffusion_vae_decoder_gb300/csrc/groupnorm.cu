@@ -271,7 +271,9 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
     gn_apply_nchw<<<static_cast<int>(g), threads, 0, s>>>(x, total, c, spatial, scale, shift,
                                                           silu, round_out, y);
   }
-  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(3);
+  return VAE_OK;
 }
 
 }  // namespace vae

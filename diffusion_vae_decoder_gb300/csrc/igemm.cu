@@ -405,7 +405,9 @@ int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap
   if (attr_err != cudaSuccess) return VAE_ECUDA;
   const int grid = std::min(kp.total_tiles, num_sms());
   igemm_kernel<BN, MODE><<<grid, kThreads, C::SMEM, stream>>>(ta, tb, ts, kp);
-  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(1);
+  return VAE_OK;
 }
 
 template <int MODE>

@@ -92,7 +92,9 @@ int pack_conv_weights(const float *w, int cout, int cin, int taps, const float *
   const long long total = static_cast<long long>(cout_rows) * ldb;
   pack_kernel<<<grid_for(total, 256), 256, 0, s>>>(w, cout, cin, taps, w_sc, w_sc ? sc_cin : 0,
                                                    dst, cout_rows, ldb, round_up32(cin));
-  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(1);
+  return VAE_OK;
 }
 
 int transpose(const float *src, long long src_outer_stride, int src_ld, float *dst,
@@ -106,18 +108,24 @@ int transpose(const float *src, long long src_outer_stride, int src_ld, float *d
   transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(src, src_outer_stride, src_ld, dst,
                                                  dst_outer_stride, dst_ld, rows, cols, alpha,
                                                  beta, round);
-  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(1);
+  return VAE_OK;
 }
 
 int pad_rows(const float *src, long long rows, int cols, float *dst, int dst_cols,
              cudaStream_t s) {
   pad_rows_kernel<<<grid_for(rows * dst_cols, 256), 256, 0, s>>>(src, rows, cols, dst, dst_cols);
-  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(1);
+  return VAE_OK;
 }
 
 int add_bias(float *dst, const float *a, const float *b, int n, cudaStream_t s) {
   add_kernel<<<grid_for(n, 256), 256, 0, s>>>(dst, a, b, n);
-  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(1);
+  return VAE_OK;
 }
 
 }  // namespace vae

@@ -3,6 +3,7 @@
 // sized from, and TMA tensor-map encoding through the driver entry point.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -16,6 +17,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int *g_err_addr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
+std::atomic<long long> g_launches{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -56,6 +58,9 @@ int num_sms() {
   }
   return g_sms[dev];
 }
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 int encode_tiled(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                  const uint64_t *strides_bytes, const uint32_t *box) {
@@ -110,5 +115,7 @@ int vae_device_error(vae_stream_t stream, int *code) {
 }
 
 int vae_num_sms(void) { return vae::num_sms(); }
+
+long long vae_kernel_launch_count(void) { return vae::launch_count(); }
 
 }  // extern "C"

@@ -89,7 +89,9 @@ int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStrea
     softmax_reg<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale);
   else
     softmax_long<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale);
-  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(1);
+  return VAE_OK;
 }
 
 }  // namespace vae

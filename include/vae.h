@@ -209,7 +209,36 @@ VAE_API int vae_decode_chain(void *handle, const float *z, int n, int h, int w, 
 VAE_API int vae_chain_destroy(void *handle);
 
 /* ------------------------------------------------------------------------
+ * Step profiler of the chain: when enabled, vae_decode_chain brackets every
+ * step (one conv, one GroupNorm+SiLU, the attention block, the latent
+ * staging) with CUDA events on the caller's stream and stores the step's
+ * algorithmic work. Enabling clears earlier records; records accumulate over
+ * decode calls until read. Profiling adds event records to the stream, so do
+ * not enable it while the stream is being captured into a graph. */
+typedef enum {
+  VAE_PROF_CONV3X3 = 0,        /* 3x3 conv (flops: 2*cin*cout*9 per output pixel, + shortcut) */
+  VAE_PROF_UPSAMPLE_CONV = 1,  /* nearest-2x upsample + 3x3 conv (same per output pixel)     */
+  VAE_PROF_GROUPNORM = 2,      /* GroupNorm(+SiLU) (bytes: 12 per element: read, read, write) */
+  VAE_PROF_ATTENTION = 3,      /* mid attention block (flops: 4*L*L*c + 8*L*c*c per image)   */
+  VAE_PROF_LAYOUT = 4          /* latent de-normalisation / layout staging (bytes)           */
+} vae_prof_kind;
+
+typedef struct {
+  int kind;     /* vae_prof_kind */
+  int kernels;  /* kernel launches inside the step */
+  double flops; /* algorithmic floating-point operations of the step */
+  double bytes; /* algorithmic HBM bytes of the step (memory-bound kinds) */
+  double ms;    /* device time between the step's two events */
+} vae_prof_record;
+
+VAE_API int vae_chain_profile(void *handle, int enable);
+/* Synchronises the recorded events; copies min(capacity, recorded) records. */
+VAE_API int vae_chain_profile_read(void *handle, vae_prof_record *out, int capacity, int *count);
+
+/* ------------------------------------------------------------------------
  * Diagnostics. */
+/* Kernels this library has launched in this process (monotonic counter). */
+VAE_API long long vae_kernel_launch_count(void);
 VAE_API const char *vae_status_string(int status);
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device; *code receives 0 or the VAE_E* status a kernel recorded. */

@@ -32,7 +32,7 @@ def test_header_declares_the_five_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     import diffusion_vae_decoder_gb300 as pkg
     names = pkg.header_symbols()
-    assert len(names) >= 17
+    assert len(names) >= 20
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
     out = subprocess.run(["nm", "-D", "--defined-only", pkg.LIB_PATH], capture_output=True,
@@ -54,7 +54,8 @@ PROBE = r"""
 #define O(T, f) printf(#T "." #f " %zu\n", offsetof(T, f));
 int main(void) {
   P(vae_conv_ref) P(vae_norm_ref) P(vae_resnet_ref) P(vae_attn_ref) P(vae_up_ref)
-  P(vae_chain_args)
+  P(vae_chain_args) P(vae_prof_record)
+  O(vae_prof_record, flops) O(vae_prof_record, ms)
   O(vae_conv_ref, k) O(vae_resnet_ref, shortcut) O(vae_attn_ref, out)
   O(vae_up_ref, resnets) O(vae_up_ref, upsample_conv)
   O(vae_chain_args, eps) O(vae_chain_args, conv_in) O(vae_chain_args, mid_attn)
@@ -75,7 +76,8 @@ def test_ctypes_struct_layout_matches_c(tmp_path):
         [str(exe)], capture_output=True, text=True, check=True).stdout.splitlines())
     m = {"vae_conv_ref": pkg.ConvRef, "vae_norm_ref": pkg.NormRef,
          "vae_resnet_ref": pkg.ResnetRef, "vae_attn_ref": pkg.AttnRef,
-         "vae_up_ref": pkg.UpRef, "vae_chain_args": pkg.ChainArgs}
+         "vae_up_ref": pkg.UpRef, "vae_chain_args": pkg.ChainArgs,
+         "vae_prof_record": pkg.ProfRecord}
     for key, val in got.items():
         if "." in key:
             t, f = key.split(".")
@@ -105,6 +107,8 @@ def test_argument_checks_reject_before_any_launch(lib):
     assert lib.vae_chain_destroy(None) == -5
     assert lib.vae_chain_workspace_size(None, 1, 8, 8) == 0
     assert lib.vae_chain_prepare(None, None, None) == -1
+    assert lib.vae_chain_profile(None, 1) == -5
+    assert lib.vae_kernel_launch_count() == 0
     assert lib.vae_groupnorm_silu(fake, 1, 32, 64, 3, 32, 1e-6, fake, fake, 1, fake, fake,
                                   1 << 20, None) == -1
     assert lib.vae_mid_attn(fake, 1, 48, 4, 4, 0, 16, 1e-6, *([fake] * 11), fake, 1 << 20,
