@@ -1,0 +1,423 @@
+"""Throughput of the FLUX-class VAE decoder on GB300: decode Mpix/s.
+
+One step = one full decode (de-normalise, conv_in, mid block, up blocks,
+norm_out, conv_out) of a seeded synthetic latent with random-init weights, the
+whole chain running in this repository's sm_103a kernels.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decoder_1024]
+  python bench.py --impl reference ...   # the float64 CPU oracle on host cores
+
+Multi-GPU (torchrun): every rank decodes its own latent (independent images,
+no exchange between ranks: "replicas", weak scaling); the timed region is
+bracketed by barriers and the max time over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import vae_synth as S  # noqa: E402
+
+WORKLOADS = {
+    "decoder_1024": dict(latent=(1, 16, 128, 128), seed=S.seed_of("decoder_1024"),
+                         text="FLUX-class AutoencoderKL decoder, latent [1,16,128,128] -> RGB "
+                              "[1,3,1024,1024], random init"),
+    "decoder_256": dict(latent=(1, 16, 32, 32), seed=S.seed_of("decoder_256"),
+                        text="FLUX-class AutoencoderKL decoder, latent [1,16,32,32] -> RGB "
+                             "[1,3,256,256], random init"),
+    "decoder_512_b4": dict(latent=(4, 16, 64, 64), seed=S.seed_of("decoder_512_b4"),
+                           text="FLUX-class AutoencoderKL decoder, latent [4,16,64,64] -> RGB "
+                                "[4,3,512,512], random init"),
+}
+METRIC = "VAE decode Mpix/s"
+# Nominal dense tensor rates (PFLOP/s): TF32 1.1 vs BF16 2.25; the TF32 peak is
+# the measured BF16 peak scaled by this ratio.
+TF32_OVER_BF16 = 1.1 / 2.25
+FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+
+
+def out_pixels(latent):
+    n, _, h, w = latent
+    return n * 8 * h * 8 * w
+
+
+# ---------------------------------------------------------------- distributed helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def rank_seed(seed, rank):
+    """Each rank decodes a different latent (independent images)."""
+    return seed + 7919 * rank
+
+
+def reduce_max(value, dist=None):
+    """Max of a float over all ranks (identity without a process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist=None):
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- peaks / clocks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def time_oracle_decode(latent, seed, repeats=1):
+    """Float64 CPU oracle decode of one latent; returns (seconds per decode, Mpix)."""
+    import oracle
+    w = S.make_decoder_weights("flux", seed)
+    z = S.make_latent(latent, seed)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
+    dt = (time.perf_counter() - t0) / repeats
+    return dt, out_pixels(latent) / 1e6
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = WORKLOADS[args.workload]
+    sample = (1, 16, 16, 16)
+    for _ in range(args.warmup):
+        time_oracle_decode(sample, wl["seed"])
+    total = 0.0
+    for _ in range(args.steps):
+        dt, mpix = time_oracle_decode(sample, wl["seed"])
+        total += dt
+    value = args.steps * mpix / total
+    cores = host_cores()
+    desc = ("float64 numpy oracle (per-tap BLAS matmuls) decoding latent [1,16,16,16] -> "
+            "128x128 with the same architecture, one decode per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Mpix/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "text": wl["text"], "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "Mpix/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "Mpix/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    import diffusion_vae_decoder_gb300 as pkg
+
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = WORKLOADS[args.workload]
+    latent = wl["latent"]
+    seed = rank_seed(wl["seed"], rank)
+
+    weights = S.make_decoder_weights("flux", wl["seed"])
+    chain = pkg.VaeChain(weights, n_up_blocks=4)
+    z_host = torch.from_numpy(S.make_latent(latent, seed)).pin_memory()
+    z = z_host.to(dev)
+    n, _, h, w = latent
+    out = torch.empty((n, 3, 8 * h, 8 * w), dtype=torch.float32, device=dev)
+    ws = torch.empty(chain.workspace_size(n, h, w), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        chain.decode(z, out=out, ws=ws)
+    torch.cuda.synchronize()
+    assert pkg.vae_device_error() == 0
+
+    # ---- device-resident timed region (profiled per step)
+    chain.profile(True)
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v for v in vis.split(",") if v.strip()]
+        if local < len(ids) and ids[local].strip().isdigit():
+            gpu_index = int(ids[local])
+    sampler = ClockSampler(gpu_index)
+    launches0 = pkg.vae_kernel_launch_count()
+    with sampler:
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            chain.decode(z, out=out, ws=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    launches = pkg.vae_kernel_launch_count() - launches0
+    ms = e0.elapsed_time(e1) / args.steps
+    recs = chain.profile_read()
+    chain.profile(False)
+    assert pkg.vae_device_error() == 0
+    ms_max = reduce_max(ms, dist)
+    mpix = out_pixels(latent) / 1e6
+    value = world * mpix / (ms_max / 1e3)
+
+    # ---- roofline of the dominant kernel (the implicit-GEMM conv) and of GroupNorm
+    peaks, peak_src = load_peaks()
+    tf32_peak = peaks["bf16_tflops_sustained"] * TF32_OVER_BF16
+    conv = [r for r in recs if r["kind"] in ("conv3x3", "upsample_conv")]
+    gn = [r for r in recs if r["kind"] == "groupnorm"]
+    conv_ms = sum(r["ms"] for r in conv)
+    conv_tflops = sum(r["flops"] for r in conv) / (conv_ms / 1e3) / 1e12
+    gn_ms = sum(r["ms"] for r in gn)
+    gn_gbs = sum(r["bytes"] for r in gn) / (gn_ms / 1e3) / 1e9
+    step_ms_sum = sum(r["ms"] for r in recs) / args.steps
+    by_kind = {}
+    for r in recs:
+        k = by_kind.setdefault(r["kind"], dict(ms=0.0, flops=0.0, bytes=0.0, steps=0))
+        k["ms"] += r["ms"] / args.steps
+        k["flops"] += r["flops"] / args.steps
+        k["bytes"] += r["bytes"] / args.steps
+        k["steps"] += 1
+    for k in by_kind.values():
+        k["steps"] //= args.steps
+
+    # ---- end to end through the public API, host buffers, copies inside
+    h2d = z_host.numel() * 4
+    out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    d2h = out_host.numel() * 4
+    barrier(dist)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        zd = z_host.to(dev, non_blocking=True)
+        rgb = chain.decode(zd, out=out, ws=ws)
+        out_host.copy_(rgb, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3 / args.steps, dist)
+    barrier(dist)
+    e2e_value = world * mpix / (e2e_ms / 1e3)
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            sample = (1, 16, 32, 32)
+            dt, smpix = time_oracle_decode(sample, wl["seed"])
+            cpu = {"value": smpix / dt, "unit": "Mpix/s", "cores": host_cores(), "kind": "oracle",
+                   "sample": "float64 numpy oracle decoding one latent [1,16,32,32] -> 256x256 "
+                             f"with the same architecture ({dt:.1f} s)"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "Mpix/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "tf32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "text": wl["text"],
+                       "latent": list(latent), "global_batch": latent[0] * world,
+                       "parallelism": f"replicas{world}",
+                       "l2": "no flush: every step streams several GB of activations, far "
+                             "beyond the 129 MB L2"},
+            "roofline": {"bound": "tensor", "kernel": "igemm_kernel (3x3 / upsample conv)",
+                         "achieved": conv_tflops, "peak": tf32_peak, "unit": "TFLOP/s",
+                         "frac": conv_tflops / tf32_peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 sustained x {TF32_OVER_BF16:.4f} "
+                                        "(nominal TF32/BF16 dense ratio)",
+                         "share_of_step": conv_ms / args.steps / ms},
+            "roofline_groupnorm": {"bound": "hbm", "achieved": gn_gbs, "peak": peaks["hbm_gbs"],
+                                   "unit": "GB/s", "frac": gn_gbs / peaks["hbm_gbs"],
+                                   "bytes_per_element": 12},
+            "steps_by_kind": by_kind, "profiled_ms_per_step": step_ms_sum,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "Mpix/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": int(launches),
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    chain.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_op(args):
+    """One op of the single-op sweep (batch 1, NHWC, the chain's internal layout;
+    inputs N(0,1), weights N(0, 1/(Cin*9))), timed with CUDA events."""
+    import torch
+
+    import diffusion_vae_decoder_gb300 as pkg
+
+    torch.cuda.set_device(0)
+    c, hw = args.c, args.hw
+    x = torch.from_numpy(S.make_normal((1, hw, hw, c), 31)).cuda()
+    wt, b = S.make_conv_params(c, c, 3, 32)
+    wt, b = torch.from_numpy(wt).cuda(), torch.from_numpy(b).cuda()
+    g, be = (torch.from_numpy(a).cuda() for a in S.make_norm_params(c, 33))
+    if args.op == "conv":
+        out = torch.empty_like(x)
+        fn = lambda: pkg.vae_conv2d(x, wt, b, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
+        work, unit = 2.0 * c * c * 9 * hw * hw, "TFLOP/s"
+    elif args.op == "upsample_conv":
+        out = torch.empty((1, 2 * hw, 2 * hw, c), device="cuda")
+        fn = lambda: pkg.vae_upsample_conv(x, wt, b, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
+        work, unit = 2.0 * c * c * 9 * 4 * hw * hw, "TFLOP/s"
+    else:
+        out = torch.empty_like(x)
+        fn = lambda: pkg.vae_groupnorm_silu(x, g, be, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
+        work, unit = 12.0 * c * hw * hw, "GB/s"
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()  # evict L2 between timed iterations
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert pkg.vae_device_error() == 0
+    ms = statistics.median(times)
+    rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    peaks, src = load_peaks()
+    peak = (peaks["bf16_tflops"] * TF32_OVER_BF16 if unit == "TFLOP/s" else peaks["hbm_gbs"])
+    print(json.dumps({"op": args.op, "c": c, "hw": hw, "layout": "NHWC", "ms_median": ms,
+                      "ms_min": min(times), "rate": rate, "unit": unit, "peak": peak,
+                      "frac": rate / peak, "peak_source": src + " burst",
+                      "l2": "flushed between iterations"}), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decoder_1024")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["conv", "upsample_conv", "groupnorm"], default=None,
+                    help="time one op of the single-op sweep instead of the decoder")
+    ap.add_argument("--c", type=int, default=128)
+    ap.add_argument("--hw", type=int, default=512)
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    if args.op:
+        return run_op(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
