@@ -83,6 +83,7 @@ _SIGS = {
     "vae_upsample_conv": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _SZ, _P]),
     "vae_groupnorm_silu_workspace_size": (_SZ, [_I, _I, _LL, _I, _I]),
     "vae_groupnorm_silu": (_I, [_P, _I, _I, _LL, _I, _I, _F, _P, _P, _I, _P, _P, _SZ, _P]),
+    "vae_groupnorm_silu_noalloc": (_I, [_P, _I, _I, _LL, _I, _I, _F, _P, _P, _I, _P, _P]),
     "vae_mid_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "vae_mid_attn": (_I, [_P, _I, _I, _I, _I, _I, _I, _F] + [_P] * 11 + [_P, _SZ, _P]),
     "vae_conv3d_causal_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
@@ -224,6 +225,24 @@ def vae_groupnorm_silu(x, gamma, beta, groups=32, eps=1e-6, apply_silu=True, lay
     _check("vae_groupnorm_silu", lib.vae_groupnorm_silu(
         _ptr(x), n, c, spatial, layout, groups, eps, _ptr(gamma), _ptr(beta), int(apply_silu),
         _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def vae_groupnorm_silu_noalloc(x, gamma, beta, groups=32, eps=1e-6, apply_silu=True,
+                               layout=VAE_NCHW, out=None, stream=None):
+    """GroupNorm(+SiLU) whose scratch is a fixed array inside the library (no
+    workspace); for callers that must not allocate device memory."""
+    lib = load_library()
+    _need(x, "x"), _need(gamma, "gamma"), _need(beta, "beta")
+    n = x.shape[0]
+    c = x.shape[1] if layout == VAE_NCHW else x.shape[-1]
+    spatial = x.numel() // (n * c)
+    if out is None:
+        import torch
+        out = torch.empty_like(x)
+    _check("vae_groupnorm_silu_noalloc", lib.vae_groupnorm_silu_noalloc(
+        _ptr(x), n, c, spatial, layout, groups, eps, _ptr(gamma), _ptr(beta), int(apply_silu),
+        _ptr(out), _stream(stream)))
     return out
 
 

@@ -109,6 +109,27 @@ VAE_API int vae_groupnorm_silu(const float *x, int n, int c, long long spatial, 
                        float eps, const float *gamma, const float *beta, int apply_silu,
                        float *y, void *ws, size_t ws_bytes, vae_stream_t stream);
 
+/* vae_groupnorm_silu_noalloc -- the same GroupNorm(+SiLU) for callers that
+ * must not allocate device memory, not even a workspace: e.g. a plug-in inside
+ * a host application that owns the whole device-memory budget and forbids
+ * libraries to allocate, or a latency-critical loop that cannot take the cost
+ * (and possible implicit device synchronisation) of cudaMalloc. The pages
+ * have no counterpart; this is a deployment convenience.
+ * Arguments and results are those of vae_groupnorm_silu without ws/ws_bytes.
+ * Its statistics scratch is one fixed 4 MiB array compiled into the library
+ * (held in the global memory of every GPU that loads the library until the
+ * process exits): enough for up to 10 samples at 32 groups; larger requests
+ * return VAE_EUNSUPPORTED before anything is launched. The first call on a
+ * device looks up the array's device address for that device (make that
+ * first call before any stream capture). All calls share the array, so calls
+ * that overlap on the GPU (e.g. on two streams at once) race; calls on one
+ * stream are ordered and safe. No part of the array needs clearing between
+ * calls. Allocates nothing. */
+VAE_API int vae_groupnorm_silu_noalloc(const float *x, int n, int c, long long spatial, int layout,
+                                       int groups, float eps, const float *gamma,
+                                       const float *beta, int apply_silu, float *y,
+                                       vae_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * vae_mid_attn -- mid-block single-head spatial attention (cortiq-engine
  * "Module vae", struct VaeAttnRef): t = GroupNorm(x); tokens p = i*w + j;
