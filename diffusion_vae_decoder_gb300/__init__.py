@@ -88,6 +88,10 @@ _SIGS = {
     "vae_mid_attn": (_I, [_P, _I, _I, _I, _I, _I, _I, _F] + [_P] * 11 + [_P, _SZ, _P]),
     "vae_conv3d_causal_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "vae_conv3d_causal": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _SZ, _P]),
+    "vae_causal_stack_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "vae_causal_stack": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_P),
+                              ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _F,
+                              _P, _P, _SZ, _P]),
     "vae_chain_prepare": (_I, [ctypes.POINTER(ChainArgs), ctypes.POINTER(_P), _P]),
     "vae_chain_workspace_size": (_SZ, [_P, _I, _I, _I]),
     "vae_decode_chain": (_I, [_P, _P, _I, _I, _I, _P, _P, _SZ, _P]),
@@ -291,6 +295,26 @@ def vae_conv3d_causal(x, weight, bias=None, residual=None, layout=VAE_NCHW, out=
 
 def vae_kernel_launch_count():
     return load_library().vae_kernel_launch_count()
+
+
+def vae_causal_stack(x, layers, groups=32, eps=1e-6, layout=VAE_NCHW, out=None, stream=None):
+    """``layers``: list of dicts with weight [c,c,3,3,3], bias, gn_weight, gn_bias (CUDA)."""
+    lib = load_library()
+    _need(x, "x")
+    if layout == VAE_NCHW:
+        n, c, t, h, w = x.shape
+    else:
+        n, t, h, w, c = x.shape
+    L = len(layers)
+    arr = lambda key: (_P * L)(*[_need(d[key], key).data_ptr() for d in layers])  # noqa: E731
+    if out is None:
+        import torch
+        out = torch.empty_like(x)
+    ws = _ws(lib.vae_causal_stack_workspace_size(n, c, t, h, w, layout, L), x.device)
+    _check("vae_causal_stack", lib.vae_causal_stack(
+        _ptr(x), n, c, t, h, w, layout, L, arr("weight"), arr("bias"), arr("gn_weight"),
+        arr("gn_bias"), groups, eps, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
 
 
 def vae_device_error(stream=None):

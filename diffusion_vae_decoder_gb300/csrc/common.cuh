@@ -116,7 +116,7 @@ int add_bias(float *dst, const float *a, const float *b, int n, cudaStream_t s);
 size_t groupnorm_ws_bytes(int n, int c, long long spatial, int groups);
 int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, int groups,
                    float eps, const float *gamma, const float *beta, int silu, int round_out,
-                   float *y, void *ws, cudaStream_t s);
+                   float *y, void *ws, cudaStream_t s, const float *residual = nullptr);
 
 // Row softmax in place: s[r][:L] <- softmax(scale * s[r][:L]), TF32-rounded.
 int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st);

@@ -177,15 +177,17 @@ __global__ void gn_finalize(const double *__restrict__ part, int nblk, int c, in
   }
 }
 
-__device__ __forceinline__ float finish(float v, int silu, int round) {
-  if (silu) v = v / (1.0f + expf(-v));
-  return round ? round_tf32(v) : v;
+__device__ __forceinline__ float act(float v, int silu) {
+  return silu ? v / (1.0f + expf(-v)) : v;
 }
 
+__device__ __forceinline__ float rnd(float v, int round) { return round ? round_tf32(v) : v; }
+
+// y = [silu](x * scale + shift) (+ res), optionally TF32-rounded.
 __global__ void gn_apply_nhwc(const float *__restrict__ x, long long total4, int c,
                               long long per_sample, const float *__restrict__ scale,
                               const float *__restrict__ shift, int silu, int round,
-                              float *__restrict__ y) {
+                              const float *__restrict__ res, float *__restrict__ y) {
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total4;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long e = 4 * i;
@@ -195,10 +197,21 @@ __global__ void gn_apply_nhwc(const float *__restrict__ x, long long total4, int
     const float4 a = *reinterpret_cast<const float4 *>(scale + n * c + ch);
     const float4 b = *reinterpret_cast<const float4 *>(shift + n * c + ch);
     float4 o;
-    o.x = finish(fmaf(v.x, a.x, b.x), silu, round);
-    o.y = finish(fmaf(v.y, a.y, b.y), silu, round);
-    o.z = finish(fmaf(v.z, a.z, b.z), silu, round);
-    o.w = finish(fmaf(v.w, a.w, b.w), silu, round);
+    o.x = act(fmaf(v.x, a.x, b.x), silu);
+    o.y = act(fmaf(v.y, a.y, b.y), silu);
+    o.z = act(fmaf(v.z, a.z, b.z), silu);
+    o.w = act(fmaf(v.w, a.w, b.w), silu);
+    if (res) {
+      const float4 r = reinterpret_cast<const float4 *>(res)[i];
+      o.x += r.x;
+      o.y += r.y;
+      o.z += r.z;
+      o.w += r.w;
+    }
+    o.x = rnd(o.x, round);
+    o.y = rnd(o.y, round);
+    o.z = rnd(o.z, round);
+    o.w = rnd(o.w, round);
     reinterpret_cast<float4 *>(y)[i] = o;
   }
 }
@@ -210,7 +223,7 @@ __global__ void gn_apply_nchw(const float *__restrict__ x, long long total, int 
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long nc = i / spatial;  // n * c + ch
-    y[i] = finish(fmaf(x[i], scale[nc], shift[nc]), silu, round);
+    y[i] = rnd(act(fmaf(x[i], scale[nc], shift[nc]), silu), round);
   }
 }
 
@@ -235,11 +248,14 @@ size_t groupnorm_ws_bytes(int n, int c, long long spatial, int groups) {
 
 int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, int groups,
                    float eps, const float *gamma, const float *beta, int silu, int round_out,
-                   float *y, void *ws, cudaStream_t s) {
+                   float *y, void *ws, cudaStream_t s, const float *residual) {
   if (!x || !y || !gamma || !beta || !ws || n <= 0 || c <= 0 || spatial <= 0 || groups <= 0)
     return VAE_EINVAL;
   if (c % groups || c % 4 || c > 1024) return VAE_EUNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) return VAE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
+       reinterpret_cast<uintptr_t>(residual)) & 15)
+    return VAE_EINVAL;
+  if (residual && !nhwc) return VAE_EUNSUPPORTED;
   Carver cv(ws, ~size_t(0));
   double *part = cv.take<double>(static_cast<size_t>(n) * groups * kMaxBlocksPerGroupSeg * 3);
   float *scale = cv.take<float>(static_cast<size_t>(n) * c);
@@ -265,7 +281,8 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
     const long long total4 = total / 4;
     const long long g = std::min<long long>((total4 + threads - 1) / threads, 8ll * num_sms());
     gn_apply_nhwc<<<static_cast<int>(g), threads, 0, s>>>(x, total4, c, spatial * c, scale,
-                                                          shift, silu, round_out, y);
+                                                          shift, silu, round_out, residual,
+                                                          y);
   } else {
     const long long g = std::min<long long>((total + threads - 1) / threads, 8ll * num_sms());
     gn_apply_nchw<<<static_cast<int>(g), threads, 0, s>>>(x, total, c, spatial, scale, shift,

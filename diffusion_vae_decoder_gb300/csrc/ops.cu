@@ -4,6 +4,7 @@
 // layout the tensor-core kernel reads, packs its weights (TF32-rounded) into
 // the caller's workspace, and enqueues kernels on the caller's stream.
 #include <cmath>
+#include <vector>
 
 #include "common.cuh"
 #include "ops.cuh"
@@ -89,6 +90,24 @@ AttnWs carve_attn(Carver &cv, int n, int c, int L, int layout) {
   w.o = cv.take<float>(nl * c);
   w.y = layout == VAE_NCHW ? cv.take<float>(nl * c) : nullptr;
   w.gn = cv.take<char>(groupnorm_ws_bytes(n, c, L, c));  // groups <= c
+  return w;
+}
+
+// ---------------------------------------------------------------- causal stack
+struct StackWs {
+  float *packed, *xs, *ring[3], *h;
+  void *gn;
+};
+
+StackWs carve_stack(Carver &cv, int n, int c, long long vox, int layout, int n_layers,
+                    int groups) {
+  StackWs w{};
+  const size_t act = static_cast<size_t>(n) * vox * c;
+  w.packed = cv.take<float>(static_cast<size_t>(n_layers) * c * packed_ldb(c, 27, 0));
+  w.xs = layout == VAE_NCHW ? cv.take<float>(act) : nullptr;
+  for (int i = 0; i < 3; ++i) w.ring[i] = cv.take<float>(act);
+  w.h = cv.take<float>(act);
+  w.gn = cv.take<char>(groupnorm_ws_bytes(n, c, vox, groups));
   return w;
 }
 
@@ -412,6 +431,82 @@ int vae_conv3d_causal(const float *x, int n, int cin, int t, int h, int w, int l
   d.bias = bias;
   d.residual = residual;
   return igemm_launch(d, s);
+}
+
+// ------------------------------------------------------------------ 3-D causal stack
+size_t vae_causal_stack_workspace_size(int n, int c, int t, int h, int w, int layout,
+                                       int n_layers) {
+  if (n <= 0 || c <= 0 || t <= 0 || h <= 0 || w <= 0 || n_layers <= 0) return 0;
+  Carver cv(nullptr, 0);
+  carve_stack(cv, n, c, static_cast<long long>(t) * h * w, layout, n_layers, c);
+  return cv.used;
+}
+
+int vae_causal_stack(const float *x, int n, int c, int t, int h, int w, int layout,
+                     int n_layers, const float *const *weight, const float *const *bias,
+                     const float *const *gn_w, const float *const *gn_b, int groups, float eps,
+                     float *y, void *ws, size_t ws_bytes, vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !y || !ws || !weight || !bias || !gn_w || !gn_b || n <= 0 || c <= 0 || t <= 0 ||
+      h <= 0 || w <= 0 || groups <= 0 || n_layers <= 0)
+    return VAE_EINVAL;
+  if (layout != VAE_NCHW && layout != VAE_NHWC) return VAE_EINVAL;
+  if (n_layers > 64 || c % 32 || c % groups || c > 1024 || h > 65535 || w > 65535 ||
+      static_cast<long long>(n) * t > 65535)
+    return VAE_EUNSUPPORTED;
+  for (int i = 0; i < n_layers; ++i)
+    if (!weight[i] || !gn_w[i] || !gn_b[i]) return VAE_EINVAL;
+  if (!aligned16(x) || !aligned16(y) || x == y) return VAE_EINVAL;
+  const long long vox = static_cast<long long>(t) * h * w;
+  Carver cv(ws, ws_bytes);
+  // groups <= c, so carving with c groups is an upper bound
+  StackWs sw = carve_stack(cv, n, c, vox, layout, n_layers, c);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  const int ldb = packed_ldb(c, 27, 0);
+  for (int i = 0; i < n_layers; ++i)
+    VAE_TRY(pack_conv_weights(weight[i], c, c, 27, nullptr, 0,
+                              sw.packed + static_cast<size_t>(i) * c * ldb, c, ldb, s));
+  const float *u0 = nullptr;
+  VAE_TRY(stage_nhwc(x, n, c, vox, layout, sw.xs, c, 1.f, 0.f, 0, &u0, s));
+  std::vector<const float *> u(n_layers + 1);
+  u[0] = u0;
+  for (int i = 1; i <= n_layers; ++i) {
+    IgemmDesc d;
+    d.mode = AMode::Conv;
+    d.a = u[i - 1];
+    d.imgs = n * t;
+    d.t = t;
+    d.hin = h;
+    d.win = w;
+    d.a_c = c;
+    d.k = 3;
+    d.kt = 3;
+    d.b = sw.packed + static_cast<size_t>(i - 1) * c * ldb;
+    d.ldb = ldb;
+    d.cout = c;
+    d.out = sw.h;
+    d.ldo = c;
+    d.bias = bias[i - 1];
+    VAE_TRY(igemm_launch(d, s));
+    // u_i goes to a ring buffer holding neither u_{i-1} nor u_{i-2}; the last
+    // layer writes the caller's y directly when y is NDHWC.
+    float *dst = nullptr;
+    if (i == n_layers && layout == VAE_NHWC) {
+      dst = y;
+    } else {
+      for (float *cand : sw.ring)
+        if (cand != u[i - 1] && (i < 2 || cand != u[i - 2])) {
+          dst = cand;
+          break;
+        }
+    }
+    const float *res = (i % 2 == 0) ? u[i - 2] : nullptr;
+    VAE_TRY(groupnorm_silu(sw.h, n, c, vox, 1, groups, eps, gn_w[i - 1], gn_b[i - 1], 1,
+                           i < n_layers ? 1 : 0, dst, sw.gn, s, res));
+    u[i] = dst;
+  }
+  if (layout == VAE_NCHW) VAE_TRY(unstage_nchw(u[n_layers], n, c, vox, y, s));
+  return VAE_OK;
 }
 
 }  // extern "C"

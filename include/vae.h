@@ -162,6 +162,25 @@ VAE_API int vae_conv3d_causal(const float *x, int n, int cin, int t, int h, int 
                       float *y, void *ws, size_t ws_bytes, vae_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * vae_causal_stack -- the LTX-style 3-D causal conv slice ("VAE decode -> GPU
+ * handoff (FLUX/LTX render services)", "The CPU VAE code": a 3-D causal conv
+ * stack with causal padding on the time axis): for i = 1..n_layers
+ *   u_i = silu(GroupNorm_i(conv3d_causal_i(u_{i-1})))   (+ u_{i-2} when i is even)
+ * with u_0 = x and y = u_{n_layers}; "residual every 2 convs" is read as adding
+ * the input of each pair of layers to the pair's output.
+ *   x, y [n,c,t,h,w] (NCDHW or NDHWC; y must not alias x)
+ *   weight, bias, gn_w, gn_b: HOST arrays of n_layers DEVICE pointers to
+ *   [c,c,3,3,3], [c], [c], [c]
+ * Limits: c % 32 == 0, c % groups == 0, c <= 1024, 1 <= n_layers <= 64.
+ */
+VAE_API size_t vae_causal_stack_workspace_size(int n, int c, int t, int h, int w, int layout,
+                                               int n_layers);
+VAE_API int vae_causal_stack(const float *x, int n, int c, int t, int h, int w, int layout,
+                             int n_layers, const float *const *weight, const float *const *bias,
+                             const float *const *gn_w, const float *const *gn_b, int groups,
+                             float eps, float *y, void *ws, size_t ws_bytes, vae_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The whole decoder (cortiq-engine "Module vae", structs VaeChainArgs and
  * VaeDecoder), in execution order: z/scaling_factor + shift_factor ->
  * conv_in -> mid_res1 -> mid_attn -> mid_res2 -> ups[0..n_ups) ->
