@@ -61,6 +61,8 @@ struct KParams {
   const float *residual;
   float alpha;
   int round_out;
+  int epi_tma;  // 1: rows leave through shared staging + TMA stores (NHWC / GEMM)
+  int has_res;  // residual present (TMA-loaded into the staging buffer when epi_tma)
   int *err;
 };
 
@@ -70,8 +72,10 @@ struct Cfg {
   static constexpr uint32_t B_BYTES = BN * 128;
   static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
-  static constexpr size_t SMEM =
-      1024 + STAGES * (kABytes + B_BYTES) + (2 * STAGES + 5) * sizeof(uint64_t) + 16;
+  // Epilogue staging: 4 warps x 2 buffers x (32 rows x 128 bytes).
+  static constexpr uint32_t STAGING = 4 * 2 * 4096;
+  static constexpr size_t SMEM = 1024 + STAGES * (kABytes + B_BYTES) + STAGING +
+                                 (2 * STAGES + 9) * sizeof(uint64_t) + 16;
 };
 
 __device__ __forceinline__ void raise_error(const KParams &p, volatile uint32_t *abort) {
@@ -90,7 +94,8 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) 
 template <int BN, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmS, const KParams p) {
+                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmO,
+                 const __grid_constant__ CUtensorMap tmR, const KParams p) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t STAGE_TX = kABytes + C::B_BYTES;
@@ -101,12 +106,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * kABytes;
-  uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_BYTES);
+  float *staging = reinterpret_cast<float *>(sB + STAGES * C::B_BYTES);  // 1024-aligned
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_BYTES + C::STAGING);
   uint64_t *empty = full + STAGES;
   uint64_t *acc_full = empty + STAGES;
   uint64_t *acc_empty = acc_full + 2;
   uint64_t *drain = acc_empty + 2;  // used only after an abort
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *res_bar = drain + 1;    // one per epilogue warp: residual box landed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(res_bar + 4);
   volatile uint32_t *abort = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -122,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[b], 4);
     }
     mbar_init(drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&res_bar[q], 1);
     *abort = 0u;
     fence_mbarrier_init();
   }
@@ -129,6 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (MODE == 0 && p.sc_chunks > 0) prefetch_tmap(&tmS);
+    if (p.epi_tma) {
+      prefetch_tmap(&tmO);
+      if (p.has_res) prefetch_tmap(&tmR);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -259,8 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;
+    float *stg = staging + q * 2 * 1024;  // this warp's two 4 KB staging buffers
+    int sbuf = 0;
+    uint32_t res_phase = 0;
+    bool failed = false;
     int local = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++local) {
+    for (int tile = blockIdx.x; tile < p.total_tiles && !failed;
+         tile += gridDim.x, ++local) {
       const int buf = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       bool ok = mbar_wait(&acc_full[buf], aph, abort);
@@ -274,12 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = tile / p.n_tiles;
       const int n0 = (tile % p.n_tiles) * BN;
       bool valid;
-      long long row;     // NHWC / GEMM row index
-      long long nchw0 = 0;  // NCHW: offset of channel 0 for this pixel
-      long long cstride = 0;
+      long long row;          // NHWC / GEMM row index
+      long long nchw0 = 0;    // NCHW: offset of channel 0 for this pixel
+      long long cstride = 0;  // NCHW: distance between channels
+      int bc1 = 0, bc2 = 0, bc3 = 0, bc4 = 0;  // this warp's TMA box coordinates
       if (MODE == 2) {
         row = static_cast<long long>(mt) * kBM + m;
         valid = row < p.M;
+        bc1 = mt * kBM + q * 32;
       } else {
         const int per_img = p.tiles_x * p.tiles_y;
         const int img = mt / per_img;
@@ -290,12 +309,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           y = ty * p.bh + m / p.bw;
           x = tx * p.bw + m % p.bw;
           valid = y < p.hout && x < p.wout;
+          bc1 = tx * p.bw + (q * 32) % p.bw;
+          bc2 = ty * p.bh + (q * 32) / p.bw;
+          bc3 = img;
         } else {
           const int ph = m >> 5, r = m & 31;
           const int yl = ty * p.bh + r / p.bw, xl = tx * p.bw + r % p.bw;
           y = 2 * yl + (ph >> 1);
           x = 2 * xl + (ph & 1);
           valid = yl < p.hin && xl < p.win;
+          bc1 = q & 1;  // px of this warp's parity block
+          bc2 = tx * p.bw;
+          bc3 = q >> 1;  // py
+          bc4 = img * p.hin + ty * p.bh;
         }
         row = (static_cast<long long>(img) * p.hout + y) * p.wout + x;
         const long long hw = static_cast<long long>(p.hout) * p.wout;
@@ -316,14 +342,86 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           tmem_ld_16cols(taddr, v);
         const int col0 = n0 + c * C::CH;
-        if (col0 >= p.cout || !valid) continue;
+        if (col0 >= p.cout) continue;  // warp-uniform
         const int ncols = min(C::CH, p.cout - col0);
+        // bias + scale (vector loads when the whole chunk is in range)
+        if (!p.bias_per_row && p.bias && ncols == C::CH) {
 #pragma unroll
-        for (int i = 0; i < C::CH; ++i) {
-          float b = rbias;
-          if (!p.bias_per_row && p.bias && i < ncols) b = __ldg(p.bias + col0 + i);
-          v[i] = fmaf(v[i], p.alpha, b);
+          for (int i = 0; i < C::CH; i += 4) {
+            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(p.bias + col0 + i));
+            v[i] = fmaf(v[i], p.alpha, b4.x);
+            v[i + 1] = fmaf(v[i + 1], p.alpha, b4.y);
+            v[i + 2] = fmaf(v[i + 2], p.alpha, b4.z);
+            v[i + 3] = fmaf(v[i + 3], p.alpha, b4.w);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < C::CH; ++i) {
+            float b = rbias;
+            if (!p.bias_per_row && p.bias && i < ncols) b = __ldg(p.bias + col0 + i);
+            v[i] = fmaf(v[i], p.alpha, b);
+          }
         }
+        if (C::CH == 32 && p.epi_tma) {
+          // Stage the warp's 32 x 32 block in the 128-byte-swizzled layout the
+          // TMA store reads (row r, 16-byte chunk j at j ^ (r % 8)); rows and
+          // channels outside the tensor are clipped by the store.
+          float *sb = stg + sbuf * 1024;
+          if (lane == 0) bulk_wait_read<1>();  // the store that used sb last is done
+          __syncwarp();
+          if (p.has_res) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&res_bar[q], 4096);
+              if (MODE == 2)
+                tma_load_2d(sb, &tmR, &res_bar[q], col0, bc1);
+              else if (MODE == 0)
+                tma_load_4d(sb, &tmR, &res_bar[q], col0, bc1, bc2, bc3);
+              else
+                tma_load_5d(sb, &tmR, &res_bar[q], col0, bc1, bc2, bc3, bc4);
+            }
+            bool rok = mbar_wait(&res_bar[q], res_phase, abort);
+            rok = __all_sync(0xffffffffu, rok);
+            res_phase ^= 1u;
+            if (!rok) {
+              if (lane == 0) raise_error(p, abort);
+              failed = true;
+              break;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4 *slot = reinterpret_cast<float4 *>(sb + lane * 32 + ((j ^ (lane & 7)) * 4));
+            float4 val = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            if (p.has_res) {
+              const float4 rv = *slot;
+              val.x += rv.x;
+              val.y += rv.y;
+              val.z += rv.z;
+              val.w += rv.w;
+            }
+            if (p.round_out) {
+              val.x = round_tf32(val.x);
+              val.y = round_tf32(val.y);
+              val.z = round_tf32(val.z);
+              val.w = round_tf32(val.w);
+            }
+            *slot = val;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (MODE == 2)
+              tma_store_2d(&tmO, sb, col0, bc1);
+            else if (MODE == 0)
+              tma_store_4d(&tmO, sb, col0, bc1, bc2, bc3);
+            else
+              tma_store_5d(&tmO, sb, col0, bc1, bc2, bc3, bc4);
+            bulk_commit();
+          }
+          sbuf ^= 1;
+          continue;
+        }
+        if (!valid) continue;
         if (p.out_nchw) {
           float *o = p.out + nchw0 + static_cast<long long>(col0) * cstride;
           const float *r = p.residual ? p.residual + nchw0 + static_cast<long long>(col0) * cstride
@@ -360,19 +458,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<float4 *>(o + i) = val;
             }
           } else {
-            for (int i = 0; i < ncols; ++i) {
-              float val = v[i];
-              if (r) val += r[i];
-              if (p.round_out) val = round_tf32(val);
-              o[i] = val;
+#pragma unroll
+            for (int i = 0; i < C::CH; ++i) {
+              if (i < ncols) {
+                float val = v[i];
+                if (r) val += r[i];
+                if (p.round_out) val = round_tf32(val);
+                o[i] = val;
+              }
             }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (lane == 0 && !failed) mbar_arrive(&acc_empty[buf]);
     }
+    // Every TMA store of this warp must finish reading shared memory (and
+    // land) before the CTA exits.
+    if (lane == 0 && p.epi_tma) bulk_wait_all();
   }
 
   // ------------------------------------------------------------ teardown
@@ -393,7 +497,8 @@ int pow2_at_least(int v) {
 
 template <int BN, int MODE>
 int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ts,
-                 const KParams &kp, cudaStream_t stream) {
+                 const CUtensorMap &to, const CUtensorMap &tr, const KParams &kp,
+                 cudaStream_t stream) {
   using C = Cfg<BN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -404,7 +509,7 @@ int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap
   });
   if (attr_err != cudaSuccess) return VAE_ECUDA;
   const int grid = std::min(kp.total_tiles, num_sms());
-  igemm_kernel<BN, MODE><<<grid, kThreads, C::SMEM, stream>>>(ta, tb, ts, kp);
+  igemm_kernel<BN, MODE><<<grid, kThreads, C::SMEM, stream>>>(ta, tb, ts, to, tr, kp);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(1);
   return VAE_OK;
@@ -412,13 +517,14 @@ int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap
 
 template <int MODE>
 int launch_mode(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ts,
-                const KParams &kp, cudaStream_t s) {
+                const CUtensorMap &to, const CUtensorMap &tr, const KParams &kp,
+                cudaStream_t s) {
   switch (bn) {
-    case 256: return launch_typed<256, MODE>(ta, tb, ts, kp, s);
-    case 128: return launch_typed<128, MODE>(ta, tb, ts, kp, s);
-    case 64: return launch_typed<64, MODE>(ta, tb, ts, kp, s);
-    case 32: return launch_typed<32, MODE>(ta, tb, ts, kp, s);
-    default: return launch_typed<16, MODE>(ta, tb, ts, kp, s);
+    case 256: return launch_typed<256, MODE>(ta, tb, ts, to, tr, kp, s);
+    case 128: return launch_typed<128, MODE>(ta, tb, ts, to, tr, kp, s);
+    case 64: return launch_typed<64, MODE>(ta, tb, ts, to, tr, kp, s);
+    case 32: return launch_typed<32, MODE>(ta, tb, ts, to, tr, kp, s);
+    default: return launch_typed<16, MODE>(ta, tb, ts, to, tr, kp, s);
   }
 }
 
@@ -445,7 +551,9 @@ size_t igemm_smem_bytes(int bn) {
 int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   if (!d.a || !d.b || !d.out || d.cout <= 0) return VAE_EINVAL;
   auto misaligned = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) != 0; };
-  if (misaligned(d.a) || misaligned(d.b) || (d.sc && misaligned(d.sc))) return VAE_EINVAL;
+  if (misaligned(d.a) || misaligned(d.b) || (d.sc && misaligned(d.sc)) ||
+      (d.bias && misaligned(d.bias)))
+    return VAE_EINVAL;
 
   const int bn = pick_bn(d.cout);
   KParams kp{};
@@ -547,10 +655,48 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   if (total <= 0 || total > (1ll << 31) - 1) return VAE_EUNSUPPORTED;
   kp.total_tiles = static_cast<int>(total);
 
+  // Output (and residual) tensor maps for the staged TMA-store epilogue: one
+  // box per epilogue warp = 32 rows x 32 channels.
+  CUtensorMap to = tb, tr = tb;
+  kp.has_res = d.residual != nullptr;
+  auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
+  bool epi = !d.out_nchw && bn >= 32 && !d.bias_per_row && d.ldo % 4 == 0 && al16(d.out) &&
+             (!d.residual || al16(d.residual));
+  if (d.mode == AMode::Upsample && d.imgs > 1 && d.hin % kp.bh) epi = false;  // rows would wrap
+  if (epi) {
+    auto encode_out = [&](CUtensorMap *m, const float *base) -> int {
+      const uint64_t ld4 = static_cast<uint64_t>(d.ldo) * 4;
+      if (d.mode == AMode::Gemm) {
+        const uint64_t dims[2] = {static_cast<uint64_t>(d.cout), static_cast<uint64_t>(d.M)};
+        const uint64_t str[1] = {ld4};
+        const uint32_t box[2] = {32, 32};
+        return encode_tiled(m, base, 2, dims, str, box);
+      }
+      if (d.mode == AMode::Conv) {
+        const uint32_t bw = std::min(kp.bw, 32);
+        const uint64_t dims[4] = {static_cast<uint64_t>(d.cout), static_cast<uint64_t>(kp.wout),
+                                  static_cast<uint64_t>(kp.hout), static_cast<uint64_t>(d.imgs)};
+        const uint64_t str[3] = {ld4, ld4 * kp.wout, ld4 * kp.wout * kp.hout};
+        const uint32_t box[4] = {32, bw, 32 / bw, 1};
+        return encode_tiled(m, base, 4, dims, str, box);
+      }
+      // Upsample: output [imgs*hin][py][win][px][cout], box (32, 1, P, 1, R).
+      const uint64_t dims[5] = {static_cast<uint64_t>(d.cout), 2, static_cast<uint64_t>(d.win),
+                                2, static_cast<uint64_t>(d.imgs) * d.hin};
+      const uint64_t str[4] = {ld4, 2 * ld4, ld4 * kp.wout, 2 * ld4 * kp.wout};
+      const uint32_t box[5] = {32, 1, static_cast<uint32_t>(kp.bw), 1,
+                               static_cast<uint32_t>(kp.bh)};
+      return encode_tiled(m, base, 5, dims, str, box);
+    };
+    VAE_TRY(encode_out(&to, d.out));
+    if (d.residual) VAE_TRY(encode_out(&tr, d.residual));
+  }
+  kp.epi_tma = epi ? 1 : 0;
+
   switch (d.mode) {
-    case AMode::Conv: return launch_mode<0>(bn, ta, tb, ts, kp, stream);
-    case AMode::Upsample: return launch_mode<1>(bn, ta, tb, ts, kp, stream);
-    default: return launch_mode<2>(bn, ta, tb, ts, kp, stream);
+    case AMode::Conv: return launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream);
+    case AMode::Upsample: return launch_mode<1>(bn, ta, tb, ts, to, tr, kp, stream);
+    default: return launch_mode<2>(bn, ta, tb, ts, to, tr, kp, stream);
   }
 }
 
