@@ -66,16 +66,25 @@ struct KParams {
   int *err;
 };
 
-template <int BN>
+// BN: output channels per tile (MMA N). MS: 128-row M sub-tiles per tile
+// sharing each B stage (1, or 2 for 128-channel convs: a 256-pixel tile keeps
+// the operand bytes per FLOP of a 128 x 256 tile).
+template <int BN, int MS>
 struct Cfg {
-  static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr uint32_t A_BYTES = MS * kABytes;
   static constexpr uint32_t B_BYTES = BN * 128;
-  static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   // Epilogue staging: 4 warps x 2 buffers x (32 rows x 128 bytes).
   static constexpr uint32_t STAGING = 4 * 2 * 4096;
-  static constexpr size_t SMEM = 1024 + STAGES * (kABytes + B_BYTES) + STAGING +
+  static constexpr int FIT = (232448 - 1024 - STAGING - 512) / STAGE_BYTES;
+  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
+  static constexpr uint32_t ACC_COLS = BN * MS;  // TMEM columns of one accumulator set
+  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
+  static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
+  static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + STAGING +
                                  (2 * STAGES + 9) * sizeof(uint64_t) + 16;
+  static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ void raise_error(const KParams &p, volatile uint32_t *abort) {
@@ -91,21 +100,21 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) 
   return true;
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, int MS>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmO,
                  const __grid_constant__ CUtensorMap tmR, const KParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, MS>;
   constexpr int STAGES = C::STAGES;
-  constexpr uint32_t STAGE_TX = kABytes + C::B_BYTES;
+  constexpr uint32_t STAGE_TX = C::STAGE_BYTES;
   constexpr uint32_t IDESC = idesc_tf32(kBM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
-  uint8_t *sB = smem + STAGES * kABytes;
+  uint8_t *sB = smem + STAGES * C::A_BYTES;
   float *staging = reinterpret_cast<float *>(sB + STAGES * C::B_BYTES);  // 1024-aligned
   uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_BYTES + C::STAGING);
   uint64_t *empty = full + STAGES;
@@ -175,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             failed = true;
             break;
           }
-          uint8_t *a_dst = sA + stage * kABytes;
+          uint8_t *a_dst = sA + stage * C::A_BYTES;
           uint8_t *b_dst = sB + stage * C::B_BYTES;
           mbar_arrive_expect_tx(&full[stage], STAGE_TX);
           if (MODE == 0) {
@@ -238,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * BN;
+        const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS;
         for (int ks = 0; ks < p.k_stages; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort)) {
             raise_error(p, abort);
@@ -246,11 +255,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + stage * kABytes));
           const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
-          for (int k = 0; k < 4; ++k)  // 4 x K=8 TF32 steps = 32 channels (128 bytes)
-            umma_tf32(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, (ks | k) != 0);
+          for (int sub = 0; sub < MS; ++sub) {
+            const uint64_t ad =
+                sw128_kmajor_desc(smem_u32(sA + stage * C::A_BYTES + sub * kABytes));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // 4 x K=8 TF32 steps = 32 channels (128 bytes)
+              umma_tf32(d_tmem + sub * BN, ad + 2 * k, bd + 2 * k, IDESC, (ks | k) != 0);
+          }
           issued = true;
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -290,13 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int mt = tile / p.n_tiles;
       const int n0 = (tile % p.n_tiles) * BN;
+      for (int sub = 0; sub < MS; ++sub) {
+      const int msub = sub * 128 + m;  // row of the (MS x 128)-row tile
       bool valid;
       long long row;          // NHWC / GEMM row index
       long long nchw0 = 0;    // NCHW: offset of channel 0 for this pixel
       long long cstride = 0;  // NCHW: distance between channels
       int bc1 = 0, bc2 = 0, bc3 = 0, bc4 = 0;  // this warp's TMA box coordinates
       if (MODE == 2) {
-        row = static_cast<long long>(mt) * kBM + m;
+        row = static_cast<long long>(mt) * kBM + msub;
         valid = row < p.M;
         bc1 = mt * kBM + q * 32;
       } else {
@@ -306,11 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ty = rem / p.tiles_x, tx = rem % p.tiles_x;
         int y, x;
         if (MODE == 0) {
-          y = ty * p.bh + m / p.bw;
-          x = tx * p.bw + m % p.bw;
+          y = ty * p.bh + msub / p.bw;
+          x = tx * p.bw + msub % p.bw;
           valid = y < p.hout && x < p.wout;
-          bc1 = tx * p.bw + (q * 32) % p.bw;
-          bc2 = ty * p.bh + (q * 32) / p.bw;
+          bc1 = tx * p.bw + (sub * 128 + q * 32) % p.bw;
+          bc2 = ty * p.bh + (sub * 128 + q * 32) / p.bw;
           bc3 = img;
         } else {
           const int ph = m >> 5, r = m & 31;
@@ -335,8 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < BN / C::CH; ++c) {
         float v[C::CH];
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(buf * BN + c * C::CH);
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+            static_cast<uint32_t>(buf * C::ACC_COLS + sub * BN + c * C::CH);
         if (C::CH == 32)
           tmem_ld_32cols(taddr, v);
         else
@@ -470,6 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (failed) break;
+      }  // sub-tiles
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && !failed) mbar_arrive(&acc_empty[buf]);
@@ -495,21 +513,21 @@ int pow2_at_least(int v) {
   return r;
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, int MS>
 int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ts,
                  const CUtensorMap &to, const CUtensorMap &tr, const KParams &kp,
                  cudaStream_t stream) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, MS>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(igemm_kernel<BN, MODE>,
+    attr_err = cudaFuncSetAttribute(igemm_kernel<BN, MODE, MS>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(C::SMEM));
   });
   if (attr_err != cudaSuccess) return VAE_ECUDA;
   const int grid = std::min(kp.total_tiles, num_sms());
-  igemm_kernel<BN, MODE><<<grid, kThreads, C::SMEM, stream>>>(ta, tb, ts, to, tr, kp);
+  igemm_kernel<BN, MODE, MS><<<grid, kThreads, C::SMEM, stream>>>(ta, tb, ts, to, tr, kp);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(1);
   return VAE_OK;
@@ -520,11 +538,13 @@ int launch_mode(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUte
                 const CUtensorMap &to, const CUtensorMap &tr, const KParams &kp,
                 cudaStream_t s) {
   switch (bn) {
-    case 256: return launch_typed<256, MODE>(ta, tb, ts, to, tr, kp, s);
-    case 128: return launch_typed<128, MODE>(ta, tb, ts, to, tr, kp, s);
-    case 64: return launch_typed<64, MODE>(ta, tb, ts, to, tr, kp, s);
-    case 32: return launch_typed<32, MODE>(ta, tb, ts, to, tr, kp, s);
-    default: return launch_typed<16, MODE>(ta, tb, ts, to, tr, kp, s);
+    case 256: return launch_typed<256, MODE, 1>(ta, tb, ts, to, tr, kp, s);
+    case 128:
+      return MODE == 0 ? launch_typed<128, MODE, 2>(ta, tb, ts, to, tr, kp, s)
+                       : launch_typed<128, MODE, 1>(ta, tb, ts, to, tr, kp, s);
+    case 64: return launch_typed<64, MODE, 1>(ta, tb, ts, to, tr, kp, s);
+    case 32: return launch_typed<32, MODE, 1>(ta, tb, ts, to, tr, kp, s);
+    default: return launch_typed<16, MODE, 1>(ta, tb, ts, to, tr, kp, s);
   }
 }
 
@@ -540,11 +560,11 @@ int pick_bn(int cout) {
 
 size_t igemm_smem_bytes(int bn) {
   switch (bn) {
-    case 256: return Cfg<256>::SMEM;
-    case 128: return Cfg<128>::SMEM;
-    case 64: return Cfg<64>::SMEM;
-    case 32: return Cfg<32>::SMEM;
-    default: return Cfg<16>::SMEM;
+    case 256: return Cfg<256, 1>::SMEM;
+    case 128: return Cfg<128, 2>::SMEM;
+    case 64: return Cfg<64, 1>::SMEM;
+    case 32: return Cfg<32, 1>::SMEM;
+    default: return Cfg<16, 1>::SMEM;
   }
 }
 
@@ -601,8 +621,9 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
       kp.taps = d.k * d.k * d.kt;
       kp.hout = d.hin;
       kp.wout = d.win;
+      const int rows = (bn == 128 ? 2 : 1) * kBM;  // M sub-tiles (see Cfg)
       kp.bw = std::min(128, pow2_at_least(d.win));
-      kp.bh = kBM / kp.bw;
+      kp.bh = rows / kp.bw;
       kp.tiles_x = ceil_div(d.win, kp.bw);
       kp.tiles_y = ceil_div(d.hin, kp.bh);
       kp.sc_chunks = d.sc ? d.sc_c / 32 : 0;
