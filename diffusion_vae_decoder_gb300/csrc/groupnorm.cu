@@ -24,16 +24,20 @@ namespace {
 constexpr int kStatThreads = 256;
 constexpr int kMaxBlocksPerGroupSeg = 512;  // partial slots per (sample, group)
 
+// (count, mean, M2) of a set of values; merged with the parallel-variance
+// combination, which works on deviations from the means (no cancellation of
+// large raw sums). FP32 arithmetic: FP64 throughput on this part is low.
 struct Triple {
-  double n, mean, m2;
+  float n, mean, m2;
 };
 
 __device__ __forceinline__ Triple merge(Triple a, Triple b) {
-  if (a.n == 0) return b;
-  if (b.n == 0) return a;
-  const double n = a.n + b.n;
-  const double d = b.mean - a.mean;
-  return {n, a.mean + d * (b.n / n), a.m2 + b.m2 + d * d * (a.n * b.n / n)};
+  if (a.n == 0.f) return b;
+  if (b.n == 0.f) return a;
+  const float n = a.n + b.n;
+  const float wb = __fdividef(b.n, n);
+  const float d = b.mean - a.mean;
+  return {n, fmaf(d, wb, a.mean), a.m2 + b.m2 + d * d * a.n * wb};
 }
 
 // NHWC: x[n][spatial][c]. grid = (nblk, n). Partials [n][groups][nblk].
@@ -51,13 +55,35 @@ __global__ void __launch_bounds__(kStatThreads)
   int cnt = 0;
   if (pl < ppi) {
     const float *base = x + (static_cast<long long>(n) * spatial) * c + 4 * lc;
-    for (long long pix = p0 + pl; pix < p1; pix += ppi) {
+    long long pix = p0 + pl;
+    if (pix < p1) {  // shift every sum by the first value this thread sees
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(base + pix * c));
+      k[0] = v.x;
+      k[1] = v.y;
+      k[2] = v.z;
+      k[3] = v.w;
+    }
+    // four independent loads in flight per iteration
+    for (; pix + 3 * ppi < p1; pix += 4 * ppi) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[u] = __ldg(reinterpret_cast<const float4 *>(base + (pix + u * ppi) * c));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float a[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float d = a[j] - k[j];
+          s[j] += d;
+          ss[j] = fmaf(d, d, ss[j]);
+        }
+      }
+      cnt += 4;
+    }
+    for (; pix < p1; pix += ppi) {
       const float4 v = __ldg(reinterpret_cast<const float4 *>(base + pix * c));
       const float a[4] = {v.x, v.y, v.z, v.w};
-      if (cnt == 0) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) k[j] = a[j];
-      }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float d = a[j] - k[j];
@@ -78,7 +104,7 @@ __global__ void __launch_bounds__(kStatThreads)
   __syncthreads();
   const int cg = c / groups;
   for (int g = tid; g < groups; g += kStatThreads) {
-    Triple acc{0, 0, 0};
+    Triple acc{0.f, 0.f, 0.f};
     for (int l = 0; l < ppi; ++l)
       for (int ch = g * cg; ch < (g + 1) * cg; ++ch) {
         const float *e = sm + (static_cast<long long>(l) * c + ch) * 3;
@@ -96,7 +122,7 @@ __global__ void __launch_bounds__(kStatThreads)
 __global__ void __launch_bounds__(kStatThreads)
     gn_stats_nchw(const float *__restrict__ x, int c, long long spatial, int groups, int nblk,
                   double *__restrict__ part) {
-  __shared__ double red[kStatThreads][3];
+  __shared__ float red[kStatThreads][3];
   const int ng = blockIdx.y, blk = blockIdx.x;
   const int cg = c / groups;
   const long long seg = static_cast<long long>(cg) * spatial;
@@ -141,13 +167,14 @@ __global__ void gn_finalize(const double *__restrict__ part, int nblk, int c, in
                             float eps, const float *__restrict__ gamma,
                             const float *__restrict__ beta, float *__restrict__ scale,
                             float *__restrict__ shift) {
-  __shared__ double red[128][3];
+  __shared__ float red[128][3];
   const int ng = blockIdx.x;
   const int n = ng / groups, g = ng % groups;
-  Triple acc{0, 0, 0};
+  Triple acc{0.f, 0.f, 0.f};
   for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
     const double *e = part + (static_cast<long long>(ng) * nblk + b) * 3;
-    acc = merge(acc, Triple{e[0], e[1], e[2]});
+    acc = merge(acc, Triple{static_cast<float>(e[0]), static_cast<float>(e[1]),
+                            static_cast<float>(e[2])});
   }
   red[threadIdx.x][0] = acc.n;
   red[threadIdx.x][1] = acc.mean;
@@ -183,37 +210,49 @@ __device__ __forceinline__ float act(float v, int silu) {
 
 __device__ __forceinline__ float rnd(float v, int round) { return round ? round_tf32(v) : v; }
 
-// y = [silu](x * scale + shift) (+ res), optionally TF32-rounded.
-__global__ void gn_apply_nhwc(const float *__restrict__ x, long long total4, int c,
-                              long long per_sample, const float *__restrict__ scale,
-                              const float *__restrict__ shift, int silu, int round,
-                              const float *__restrict__ res, float *__restrict__ y) {
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total4;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long e = 4 * i;
-    const int n = static_cast<int>(e / per_sample);
-    const int ch = static_cast<int>(e % c);
-    const float4 v = reinterpret_cast<const float4 *>(x)[i];
-    const float4 a = *reinterpret_cast<const float4 *>(scale + n * c + ch);
-    const float4 b = *reinterpret_cast<const float4 *>(shift + n * c + ch);
+// y = [silu](x * scale + shift) (+ res), optionally TF32-rounded. Grid
+// (blocks, n): blockIdx.y is the sample; the float4 stride of the loop is a
+// multiple of c/4, so every thread keeps the same four channels and loads
+// their scale/shift once.
+__global__ void __launch_bounds__(256)
+    gn_apply_nhwc(const float *__restrict__ x, unsigned per_sample4, int c,
+                  const float *__restrict__ scale, const float *__restrict__ shift, int silu,
+                  int round, const float *__restrict__ res, float *__restrict__ y) {
+  const int n = blockIdx.y;
+  const size_t base4 = static_cast<size_t>(n) * per_sample4;
+  const float4 *xv = reinterpret_cast<const float4 *>(x) + base4;
+  float4 *yv = reinterpret_cast<float4 *>(y) + base4;
+  const float4 *rv = res ? reinterpret_cast<const float4 *>(res) + base4 : nullptr;
+  const unsigned i0 = blockIdx.x * 256u + threadIdx.x;
+  const unsigned stride = gridDim.x * 256u;
+  const int ch = static_cast<int>((i0 * 4u) % static_cast<unsigned>(c));
+  const float4 a = *reinterpret_cast<const float4 *>(scale + n * c + ch);
+  const float4 b = *reinterpret_cast<const float4 *>(shift + n * c + ch);
+  auto one = [&](float4 v, float4 r) {
     float4 o;
-    o.x = act(fmaf(v.x, a.x, b.x), silu);
-    o.y = act(fmaf(v.y, a.y, b.y), silu);
-    o.z = act(fmaf(v.z, a.z, b.z), silu);
-    o.w = act(fmaf(v.w, a.w, b.w), silu);
-    if (res) {
-      const float4 r = reinterpret_cast<const float4 *>(res)[i];
-      o.x += r.x;
-      o.y += r.y;
-      o.z += r.z;
-      o.w += r.w;
-    }
+    o.x = act(fmaf(v.x, a.x, b.x), silu) + r.x;
+    o.y = act(fmaf(v.y, a.y, b.y), silu) + r.y;
+    o.z = act(fmaf(v.z, a.z, b.z), silu) + r.z;
+    o.w = act(fmaf(v.w, a.w, b.w), silu) + r.w;
     o.x = rnd(o.x, round);
     o.y = rnd(o.y, round);
     o.z = rnd(o.z, round);
     o.w = rnd(o.w, round);
-    reinterpret_cast<float4 *>(y)[i] = o;
+    return o;
+  };
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  unsigned i = i0;
+  for (; i + 3 * stride < per_sample4; i += 4 * stride) {
+    float4 v[4], r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      v[u] = __ldg(xv + i + u * stride);
+      r[u] = rv ? __ldg(rv + i + u * stride) : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) yv[i + u * stride] = one(v[u], r[u]);
   }
+  for (; i < per_sample4; i += stride) yv[i] = one(__ldg(xv + i), rv ? __ldg(rv + i) : zero);
 }
 
 __global__ void gn_apply_nchw(const float *__restrict__ x, long long total, int c,
@@ -278,11 +317,23 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
   const long long total = static_cast<long long>(n) * c * spatial;
   const int threads = 256;
   if (nhwc) {
-    const long long total4 = total / 4;
-    const long long g = std::min<long long>((total4 + threads - 1) / threads, 8ll * num_sms());
-    gn_apply_nhwc<<<static_cast<int>(g), threads, 0, s>>>(x, total4, c, spatial * c, scale,
-                                                          shift, silu, round_out, residual,
-                                                          y);
+    const long long per4 = spatial * c / 4;
+    if (per4 > 0xffffffffll / 2) return VAE_EUNSUPPORTED;
+    // blocks per sample: a multiple of c / gcd(c, 1024), so the loop stride
+    // (blocks * 1024 elements) is a multiple of c and channels stay fixed
+    long long g = std::min<long long>((per4 + threads - 1) / threads,
+                                      std::max(1ll, 8ll * num_sms() / n));
+    long long gcd = c, b2 = 1024;
+    while (b2) {
+      const long long t = gcd % b2;
+      gcd = b2;
+      b2 = t;
+    }
+    const long long unit = c / gcd;
+    g = std::max(unit, g / unit * unit);
+    if ((g * 1024) % c != 0) return VAE_EUNSUPPORTED;
+    gn_apply_nhwc<<<dim3(static_cast<unsigned>(g), n), threads, 0, s>>>(
+        x, static_cast<unsigned>(per4), c, scale, shift, silu, round_out, residual, y);
   } else {
     const long long g = std::min<long long>((total + threads - 1) / threads, 8ll * num_sms());
     gn_apply_nchw<<<static_cast<int>(g), threads, 0, s>>>(x, total, c, spatial, scale, shift,
