@@ -242,13 +242,25 @@ struct Plan {
   size_t max_elems = 0;  // largest activation (n * H * W * C) of the chain
   int max_c = 0;
   int attn_c = 0, attn_l = 0;
+  long long max_slots = 0;  // GroupNorm partial slots of the largest producer conv
 };
+
+long long stat_slots_of(AMode mode, int hin, int win, int cout) {
+  IgemmDesc d;
+  d.mode = mode;
+  d.hin = hin;
+  d.win = win;
+  d.cout = cout;
+  return igemm_stat_slots(d);
+}
 
 Plan make_plan(const Chain &ch, int n, int h, int w) {
   Plan p;
   auto see = [&](long long hh, long long ww, int c) {
     p.max_elems = std::max(p.max_elems, static_cast<size_t>(n * hh * ww * c));
     p.max_c = std::max(p.max_c, c);
+    p.max_slots = std::max(p.max_slots, stat_slots_of(AMode::Conv, static_cast<int>(hh),
+                                                      static_cast<int>(ww), c));
   };
   long long hh = h, ww = w;
   see(hh, ww, ch.conv_in.cout);
@@ -260,6 +272,8 @@ Plan make_plan(const Chain &ch, int n, int h, int w) {
       see(hh, ww, r.c1.cout);
     }
     if (u.has_up) {
+      p.max_slots = std::max(p.max_slots, stat_slots_of(AMode::Upsample, static_cast<int>(hh),
+                                                        static_cast<int>(ww), u.up.cout));
       hh *= 2;
       ww *= 2;
       see(hh, ww, u.up.cout);
@@ -270,8 +284,16 @@ Plan make_plan(const Chain &ch, int n, int h, int w) {
 
 struct DecodeWs {
   float *lat, *X, *Y, *T, *H;
+  float *part;  // GroupNorm partials written by the producer conv's epilogue
   AttnScratch attn;
   void *gn;
+};
+
+// Whether `part` currently holds the statistics of the tensor about to be
+// normalised, and with how many slots per (sample, group).
+struct Stats {
+  bool ready = false;
+  long long slots = 0;
 };
 
 DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, int w) {
@@ -281,6 +303,7 @@ DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, 
   d.Y = cv.take<float>(p.max_elems);
   d.T = cv.take<float>(p.max_elems);
   d.H = cv.take<float>(p.max_elems);
+  d.part = cv.take<float>(static_cast<size_t>(n) * ch.groups * std::max(1ll, p.max_slots) * 3);
   const size_t nl = static_cast<size_t>(n) * p.attn_l;
   const size_t lp = static_cast<size_t>(round_up32(p.attn_l));
   const int c = p.attn_c;
@@ -310,10 +333,11 @@ double conv_flops(const ConvW &c, long long out_pixels) {
 
 int run_conv(Profiler &prof, const ConvW &c, const float *in, int n, int h, int w,
              const float *sc_in, const float *residual, float *out, int round_out,
-             cudaStream_t s, bool upsample = false, bool nchw_out = false) {
+             cudaStream_t s, bool upsample = false, bool nchw_out = false,
+             Stats *st = nullptr, float *part = nullptr, int groups = 0) {
   const long long out_px = static_cast<long long>(n) * h * w * (upsample ? 4 : 1);
-  Step st(prof, upsample ? VAE_PROF_UPSAMPLE_CONV : VAE_PROF_CONV3X3, conv_flops(c, out_px), 0,
-          s);
+  Step step(prof, upsample ? VAE_PROF_UPSAMPLE_CONV : VAE_PROF_CONV3X3, conv_flops(c, out_px),
+            0, s);
   IgemmDesc d;
   d.mode = upsample ? AMode::Upsample : AMode::Conv;
   d.a = in;
@@ -333,25 +357,48 @@ int run_conv(Profiler &prof, const ConvW &c, const float *in, int n, int h, int 
   d.bias = c.b;
   d.residual = residual;
   d.round_out = round_out;
-  return igemm_launch(d, s);
+  int fused = 0;
+  if (st) {
+    d.stat_part = part;
+    d.stat_groups = groups;
+    d.stat_ok = &fused;
+  }
+  const int rc = igemm_launch(d, s);
+  if (st) {
+    st->ready = rc == VAE_OK && fused;
+    st->slots = st->ready ? igemm_stat_slots(d) : 0;
+  }
+  return rc;
 }
 
 // One resnet on NHWC data: `in` [n,h,w,cin] -> `out` [n,h,w,cout]; out == in
 // is allowed when there is no shortcut.
+// GroupNorm+SiLU of `in` into `out` (TF32-rounded: the next conv's operand).
+// With statistics fused into the producer conv only the finalize and apply
+// passes run (8 bytes per element); otherwise the two-pass kernels (12).
 int run_gn(Chain &ch, const NormW &nw, const float *in, int n, long long sp, float *out,
-           void *gnws, cudaStream_t s) {
-  Step st(ch.prof, VAE_PROF_GROUPNORM, 0, 12.0 * n * sp * nw.c, s);
-  return groupnorm_silu(in, n, nw.c, sp, 1, ch.groups, ch.eps, nw.g, nw.b, 1, 1, out, gnws, s);
+           const DecodeWs &ws, const Stats &stats, cudaStream_t s) {
+  Step step(ch.prof, VAE_PROF_GROUPNORM, 0, (stats.ready ? 8.0 : 12.0) * n * sp * nw.c, s);
+  if (stats.ready)
+    return groupnorm_from_partials(in, n, nw.c, sp, ch.groups, ch.eps, nw.g, nw.b, 1, 1, ws.part,
+                                   stats.slots, out, ws.gn, s);
+  return groupnorm_silu(in, n, nw.c, sp, 1, ch.groups, ch.eps, nw.g, nw.b, 1, 1, out, ws.gn, s);
 }
 
+// One resnet on NHWC data; `st` holds the statistics of `in` on entry and
+// those of `out` on return.
 int run_resnet(Chain &ch, const ResW &r, const float *in, float *out, const DecodeWs &ws, int n,
-               int h, int w, int round_out, cudaStream_t s) {
+               int h, int w, int round_out, Stats &st, cudaStream_t s) {
   const long long sp = static_cast<long long>(h) * w;
-  VAE_TRY(run_gn(ch, r.n1, in, n, sp, ws.T, ws.gn, s));
-  VAE_TRY(run_conv(ch.prof, r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s));
-  VAE_TRY(run_gn(ch, r.n2, ws.H, n, sp, ws.T, ws.gn, s));
-  if (r.c2.sc_cin) return run_conv(ch.prof, r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s);
-  return run_conv(ch.prof, r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s);
+  VAE_TRY(run_gn(ch, r.n1, in, n, sp, ws.T, ws, st, s));
+  VAE_TRY(run_conv(ch.prof, r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s, false, false, &st,
+                   ws.part, ch.groups));
+  VAE_TRY(run_gn(ch, r.n2, ws.H, n, sp, ws.T, ws, st, s));
+  if (r.c2.sc_cin)
+    return run_conv(ch.prof, r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s, false, false,
+                    &st, ws.part, ch.groups);
+  return run_conv(ch.prof, r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s, false, false,
+                  &st, ws.part, ch.groups);
 }
 
 }  // namespace
@@ -452,8 +499,10 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
   }
   float *cur = d.X, *other = d.Y;
   int hh = h, ww = w;
-  VAE_TRY(run_conv(ch->prof, ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s));
-  VAE_TRY(run_resnet(*ch, ch->mid1, cur, cur, d, n, hh, ww, 0, s));
+  Stats st;
+  VAE_TRY(run_conv(ch->prof, ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s, false,
+                   false, &st, d.part, ch->groups));
+  VAE_TRY(run_resnet(*ch, ch->mid1, cur, cur, d, n, hh, ww, 0, st, s));
   {
     const double c = ch->attn.c;
     Step st(ch->prof, VAE_PROF_ATTENTION, n * (4.0 * L * L * c + 8.0 * L * c * c), 0, s);
@@ -461,7 +510,8 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
                            ch->attn.n.g, ch->attn.n.b, ch->attn.wqkv, ch->attn.bqkv, ch->attn.wo,
                            ch->attn.bo, cur, d.attn, s));
   }
-  VAE_TRY(run_resnet(*ch, ch->mid2, cur, cur, d, n, hh, ww, 0, s));
+  st.ready = false;  // the attention changed `cur`
+  VAE_TRY(run_resnet(*ch, ch->mid2, cur, cur, d, n, hh, ww, 0, st, s));
   for (const UpW &u : ch->ups) {
     for (size_t j = 0; j < u.res.size(); ++j) {
       const ResW &r = u.res[j];
@@ -469,18 +519,19 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
       // an MMA operand, so it is stored TF32-rounded.
       const int round = (u.has_up && j + 1 == u.res.size()) ? 1 : 0;
       float *dst = r.c2.sc_cin ? other : cur;
-      VAE_TRY(run_resnet(*ch, r, cur, dst, d, n, hh, ww, round, s));
+      VAE_TRY(run_resnet(*ch, r, cur, dst, d, n, hh, ww, round, st, s));
       if (dst != cur) std::swap(cur, other);
     }
     if (u.has_up) {
       // Output rounded: the next resnet may read it through its shortcut MMA.
-      VAE_TRY(run_conv(ch->prof, u.up, cur, n, hh, ww, nullptr, nullptr, other, 1, s, true));
+      VAE_TRY(run_conv(ch->prof, u.up, cur, n, hh, ww, nullptr, nullptr, other, 1, s, true,
+                       false, &st, d.part, ch->groups));
       std::swap(cur, other);
       hh *= 2;
       ww *= 2;
     }
   }
-  VAE_TRY(run_gn(*ch, ch->norm_out, cur, n, static_cast<long long>(hh) * ww, d.T, d.gn, s));
+  VAE_TRY(run_gn(*ch, ch->norm_out, cur, n, static_cast<long long>(hh) * ww, d.T, d, st, s));
   return run_conv(ch->prof, ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, rgb, 0, s, false,
                   true);
 }

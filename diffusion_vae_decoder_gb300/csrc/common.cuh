@@ -88,8 +88,15 @@ struct IgemmDesc {
   const float *residual = nullptr;  // same layout / ld as out
   float alpha = 1.0f;
   int round_out = 0;  // store TF32-rounded values (output feeds another MMA)
+  // Optional GroupNorm statistics of the stored output (Conv / Upsample
+  // modes, NHWC): partials [n][stat_groups][igemm_stat_slots(d)] x (count,
+  // mean, M2), consumed by groupnorm_from_partials.
+  float *stat_part = nullptr;
+  int stat_groups = 0;
+  int *stat_ok = nullptr;  // set on the host: 1 if the statistics were requested and fused
 };
 size_t igemm_smem_bytes(int bn);
+long long igemm_stat_slots(const IgemmDesc &d);
 int igemm_launch(const IgemmDesc &d, cudaStream_t stream);
 
 // Weight packing (layout.cu): w [cout][cin][taps] (+ shortcut [cout][sc_cin])
@@ -117,6 +124,14 @@ size_t groupnorm_ws_bytes(int n, int c, long long spatial, int groups);
 int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, int groups,
                    float eps, const float *gamma, const float *beta, int silu, int round_out,
                    float *y, void *ws, cudaStream_t s, const float *residual = nullptr);
+
+// GroupNorm(+SiLU) of NHWC x whose statistics were produced by the conv
+// epilogue (float partials [n][groups][slots][3]); ws holds scale/shift.
+size_t groupnorm_partials_ws_bytes(int n, int c);
+int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int groups,
+                            float eps, const float *gamma, const float *beta, int silu,
+                            int round_out, const float *part, long long slots, float *y,
+                            void *ws, cudaStream_t s, const float *residual = nullptr);
 
 // Row softmax in place: s[r][:L] <- softmax(scale * s[r][:L]), TF32-rounded.
 int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st);

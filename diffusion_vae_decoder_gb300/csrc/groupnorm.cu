@@ -163,7 +163,8 @@ __global__ void __launch_bounds__(kStatThreads)
 }
 
 // One CTA per (n, g): merge nblk partials, write scale/shift per channel.
-__global__ void gn_finalize(const double *__restrict__ part, int nblk, int c, int groups,
+template <class P>
+__global__ void gn_finalize(const P *__restrict__ part, long long nblk, int c, int groups,
                             float eps, const float *__restrict__ gamma,
                             const float *__restrict__ beta, float *__restrict__ scale,
                             float *__restrict__ shift) {
@@ -171,8 +172,8 @@ __global__ void gn_finalize(const double *__restrict__ part, int nblk, int c, in
   const int ng = blockIdx.x;
   const int n = ng / groups, g = ng % groups;
   Triple acc{0.f, 0.f, 0.f};
-  for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
-    const double *e = part + (static_cast<long long>(ng) * nblk + b) * 3;
+  for (long long b = threadIdx.x; b < nblk; b += blockDim.x) {
+    const P *e = part + (static_cast<long long>(ng) * nblk + b) * 3;
     acc = merge(acc, Triple{static_cast<float>(e[0]), static_cast<float>(e[1]),
                             static_cast<float>(e[2])});
   }
@@ -266,6 +267,30 @@ __global__ void gn_apply_nchw(const float *__restrict__ x, long long total, int 
   }
 }
 
+int launch_apply_nhwc(const float *x, int n, int c, long long spatial, const float *scale,
+                      const float *shift, int silu, int round_out, const float *residual,
+                      float *y, cudaStream_t s) {
+  const int threads = 256;
+  const long long per4 = spatial * c / 4;
+  if (per4 > 0xffffffffll / 2) return VAE_EUNSUPPORTED;
+  // blocks per sample: a multiple of c / gcd(c, 1024), so the loop stride
+  // (blocks * 1024 elements) is a multiple of c and channels stay fixed
+  long long g = std::min<long long>((per4 + threads - 1) / threads,
+                                    std::max(1ll, 8ll * num_sms() / n));
+  long long gcd = c, b2 = 1024;
+  while (b2) {
+    const long long t = gcd % b2;
+    gcd = b2;
+    b2 = t;
+  }
+  const long long unit = c / gcd;
+  g = std::max(unit, g / unit * unit);
+  if ((g * 1024) % c != 0) return VAE_EUNSUPPORTED;
+  gn_apply_nhwc<<<dim3(static_cast<unsigned>(g), n), threads, 0, s>>>(
+      x, static_cast<unsigned>(per4), c, scale, shift, silu, round_out, residual, y);
+  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+}
+
 int nblk_for(long long elems_per_seg, int segs) {
   long long want = elems_per_seg / (kStatThreads * 16);
   const long long cap = std::max(1ll, 4ll * num_sms() / std::max(1, segs));
@@ -312,28 +337,13 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
                                                                    part);
   }
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
-  gn_finalize<<<n * groups, 128, 0, s>>>(part, nblk, c, groups, eps, gamma, beta, scale, shift);
+  gn_finalize<double><<<n * groups, 128, 0, s>>>(part, nblk, c, groups, eps, gamma, beta, scale,
+                                                  shift);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   const long long total = static_cast<long long>(n) * c * spatial;
   const int threads = 256;
   if (nhwc) {
-    const long long per4 = spatial * c / 4;
-    if (per4 > 0xffffffffll / 2) return VAE_EUNSUPPORTED;
-    // blocks per sample: a multiple of c / gcd(c, 1024), so the loop stride
-    // (blocks * 1024 elements) is a multiple of c and channels stay fixed
-    long long g = std::min<long long>((per4 + threads - 1) / threads,
-                                      std::max(1ll, 8ll * num_sms() / n));
-    long long gcd = c, b2 = 1024;
-    while (b2) {
-      const long long t = gcd % b2;
-      gcd = b2;
-      b2 = t;
-    }
-    const long long unit = c / gcd;
-    g = std::max(unit, g / unit * unit);
-    if ((g * 1024) % c != 0) return VAE_EUNSUPPORTED;
-    gn_apply_nhwc<<<dim3(static_cast<unsigned>(g), n), threads, 0, s>>>(
-        x, static_cast<unsigned>(per4), c, scale, shift, silu, round_out, residual, y);
+    VAE_TRY(launch_apply_nhwc(x, n, c, spatial, scale, shift, silu, round_out, residual, y, s));
   } else {
     const long long g = std::min<long long>((total + threads - 1) / threads, 8ll * num_sms());
     gn_apply_nchw<<<static_cast<int>(g), threads, 0, s>>>(x, total, c, spatial, scale, shift,
@@ -341,6 +351,32 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
   }
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(3);
+  return VAE_OK;
+}
+
+size_t groupnorm_partials_ws_bytes(int n, int c) {
+  Carver cv(nullptr, 0);
+  cv.take<float>(static_cast<size_t>(n) * c);
+  cv.take<float>(static_cast<size_t>(n) * c);
+  return cv.used;
+}
+
+int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int groups,
+                            float eps, const float *gamma, const float *beta, int silu,
+                            int round_out, const float *part, long long slots, float *y,
+                            void *ws, cudaStream_t s, const float *residual) {
+  if (!x || !y || !gamma || !beta || !ws || !part || n <= 0 || c <= 0 || spatial <= 0 ||
+      groups <= 0 || slots <= 0)
+    return VAE_EINVAL;
+  if (c % groups || c % 4 || c > 1024) return VAE_EUNSUPPORTED;
+  Carver cv(ws, ~size_t(0));
+  float *scale = cv.take<float>(static_cast<size_t>(n) * c);
+  float *shift = cv.take<float>(static_cast<size_t>(n) * c);
+  gn_finalize<float><<<n * groups, 128, 0, s>>>(part, slots, c, groups, eps, gamma, beta, scale,
+                                                shift);
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_TRY(launch_apply_nhwc(x, n, c, spatial, scale, shift, silu, round_out, residual, y, s));
+  count_launches(2);
   return VAE_OK;
 }
 

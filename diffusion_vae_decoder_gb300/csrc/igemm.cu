@@ -63,6 +63,12 @@ struct KParams {
   int round_out;
   int epi_tma;  // 1: rows leave through shared staging + TMA stores (NHWC / GEMM)
   int has_res;  // residual present (TMA-loaded into the staging buffer when epi_tma)
+  // GroupNorm statistics of the output (optional): per (sample, group, slot)
+  // partial (count, mean, M2); slot = (frame, tile, sub-tile, warp).
+  float *stat_part;
+  int stat_cg;       // channels per group (power of two dividing 32)
+  int stat_groups;   // groups over cout
+  int stat_slots;    // slots per (sample, group)
   int *err;
 };
 
@@ -86,6 +92,74 @@ struct Cfg {
   static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum each of NG per-lane values over the warp with a reduce-scatter
+// butterfly: every step sends half of the remaining values to the partner
+// lane, so NG - 1 + (5 - log2 NG) shuffles replace NG * 5. On return a[0]
+// holds, in every lane, the total of group (lane >> (5 - log2 NG)).
+template <int NG>
+__device__ __forceinline__ void warp_reduce_scatter(float (&a)[NG], int lane) {
+#pragma unroll
+  for (int half = NG / 2, o = 16; half >= 1; half /= 2, o /= 2) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? a[i] : a[half + i];
+      const float keep = upper ? a[half + i] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  constexpr int kLog = NG >= 32 ? 5 : NG >= 16 ? 4 : NG >= 8 ? 3 : NG >= 4 ? 2 : NG >= 2 ? 1 : 0;
+#pragma unroll
+  for (int o = 16 >> kLog; o >= 1; o /= 2) a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
+}
+
+// Exact two-pass (count, mean, M2) of each CG-channel group of a warp's 32
+// rows x 32 channels (invalid rows excluded). The lanes holding a group's
+// totals write its partial; successive groups are `gstride` floats apart.
+template <int CG>
+__device__ __forceinline__ void emit_group_stats(const float *v, bool valid, float nrows,
+                                                 float *out, long long gstride, int lane) {
+  constexpr int NG = 32 / CG;
+  constexpr int kShift = NG >= 32 ? 0 : NG >= 16 ? 1 : NG >= 8 ? 2 : NG >= 4 ? 3 : NG >= 2 ? 4 : 5;
+  const float cnt = nrows * CG;
+  const float inv = cnt > 0.f ? __fdividef(1.0f, cnt) : 0.f;
+  float a[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < CG; ++j) sum += v[g * CG + j];
+    a[g] = valid ? sum : 0.f;
+  }
+  warp_reduce_scatter<NG>(a, lane);
+  const float my_mean = a[0] * inv;  // mean of group (lane >> kShift)
+  float m2[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const float mean = __shfl_sync(0xffffffffu, my_mean, g << kShift);
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < CG; ++j) {
+      const float d = v[g * CG + j] - mean;
+      acc = fmaf(d, d, acc);
+    }
+    m2[g] = valid ? acc : 0.f;
+  }
+  warp_reduce_scatter<NG>(m2, lane);
+  if ((lane & ((1 << kShift) - 1)) == 0) {
+    float *o = out + (lane >> kShift) * gstride;
+    o[0] = cnt;
+    o[1] = my_mean;
+    o[2] = m2[0];
+  }
+}
 
 __device__ __forceinline__ void raise_error(const KParams &p, volatile uint32_t *abort) {
   *abort = 1u;
@@ -422,6 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               val.w = round_tf32(val.w);
             }
             *slot = val;
+            v[4 * j] = val.x;  // keep the stored values for the statistics
+            v[4 * j + 1] = val.y;
+            v[4 * j + 2] = val.z;
+            v[4 * j + 3] = val.w;
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -435,6 +513,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit();
           }
           sbuf ^= 1;
+          if (MODE != 2 && p.stat_part) {
+            const int per_img = p.tiles_x * p.tiles_y;
+            const int img = mt / per_img;
+            const long long slot =
+                ((static_cast<long long>(img % p.t) * per_img + mt % per_img) * MS + sub) * 4 + q;
+            const int gbase = col0 / p.stat_cg;
+            float *out = p.stat_part +
+                         ((static_cast<long long>(img / p.t) * p.stat_groups + gbase) *
+                              p.stat_slots + slot) * 3;
+            const long long gs = static_cast<long long>(p.stat_slots) * 3;
+            const float nrows = static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid)));
+            switch (p.stat_cg) {
+              case 1: emit_group_stats<1>(v, valid, nrows, out, gs, lane); break;
+              case 2: emit_group_stats<2>(v, valid, nrows, out, gs, lane); break;
+              case 4: emit_group_stats<4>(v, valid, nrows, out, gs, lane); break;
+              case 8: emit_group_stats<8>(v, valid, nrows, out, gs, lane); break;
+              case 16: emit_group_stats<16>(v, valid, nrows, out, gs, lane); break;
+              default: emit_group_stats<32>(v, valid, nrows, out, gs, lane); break;
+            }
+          }
           continue;
         }
         if (!valid) continue;
@@ -558,6 +656,24 @@ int pick_bn(int cout) {
 
 }  // namespace
 
+long long igemm_stat_slots(const IgemmDesc &d) {
+  const int bn = pick_bn(d.cout);
+  long long tiles;
+  int ms = 1;
+  if (d.mode == AMode::Conv) {
+    ms = bn == 128 ? 2 : 1;
+    const int bw = std::min(128, pow2_at_least(d.win));
+    const int bh = ms * kBM / bw;
+    tiles = static_cast<long long>(ceil_div(d.win, bw)) * ceil_div(d.hin, bh);
+  } else if (d.mode == AMode::Upsample) {
+    const int pw = std::min(32, pow2_at_least(d.win));
+    tiles = static_cast<long long>(ceil_div(d.win, pw)) * ceil_div(d.hin, 32 / pw);
+  } else {
+    return 0;
+  }
+  return static_cast<long long>(d.t > 0 ? d.t : 1) * tiles * ms * 4;
+}
+
 size_t igemm_smem_bytes(int bn) {
   switch (bn) {
     case 256: return Cfg<256, 1>::SMEM;
@@ -680,6 +796,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // box per epilogue warp = 32 rows x 32 channels.
   CUtensorMap to = tb, tr = tb;
   kp.has_res = d.residual != nullptr;
+  kp.stat_part = nullptr;
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   bool epi = !d.out_nchw && bn >= 32 && !d.bias_per_row && d.ldo % 4 == 0 && al16(d.out) &&
              (!d.residual || al16(d.residual));
@@ -713,6 +830,21 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
     if (d.residual) VAE_TRY(encode_out(&tr, d.residual));
   }
   kp.epi_tma = epi ? 1 : 0;
+  // Fused GroupNorm statistics need the staged epilogue and groups that sit
+  // inside one 32-channel chunk; otherwise the caller computes them itself.
+  if (d.stat_part) {
+    const int cg = d.stat_groups > 0 ? d.cout / d.stat_groups : 0;
+    const long long slots = igemm_stat_slots(d);
+    if (epi && d.mode != AMode::Gemm && d.cout % 32 == 0 && d.stat_groups > 0 &&
+        d.cout % d.stat_groups == 0 && cg >= 1 && cg <= 32 && (cg & (cg - 1)) == 0 &&
+        slots > 0 && slots < (1ll << 31)) {
+      kp.stat_part = d.stat_part;
+      kp.stat_cg = cg;
+      kp.stat_groups = d.stat_groups;
+      kp.stat_slots = static_cast<int>(slots);
+    }
+  }
+  if (d.stat_ok) *d.stat_ok = kp.stat_part != nullptr;
 
   switch (d.mode) {
     case AMode::Conv: return launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream);
