@@ -35,6 +35,9 @@ WORKLOADS = {
     "decoder_256": dict(latent=(1, 16, 32, 32), seed=S.seed_of("decoder_256"),
                         text="FLUX-class AutoencoderKL decoder, latent [1,16,32,32] -> RGB "
                              "[1,3,256,256], random init"),
+    "decoder_512": dict(latent=(1, 16, 64, 64), seed=S.seed_of("decoder_512_b4"),
+                        text="FLUX-class AutoencoderKL decoder, latent [1,16,64,64] -> RGB "
+                             "[1,3,512,512], random init (profiling size)"),
     "decoder_512_b4": dict(latent=(4, 16, 64, 64), seed=S.seed_of("decoder_512_b4"),
                            text="FLUX-class AutoencoderKL decoder, latent [4,16,64,64] -> RGB "
                                 "[4,3,512,512], random init"),

@@ -72,7 +72,8 @@ class ProfRecord(ctypes.Structure):
                 ("bytes", ctypes.c_double), ("ms", ctypes.c_double)]
 
 
-PROF_KINDS = {0: "conv3x3", 1: "upsample_conv", 2: "groupnorm", 3: "attention", 4: "layout"}
+PROF_KINDS = {0: "conv3x3", 1: "upsample_conv", 2: "groupnorm", 3: "attention", 4: "layout",
+              5: "head"}
 
 _I, _LL, _F, _SZ = ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_size_t
 _SIGS = {

@@ -111,6 +111,7 @@ struct Chain {
   AttnW attn;
   std::vector<UpW> ups;
   NormW norm_out;
+  float *head_w = nullptr;  // conv_out packed for the fused CUDA-core head (cout <= 4)
   std::vector<void *> allocs;
 };
 
@@ -284,6 +285,7 @@ Plan make_plan(const Chain &ch, int n, int h, int w) {
 
 struct DecodeWs {
   float *lat, *X, *Y, *T, *H;
+  float *ss;    // GroupNorm scale / shift for the fused head
   float *part;  // GroupNorm partials written by the producer conv's epilogue
   AttnScratch attn;
   void *gn;
@@ -303,6 +305,7 @@ DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, 
   d.Y = cv.take<float>(p.max_elems);
   d.T = cv.take<float>(p.max_elems);
   d.H = cv.take<float>(p.max_elems);
+  d.ss = cv.take<float>(2ull * n * std::max(p.max_c, ch.norm_out.c));
   d.part = cv.take<float>(static_cast<size_t>(n) * ch.groups * std::max(1ll, p.max_slots) * 3);
   const size_t nl = static_cast<size_t>(n) * p.attn_l;
   const size_t lp = static_cast<size_t>(round_up32(p.attn_l));
@@ -451,6 +454,12 @@ int vae_chain_prepare(const vae_chain_args *a, void **handle, vae_stream_t strea
   ch->norm_out = b.norm(a->norm_out, c);
   ch->conv_out = b.conv(a->conv_out, c, a->conv_out.cout);
   if (ch->conv_out.k != 3 && b.status == VAE_OK) b.fail(VAE_EINVAL);
+  if (b.status == VAE_OK && head_supported(c, a->conv_out.cout, a->conv_out.k)) {
+    const float *wt =
+        b.upload_tmp(a->conv_out.weight, static_cast<size_t>(a->conv_out.cout) * c * 9);
+    ch->head_w = b.dev<float>(head_packed_floats(c));
+    if (b.status == VAE_OK) b.fail(head_pack_weights(wt, a->conv_out.cout, c, ch->head_w, s));
+  }
   if (b.status == VAE_OK && cudaStreamSynchronize(s) != cudaSuccess) b.fail(VAE_ECUDA);
   cudaStreamSynchronize(s);
   for (void *p : b.temps) cudaFree(p);
@@ -531,7 +540,19 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
       ww *= 2;
     }
   }
-  VAE_TRY(run_gn(*ch, ch->norm_out, cur, n, static_cast<long long>(hh) * ww, d.T, d, st, s));
+  const long long hw = static_cast<long long>(hh) * ww;
+  if (ch->head_w) {
+    const int c = ch->norm_out.c, co = ch->conv_out.cout;
+    Step step(ch->prof, VAE_PROF_HEAD, 2.0 * 9 * c * co * n * hw, (4.0 * c + 4.0 * co) * n * hw,
+              s);
+    float *scale = d.ss, *shift = d.ss + static_cast<size_t>(n) * c;
+    VAE_TRY(groupnorm_scale_shift(cur, n, c, hw, ch->groups, ch->eps, ch->norm_out.g,
+                                  ch->norm_out.b, st.ready ? d.part : nullptr, st.slots, scale,
+                                  shift, d.gn, s));
+    return head_gn_silu_conv(cur, n, hh, ww, c, scale, shift, ch->head_w, ch->conv_out.b, co, rgb,
+                             s);
+  }
+  VAE_TRY(run_gn(*ch, ch->norm_out, cur, n, hw, d.T, d, st, s));
   return run_conv(ch->prof, ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, rgb, 0, s, false,
                   true);
 }

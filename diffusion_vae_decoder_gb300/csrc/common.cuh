@@ -133,6 +133,22 @@ int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int
                             int round_out, const float *part, long long slots, float *y,
                             void *ws, cudaStream_t s, const float *residual = nullptr);
 
+// Only the per-(sample, channel) affine of GroupNorm: y = x * scale + shift
+// (from fused partials when `part` is given, else from a statistics pass over
+// NHWC x using ws as groupnorm_ws_bytes describes).
+int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int groups, float eps,
+                          const float *gamma, const float *beta, const float *part,
+                          long long slots, float *scale, float *shift, void *ws, cudaStream_t s);
+
+// Fused norm_out GroupNorm+SiLU + conv_out (3x3, cout <= 4) on the CUDA cores
+// (head.cu): x NHWC [n][h][w][c], y NCHW [n][cout][h][w].
+bool head_supported(int cin, int cout, int k);
+size_t head_packed_floats(int cin);
+int head_pack_weights(const float *w, int cout, int cin, float *dst, cudaStream_t s);
+int head_gn_silu_conv(const float *x, int n, int h, int w, int c, const float *scale,
+                      const float *shift, const float *wpk, const float *bias, int cout,
+                      float *y, cudaStream_t s);
+
 // Row softmax in place: s[r][:L] <- softmax(scale * s[r][:L]), TF32-rounded.
 int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st);
 

@@ -354,6 +354,36 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
   return VAE_OK;
 }
 
+int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int groups, float eps,
+                          const float *gamma, const float *beta, const float *part,
+                          long long slots, float *scale, float *shift, void *ws,
+                          cudaStream_t s) {
+  if (!x || !gamma || !beta || !scale || !shift || n <= 0 || c <= 0 || spatial <= 0 ||
+      groups <= 0)
+    return VAE_EINVAL;
+  if (c % groups || c % 4 || c > 1024) return VAE_EUNSUPPORTED;
+  if (part) {
+    gn_finalize<float><<<n * groups, 128, 0, s>>>(part, slots, c, groups, eps, gamma, beta,
+                                                  scale, shift);
+    if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+    count_launches(1);
+    return VAE_OK;
+  }
+  if (!ws) return VAE_EINVAL;
+  Carver cv(ws, ~size_t(0));
+  double *dpart = cv.take<double>(static_cast<size_t>(n) * groups * kMaxBlocksPerGroupSeg * 3);
+  const int nblk = nblk_for(spatial * c, n);
+  const int tpp = c / 4, ppi = kStatThreads / tpp;
+  const size_t sm = static_cast<size_t>(ppi) * c * 3 * sizeof(float);
+  gn_stats_nhwc<<<dim3(nblk, n), kStatThreads, sm, s>>>(x, c, spatial, groups, nblk, dpart);
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  gn_finalize<double><<<n * groups, 128, 0, s>>>(dpart, nblk, c, groups, eps, gamma, beta,
+                                                 scale, shift);
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(2);
+  return VAE_OK;
+}
+
 size_t groupnorm_partials_ws_bytes(int n, int c) {
   Carver cv(nullptr, 0);
   cv.take<float>(static_cast<size_t>(n) * c);

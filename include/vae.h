@@ -260,7 +260,9 @@ typedef enum {
   VAE_PROF_UPSAMPLE_CONV = 1,  /* nearest-2x upsample + 3x3 conv (same per output pixel)     */
   VAE_PROF_GROUPNORM = 2,      /* GroupNorm(+SiLU) (bytes: 12 per element: read, read, write) */
   VAE_PROF_ATTENTION = 3,      /* mid attention block (flops: 4*L*L*c + 8*L*c*c per image)   */
-  VAE_PROF_LAYOUT = 4          /* latent de-normalisation / layout staging (bytes)           */
+  VAE_PROF_LAYOUT = 4,         /* latent de-normalisation / layout staging (bytes)           */
+  VAE_PROF_HEAD = 5            /* norm_out GroupNorm+SiLU fused into conv_out (CUDA cores):
+                                  flops 2*9*cin*cout, bytes 4*cin + 4*cout per output pixel */
 } vae_prof_kind;
 
 typedef struct {
