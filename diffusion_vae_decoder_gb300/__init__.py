@@ -412,6 +412,16 @@ class VaeChain:
             self.handle, _ptr(z), n, h, w, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
         return out
 
+    def capture_graph(self, z, out, ws):
+        """Capture one vae_decode_chain call on fixed buffers into a CUDA graph
+        (the chain neither synchronises nor allocates); replay() re-runs the
+        whole decode with one launch. Make one eager decode first."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.decode(z, out=out, ws=ws)
+        return g
+
     def profile(self, enable=True):
         _check("vae_chain_profile", load_library().vae_chain_profile(self.handle, int(enable)))
 

@@ -70,7 +70,10 @@ struct Profiler {
       if (cudaEventCreate(&e) != cudaSuccess) return -1;
       events.push_back(e);
     }
-    if (cudaEventRecord(events[next], s) != cudaSuccess) return -1;
+    // External record: inside a stream capture this becomes an event-record
+    // node of the graph, so every replay re-records it.
+    if (cudaEventRecordWithFlags(events[next], s, cudaEventRecordExternal) != cudaSuccess)
+      return -1;
     return next++;
   }
   // Opens a step; returns its record index, or -1 when profiling is off.

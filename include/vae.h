@@ -253,8 +253,9 @@ VAE_API int vae_chain_destroy(void *handle);
  * step (one conv, one GroupNorm+SiLU, the attention block, the latent
  * staging) with CUDA events on the caller's stream and stores the step's
  * algorithmic work. Enabling clears earlier records; records accumulate over
- * decode calls until read. Profiling adds event records to the stream, so do
- * not enable it while the stream is being captured into a graph. */
+ * decode calls until read. Inside a stream capture the events become
+ * event-record nodes of the graph: every replay re-records them, and a read
+ * after replays returns the last replay's times. */
 typedef enum {
   VAE_PROF_CONV3X3 = 0,        /* 3x3 conv (flops: 2*cin*cout*9 per output pixel, + shortcut) */
   VAE_PROF_UPSAMPLE_CONV = 1,  /* nearest-2x upsample + 3x3 conv (same per output pixel)     */
