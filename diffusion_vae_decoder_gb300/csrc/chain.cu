@@ -290,6 +290,7 @@ struct DecodeWs {
   float *lat, *X, *Y, *T, *H;
   float *ss;    // GroupNorm scale / shift for the fused head
   float *part;  // GroupNorm partials written by the producer conv's epilogue
+  float *split; // split-K partial sums of the low-resolution convs
   AttnScratch attn;
   void *gn;
 };
@@ -309,6 +310,7 @@ DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, 
   d.T = cv.take<float>(p.max_elems);
   d.H = cv.take<float>(p.max_elems);
   d.ss = cv.take<float>(2ull * n * std::max(p.max_c, ch.norm_out.c));
+  d.split = cv.take<float>(kSplitWsFloats);
   d.part = cv.take<float>(static_cast<size_t>(n) * ch.groups * std::max(1ll, p.max_slots) * 3);
   const size_t nl = static_cast<size_t>(n) * p.attn_l;
   const size_t lp = static_cast<size_t>(round_up32(p.attn_l));
@@ -340,7 +342,8 @@ double conv_flops(const ConvW &c, long long out_pixels) {
 int run_conv(Profiler &prof, const ConvW &c, const float *in, int n, int h, int w,
              const float *sc_in, const float *residual, float *out, int round_out,
              cudaStream_t s, bool upsample = false, bool nchw_out = false,
-             Stats *st = nullptr, float *part = nullptr, int groups = 0) {
+             Stats *st = nullptr, float *part = nullptr, int groups = 0,
+             float *split = nullptr) {
   const long long out_px = static_cast<long long>(n) * h * w * (upsample ? 4 : 1);
   Step step(prof, upsample ? VAE_PROF_UPSAMPLE_CONV : VAE_PROF_CONV3X3, conv_flops(c, out_px),
             0, s);
@@ -363,6 +366,8 @@ int run_conv(Profiler &prof, const ConvW &c, const float *in, int n, int h, int 
   d.bias = c.b;
   d.residual = residual;
   d.round_out = round_out;
+  d.split_ws = split;
+  d.split_ws_floats = split ? kSplitWsFloats : 0;
   int fused = 0;
   if (st) {
     d.stat_part = part;
@@ -398,13 +403,13 @@ int run_resnet(Chain &ch, const ResW &r, const float *in, float *out, const Deco
   const long long sp = static_cast<long long>(h) * w;
   VAE_TRY(run_gn(ch, r.n1, in, n, sp, ws.T, ws, st, s));
   VAE_TRY(run_conv(ch.prof, r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s, false, false, &st,
-                   ws.part, ch.groups));
+                   ws.part, ch.groups, ws.split));
   VAE_TRY(run_gn(ch, r.n2, ws.H, n, sp, ws.T, ws, st, s));
   if (r.c2.sc_cin)
     return run_conv(ch.prof, r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s, false, false,
-                    &st, ws.part, ch.groups);
+                    &st, ws.part, ch.groups, ws.split);
   return run_conv(ch.prof, r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s, false, false,
-                  &st, ws.part, ch.groups);
+                  &st, ws.part, ch.groups, ws.split);
 }
 
 }  // namespace
@@ -513,7 +518,7 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
   int hh = h, ww = w;
   Stats st;
   VAE_TRY(run_conv(ch->prof, ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s, false,
-                   false, &st, d.part, ch->groups));
+                   false, &st, d.part, ch->groups, d.split));
   VAE_TRY(run_resnet(*ch, ch->mid1, cur, cur, d, n, hh, ww, 0, st, s));
   {
     const double c = ch->attn.c;
@@ -537,7 +542,7 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
     if (u.has_up) {
       // Output rounded: the next resnet may read it through its shortcut MMA.
       VAE_TRY(run_conv(ch->prof, u.up, cur, n, hh, ww, nullptr, nullptr, other, 1, s, true,
-                       false, &st, d.part, ch->groups));
+                       false, &st, d.part, ch->groups, d.split));
       std::swap(cur, other);
       hh *= 2;
       ww *= 2;

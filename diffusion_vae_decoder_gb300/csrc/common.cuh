@@ -94,7 +94,13 @@ struct IgemmDesc {
   float *stat_part = nullptr;
   int stat_groups = 0;
   int *stat_ok = nullptr;  // set on the host: 1 if the statistics were requested and fused
+  // Optional split-K workspace (NHWC Conv / Upsample with ldo == cout): used
+  // when the output tiles alone would leave most SMs idle.
+  float *split_ws = nullptr;
+  size_t split_ws_floats = 0;
 };
+// Split-K workspace that always suffices for one conv (floats).
+constexpr size_t kSplitWsFloats = 160ull * 65536;
 size_t igemm_smem_bytes(int bn);
 long long igemm_stat_slots(const IgemmDesc &d);
 int igemm_launch(const IgemmDesc &d, cudaStream_t stream);

@@ -53,6 +53,11 @@ struct KParams {
   int M;
   int k, kt, taps;
   int cin_chunks, sc_chunks, k_stages, cin_pad;
+  // split-K: tile index = (split, m tile, n tile); split s covers reduction
+  // steps [s * ks_per, min((s + 1) * ks_per, k_stages)) and writes its raw
+  // partial sums at out + s * split_stride.
+  int splits, ks_per;
+  long long split_stride;
   int cout;
   float *out;
   int ldo, out_nchw;
@@ -241,8 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pending = 0, pend_par = 0;  // stages with a copy issued, and its parity
       bool failed = false;
       for (int tile = blockIdx.x; tile < p.total_tiles && !failed; tile += gridDim.x) {
-        const int mt = tile / p.n_tiles;
-        const int n0 = (tile % p.n_tiles) * BN;
+        const int mn = tile % (p.m_tiles * p.n_tiles);
+        const int split = tile / (p.m_tiles * p.n_tiles);
+        const int mt = mn / p.n_tiles;
+        const int n0 = (mn % p.n_tiles) * BN;
+        const int ks0 = split * p.ks_per, ks1 = min(ks0 + p.ks_per, p.k_stages);
         int img = 0, ty = 0, tx = 0;
         if (MODE != 2) {
           const int per_img = p.tiles_x * p.tiles_y;
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tx = rem % p.tiles_x;
         }
         const int n_idx = img / p.t, t_idx = img % p.t;
-        for (int ks = 0; ks < p.k_stages; ++ks) {
+        for (int ks = ks0; ks < ks1; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
             raise_error(p, abort);
             failed = true;
@@ -322,7 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS;
-        for (int ks = 0; ks < p.k_stages; ++ks) {
+        const int split = tile / (p.m_tiles * p.n_tiles);
+        const int ks0 = split * p.ks_per, ks1 = min(ks0 + p.ks_per, p.k_stages);
+        for (int ks = ks0; ks < ks1; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort)) {
             raise_error(p, abort);
             failed = true;
@@ -336,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sw128_kmajor_desc(smem_u32(sA + stage * C::A_BYTES + sub * kABytes));
 #pragma unroll
             for (int k = 0; k < 4; ++k)  // 4 x K=8 TF32 steps = 32 channels (128 bytes)
-              umma_tf32(d_tmem + sub * BN, ad + 2 * k, bd + 2 * k, IDESC, (ks | k) != 0);
+              umma_tf32(d_tmem + sub * BN, ad + 2 * k, bd + 2 * k, IDESC,
+                        (ks != ks0) || (k != 0));
           }
           issued = true;
           umma_commit(&empty[stage]);
@@ -375,8 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
 
-      const int mt = tile / p.n_tiles;
-      const int n0 = (tile % p.n_tiles) * BN;
+      const int mn = tile % (p.m_tiles * p.n_tiles);
+      const int split = tile / (p.m_tiles * p.n_tiles);
+      const int mt = mn / p.n_tiles;
+      const int n0 = (mn % p.n_tiles) * BN;
+      float *const obase = p.out + split * p.split_stride;
       for (int sub = 0; sub < MS; ++sub) {
       const int msub = sub * 128 + m;  // row of the (MS x 128)-row tile
       bool valid;
@@ -537,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!valid) continue;
         if (p.out_nchw) {
-          float *o = p.out + nchw0 + static_cast<long long>(col0) * cstride;
+          float *o = obase + nchw0 + static_cast<long long>(col0) * cstride;
           const float *r = p.residual ? p.residual + nchw0 + static_cast<long long>(col0) * cstride
                                       : nullptr;
 #pragma unroll
@@ -550,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          float *o = p.out + row * p.ldo + col0;
+          float *o = obase + row * p.ldo + col0;
           const float *r = p.residual ? p.residual + row * p.ldo + col0 : nullptr;
           if (ncols == C::CH) {
 #pragma unroll
@@ -601,6 +615,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// Sum of the split-K partial sums in a fixed order, then the epilogue:
+// out = alpha * sum + bias (+ residual), optionally TF32-rounded (NHWC rows).
+__global__ void splitk_reduce_kernel(const float4 *__restrict__ part, int splits, long long n4,
+                                     long long stride4, int cout, const float *__restrict__ bias,
+                                     float alpha, const float4 *__restrict__ res, int round,
+                                     float4 *__restrict__ out) {
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n4; i += gridDim.x * 256ll) {
+    float4 a = part[i];
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 b = part[i + sp * stride4];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    const int col = static_cast<int>((i * 4) % cout);
+    float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (bias) bv = *reinterpret_cast<const float4 *>(bias + col);
+    a.x = fmaf(a.x, alpha, bv.x);
+    a.y = fmaf(a.y, alpha, bv.y);
+    a.z = fmaf(a.z, alpha, bv.z);
+    a.w = fmaf(a.w, alpha, bv.w);
+    if (res) {
+      const float4 r = res[i];
+      a.x += r.x;
+      a.y += r.y;
+      a.z += r.z;
+      a.w += r.w;
+    }
+    if (round) {
+      a.x = round_tf32(a.x);
+      a.y = round_tf32(a.y);
+      a.z = round_tf32(a.z);
+      a.w = round_tf32(a.w);
+    }
+    out[i] = a;
   }
 }
 
@@ -790,16 +843,50 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   }
   const long long total = static_cast<long long>(kp.m_tiles) * kp.n_tiles;
   if (total <= 0 || total > (1ll << 31) - 1) return VAE_EUNSUPPORTED;
-  kp.total_tiles = static_cast<int>(total);
+
+  // Split-K when the output tiles fill less than ~60% of the SMs: each split
+  // accumulates a slice of the reduction into the caller's split workspace and
+  // a fixed-order reduce applies bias, residual and rounding.
+  kp.splits = 1;
+  kp.ks_per = kp.k_stages;
+  kp.split_stride = 0;
+  const long long rows_total = d.mode == AMode::Gemm
+                                   ? static_cast<long long>(d.M)
+                                   : static_cast<long long>(d.imgs) * kp.hout * kp.wout;
+  if (d.split_ws && d.mode != AMode::Gemm && !d.out_nchw && d.cout % 4 == 0 &&
+      d.ldo == d.cout && !d.bias_per_row) {
+    const int sms = num_sms();
+    if (total * 5 < static_cast<long long>(sms) * 3) {
+      long long sp = std::min<long long>(sms / total, kp.k_stages / 8);
+      sp = std::min<long long>(sp, 16);
+      const long long per = rows_total * d.cout;
+      while (sp > 1 && sp * per > static_cast<long long>(d.split_ws_floats)) --sp;
+      if (sp > 1) {
+        kp.ks_per = ceil_div(kp.k_stages, sp);
+        kp.splits = ceil_div(kp.k_stages, kp.ks_per);
+        kp.split_stride = per;
+      }
+    }
+  }
+  if (total * kp.splits > (1ll << 31) - 1) return VAE_EUNSUPPORTED;
+  kp.total_tiles = static_cast<int>(total * kp.splits);
+  if (kp.splits > 1) {  // the kernel writes raw partial sums
+    kp.out = d.split_ws;
+    kp.ldo = d.cout;
+    kp.bias = nullptr;
+    kp.residual = nullptr;
+    kp.round_out = 0;
+    kp.alpha = 1.0f;
+  }
 
   // Output (and residual) tensor maps for the staged TMA-store epilogue: one
   // box per epilogue warp = 32 rows x 32 channels.
   CUtensorMap to = tb, tr = tb;
-  kp.has_res = d.residual != nullptr;
+  kp.has_res = kp.residual != nullptr;
   kp.stat_part = nullptr;
   auto al16 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
-  bool epi = !d.out_nchw && bn >= 32 && !d.bias_per_row && d.ldo % 4 == 0 && al16(d.out) &&
-             (!d.residual || al16(d.residual));
+  bool epi = kp.splits == 1 && !d.out_nchw && bn >= 32 && !d.bias_per_row && d.ldo % 4 == 0 &&
+             al16(d.out) && (!d.residual || al16(d.residual));
   if (d.mode == AMode::Upsample && d.imgs > 1 && d.hin % kp.bh) epi = false;  // rows would wrap
   if (epi) {
     auto encode_out = [&](CUtensorMap *m, const float *base) -> int {
@@ -846,11 +933,22 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   }
   if (d.stat_ok) *d.stat_ok = kp.stat_part != nullptr;
 
+  int rc;
   switch (d.mode) {
-    case AMode::Conv: return launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream);
-    case AMode::Upsample: return launch_mode<1>(bn, ta, tb, ts, to, tr, kp, stream);
-    default: return launch_mode<2>(bn, ta, tb, ts, to, tr, kp, stream);
+    case AMode::Conv: rc = launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream); break;
+    case AMode::Upsample: rc = launch_mode<1>(bn, ta, tb, ts, to, tr, kp, stream); break;
+    default: rc = launch_mode<2>(bn, ta, tb, ts, to, tr, kp, stream); break;
   }
+  if (rc != VAE_OK || kp.splits == 1) return rc;
+  const long long n4 = rows_total * d.cout / 4;
+  const long long blocks = std::min<long long>((n4 + 255) / 256, 8ll * num_sms());
+  splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const float4 *>(d.split_ws), kp.splits, n4, kp.split_stride / 4, d.cout,
+      d.bias, d.alpha, reinterpret_cast<const float4 *>(d.residual), d.round_out,
+      reinterpret_cast<float4 *>(d.out));
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(1);
+  return VAE_OK;
 }
 
 }  // namespace vae

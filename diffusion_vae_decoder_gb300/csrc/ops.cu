@@ -51,11 +51,13 @@ bool needs_stage(int layout, int c) { return layout == VAE_NCHW || c % 32 != 0; 
 
 // ---------------------------------------------------------------- conv2d
 struct ConvWs {
-  float *packed, *bias_sum, *xs, *scs;
+  float *packed, *bias_sum, *xs, *scs, *split;
+  size_t split_floats;
 };
 
+// out_scale: output pixels per input pixel (4 for the upsample conv).
 ConvWs carve_conv(Carver &cv, int n, int cin, long long spatial, int layout, int cout, int taps,
-                  int sc_cin) {
+                  int sc_cin, int out_scale = 1) {
   ConvWs w{};
   const int ldb = packed_ldb(cin, taps, sc_cin);
   w.packed = cv.take<float>(static_cast<size_t>(cout) * ldb);
@@ -66,6 +68,10 @@ ConvWs carve_conv(Carver &cv, int n, int cin, long long spatial, int layout, int
   w.scs = (sc_cin && needs_stage(layout, sc_cin))
               ? cv.take<float>(static_cast<size_t>(n) * spatial * round_up32(sc_cin))
               : nullptr;
+  // split-K partials: at most 16 splits of the output
+  w.split_floats = std::min<size_t>(kSplitWsFloats,
+                            16ull * n * static_cast<size_t>(spatial) * out_scale * cout);
+  w.split = cv.take<float>(w.split_floats);
   return w;
 }
 
@@ -268,6 +274,8 @@ int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout, const f
   d.out_nchw = layout == VAE_NCHW;
   d.bias = bsum;
   d.residual = residual;
+  d.split_ws = cw.split;
+  d.split_ws_floats = cw.split_floats;
   return igemm_launch(d, s);
 }
 
@@ -275,7 +283,7 @@ int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout, const f
 size_t vae_upsample_conv_workspace_size(int n, int cin, int h, int w, int layout, int cout) {
   if (n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0) return 0;
   Carver cv(nullptr, 0);
-  carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout, 9, 0);
+  carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout, 9, 0, 4);
   return cv.used;
 }
 
@@ -291,7 +299,7 @@ int vae_upsample_conv(const float *x, int n, int cin, int h, int w, int layout,
   if (layout == VAE_NHWC && cout % 4) return VAE_EUNSUPPORTED;
   const long long spatial = static_cast<long long>(h) * w;
   Carver cv(ws, ws_bytes);
-  ConvWs cw = carve_conv(cv, n, cin, spatial, layout, cout, 9, 0);
+  ConvWs cw = carve_conv(cv, n, cin, spatial, layout, cout, 9, 0, 4);
   if (!cv.ok()) return VAE_EWORKSPACE;
   const int ldb = packed_ldb(cin, 9, 0);
   VAE_TRY(pack_conv_weights(weight, cout, cin, 9, nullptr, 0, cw.packed, cout, ldb, s));
@@ -311,6 +319,8 @@ int vae_upsample_conv(const float *x, int n, int cin, int h, int w, int layout,
   d.ldo = cout;
   d.out_nchw = layout == VAE_NCHW;
   d.bias = bias;
+  d.split_ws = cw.split;
+  d.split_ws_floats = cw.split_floats;
   return igemm_launch(d, s);
 }
 
@@ -430,6 +440,8 @@ int vae_conv3d_causal(const float *x, int n, int cin, int t, int h, int w, int l
   d.out_nchw = layout == VAE_NCHW;
   d.bias = bias;
   d.residual = residual;
+  d.split_ws = cw.split;
+  d.split_ws_floats = cw.split_floats;
   return igemm_launch(d, s);
 }
 
