@@ -159,6 +159,28 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
+def conv_traffic_from_profile(workload):
+    """DRAM bytes per decode of the implicit-GEMM conv launches, from the
+    committed ncu summary of this workload -- None when that summary is
+    missing or was taken on a different igemm.cu (the kernel has changed)."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", f"launch_list_{workload}.md")
+    src = os.path.join(ROOT, "diffusion_vae_decoder_gb300", "csrc", "igemm.cu")
+    if not os.path.exists(path):
+        return None, None
+    text = open(path).read()
+    sha = re.search(r"igemm\.cu sha256 at capture: ([0-9a-f]{64})", text)
+    nbytes = re.search(r"igemm conv DRAM bytes per decode \(read \+ write\): (\d+)", text)
+    nlaunch = re.search(r"igemm conv launches per decode: (\d+)", text)
+    if not (sha and nbytes and nlaunch):
+        return None, None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != sha.group(1):
+            return None, None
+    return float(nbytes.group(1)), int(nlaunch.group(1))
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 def time_oracle_decode(latent, seed, repeats=1):
     """Float64 CPU oracle decode of one latent; returns (seconds per decode, Mpix)."""
@@ -316,6 +338,7 @@ def run_ours(args):
     barrier(dist)
     e2e_value = world * mpix / (e2e_ms / 1e3)
 
+    traffic, traffic_launches = conv_traffic_from_profile(args.workload)
     line = None
     if rank == 0:
         cpu = None
@@ -337,7 +360,9 @@ def run_ours(args):
                              "beyond the 129 MB L2"},
             "roofline": {"bound": "tensor", "kernel": "igemm_kernel (3x3 / upsample conv)",
                          "achieved": conv_tflops, "peak": tf32_peak, "unit": "TFLOP/s",
-                         "frac": conv_tflops / tf32_peak, "traffic": None,
+                         "frac": conv_tflops / tf32_peak, "traffic": traffic,
+                         "traffic_per": "decode: sum over the igemm conv launches of one decode "
+                                        f"({traffic_launches} launches), ncu dram bytes read+write",
                          "peak_source": f"{peak_src} bf16 sustained x {TF32_OVER_BF16:.4f} "
                                         "(nominal TF32/BF16 dense ratio)",
                          "share_of_step": conv_ms / n_prof / ms,

@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kStatThreads = 256;
 constexpr int kMaxBlocksPerGroupSeg = 512;  // partial slots per (sample, group)
+constexpr int kFinalizeThreads = 512;       // threads merging one (sample, group)
 
 // (count, mean, M2) of a set of values; merged with the parallel-variance
 // combination, which works on deviations from the means (no cancellation of
@@ -168,7 +169,7 @@ __global__ void gn_finalize(const P *__restrict__ part, long long nblk, int c, i
                             float eps, const float *__restrict__ gamma,
                             const float *__restrict__ beta, float *__restrict__ scale,
                             float *__restrict__ shift) {
-  __shared__ float red[128][3];
+  __shared__ float red[kFinalizeThreads][3];
   const int ng = blockIdx.x;
   const int n = ng / groups, g = ng % groups;
   Triple acc{0.f, 0.f, 0.f};
@@ -337,8 +338,8 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
                                                                    part);
   }
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
-  gn_finalize<double><<<n * groups, 128, 0, s>>>(part, nblk, c, groups, eps, gamma, beta, scale,
-                                                  shift);
+  gn_finalize<double><<<n * groups, kFinalizeThreads, 0, s>>>(part, nblk, c, groups, eps, gamma,
+                                                               beta, scale, shift);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   const long long total = static_cast<long long>(n) * c * spatial;
   const int threads = 256;
@@ -363,7 +364,7 @@ int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int g
     return VAE_EINVAL;
   if (c % groups || c % 4 || c > 1024) return VAE_EUNSUPPORTED;
   if (part) {
-    gn_finalize<float><<<n * groups, 128, 0, s>>>(part, slots, c, groups, eps, gamma, beta,
+    gn_finalize<float><<<n * groups, kFinalizeThreads, 0, s>>>(part, slots, c, groups, eps, gamma, beta,
                                                   scale, shift);
     if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
     count_launches(1);
@@ -377,7 +378,7 @@ int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int g
   const size_t sm = static_cast<size_t>(ppi) * c * 3 * sizeof(float);
   gn_stats_nhwc<<<dim3(nblk, n), kStatThreads, sm, s>>>(x, c, spatial, groups, nblk, dpart);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
-  gn_finalize<double><<<n * groups, 128, 0, s>>>(dpart, nblk, c, groups, eps, gamma, beta,
+  gn_finalize<double><<<n * groups, kFinalizeThreads, 0, s>>>(dpart, nblk, c, groups, eps, gamma, beta,
                                                  scale, shift);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(2);
@@ -402,7 +403,7 @@ int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int
   Carver cv(ws, ~size_t(0));
   float *scale = cv.take<float>(static_cast<size_t>(n) * c);
   float *shift = cv.take<float>(static_cast<size_t>(n) * c);
-  gn_finalize<float><<<n * groups, 128, 0, s>>>(part, slots, c, groups, eps, gamma, beta, scale,
+  gn_finalize<float><<<n * groups, kFinalizeThreads, 0, s>>>(part, slots, c, groups, eps, gamma, beta, scale,
                                                 shift);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   VAE_TRY(launch_apply_nhwc(x, n, c, spatial, scale, shift, silu, round_out, residual, y, s));
