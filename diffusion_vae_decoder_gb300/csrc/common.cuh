@@ -155,6 +155,12 @@ int head_gn_silu_conv(const float *x, int n, int h, int w, int c, const float *s
                       const float *shift, const float *wpk, const float *bias, int cout,
                       float *y, cudaStream_t s);
 
+// Fused attention (flash.cu): O = softmax(Q K^T * scale) V for one head of
+// width d; q, k token-major [L][ld]; vt [d][ldv] (zero beyond L); out [L][ldo].
+bool flash_supported(int d);
+int flash_attention(const float *q, const float *k, int ld, const float *vt, int ldv, int L, int d,
+                    float scale, float *out, int ldo, cudaStream_t s);
+
 // Row softmax in place: s[r][:L] <- softmax(scale * s[r][:L]), TF32-rounded.
 int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st);
 

@@ -4,6 +4,8 @@
 // layout the tensor-core kernel reads, packs its weights (TF32-rounded) into
 // the caller's workspace, and enqueues kernels on the caller's stream.
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 #include <vector>
 
 #include "common.cuh"
@@ -125,6 +127,23 @@ size_t attn_ws_bytes(int n, int c, int L, int layout) {
   return cv.used;
 }
 
+// Which attention path runs. The fused kernel keeps S on chip but TMEM holds
+// at most a 256-column slice of O next to S, so a wider head recomputes S once
+// per slice (1.5x the FLOPs at c = 512); measured on GB300 at 16384 tokens,
+// c = 512, that is 1.71 ms against 1.37 ms for the score-matrix path (GEMM,
+// row softmax, GEMM). Default: fused when the head fits one slice.
+// VAE_ATTN=flash or VAE_ATTN=unfused forces a path (profiling comparisons).
+bool use_fused_attention(int c) {
+  static const int mode = [] {
+    const char *e = std::getenv("VAE_ATTN");
+    if (e && std::strcmp(e, "unfused") == 0) return 1;
+    if (e && std::strcmp(e, "flash") == 0) return 2;
+    return 0;
+  }();
+  if (!flash_supported(c) || mode == 1) return false;
+  return mode == 2 || c <= 256;
+}
+
 // Attention on NHWC data (token-major): x_nhwc [n][L][c] -> y_nhwc (may equal
 // x_nhwc). Weights are pre-packed: wqkv [3c][c], bqkv [3c], wo [c][c].
 int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
@@ -152,10 +171,17 @@ int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
     VAE_TRY(igemm_launch(d, s));
   }
   if (lp != L) VAE_CUDA_TRY(cudaMemsetAsync(sc.vt, 0, static_cast<size_t>(c) * lp * 4, s));
+  const bool fused = use_fused_attention(c);
   for (int b = 0; b < n; ++b) {
     const float *qkv_b = sc.qkv + static_cast<size_t>(b) * L * 3 * c;
     // V^T [c][L] (row stride lp): the K-major B operand of P.V.
     VAE_TRY(transpose(qkv_b + 2 * c, 0, 3 * c, sc.vt, 0, lp, 1, L, c, 1.0f, 0.0f, 0, s));
+    if (fused) {  // scores stay on chip
+      VAE_TRY(flash_attention(qkv_b, qkv_b + c, 3 * c, sc.vt, lp, L, c,
+                              1.0f / std::sqrt(static_cast<float>(c)),
+                              sc.o + static_cast<size_t>(b) * L * c, c, s));
+      continue;
+    }
     // S = q k^T (scale applied inside the softmax).
     {
       IgemmDesc d;
