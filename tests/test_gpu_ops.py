@@ -250,3 +250,38 @@ def test_mid_attn_growing_scores_exercise_rescaling(c, h, w):
     # is twice that model.
     m = metrics(got - x, ref - x)
     assert m["cos"] >= 0.99999 and m["rel_l2"] <= 2.5e-3, m
+
+
+_FORCED_FLASH = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, {root!r})
+import oracle as O, vae_synth as S
+import diffusion_vae_decoder_gb300 as pkg
+from tests._parity import metrics
+for (n, c, h, w) in [(1, 512, 16, 20), (2, 256, 9, 15)]:
+    x = S.make_normal((n, c, h, w), 33)
+    wt = S.make_attn_params(c, 34)
+    p = {{k: (wt[k + ".weight"], wt[k + ".bias"]) for k in
+         ("group_norm", "to_q", "to_k", "to_v", "to_out")}}
+    pd = {{k: (torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()) for k, (a, b) in p.items()}}
+    got = pkg.vae_mid_attn(torch.from_numpy(x).cuda(), pd).cpu().numpy()
+    ref = O.mid_attention(x, p)
+    m = metrics(got - x, ref - x)
+    assert m["cos"] >= 0.99999 and m["rel_l2"] <= 1e-3, (c, m)
+assert pkg.vae_device_error() == 0
+print("ok")
+"""
+
+
+def test_fused_attention_forced_on_wide_heads():
+    """The fused kernel on heads wider than one TMEM slice (c = 512: two
+    256-column output slices, S recomputed per slice), selected with
+    VAE_ATTN=flash in a child process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, VAE_ATTN="flash")
+    r = subprocess.run([sys.executable, "-c", _FORCED_FLASH.format(root=root)], env=env,
+                       cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
