@@ -294,6 +294,12 @@ def run_ours(args):
     launches = launches_per_decode * args.steps
     ms = e0.elapsed_time(e1) / args.steps
     recs = chain.profile_read()  # the events of the last replay
+    if args.detail and rank == 0:
+        for i, r in enumerate(recs):
+            rate = (f"{r['flops'] / r['ms'] / 1e9:8.1f} TF/s" if r["flops"] else
+                    f"{r['bytes'] / r['ms'] / 1e6:8.1f} GB/s")
+            print(f"step {i:3d} {r['kind']:14s} kernels {r['kernels']:2d} {r['ms']:8.4f} ms {rate}",
+                  file=sys.stderr)
     chain.profile(False)
     assert pkg.vae_device_error() == 0
     ms_max = reduce_max(ms, dist)
@@ -444,6 +450,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decoder_1024")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--detail", action="store_true",
+                    help="also print every profiled step of one decode (stderr)")
     ap.add_argument("--op", choices=["conv", "upsample_conv", "groupnorm"], default=None,
                     help="time one op of the single-op sweep instead of the decoder")
     ap.add_argument("--c", type=int, default=128)

@@ -311,7 +311,9 @@ DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, 
   d.H = cv.take<float>(p.max_elems);
   d.ss = cv.take<float>(2ull * n * std::max(p.max_c, ch.norm_out.c));
   d.split = cv.take<float>(kSplitWsFloats);
-  d.part = cv.take<float>(static_cast<size_t>(n) * ch.groups * std::max(1ll, p.max_slots) * 3);
+  // slots: the largest tile-based count, and at least the 1024 CTAs a split-K
+  // reduce may use
+  d.part = cv.take<float>(static_cast<size_t>(n) * ch.groups * std::max(1024ll, p.max_slots) * 3);
   const size_t nl = static_cast<size_t>(n) * p.attn_l;
   const size_t lp = static_cast<size_t>(round_up32(p.attn_l));
   const int c = p.attn_c;
@@ -369,15 +371,17 @@ int run_conv(Profiler &prof, const ConvW &c, const float *in, int n, int h, int 
   d.split_ws = split;
   d.split_ws_floats = split ? kSplitWsFloats : 0;
   int fused = 0;
+  long long slots = 0;
   if (st) {
     d.stat_part = part;
     d.stat_groups = groups;
     d.stat_ok = &fused;
+    d.stat_slots = &slots;
   }
   const int rc = igemm_launch(d, s);
   if (st) {
-    st->ready = rc == VAE_OK && fused;
-    st->slots = st->ready ? igemm_stat_slots(d) : 0;
+    st->ready = rc == VAE_OK && fused && slots > 0;
+    st->slots = st->ready ? slots : 0;
   }
   return rc;
 }

@@ -94,11 +94,19 @@ struct IgemmDesc {
   float *stat_part = nullptr;
   int stat_groups = 0;
   int *stat_ok = nullptr;  // set on the host: 1 if the statistics were requested and fused
+  long long *stat_slots = nullptr;  // set on the host: partial slots per (sample, group)
   // Optional split-K workspace (NHWC Conv / Upsample with ldo == cout): used
   // when the output tiles alone would leave most SMs idle.
   float *split_ws = nullptr;
   size_t split_ws_floats = 0;
 };
+// Split-K reduce (splitk.cu): out = alpha * sum of the partials + bias
+// (+ residual), rounded on request; GroupNorm partials [samples][groups][slots]
+// of the result when stat_part is given (*stat_slots receives slots, 0 if none).
+int splitk_reduce(const float *part, int splits, long long split_stride, int samples,
+                  long long rows_per_sample, int cout, const float *bias, float alpha,
+                  const float *residual, int round, float *out, float *stat_part,
+                  int stat_groups, long long *stat_slots, cudaStream_t s);
 // Split-K workspace that always suffices for one conv (floats).
 constexpr size_t kSplitWsFloats = 160ull * 65536;
 size_t igemm_smem_bytes(int bn);

@@ -268,6 +268,69 @@ __global__ void gn_apply_nchw(const float *__restrict__ x, long long total, int 
   }
 }
 
+// Finalize and apply in one kernel, for few partials per group: every CTA
+// merges its sample's partials into shared scale/shift, then runs the same
+// vectorised apply loop as gn_apply_nhwc.
+constexpr int kFusedMaxSlots = 64;  // above this, finalize + apply measured faster
+
+__global__ void __launch_bounds__(256)
+    gn_apply_fused_nhwc(const float *__restrict__ x, unsigned per_sample4, int c,
+                        const float *__restrict__ part, int slots, int groups, float eps,
+                        const float *__restrict__ gamma, const float *__restrict__ beta, int silu,
+                        int round, const float *__restrict__ res, float *__restrict__ y) {
+  __shared__ __align__(16) float ssc[1024];
+  __shared__ __align__(16) float ssh[1024];
+  const int n = blockIdx.y;
+  const int cg = c / groups;
+  for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+    Triple acc{0.f, 0.f, 0.f};
+    const float *e = part + (static_cast<size_t>(n) * groups + g) * slots * 3;
+    for (int sl = 0; sl < slots; ++sl) acc = merge(acc, Triple{e[3 * sl], e[3 * sl + 1], e[3 * sl + 2]});
+    const float var = acc.n > 0.f ? acc.m2 / acc.n : 0.f;
+    const float rstd = rsqrtf(var + eps);
+    for (int ch = g * cg; ch < (g + 1) * cg; ++ch) {
+      const float a = rstd * gamma[ch];
+      ssc[ch] = a;
+      ssh[ch] = beta[ch] - acc.mean * a;
+    }
+  }
+  __syncthreads();
+  const size_t base4 = static_cast<size_t>(n) * per_sample4;
+  const float4 *xv = reinterpret_cast<const float4 *>(x) + base4;
+  float4 *yv = reinterpret_cast<float4 *>(y) + base4;
+  const float4 *rv = res ? reinterpret_cast<const float4 *>(res) + base4 : nullptr;
+  const unsigned i0 = blockIdx.x * 256u + threadIdx.x;
+  const unsigned stride = gridDim.x * 256u;
+  const int ch = static_cast<int>((i0 * 4u) % static_cast<unsigned>(c));
+  const float4 a = *reinterpret_cast<const float4 *>(ssc + ch);
+  const float4 b = *reinterpret_cast<const float4 *>(ssh + ch);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (unsigned i = i0; i < per_sample4; i += stride) {
+    const float4 v = __ldg(xv + i);
+    const float4 r = rv ? __ldg(rv + i) : zero;
+    float4 o;
+    o.x = rnd(act(fmaf(v.x, a.x, b.x), silu) + r.x, round);
+    o.y = rnd(act(fmaf(v.y, a.y, b.y), silu) + r.y, round);
+    o.z = rnd(act(fmaf(v.z, a.z, b.z), silu) + r.z, round);
+    o.w = rnd(act(fmaf(v.w, a.w, b.w), silu) + r.w, round);
+    yv[i] = o;
+  }
+}
+
+// Blocks per sample for the apply loops: a multiple of c / gcd(c, 1024) so
+// the loop stride (blocks * 1024 elements) is a multiple of c.
+long long apply_blocks(long long per4, int c, int n) {
+  long long g = std::min<long long>((per4 + 255) / 256, std::max(1ll, 8ll * num_sms() / n));
+  long long gcd = c, b2 = 1024;
+  while (b2) {
+    const long long t = gcd % b2;
+    gcd = b2;
+    b2 = t;
+  }
+  const long long unit = c / gcd;
+  return std::max(unit, g / unit * unit);
+}
+
 int launch_apply_nhwc(const float *x, int n, int c, long long spatial, const float *scale,
                       const float *shift, int silu, int round_out, const float *residual,
                       float *y, cudaStream_t s) {
@@ -400,11 +463,23 @@ int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int
       groups <= 0 || slots <= 0)
     return VAE_EINVAL;
   if (c % groups || c % 4 || c > 1024) return VAE_EUNSUPPORTED;
+  if (slots <= kFusedMaxSlots) {
+    const long long per4 = spatial * c / 4;
+    if (per4 > 0xffffffffll / 2) return VAE_EUNSUPPORTED;
+    const long long g = apply_blocks(per4, c, n);
+    if ((g * 1024) % c != 0) return VAE_EUNSUPPORTED;
+    gn_apply_fused_nhwc<<<dim3(static_cast<unsigned>(g), n), 256, 0, s>>>(
+        x, static_cast<unsigned>(per4), c, part, static_cast<int>(slots), groups, eps, gamma, beta,
+        silu, round_out, residual, y);
+    if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+    count_launches(1);
+    return VAE_OK;
+  }
   Carver cv(ws, ~size_t(0));
   float *scale = cv.take<float>(static_cast<size_t>(n) * c);
   float *shift = cv.take<float>(static_cast<size_t>(n) * c);
-  gn_finalize<float><<<n * groups, kFinalizeThreads, 0, s>>>(part, slots, c, groups, eps, gamma, beta, scale,
-                                                shift);
+  gn_finalize<float><<<n * groups, kFinalizeThreads, 0, s>>>(part, slots, c, groups, eps, gamma,
+                                                             beta, scale, shift);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   VAE_TRY(launch_apply_nhwc(x, n, c, spatial, scale, shift, silu, round_out, residual, y, s));
   count_launches(2);

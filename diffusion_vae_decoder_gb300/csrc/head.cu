@@ -11,6 +11,8 @@
 // after the normalisation); every thread accumulates four adjacent output
 // pixels, reading the halo with 16-byte loads and each weight once for all
 // four. The RGB result is written NCHW.
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -18,30 +20,38 @@ namespace vae {
 
 namespace {
 
-// Output tile 8 rows x 128 pixels; thread (ty, tx) computes pixels
+// Output tile TH rows x 128 pixels (TH = 8); thread (ty, tx) computes pixels
 // 4*tx .. 4*tx+3 of row ty. Channels are staged 16 at a time.
-constexpr int kTW = 128, kTH = 8, kCC = 16;
-constexpr int kHW = kTW + 2, kHH = kTH + 2;  // halo tile 10 x 130
-constexpr int kRow = 132;                    // padded halo row (16-byte aligned rows)
-constexpr int kChan = kHH * kRow;            // floats per staged channel
-constexpr size_t kHeadSmem = (kCC * kChan) * sizeof(float) + 9 * kCC * sizeof(float4);
-constexpr int kItems = kHH * kHW * (kCC / 4);  // float4 halo loads per chunk
-constexpr int kPer = (kItems + 255) / 256;      // per thread
+constexpr int kTW = 128, kCC = 16;
+constexpr int kHW = kTW + 2;  // halo width 130
+constexpr int kRow = 132;     // padded halo row (16-byte aligned rows)
 constexpr int kBatch = 7;
+template <int TH>
+struct HeadCfg {
+  static constexpr int kHH = TH + 2;                   // halo rows
+  static constexpr int kChan = kHH * kRow;             // floats per staged channel
+  static constexpr int kThr = TH * 32;                 // threads
+  static constexpr size_t kSmem = (kCC * kChan) * sizeof(float) + 9 * kCC * sizeof(float4);
+  static constexpr int kItems = kHH * kHW * (kCC / 4);  // float4 halo loads per chunk
+  static constexpr int kPer = (kItems + kThr - 1) / kThr;
+};
 
 // wpk: [C/32][9 taps][32 channels] x float4 (output channels padded to 4);
 // CO output channels are accumulated (CO <= 4).
-template <int CO>
-__global__ void __launch_bounds__(256)
+template <int CO, int TH>
+__global__ void __launch_bounds__(TH * 32)
     head_kernel(const float *__restrict__ x, int H, int W, int C, const float *__restrict__ scale,
                 const float *__restrict__ shift, const float4 *__restrict__ wpk,
                 const float *__restrict__ bias, float *__restrict__ y) {
   constexpr int cout = CO;
+  using HC = HeadCfg<TH>;
+  constexpr int kHH = HC::kHH, kChan = HC::kChan, kItems = HC::kItems, kPer = HC::kPer;
+  constexpr int kThr = HC::kThr;
   extern __shared__ float4 head_smem[];
   float *hal = reinterpret_cast<float *>(head_smem);
   float4 *wsm = reinterpret_cast<float4 *>(hal + kCC * kChan);
   const int n = blockIdx.z;
-  const int x0 = blockIdx.x * kTW, y0 = blockIdx.y * kTH;
+  const int x0 = blockIdx.x * kTW, y0 = blockIdx.y * TH;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   float acc[4][4];  // [pixel][output channel]
 #pragma unroll
@@ -60,7 +70,7 @@ __global__ void __launch_bounds__(256)
     // Each lane stores its four channels in an order rotated by its quad
     // index, so the transposing shared stores of a warp hit 32 distinct banks
     // (one channel plane is 8 banks from the next: kChan = 8 mod 32).
-    const int q4 = threadIdx.x & 3;  // fixed: the item stride 256 is a multiple of 4
+    const int q4 = threadIdx.x & 3;  // fixed: the item stride (threads) is a multiple of 4
     const int cq = c0 + q4 * 4;
     const float4 ga = __ldg(reinterpret_cast<const float4 *>(sc + cq));
     const float4 gb = __ldg(reinterpret_cast<const float4 *>(sh + cq));
@@ -71,7 +81,7 @@ __global__ void __launch_bounds__(256)
       bool in[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const int l = threadIdx.x + (b0 + u) * 256;
+        const int l = threadIdx.x + (b0 + u) * kThr;
         const int pix = l >> 2;
         const int gy = y0 + pix / kHW - 1, gx = x0 + pix % kHW - 1;
         in[u] = l < kItems && gy >= 0 && gy < H && gx >= 0 && gx < W;
@@ -81,7 +91,7 @@ __global__ void __launch_bounds__(256)
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const int l = threadIdx.x + (b0 + u) * 256;
+        const int l = threadIdx.x + (b0 + u) * kThr;
         if (l >= kItems) break;
         const int pix = l >> 2;
         float4 t = v[u];
@@ -103,7 +113,7 @@ __global__ void __launch_bounds__(256)
         }
       }
     }
-    for (int l = threadIdx.x; l < 9 * kCC; l += 256) {
+    for (int l = threadIdx.x; l < 9 * kCC; l += kThr) {
       const int tap = l / kCC, c = l % kCC;
       const int cg = c0 + c;
       wsm[l] = wpk[(cg / 32) * 288 + tap * 32 + (cg % 32)];
@@ -176,36 +186,51 @@ int head_pack_weights(const float *w, int cout, int cin, float *dst, cudaStream_
   return VAE_OK;
 }
 
+namespace {
+
+template <int CO, int TH>
+int launch_head(const float *x, int n, int h, int w, int c, const float *scale,
+                const float *shift, const float4 *wv, const float *bias, float *y,
+                cudaStream_t s) {
+  using HC = HeadCfg<TH>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(head_kernel<CO, TH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(HC::kSmem));
+  });
+  if (attr != cudaSuccess) return VAE_ECUDA;
+  if ((h + TH - 1) / TH > 65535) return VAE_EUNSUPPORTED;
+  dim3 grid((w + kTW - 1) / kTW, (h + TH - 1) / TH, n);
+  head_kernel<CO, TH><<<grid, HC::kThr, HC::kSmem, s>>>(x, h, w, c, scale, shift, wv, bias, y);
+  return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
+}
+
+template <int TH>
+int launch_head_co(int cout, const float *x, int n, int h, int w, int c, const float *scale,
+                   const float *shift, const float4 *wv, const float *bias, float *y,
+                   cudaStream_t s) {
+  switch (cout) {
+    case 1: return launch_head<1, TH>(x, n, h, w, c, scale, shift, wv, bias, y, s);
+    case 2: return launch_head<2, TH>(x, n, h, w, c, scale, shift, wv, bias, y, s);
+    case 3: return launch_head<3, TH>(x, n, h, w, c, scale, shift, wv, bias, y, s);
+    default: return launch_head<4, TH>(x, n, h, w, c, scale, shift, wv, bias, y, s);
+  }
+}
+
+}  // namespace
+
 int head_gn_silu_conv(const float *x, int n, int h, int w, int c, const float *scale,
                       const float *shift, const float *wpk, const float *bias, int cout,
                       float *y, cudaStream_t s) {
   if (!x || !scale || !shift || !wpk || !y || n <= 0 || h <= 0 || w <= 0) return VAE_EINVAL;
-  if (c % 32 || cout < 1 || cout > 4 || n > 65535 || (h + kTH - 1) / kTH > 65535)
-    return VAE_EUNSUPPORTED;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(head_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kHeadSmem)) != cudaSuccess ||
-        cudaFuncSetAttribute(head_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kHeadSmem)) != cudaSuccess ||
-        cudaFuncSetAttribute(head_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kHeadSmem)) != cudaSuccess ||
-        cudaFuncSetAttribute(head_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kHeadSmem)) != cudaSuccess)
-      return VAE_ECUDA;
-    attr_done = true;
-  }
-  dim3 grid((w + kTW - 1) / kTW, (h + kTH - 1) / kTH, n);
+  if (c % 32 || cout < 1 || cout > 4 || n > 65535) return VAE_EUNSUPPORTED;
   const float4 *wv = reinterpret_cast<const float4 *>(wpk);
-  switch (cout) {
-    case 1: head_kernel<1><<<grid, 256, kHeadSmem, s>>>(x, h, w, c, scale, shift, wv, bias, y); break;
-    case 2: head_kernel<2><<<grid, 256, kHeadSmem, s>>>(x, h, w, c, scale, shift, wv, bias, y); break;
-    case 3: head_kernel<3><<<grid, 256, kHeadSmem, s>>>(x, h, w, c, scale, shift, wv, bias, y); break;
-    default: head_kernel<4><<<grid, 256, kHeadSmem, s>>>(x, h, w, c, scale, shift, wv, bias, y); break;
-  }
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
-  count_launches(1);
-  return VAE_OK;
+  // 8-row tiles (2-row tiles measured slower even on small images: the halo
+  // overhead outweighs the extra CTAs)
+  const int rc = launch_head_co<8>(cout, x, n, h, w, c, scale, shift, wv, bias, y, s);
+  if (rc == VAE_OK) count_launches(1);
+  return rc;
 }
 
 }  // namespace vae

@@ -618,45 +618,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Sum of the split-K partial sums in a fixed order, then the epilogue:
-// out = alpha * sum + bias (+ residual), optionally TF32-rounded (NHWC rows).
-__global__ void splitk_reduce_kernel(const float4 *__restrict__ part, int splits, long long n4,
-                                     long long stride4, int cout, const float *__restrict__ bias,
-                                     float alpha, const float4 *__restrict__ res, int round,
-                                     float4 *__restrict__ out) {
-  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n4; i += gridDim.x * 256ll) {
-    float4 a = part[i];
-    for (int sp = 1; sp < splits; ++sp) {
-      const float4 b = part[i + sp * stride4];
-      a.x += b.x;
-      a.y += b.y;
-      a.z += b.z;
-      a.w += b.w;
-    }
-    const int col = static_cast<int>((i * 4) % cout);
-    float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (bias) bv = *reinterpret_cast<const float4 *>(bias + col);
-    a.x = fmaf(a.x, alpha, bv.x);
-    a.y = fmaf(a.y, alpha, bv.y);
-    a.z = fmaf(a.z, alpha, bv.z);
-    a.w = fmaf(a.w, alpha, bv.w);
-    if (res) {
-      const float4 r = res[i];
-      a.x += r.x;
-      a.y += r.y;
-      a.z += r.z;
-      a.w += r.w;
-    }
-    if (round) {
-      a.x = round_tf32(a.x);
-      a.y = round_tf32(a.y);
-      a.z = round_tf32(a.z);
-      a.w = round_tf32(a.w);
-    }
-    out[i] = a;
-  }
-}
-
 // ---------------------------------------------------------------- host side
 int pow2_at_least(int v) {
   int r = 1;
@@ -932,6 +893,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
     }
   }
   if (d.stat_ok) *d.stat_ok = kp.stat_part != nullptr;
+  if (d.stat_slots) *d.stat_slots = kp.stat_part ? kp.stat_slots : 0;
 
   int rc;
   switch (d.mode) {
@@ -940,14 +902,13 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
     default: rc = launch_mode<2>(bn, ta, tb, ts, to, tr, kp, stream); break;
   }
   if (rc != VAE_OK || kp.splits == 1) return rc;
-  const long long n4 = rows_total * d.cout / 4;
-  const long long blocks = std::min<long long>((n4 + 255) / 256, 8ll * num_sms());
-  splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const float4 *>(d.split_ws), kp.splits, n4, kp.split_stride / 4, d.cout,
-      d.bias, d.alpha, reinterpret_cast<const float4 *>(d.residual), d.round_out,
-      reinterpret_cast<float4 *>(d.out));
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
-  count_launches(1);
+  // Split-K: fixed-order reduce + epilogue (+ GroupNorm partials of the output).
+  long long slots = 0;
+  VAE_TRY(splitk_reduce(d.split_ws, kp.splits, kp.split_stride, d.imgs / kp.t,
+                        rows_total / (d.imgs / kp.t), d.cout, d.bias, d.alpha, d.residual,
+                        d.round_out, d.out, d.stat_part, d.stat_groups, &slots, stream));
+  if (d.stat_ok) *d.stat_ok = slots > 0;
+  if (d.stat_slots) *d.stat_slots = slots;
   return VAE_OK;
 }
 
