@@ -31,7 +31,14 @@
 //             floor((p + k - 1) / 2), so four TMA boxes per step build the
 //             tile and the upsampled tensor is never materialised.
 //   Gemm      row-major A [M, K] (token-major activations for attention).
+//   Halo      3x3 conv, 256-channel tiles of 128 pixels in one row: per
+//             32-channel chunk one 3 x 130-pixel box (the tile's rows with a
+//             one-pixel border) is staged once; each tap's A operand is a
+//             view starting at row ky * 130 + kx of that swizzled buffer, so
+//             the ring stages carry weights only.
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -79,21 +86,31 @@ struct KParams {
 
 // BN: output channels per tile (MMA N). MS: 128-row M sub-tiles per tile
 // sharing each B stage (1, or 2 for 128-channel convs: a 256-pixel tile keeps
-// the operand bytes per FLOP of a 128 x 256 tile).
-template <int BN, int MS>
+// the operand bytes per FLOP of a 128 x 256 tile). MODE 3 (halo conv): the
+// input tile of a 32-channel chunk is staged once, with a one-pixel halo
+// ((MS + 2) rows x 130 pixels, two buffers), and serves all nine taps; the
+// ring stages then carry weights only.
+template <int BN, int MS, int MODE = 0>
 struct Cfg {
-  static constexpr uint32_t A_BYTES = MS * kABytes;
+  static constexpr bool HALO = MODE == 3;
+  static constexpr uint32_t HALO_BYTES =
+      HALO ? ((MS + 2) * 130 * 128 + 1023) / 1024 * 1024 : 0;
+  static constexpr int HALO_BUFS = HALO ? 2 : 0;
+  static constexpr uint32_t A_BYTES = HALO ? 0 : MS * kABytes;
   static constexpr uint32_t B_BYTES = BN * 128;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  // Epilogue staging: 4 warps x 2 buffers x (32 rows x 128 bytes).
-  static constexpr uint32_t STAGING = 4 * 2 * 4096;
-  static constexpr int FIT = (232448 - 1024 - STAGING - 512) / STAGE_BYTES;
+  // Epilogue staging: 4 warps x NSTG buffers x (32 rows x 128 bytes).
+  static constexpr int NSTG = HALO ? 1 : 2;
+  static constexpr uint32_t STAGING = 4 * NSTG * 4096;
+  static constexpr int FIT =
+      (232448 - 1024 - STAGING - 1024 - HALO_BUFS * HALO_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
   static constexpr uint32_t ACC_COLS = BN * MS;  // TMEM columns of one accumulator set
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
   static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
-  static constexpr size_t SMEM = 1024 + STAGES * STAGE_BYTES + STAGING +
-                                 (2 * STAGES + 9) * sizeof(uint64_t) + 16;
+  static constexpr size_t SMEM = 1024 + HALO_BUFS * HALO_BYTES + STAGES * STAGE_BYTES + STAGING +
+                                 (2 * STAGES + 13) * sizeof(uint64_t) + 16;
+  static_assert(!HALO || STAGES >= 3, "halo mode needs a weight ring");
   static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -184,16 +201,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     igemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmO,
                  const __grid_constant__ CUtensorMap tmR, const KParams p) {
-  using C = Cfg<BN, MS>;
+  using C = Cfg<BN, MS, MODE>;
   constexpr int STAGES = C::STAGES;
+  constexpr bool kConv = MODE == 0 || MODE == 3;  // conv tiles (epilogue geometry)
   constexpr uint32_t STAGE_TX = C::STAGE_BYTES;
   constexpr uint32_t IDESC = idesc_tf32(kBM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *sA = smem;
-  uint8_t *sB = smem + STAGES * C::A_BYTES;
+  uint8_t *sH = smem;  // halo buffers (MODE 3)
+  uint8_t *sA = smem + C::HALO_BUFS * C::HALO_BYTES;
+  uint8_t *sB = sA + STAGES * C::A_BYTES;
   float *staging = reinterpret_cast<float *>(sB + STAGES * C::B_BYTES);  // 1024-aligned
   uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_BYTES + C::STAGING);
   uint64_t *empty = full + STAGES;
@@ -201,7 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *acc_empty = acc_full + 2;
   uint64_t *drain = acc_empty + 2;  // used only after an abort
   uint64_t *res_bar = drain + 1;    // one per epilogue warp: residual box landed
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(res_bar + 4);
+  uint64_t *a_full = res_bar + 4;   // MODE 3: halo buffer landed / free
+  uint64_t *a_empty = a_full + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(a_empty + 2);
   volatile uint32_t *abort = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -218,13 +239,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) mbar_init(&res_bar[q], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&a_full[b], 1);
+      mbar_init(&a_empty[b], 1);
+    }
     *abort = 0u;
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (MODE == 0 && p.sc_chunks > 0) prefetch_tmap(&tmS);
+    if (kConv && p.sc_chunks > 0) prefetch_tmap(&tmS);
     if (p.epi_tma) {
       prefetch_tmap(&tmO);
       if (p.has_res) prefetch_tmap(&tmR);
@@ -244,6 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       uint32_t pending = 0, pend_par = 0;  // stages with a copy issued, and its parity
+      uint32_t abuf = 0, aphase = 0;       // MODE 3 halo buffer ring
+      uint32_t a_pending = 0, a_par = 0;
       bool failed = false;
       for (int tile = blockIdx.x; tile < p.total_tiles && !failed; tile += gridDim.x) {
         const int mn = tile % (p.m_tiles * p.n_tiles);
@@ -260,6 +287,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           tx = rem % p.tiles_x;
         }
         const int n_idx = img / p.t, t_idx = img % p.t;
+        if constexpr (MODE == 3) {
+          // One halo tile per 32-channel chunk, then one weight stage per tap
+          // (no appended shortcut in this mode).
+          for (int cc = 0; cc < p.cin_chunks && !failed; ++cc) {
+            if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort)) {
+              raise_error(p, abort);
+              failed = true;
+              break;
+            }
+            mbar_arrive_expect_tx(&a_full[abuf], (MS + 2) * 130 * 128);
+            tma_load_4d(sH + abuf * C::HALO_BYTES, &tmA, &a_full[abuf], cc * 32, tx * p.bw - 1,
+                        ty * p.bh - 1, img);
+            a_pending |= 1u << abuf;
+            a_par = (a_par & ~(1u << abuf)) | (aphase << abuf);
+            if (++abuf == 2) {
+              abuf = 0;
+              aphase ^= 1u;
+            }
+            for (int tap = 0; tap < p.taps; ++tap) {
+              if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+                raise_error(p, abort);
+                failed = true;
+                break;
+              }
+              mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+              tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], tap * p.cin_pad + cc * 32,
+                          n0);
+              pending |= 1u << stage;
+              pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+          continue;
+        }
         for (int ks = ks0; ks < ks1; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
             raise_error(p, abort);
@@ -313,12 +377,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Let every copy this thread issued land before the CTA exits.
         for (int s = 0; s < STAGES; ++s)
           if (pending & (1u << s)) mbar_wait_drain(&full[s], (pend_par >> s) & 1u);
+        for (int b = 0; b < 2; ++b)
+          if (a_pending & (1u << b)) mbar_wait_drain(&a_full[b], (a_par >> b) & 1u);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
+      uint32_t abuf = 0, aphase = 0;
       int local = 0;
       bool failed = false, issued = false;
       for (int tile = blockIdx.x; tile < p.total_tiles && !failed; tile += gridDim.x, ++local) {
@@ -332,6 +399,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS;
         const int split = tile / (p.m_tiles * p.n_tiles);
         const int ks0 = split * p.ks_per, ks1 = min(ks0 + p.ks_per, p.k_stages);
+        if constexpr (MODE == 3) {
+          // Tap (ky, kx) of output sub-tile `sub` reads the 128 halo pixels
+          // starting at halo row sub + ky, column kx: a row offset into the
+          // swizzled halo buffer.
+          for (int cc = 0; cc < p.cin_chunks && !failed; ++cc) {
+            if (!mbar_wait(&a_full[abuf], aphase, abort)) {
+              raise_error(p, abort);
+              failed = true;
+              break;
+            }
+            const uint32_t hbase = smem_u32(sH + abuf * C::HALO_BYTES);
+            for (int tap = 0; tap < p.taps; ++tap) {
+              if (!mbar_wait(&full[stage], phase, abort)) {
+                raise_error(p, abort);
+                failed = true;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+              for (int sub = 0; sub < MS; ++sub) {
+                const uint64_t ad = sw128_kmajor_desc_row(hbase, (sub + tap / 3) * 130 + tap % 3);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  umma_tf32(d_tmem + sub * BN, ad + 2 * k, bd + 2 * k, IDESC,
+                            (cc != 0) || (tap != 0) || (k != 0));
+              }
+              issued = true;
+              umma_commit(&empty[stage]);
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+            if (failed) break;
+            umma_commit(&a_empty[abuf]);
+            if (++abuf == 2) {
+              abuf = 0;
+              aphase ^= 1u;
+            }
+          }
+          if (!failed) umma_commit(&acc_full[buf]);
+          continue;
+        }
         for (int ks = ks0; ks < ks1; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort)) {
             raise_error(p, abort);
@@ -369,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;
-    float *stg = staging + q * 2 * 1024;  // this warp's two 4 KB staging buffers
+    float *stg = staging + q * C::NSTG * 1024;  // this warp's 4 KB staging buffer(s)
     int sbuf = 0;
     uint32_t res_phase = 0;
     bool failed = false;
@@ -408,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rem = mt % per_img;
         const int ty = rem / p.tiles_x, tx = rem % p.tiles_x;
         int y, x;
-        if (MODE == 0) {
+        if (kConv) {
           y = ty * p.bh + msub / p.bw;
           x = tx * p.bw + msub % p.bw;
           valid = y < p.hout && x < p.wout;
@@ -471,14 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // TMA store reads (row r, 16-byte chunk j at j ^ (r % 8)); rows and
           // channels outside the tensor are clipped by the store.
           float *sb = stg + sbuf * 1024;
-          if (lane == 0) bulk_wait_read<1>();  // the store that used sb last is done
+          if (lane == 0) bulk_wait_read<C::NSTG - 1>();  // the store that used sb last is done
           __syncwarp();
           if (p.has_res) {
             if (lane == 0) {
               mbar_arrive_expect_tx(&res_bar[q], 4096);
               if (MODE == 2)
                 tma_load_2d(sb, &tmR, &res_bar[q], col0, bc1);
-              else if (MODE == 0)
+              else if (kConv)
                 tma_load_4d(sb, &tmR, &res_bar[q], col0, bc1, bc2, bc3);
               else
                 tma_load_5d(sb, &tmR, &res_bar[q], col0, bc1, bc2, bc3, bc4);
@@ -520,13 +631,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             if (MODE == 2)
               tma_store_2d(&tmO, sb, col0, bc1);
-            else if (MODE == 0)
+            else if (kConv)
               tma_store_4d(&tmO, sb, col0, bc1, bc2, bc3);
             else
               tma_store_5d(&tmO, sb, col0, bc1, bc2, bc3, bc4);
             bulk_commit();
           }
-          sbuf ^= 1;
+          if (C::NSTG == 2) sbuf ^= 1;
           if (MODE != 2 && p.stat_part) {
             const int per_img = p.tiles_x * p.tiles_y;
             const int img = mt / per_img;
@@ -629,7 +740,7 @@ template <int BN, int MODE, int MS>
 int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ts,
                  const CUtensorMap &to, const CUtensorMap &tr, const KParams &kp,
                  cudaStream_t stream) {
-  using C = Cfg<BN, MS>;
+  using C = Cfg<BN, MS, MODE>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -658,6 +769,15 @@ int launch_mode(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUte
     case 32: return launch_typed<32, MODE, 1>(ta, tb, ts, to, tr, kp, s);
     default: return launch_typed<16, MODE, 1>(ta, tb, ts, to, tr, kp, s);
   }
+}
+
+// VAE_CONV=taps turns the halo staging off (comparisons).
+bool halo_enabled() {
+  static const bool on = [] {
+    const char *e = std::getenv("VAE_CONV");
+    return !(e && std::strcmp(e, "taps") == 0);
+  }();
+  return on;
 }
 
 int pick_bn(int cout) {
@@ -895,9 +1015,32 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   if (d.stat_ok) *d.stat_ok = kp.stat_part != nullptr;
   if (d.stat_slots) *d.stat_slots = kp.stat_part ? kp.stat_slots : 0;
 
+  // Halo staging for 3x3 single-frame convs with 256-channel tiles spanning
+  // 128 pixels of a row: one 3 x 130-pixel box per 32-channel chunk serves
+  // all nine taps. Per reduction step shared memory then takes in 37.6 KB
+  // instead of 48 KB, while the MMAs read 48 KB from it; with the two near
+  // its bandwidth, that is 7-12% per conv on GB300. Measured slower (so left
+  // to the per-tap path): 128-channel tiles (two 128-row sub-tiles), and
+  // convs with an appended shortcut (its chunks get only the two halo
+  // buffers of prefetch).
+  const bool halo = d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 && kp.bw == 128 &&
+                    kp.splits == 1 && bn == 256 && kp.sc_chunks == 0 && halo_enabled();
+  if (halo) {
+    const uint64_t dims[4] = {static_cast<uint64_t>(d.a_c), static_cast<uint64_t>(d.win),
+                              static_cast<uint64_t>(d.hin), static_cast<uint64_t>(d.imgs)};
+    const uint64_t str[3] = {static_cast<uint64_t>(d.a_c) * 4,
+                             static_cast<uint64_t>(d.win) * d.a_c * 4,
+                             static_cast<uint64_t>(d.hin) * d.win * d.a_c * 4};
+    const uint32_t box[4] = {32, 130, static_cast<uint32_t>(kp.bh + 2), 1};
+    VAE_TRY(encode_tiled(&ta, d.a, 4, dims, str, box));
+  }
+
   int rc;
   switch (d.mode) {
-    case AMode::Conv: rc = launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream); break;
+    case AMode::Conv:
+      rc = halo ? launch_typed<256, 3, 1>(ta, tb, ts, to, tr, kp, stream)
+                : launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream);
+      break;
     case AMode::Upsample: rc = launch_mode<1>(bn, ta, tb, ts, to, tr, kp, stream); break;
     default: rc = launch_mode<2>(bn, ta, tb, ts, to, tr, kp, stream); break;
   }

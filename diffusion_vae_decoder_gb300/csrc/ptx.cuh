@@ -195,6 +195,16 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
+// The same descriptor for a view that starts `row` rows (128 bytes each) into
+// a 1024-byte-aligned buffer written with the 128-byte swizzle. The swizzle
+// is a function of the absolute shared-memory address (bits 4-6 XOR bits
+// 7-9), so the view needs only its start address; the matrix base offset
+// stays 0. (Pinned by the exact-integer tests of the halo-staged conv, whose
+// tap views start at rows 0, 1, 2, 130, 131, ...)
+__device__ __forceinline__ uint64_t sw128_kmajor_desc_row(uint32_t base, uint32_t row) {
+  return sw128_kmajor_desc(base + row * 128);
+}
+
 // Instruction descriptor of tcgen05.mma .kind::tf32: D f32 (bits 4-5 = 1),
 // A tf32 (bits 7-9 = 2), B tf32 (bits 10-12 = 2), both K-major (bits 15/16 =
 // 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.

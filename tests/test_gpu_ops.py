@@ -122,6 +122,106 @@ def test_conv2d_float_parity(layout, c, hw):
     assert_layer_parity(got, ref, f"conv2d c={c} hw={hw}")
 
 
+# 3x3 convs whose tiles span 128 pixels of a row (width > 64) with 129-256
+# output channels (256-channel tiles) and no appended shortcut stage one halo
+# box per 32-channel chunk for all nine taps. cin = 32 keeps the reduction
+# short enough that the op runs without split-K, so these shapes take that
+# path; widths 150 / 200 / 129 leave a ragged last tile in x, batch 2 and
+# heights 7 / 3 / 1 several rows of tiles.
+HALO_SHAPES = [(2, 32, 256, 7, 150), (1, 32, 256, 3, 200), (1, 32, 200, 4, 129),
+               (1, 32, 160, 1, 128)]
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("n,cin,cout,h,w", HALO_SHAPES)
+def test_conv2d_halo_exact_integer(layout, n, cin, cout, h, w):
+    x = S.integer_tensor((n, cin, h, w), 21, -3, 3)
+    wt = S.integer_tensor((cout, cin, 3, 3), 22, -2, 2)
+    b = S.integer_tensor((cout,), 23, -8, 8)
+    ref = O.conv2d(x, wt, b)
+    y = sentinel_like(out_shape(ref.shape, layout))
+    pkg().vae_conv2d(dev(to_layout(x, layout)), dev(wt), dev(b), layout=layout, out=y)
+    got = from_layout(y.cpu().numpy(), layout)
+    assert_all_written(got, "conv2d halo")
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("cout", [128, 256])
+def test_conv2d_halo_shortcut_and_residual_exact(cout):
+    """At halo-eligible widths: the conv with an appended 1x1 shortcut (per-tap
+    staging) and the in-place identity skip (halo staging when cout = 256)."""
+    n, cin, sc_c, h, w = 2, 32, 64, 5, 150
+    lay = pkg().VAE_NHWC
+    x = S.integer_tensor((n, cin, h, w), 24, -3, 3)
+    wt = S.integer_tensor((cout, cin, 3, 3), 25, -2, 2)
+    b = S.integer_tensor((cout,), 26, -4, 4)
+    sx = S.integer_tensor((n, sc_c, h, w), 27, -3, 3)
+    sw = S.integer_tensor((cout, sc_c, 1, 1), 28, -2, 2)
+    sb = S.integer_tensor((cout,), 29, -4, 4)
+    res = S.integer_tensor((n, cout, h, w), 30, -5, 5)
+    ref = O.conv2d(x, wt, b) + O.conv2d(sx, sw, sb)
+    y = sentinel_like(out_shape(ref.shape, lay))
+    pkg().vae_conv2d(dev(to_layout(x, lay)), dev(wt), dev(b), sc_x=dev(to_layout(sx, lay)),
+                     sc_w=dev(sw), sc_b=dev(sb), layout=lay, out=y)
+    got = from_layout(y.cpu().numpy(), lay)
+    assert_all_written(got)
+    np.testing.assert_array_equal(got, ref)
+    ref2 = O.conv2d(x, wt, b) + res
+    y2 = dev(to_layout(res, lay))
+    pkg().vae_conv2d(dev(to_layout(x, lay)), dev(wt), dev(b), residual=y2, layout=lay, out=y2)
+    np.testing.assert_array_equal(from_layout(y2.cpu().numpy(), lay), ref2)
+
+
+@pytest.mark.parametrize("c", [256, 512])
+def test_conv2d_halo_float_parity(c):
+    hw = 256  # enough tiles that no split-K is chosen
+    lay = pkg().VAE_NHWC
+    x = S.make_normal((1, c, hw, hw), 31)
+    wt, b = S.make_conv_params(c, c, 3, 32)
+    ref = O.conv2d(x, wt, b)
+    y = sentinel_like(out_shape(ref.shape, lay))
+    pkg().vae_conv2d(dev(to_layout(x, lay)), dev(wt), dev(b), layout=lay, out=y)
+    got = from_layout(y.cpu().numpy(), lay)
+    assert_all_written(got)
+    assert_layer_parity(got, ref, f"conv2d halo c={c}")
+
+
+_FORCED_TAPS = """
+import sys
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import oracle as O, vae_synth as S
+import diffusion_vae_decoder_gb300 as pkg
+pkg.load_library()
+lay = pkg.VAE_NHWC
+for (n, cin, cout, h, w) in [(2, 32, 256, 7, 150), (1, 32, 200, 4, 129)]:
+    x = S.integer_tensor((n, cin, h, w), 21, -3, 3)
+    wt = S.integer_tensor((cout, cin, 3, 3), 22, -2, 2)
+    b = S.integer_tensor((cout,), 23, -8, 8)
+    ref = O.conv2d(x, wt, b)
+    xd = torch.from_numpy(np.ascontiguousarray(np.moveaxis(x, 1, -1), dtype=np.float32)).cuda()
+    y = torch.empty((n, h, w, cout), device="cuda")
+    pkg.vae_conv2d(xd, torch.from_numpy(wt.astype(np.float32)).cuda(),
+                   torch.from_numpy(b.astype(np.float32)).cuda(), layout=lay, out=y)
+    np.testing.assert_array_equal(np.moveaxis(y.cpu().numpy(), -1, 1), ref)
+assert pkg.vae_device_error() == 0
+print("ok")
+"""
+
+
+def test_conv2d_per_tap_staging_forced():
+    """The per-tap staging path on the shapes above (the default picks halo
+    staging there), selected with VAE_CONV=taps in a child process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, VAE_CONV="taps")
+    r = subprocess.run([sys.executable, "-c", _FORCED_TAPS.format(root=root)], env=env,
+                       cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
 # ------------------------------------------------------------------ upsample + conv
 @pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("n,cin,cout,h,w", [(1, 32, 32, 4, 4), (2, 64, 80, 9, 37),
