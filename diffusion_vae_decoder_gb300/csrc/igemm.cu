@@ -36,6 +36,11 @@
 //             one-pixel border) is staged once; each tap's A operand is a
 //             view starting at row ky * 130 + kx of that swizzled buffer, so
 //             the ring stages carry weights only.
+//   Channel-major  3x3 conv, 128-channel tiles of 256 pixels: the MMA's M
+//             is the 128 output channels (weights as the A operand), N the
+//             256 pixels; per 32-channel chunk and kx one band of bh + 2
+//             rows serves the three ky taps (views from row ky * bw). The
+//             epilogue transposes each 32 x 32 block into pixel-major rows.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -84,7 +89,7 @@ struct KParams {
   int *err;
 };
 
-// BN: output channels per tile (MMA N). MS: 128-row M sub-tiles per tile
+// BN: output channels per tile (MMA N; MMA M in MODE 4). MS: 128-row M sub-tiles per tile
 // sharing each B stage (1, or 2 for 128-channel convs: a 256-pixel tile keeps
 // the operand bytes per FLOP of a 128 x 256 tile). MODE 3 (halo conv): the
 // input tile of a 32-channel chunk is staged once, with a one-pixel halo
@@ -93,10 +98,14 @@ struct KParams {
 template <int BN, int MS, int MODE = 0>
 struct Cfg {
   static constexpr bool HALO = MODE == 3;
+  static constexpr bool SWAP = MODE == 4;
+  // Separately buffered A operand (MODES 3 and 4): two buffers, each serving
+  // several reduction steps. MODE 4 holds (bh + 2) rows x bw pixels with
+  // bh * bw = 256, at most 64 KB (bw <= 128).
   static constexpr uint32_t HALO_BYTES =
-      HALO ? ((MS + 2) * 130 * 128 + 1023) / 1024 * 1024 : 0;
-  static constexpr int HALO_BUFS = HALO ? 2 : 0;
-  static constexpr uint32_t A_BYTES = HALO ? 0 : MS * kABytes;
+      HALO ? ((MS + 2) * 130 * 128 + 1023) / 1024 * 1024 : SWAP ? 65536 : 0;
+  static constexpr int HALO_BUFS = (HALO || SWAP) ? 2 : 0;
+  static constexpr uint32_t A_BYTES = (HALO || SWAP) ? 0 : MS * kABytes;
   static constexpr uint32_t B_BYTES = BN * 128;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   // Epilogue staging: 4 warps x NSTG buffers x (32 rows x 128 bytes).
@@ -110,7 +119,8 @@ struct Cfg {
   static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
   static constexpr size_t SMEM = 1024 + HALO_BUFS * HALO_BYTES + STAGES * STAGE_BYTES + STAGING +
                                  (2 * STAGES + 13) * sizeof(uint64_t) + 16;
-  static_assert(!HALO || STAGES >= 3, "halo mode needs a weight ring");
+  static_assert(!(HALO || SWAP) || STAGES >= 3, "buffered-A modes need a weight ring");
+  static_assert(!SWAP || (BN == 128 && MS == 2), "MODE 4 tiles are 128 channels x 256 pixels");
   static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -203,14 +213,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap tmR, const KParams p) {
   using C = Cfg<BN, MS, MODE>;
   constexpr int STAGES = C::STAGES;
-  constexpr bool kConv = MODE == 0 || MODE == 3;  // conv tiles (epilogue geometry)
+  constexpr bool kConv = MODE == 0 || MODE == 3 || MODE == 4;  // conv tiles (epilogue geometry)
   constexpr uint32_t STAGE_TX = C::STAGE_BYTES;
   constexpr uint32_t IDESC = idesc_tf32(kBM, BN);
+  constexpr uint32_t IDESC_SWAP = idesc_tf32(kBM, 256);  // MODE 4: M = channels, N = pixels
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *sH = smem;  // halo buffers (MODE 3)
+  uint8_t *sH = smem;  // A buffers (MODES 3 and 4)
   uint8_t *sA = smem + C::HALO_BUFS * C::HALO_BYTES;
   uint8_t *sB = sA + STAGES * C::A_BYTES;
   float *staging = reinterpret_cast<float *>(sB + STAGES * C::B_BYTES);  // 1024-aligned
@@ -220,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *acc_empty = acc_full + 2;
   uint64_t *drain = acc_empty + 2;  // used only after an abort
   uint64_t *res_bar = drain + 1;    // one per epilogue warp: residual box landed
-  uint64_t *a_full = res_bar + 4;   // MODE 3: halo buffer landed / free
+  uint64_t *a_full = res_bar + 4;   // MODES 3, 4: A buffer landed / free
   uint64_t *a_empty = a_full + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(a_empty + 2);
   volatile uint32_t *abort = tmem_slot + 1;
@@ -319,6 +330,58 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
+              }
+            }
+          }
+          continue;
+        }
+        if constexpr (MODE == 4) {
+          // Per 32-channel chunk and kx: one band of bh + 2 rows shifted by
+          // kx - 1 serves the three ky taps; then the shortcut chunks, one
+          // plain tile each.
+          const int chunks = p.cin_chunks + p.sc_chunks;
+          for (int cc = 0; cc < chunks && !failed; ++cc) {
+            const bool is_sc = cc >= p.cin_chunks;
+            const int nkx = is_sc ? 1 : 3;
+            for (int kx = 0; kx < nkx && !failed; ++kx) {
+              if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort)) {
+                raise_error(p, abort);
+                failed = true;
+                break;
+              }
+              uint8_t *a_dst = sH + abuf * C::HALO_BYTES;
+              if (!is_sc) {
+                mbar_arrive_expect_tx(&a_full[abuf], (p.bh + 2) * p.bw * 128);
+                tma_load_4d(a_dst, &tmA, &a_full[abuf], cc * 32, tx * p.bw + kx - 1,
+                            ty * p.bh - 1, img);
+              } else {
+                mbar_arrive_expect_tx(&a_full[abuf], p.bh * p.bw * 128);
+                tma_load_4d(a_dst, &tmS, &a_full[abuf], (cc - p.cin_chunks) * 32, tx * p.bw,
+                            ty * p.bh, img);
+              }
+              a_pending |= 1u << abuf;
+              a_par = (a_par & ~(1u << abuf)) | (aphase << abuf);
+              if (++abuf == 2) {
+                abuf = 0;
+                aphase ^= 1u;
+              }
+              const int nky = is_sc ? 1 : 3;
+              for (int ky = 0; ky < nky; ++ky) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+                  raise_error(p, abort);
+                  failed = true;
+                  break;
+                }
+                const int kcol = is_sc ? p.taps * p.cin_pad + (cc - p.cin_chunks) * 32
+                                       : (ky * 3 + kx) * p.cin_pad + cc * 32;
+                mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+                tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kcol, n0);
+                pending |= 1u << stage;
+                pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                  stage = 0;
+                  phase ^= 1u;
+                }
               }
             }
           }
@@ -443,6 +506,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!failed) umma_commit(&acc_full[buf]);
           continue;
         }
+        if constexpr (MODE == 4) {
+          // D[channel][pixel] += W[channel][k] . X[pixel][k]: the weight
+          // stage is the 128-row M operand, the pixel band the 256-row N
+          // operand, viewed from row ky * bw.
+          const int chunks = p.cin_chunks + p.sc_chunks;
+          bool first = true;
+          for (int cc = 0; cc < chunks && !failed; ++cc) {
+            const bool is_sc = cc >= p.cin_chunks;
+            const int nkx = is_sc ? 1 : 3;
+            for (int kx = 0; kx < nkx && !failed; ++kx) {
+              if (!mbar_wait(&a_full[abuf], aphase, abort)) {
+                raise_error(p, abort);
+                failed = true;
+                break;
+              }
+              const uint32_t abase = smem_u32(sH + abuf * C::HALO_BYTES);
+              const int nky = is_sc ? 1 : 3;
+              for (int ky = 0; ky < nky; ++ky) {
+                if (!mbar_wait(&full[stage], phase, abort)) {
+                  raise_error(p, abort);
+                  failed = true;
+                  break;
+                }
+                tc_fence_after();
+                const uint64_t wd = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
+                const uint64_t xd = sw128_kmajor_desc_row(abase, ky * p.bw);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  umma_tf32(d_tmem, wd + 2 * k, xd + 2 * k, IDESC_SWAP, !first || (k != 0));
+                first = false;
+                issued = true;
+                umma_commit(&empty[stage]);
+                if (++stage == STAGES) {
+                  stage = 0;
+                  phase ^= 1u;
+                }
+              }
+              if (failed) break;
+              umma_commit(&a_empty[abuf]);
+              if (++abuf == 2) {
+                abuf = 0;
+                aphase ^= 1u;
+              }
+            }
+          }
+          if (!failed) umma_commit(&acc_full[buf]);
+          continue;
+        }
         for (int ks = ks0; ks < ks1; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort)) {
             raise_error(p, abort);
@@ -502,6 +613,116 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = mn / p.n_tiles;
       const int n0 = (mn % p.n_tiles) * BN;
       float *const obase = p.out + split * p.split_stride;
+      if constexpr (MODE == 4) {
+        // Accumulator lanes are output channels, columns pixels: each lane
+        // owns one channel and reads 32 pixels at a time, transposing into
+        // the pixel-major staging block on its way to the TMA store.
+        const int per_img = p.tiles_x * p.tiles_y;
+        const int img = mt / per_img;
+        const int rem = mt % per_img;
+        const int ty = rem / p.tiles_x, tx = rem % p.tiles_x;
+        const int c0 = n0 + q * 32;  // this warp's first channel (warp-uniform)
+        const int ch = c0 + lane;
+        const bool ch_ok = ch < p.cout;
+        const float bch = (p.bias && ch_ok) ? __ldg(p.bias + ch) : 0.f;
+        const int lbw = __ffs(p.bw) - 1;  // bw is a power of two
+        // In-image mask of a 32-pixel chunk: lane j tests pixel j.
+        auto chunk_mask = [&](int mp0) -> uint32_t {
+          const int py = ty * p.bh + ((mp0 + lane) >> lbw);
+          const int px = tx * p.bw + ((mp0 + lane) & (p.bw - 1));
+          return __ballot_sync(0xffffffffu, py < p.hout && px < p.wout);
+        };
+        // Residual of a chunk: for pixel j the 32 lanes read 32 adjacent
+        // channels (one 128-byte line), so plain loads are coalesced; they
+        // are issued one chunk ahead of their use.
+        const float *rcol = (p.has_res && ch_ok)
+                                ? p.residual + static_cast<long long>(img) * p.hout * p.wout * p.ldo + ch
+                                : nullptr;
+        auto load_res = [&](int mp0, uint32_t mask, float(&dst)[32]) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int y = ty * p.bh + ((mp0 + j) >> lbw);
+            const int x = tx * p.bw + ((mp0 + j) & (p.bw - 1));
+            dst[j] = (rcol && ((mask >> j) & 1u))
+                         ? __ldcg(rcol + (static_cast<long long>(y) * p.wout + x) * p.ldo)
+                         : 0.f;
+          }
+        };
+        float rnext[32], rcur[32];
+        uint32_t mnext = chunk_mask(0);
+        if (p.has_res) load_res(0, mnext, rnext);
+        for (int pc = 0; pc < 8 && c0 < p.cout; ++pc) {
+          const uint32_t vmask = mnext;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rcur[j] = rnext[j];
+          if (pc + 1 < 8) {
+            mnext = chunk_mask((pc + 1) * 32);
+            if (p.has_res) load_res((pc + 1) * 32, mnext, rnext);
+          }
+          float v[32];
+          tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(buf * C::ACC_COLS + pc * 32),
+                         v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], p.alpha, bch);
+          const int mp0 = pc * 32;  // first pixel of the chunk within the tile
+          const int bx = tx * p.bw + (mp0 & (p.bw - 1)), by = ty * p.bh + (mp0 >> lbw);
+          float *sb = stg + sbuf * 1024;
+          if (lane == 0) bulk_wait_read<1>();  // the store that used sb last is done
+          __syncwarp();
+          // Pixel j is row j of the block, this lane's channel its column;
+          // the 128-byte swizzle puts 16-byte chunk (lane / 4) at
+          // (lane / 4) ^ (j % 8), so each row's 32 stores hit 32 banks.
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int idx = j * 32 + ((((lane >> 2) ^ (j & 7)) << 2) | (lane & 3));
+            float val = p.has_res ? v[j] + rcur[j] : v[j];
+            if (p.round_out) val = round_tf32(val);
+            sb[idx] = val;
+            v[j] = val;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&tmO, sb, c0, bx, by, img);
+            bulk_commit();
+          }
+          sbuf ^= 1;
+          if (p.stat_part) {
+            // (count, mean, M2) of each group (stat_cg adjacent lanes) over
+            // the chunk's in-image pixels; slot = (frame, tile, chunk).
+            const int nv = __popc(vmask);
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sum += ((vmask >> j) & 1u) ? v[j] : 0.f;
+            for (int o = 1; o < p.stat_cg; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float cnt = static_cast<float>(nv * p.stat_cg);
+            const float mean = cnt > 0.f ? __fdividef(sum, cnt) : 0.f;
+            float m2 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float d = v[j] - mean;
+              m2 = ((vmask >> j) & 1u) ? fmaf(d, d, m2) : m2;
+            }
+            for (int o = 1; o < p.stat_cg; o <<= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
+            if (ch_ok && (lane & (p.stat_cg - 1)) == 0) {
+              const long long slot =
+                  (static_cast<long long>(img % p.t) * per_img + rem) * 8 + pc;
+              float *o = p.stat_part +
+                         ((static_cast<long long>(img / p.t) * p.stat_groups + ch / p.stat_cg) *
+                              p.stat_slots + slot) * 3;
+              o[0] = cnt;
+              o[1] = mean;
+              o[2] = m2;
+            }
+          }
+        }
+        if (failed) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        continue;
+      }
       for (int sub = 0; sub < MS; ++sub) {
       const int msub = sub * 128 + m;  // row of the (MS x 128)-row tile
       bool valid;
@@ -771,8 +992,9 @@ int launch_mode(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUte
   }
 }
 
-// VAE_CONV=taps turns the halo staging off (comparisons).
-bool halo_enabled() {
+// VAE_CONV=taps turns the buffered-A modes (halo, channel-major) off, leaving
+// every conv on per-tap staging (comparisons).
+bool buffered_a_enabled() {
   static const bool on = [] {
     const char *e = std::getenv("VAE_CONV");
     return !(e && std::strcmp(e, "taps") == 0);
@@ -1024,7 +1246,24 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // convs with an appended shortcut (its chunks get only the two halo
   // buffers of prefetch).
   const bool halo = d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 && kp.bw == 128 &&
-                    kp.splits == 1 && bn == 256 && kp.sc_chunks == 0 && halo_enabled();
+                    kp.splits == 1 && bn == 256 && kp.sc_chunks == 0 && buffered_a_enabled();
+  // Channel-major tiles for 3x3 single-frame convs with 65-128 output
+  // channels: the MMA runs M = 128 channels x N = 256 pixels (one wide
+  // instruction where the pixel-major tile needs two 128 x 128 ones that both
+  // read the weights), and per 32-channel chunk one band of bh + 2 rows per
+  // kx serves the three ky taps. Needs the staged epilogue (it transposes).
+  const bool swap = !halo && d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 && bn == 128 &&
+                    kp.splits == 1 && epi && kp.bw >= 2 && buffered_a_enabled();
+  if (swap) {
+    const uint64_t dims[4] = {static_cast<uint64_t>(d.a_c), static_cast<uint64_t>(d.win),
+                              static_cast<uint64_t>(d.hin), static_cast<uint64_t>(d.imgs)};
+    const uint64_t str[3] = {static_cast<uint64_t>(d.a_c) * 4,
+                             static_cast<uint64_t>(d.win) * d.a_c * 4,
+                             static_cast<uint64_t>(d.hin) * d.win * d.a_c * 4};
+    const uint32_t box[4] = {32, static_cast<uint32_t>(kp.bw), static_cast<uint32_t>(kp.bh + 2),
+                             1};
+    VAE_TRY(encode_tiled(&ta, d.a, 4, dims, str, box));
+  }
   if (halo) {
     const uint64_t dims[4] = {static_cast<uint64_t>(d.a_c), static_cast<uint64_t>(d.win),
                               static_cast<uint64_t>(d.hin), static_cast<uint64_t>(d.imgs)};
@@ -1038,8 +1277,9 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   int rc;
   switch (d.mode) {
     case AMode::Conv:
-      rc = halo ? launch_typed<256, 3, 1>(ta, tb, ts, to, tr, kp, stream)
-                : launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream);
+      rc = halo   ? launch_typed<256, 3, 1>(ta, tb, ts, to, tr, kp, stream)
+           : swap ? launch_typed<128, 4, 2>(ta, tb, ts, to, tr, kp, stream)
+                  : launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream);
       break;
     case AMode::Upsample: rc = launch_mode<1>(bn, ta, tb, ts, to, tr, kp, stream); break;
     default: rc = launch_mode<2>(bn, ta, tb, ts, to, tr, kp, stream); break;

@@ -186,6 +186,68 @@ def test_conv2d_halo_float_parity(c):
     assert_layer_parity(got, ref, f"conv2d halo c={c}")
 
 
+# 3x3 convs with 65-128 output channels and NHWC output run channel-major
+# tiles (MMA M = channels, N = 256 pixels, bands of bh + 2 rows per kx) with a
+# transposing epilogue. Widths 150 / 33 / 17 / 5 give tile widths 128 / 64 /
+# 32 / 8 (bands of 4 / 6 / 10 / 34 rows); cout 96 and 72 leave epilogue warps
+# with partial or no channels.
+SWAP_SHAPES = [(2, 32, 128, 7, 150), (1, 32, 96, 5, 33), (1, 32, 128, 3, 17),
+               (1, 32, 72, 9, 5)]
+
+
+@pytest.mark.parametrize("n,cin,cout,h,w", SWAP_SHAPES)
+def test_conv2d_channel_major_exact_integer(n, cin, cout, h, w):
+    lay = pkg().VAE_NHWC
+    x = S.integer_tensor((n, cin, h, w), 41, -3, 3)
+    wt = S.integer_tensor((cout, cin, 3, 3), 42, -2, 2)
+    b = S.integer_tensor((cout,), 43, -8, 8)
+    ref = O.conv2d(x, wt, b)
+    y = sentinel_like(out_shape(ref.shape, lay))
+    pkg().vae_conv2d(dev(to_layout(x, lay)), dev(wt), dev(b), layout=lay, out=y)
+    got = from_layout(y.cpu().numpy(), lay)
+    assert_all_written(got, "conv2d channel-major")
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("cout", [128, 80])
+def test_conv2d_channel_major_shortcut_and_residual_exact(cout):
+    """Channel-major tiles with appended 1x1 shortcut chunks, and with the
+    in-place identity skip (residual read through the transposing staging)."""
+    n, cin, sc_c, h, w = 2, 32, 64, 5, 150
+    lay = pkg().VAE_NHWC
+    x = S.integer_tensor((n, cin, h, w), 44, -3, 3)
+    wt = S.integer_tensor((cout, cin, 3, 3), 45, -2, 2)
+    b = S.integer_tensor((cout,), 46, -4, 4)
+    sx = S.integer_tensor((n, sc_c, h, w), 47, -3, 3)
+    sw = S.integer_tensor((cout, sc_c, 1, 1), 48, -2, 2)
+    sb = S.integer_tensor((cout,), 49, -4, 4)
+    res = S.integer_tensor((n, cout, h, w), 50, -5, 5)
+    ref = O.conv2d(x, wt, b) + O.conv2d(sx, sw, sb)
+    y = sentinel_like(out_shape(ref.shape, lay))
+    pkg().vae_conv2d(dev(to_layout(x, lay)), dev(wt), dev(b), sc_x=dev(to_layout(sx, lay)),
+                     sc_w=dev(sw), sc_b=dev(sb), layout=lay, out=y)
+    got = from_layout(y.cpu().numpy(), lay)
+    assert_all_written(got)
+    np.testing.assert_array_equal(got, ref)
+    ref2 = O.conv2d(x, wt, b) + res
+    y2 = dev(to_layout(res, lay))
+    pkg().vae_conv2d(dev(to_layout(x, lay)), dev(wt), dev(b), residual=y2, layout=lay, out=y2)
+    np.testing.assert_array_equal(from_layout(y2.cpu().numpy(), lay), ref2)
+
+
+def test_conv2d_channel_major_float_parity():
+    c, hw = 128, 256  # enough tiles that no split-K is chosen
+    lay = pkg().VAE_NHWC
+    x = S.make_normal((1, c, hw, hw), 51)
+    wt, b = S.make_conv_params(c, c, 3, 52)
+    ref = O.conv2d(x, wt, b)
+    y = sentinel_like(out_shape(ref.shape, lay))
+    pkg().vae_conv2d(dev(to_layout(x, lay)), dev(wt), dev(b), layout=lay, out=y)
+    got = from_layout(y.cpu().numpy(), lay)
+    assert_all_written(got)
+    assert_layer_parity(got, ref, "conv2d channel-major c=128")
+
+
 _FORCED_TAPS = """
 import sys
 sys.path.insert(0, {root!r})
@@ -194,7 +256,8 @@ import oracle as O, vae_synth as S
 import diffusion_vae_decoder_gb300 as pkg
 pkg.load_library()
 lay = pkg.VAE_NHWC
-for (n, cin, cout, h, w) in [(2, 32, 256, 7, 150), (1, 32, 200, 4, 129)]:
+for (n, cin, cout, h, w) in [(2, 32, 256, 7, 150), (1, 32, 200, 4, 129),
+                             (2, 32, 128, 7, 150), (1, 32, 72, 9, 5)]:
     x = S.integer_tensor((n, cin, h, w), 21, -3, 3)
     wt = S.integer_tensor((cout, cin, 3, 3), 22, -2, 2)
     b = S.integer_tensor((cout,), 23, -8, 8)
@@ -211,7 +274,8 @@ print("ok")
 
 def test_conv2d_per_tap_staging_forced():
     """The per-tap staging path on the shapes above (the default picks halo
-    staging there), selected with VAE_CONV=taps in a child process."""
+    or channel-major staging there), selected with VAE_CONV=taps in a child
+    process."""
     import os
     import subprocess
     import sys
