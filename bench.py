@@ -412,7 +412,8 @@ def run_op(args):
     elif args.op == "upsample_conv":
         out = torch.empty((1, 2 * hw, 2 * hw, c), device="cuda")
         fn = lambda: pkg.vae_upsample_conv(x, wt, b, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
-        work, unit = 2.0 * c * c * 9 * 4 * hw * hw, "TFLOP/s"
+        # executed work: four parity 2x2 convs, 4 taps per output pixel
+        work, unit = 2.0 * c * c * 4 * 4 * hw * hw, "TFLOP/s"
     else:
         out = torch.empty_like(x)
         fn = lambda: pkg.vae_groupnorm_silu(x, g, be, layout=pkg.VAE_NHWC, out=out)  # noqa: E731

@@ -202,6 +202,23 @@ struct Builder {
     }
     return c;
   }
+  // Upsample conv: 3x3 weights packed as four parity-specific 2x2 kernels
+  // (k = 2 in the returned ConvW: 4 taps per output pixel).
+  ConvW upconv(const vae_conv_ref &r, int cin, int cout) {
+    ConvW c;
+    if (r.cin != cin || r.cout != cout || r.k != 3) fail(VAE_EINVAL);
+    if (status != VAE_OK) return c;
+    c.cin = cin;
+    c.cout = cout;
+    c.k = 2;
+    c.ldb = upsample_ldb(cin);
+    const float *wt = upload_tmp(r.weight, static_cast<size_t>(cout) * cin * 9);
+    c.w = dev<float>(4ull * cout * c.ldb);
+    if (status != VAE_OK) return c;
+    fail(pack_upsample_weights(wt, cout, cin, c.w, s));
+    if (r.bias) c.b = upload(r.bias, cout);
+    return c;
+  }
   ResW resnet(const vae_resnet_ref &r, int cin, int cout) {
     ResW w;
     if ((cin != cout) != (r.shortcut.weight != nullptr)) fail(VAE_EINVAL);
@@ -457,8 +474,7 @@ int vae_chain_prepare(const vae_chain_args *a, void **handle, vae_stream_t strea
     }
     uw.has_up = u.upsample_conv.weight != nullptr;
     if (uw.has_up) {
-      uw.up = b.conv(u.upsample_conv, c, u.upsample_conv.cout);
-      if (uw.up.k != 3) b.fail(VAE_EINVAL);
+      uw.up = b.upconv(u.upsample_conv, c, u.upsample_conv.cout);
       c = u.upsample_conv.cout;
     }
     ch->ups.push_back(std::move(uw));

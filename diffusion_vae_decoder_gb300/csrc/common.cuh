@@ -121,6 +121,11 @@ int pack_conv_weights(const float *w, int cout, int cin, int taps, const float *
 inline int packed_ldb(int cin, int taps, int sc_cin) {
   return taps * round_up32(cin) + (sc_cin ? round_up32(sc_cin) : 0);
 }
+// Upsample conv weights as four parity-specific 2x2 kernels (layout.cu):
+// w [cout][cin][3][3] -> dst [4 parities][cout][upsample_ldb(cin)], K index
+// (a * 2 + b) * cin_pad + c, parity = py * 2 + px.
+inline int upsample_ldb(int cin) { return 4 * round_up32(cin); }
+int pack_upsample_weights(const float *w, int cout, int cin, float *dst, cudaStream_t s);
 
 // Layout transforms (layout.cu). src [outer][rows][cols] (row stride src_ld)
 // -> dst [outer][cols][rows] (row stride dst_ld), dst = src * alpha + beta,

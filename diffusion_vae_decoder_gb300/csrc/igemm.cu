@@ -25,11 +25,13 @@
 //   Conv      NHWC input, k x k (x kt causal) taps; the 1x1 resnet shortcut is
 //             appended as extra reduction steps over its own input.
 //   Upsample  nearest-2x upsample folded into a 3x3 conv (cortiq-engine
-//             "Module vae", VaeUpRef). Output rows of a tile are ordered by
-//             output-pixel parity (py, px); for each parity and tap the needed
-//             low-resolution pixels form a plain R x P box offset by
-//             floor((p + k - 1) / 2), so four TMA boxes per step build the
-//             tile and the upsampled tensor is never materialised.
+//             "Module vae", VaeUpRef). Every output pixel of parity (py, px)
+//             sees its 3x3 taps land on only 2 x 2 distinct low-res pixels
+//             (tap ky reads low-res row offset floor((py + ky - 1) / 2)), so
+//             the layer is four 2x2 convs of the low-res input with summed
+//             weights: 4 instead of 9 taps per output pixel. A tile is a
+//             block of low-res pixels of one parity; each step is one plain
+//             TMA box, and the upsampled tensor is never materialised.
 //   Gemm      row-major A [M, K] (token-major activations for attention).
 //   Halo      3x3 conv, 256-channel tiles of 128 pixels in one row: per
 //             32-channel chunk one 3 x 130-pixel box (the tile's rows with a
@@ -59,7 +61,7 @@ constexpr uint32_t kABytes = kBM * 128;
 
 struct KParams {
   int imgs, t, hin, win, hout, wout;
-  int bh, bw;  // Conv: tile rows/cols of output pixels; Upsample: R, P (low-res box)
+  int bh, bw;  // tile rows / cols (Conv: output pixels; Upsample: low-res pixels)
   int tiles_x, tiles_y;
   int m_tiles, n_tiles, total_tiles;
   int M;
@@ -289,11 +291,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mt = mn / p.n_tiles;
         const int n0 = (mn % p.n_tiles) * BN;
         const int ks0 = split * p.ks_per, ks1 = min(ks0 + p.ks_per, p.k_stages);
-        int img = 0, ty = 0, tx = 0;
+        int img = 0, ty = 0, tx = 0, par = 0;
         if (MODE != 2) {
-          const int per_img = p.tiles_x * p.tiles_y;
+          const int per_img = p.tiles_x * p.tiles_y * (MODE == 1 ? 4 : 1);
           img = mt / per_img;
-          const int rem = mt % per_img;
+          int rem = mt % per_img;
+          if (MODE == 1) {  // the four output parities of a low-res tile are adjacent tiles
+            par = rem & 3;
+            rem >>= 2;
+          }
           ty = rem / p.tiles_x;
           tx = rem % p.tiles_x;
         }
@@ -414,16 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(b_dst, &tmB, &full[stage], p.taps * p.cin_pad + cc * 32, n0);
             }
           } else if (MODE == 1) {
+            // 2x2 tap (a, b) of parity (py, px) reads the low-res tile shifted
+            // by (py - 1 + a, px - 1 + b); weights of that parity's kernel.
             const int tap = ks / p.cin_chunks, cc = ks % p.cin_chunks;
-            const int ky = tap / 3, kx = tap % 3;
-#pragma unroll
-            for (int ph = 0; ph < 4; ++ph) {
-              const int oy = ((ph >> 1) + ky - 1) >> 1;  // floor((py + ky - 1) / 2)
-              const int ox = ((ph & 1) + kx - 1) >> 1;
-              tma_load_4d(a_dst + ph * 4096, &tmA, &full[stage], cc * 32, tx * p.bw + ox,
-                          ty * p.bh + oy, img);
-            }
-            tma_load_2d(b_dst, &tmB, &full[stage], tap * p.cin_pad + cc * 32, n0);
+            tma_load_4d(a_dst, &tmA, &full[stage], cc * 32, tx * p.bw + (par & 1) - 1 + (tap & 1),
+                        ty * p.bh + (par >> 1) - 1 + (tap >> 1), img);
+            tma_load_2d(b_dst, &tmB, &full[stage], tap * p.cin_pad + cc * 32, par * p.cout + n0);
           } else {
             tma_load_2d(a_dst, &tmA, &full[stage], ks * 32, mt * kBM);
             tma_load_2d(b_dst, &tmB, &full[stage], ks * 32, n0);
@@ -735,9 +737,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         valid = row < p.M;
         bc1 = mt * kBM + q * 32;
       } else {
-        const int per_img = p.tiles_x * p.tiles_y;
+        const int per_img = p.tiles_x * p.tiles_y * (MODE == 1 ? 4 : 1);
         const int img = mt / per_img;
-        const int rem = mt % per_img;
+        int rem = mt % per_img;
+        const int par = MODE == 1 ? (rem & 3) : 0;
+        if (MODE == 1) rem >>= 2;
         const int ty = rem / p.tiles_x, tx = rem % p.tiles_x;
         int y, x;
         if (kConv) {
@@ -748,15 +752,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           bc2 = ty * p.bh + (sub * 128 + q * 32) / p.bw;
           bc3 = img;
         } else {
-          const int ph = m >> 5, r = m & 31;
-          const int yl = ty * p.bh + r / p.bw, xl = tx * p.bw + r % p.bw;
-          y = 2 * yl + (ph >> 1);
-          x = 2 * xl + (ph & 1);
+          // rows are low-res pixels of the tile; all share the parity par
+          const int yl = ty * p.bh + msub / p.bw, xl = tx * p.bw + msub % p.bw;
+          y = 2 * yl + (par >> 1);
+          x = 2 * xl + (par & 1);
           valid = yl < p.hin && xl < p.win;
-          bc1 = q & 1;  // px of this warp's parity block
-          bc2 = tx * p.bw;
-          bc3 = q >> 1;  // py
-          bc4 = img * p.hin + ty * p.bh;
+          const int r0 = sub * 128 + q * 32;  // this warp's first row
+          bc1 = par & 1;                      // px
+          bc2 = tx * p.bw + r0 % p.bw;        // xl
+          bc3 = par >> 1;                     // py
+          bc4 = img * p.hin + ty * p.bh + r0 / p.bw;
         }
         row = (static_cast<long long>(img) * p.hout + y) * p.wout + x;
         const long long hw = static_cast<long long>(p.hout) * p.wout;
@@ -860,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (C::NSTG == 2) sbuf ^= 1;
           if (MODE != 2 && p.stat_part) {
-            const int per_img = p.tiles_x * p.tiles_y;
+            const int per_img = p.tiles_x * p.tiles_y * (MODE == 1 ? 4 : 1);
             const int img = mt / per_img;
             const long long slot =
                 ((static_cast<long long>(img % p.t) * per_img + mt % per_img) * MS + sub) * 4 + q;
@@ -984,7 +989,7 @@ int launch_mode(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUte
   switch (bn) {
     case 256: return launch_typed<256, MODE, 1>(ta, tb, ts, to, tr, kp, s);
     case 128:
-      return MODE == 0 ? launch_typed<128, MODE, 2>(ta, tb, ts, to, tr, kp, s)
+      return MODE != 2 ? launch_typed<128, MODE, 2>(ta, tb, ts, to, tr, kp, s)
                        : launch_typed<128, MODE, 1>(ta, tb, ts, to, tr, kp, s);
     case 64: return launch_typed<64, MODE, 1>(ta, tb, ts, to, tr, kp, s);
     case 32: return launch_typed<32, MODE, 1>(ta, tb, ts, to, tr, kp, s);
@@ -1016,14 +1021,12 @@ long long igemm_stat_slots(const IgemmDesc &d) {
   const int bn = pick_bn(d.cout);
   long long tiles;
   int ms = 1;
-  if (d.mode == AMode::Conv) {
+  if (d.mode == AMode::Conv || d.mode == AMode::Upsample) {
     ms = bn == 128 ? 2 : 1;
     const int bw = std::min(128, pow2_at_least(d.win));
     const int bh = ms * kBM / bw;
     tiles = static_cast<long long>(ceil_div(d.win, bw)) * ceil_div(d.hin, bh);
-  } else if (d.mode == AMode::Upsample) {
-    const int pw = std::min(32, pow2_at_least(d.win));
-    tiles = static_cast<long long>(ceil_div(d.win, pw)) * ceil_div(d.hin, 32 / pw);
+    if (d.mode == AMode::Upsample) tiles *= 4;  // one tile per output parity
   } else {
     return 0;
   }
@@ -1105,11 +1108,15 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
       box[2] = kp.bh;
       box[3] = 1;
     } else {
-      kp.taps = 9;
+      // Nearest-2x upsample + 3x3 conv as four parity-specific 2x2 convs of
+      // the low-res input (weights packed by pack_upsample_weights): a tile
+      // is bw x bh low-res pixels of one output parity.
+      kp.taps = 4;
       kp.hout = 2 * d.hin;
       kp.wout = 2 * d.win;
-      kp.bw = std::min(32, pow2_at_least(d.win));  // P
-      kp.bh = 32 / kp.bw;                          // R
+      const int rows = (bn == 128 ? 2 : 1) * kBM;
+      kp.bw = std::min(128, pow2_at_least(d.win));
+      kp.bh = rows / kp.bw;
       kp.tiles_x = ceil_div(d.win, kp.bw);
       kp.tiles_y = ceil_div(d.hin, kp.bh);
       box[0] = 32;
@@ -1117,7 +1124,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
       box[2] = kp.bh;
       box[3] = 1;
     }
-    kp.m_tiles = d.imgs * kp.tiles_x * kp.tiles_y;
+    kp.m_tiles = d.imgs * kp.tiles_x * kp.tiles_y * (d.mode == AMode::Upsample ? 4 : 1);
     kp.k_stages = kp.taps * kp.cin_chunks + kp.sc_chunks;
     const uint64_t dims[4] = {static_cast<uint64_t>(d.a_c), static_cast<uint64_t>(d.win),
                               static_cast<uint64_t>(d.hin), static_cast<uint64_t>(d.imgs)};
@@ -1139,7 +1146,9 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   }
   if (d.ldb % 4 || bkdim <= 0) return VAE_EINVAL;
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(bkdim), static_cast<uint64_t>(d.cout)};
+    // Upsample: four parities' weight rows, parity-major
+    const uint64_t brows = static_cast<uint64_t>(d.cout) * (d.mode == AMode::Upsample ? 4 : 1);
+    const uint64_t dims[2] = {static_cast<uint64_t>(bkdim), brows};
     const uint64_t str[1] = {static_cast<uint64_t>(d.ldb) * 4};
     const uint32_t box[2] = {32, static_cast<uint32_t>(bn)};
     VAE_TRY(encode_tiled(&tb, d.b, 2, dims, str, box));
@@ -1208,12 +1217,13 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
         const uint32_t box[4] = {32, bw, 32 / bw, 1};
         return encode_tiled(m, base, 4, dims, str, box);
       }
-      // Upsample: output [imgs*hin][py][win][px][cout], box (32, 1, P, 1, R).
+      // Upsample: output [imgs*hin][py][win][px][cout]; a warp's 32 rows of
+      // one parity are box (32, 1, min(bw, 32), 1, 32 / min(bw, 32)).
+      const uint32_t bw = std::min(kp.bw, 32);
       const uint64_t dims[5] = {static_cast<uint64_t>(d.cout), 2, static_cast<uint64_t>(d.win),
                                 2, static_cast<uint64_t>(d.imgs) * d.hin};
       const uint64_t str[4] = {ld4, 2 * ld4, ld4 * kp.wout, 2 * ld4 * kp.wout};
-      const uint32_t box[5] = {32, 1, static_cast<uint32_t>(kp.bw), 1,
-                               static_cast<uint32_t>(kp.bh)};
+      const uint32_t box[5] = {32, 1, bw, 1, 32 / bw};
       return encode_tiled(m, base, 5, dims, str, box);
     };
     VAE_TRY(encode_out(&to, d.out));

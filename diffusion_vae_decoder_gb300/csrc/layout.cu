@@ -34,6 +34,34 @@ __global__ void pack_kernel(const float *__restrict__ w, int cout, int cin, int 
   }
 }
 
+// Nearest-2x upsample followed by a 3x3 conv, per output parity (py, px): the
+// taps ky that land on low-res row offset py - 1 + a (a = 0, 1) are those with
+// floor((py + ky - 1) / 2) = py - 1 + a, and likewise for kx. Their weights
+// act on the same input pixel, so they are summed into a 2x2 kernel:
+// dst[par][o][(a * 2 + b) * cin_pad + c], par = py * 2 + px, TF32-rounded.
+__global__ void pack_upsample_kernel(const float *__restrict__ w, int cout, int cin,
+                                     float *__restrict__ dst, int ldb, int cin_pad) {
+  const long long total = 4ll * cout * ldb;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = i / ldb;
+    const int par = static_cast<int>(row / cout), o = static_cast<int>(row % cout);
+    const int kidx = static_cast<int>(i % ldb);
+    const int tap = kidx / cin_pad, c = kidx % cin_pad;
+    const int py = par >> 1, px = par & 1, a = tap >> 1, b = tap & 1;
+    float v = 0.f;
+    if (c < cin) {
+      const float *wc = w + (static_cast<long long>(o) * cin + c) * 9;
+      for (int ky = 0; ky < 3; ++ky) {
+        if (((py + ky + 1) >> 1) - py != a) continue;  // floor((py+ky-1)/2) - (py-1)
+        for (int kx = 0; kx < 3; ++kx)
+          if (((px + kx + 1) >> 1) - px == b) v += wc[ky * 3 + kx];
+      }
+    }
+    dst[i] = round_tf32(v);
+  }
+}
+
 // 32x32 tile transpose through shared memory, with an affine map and optional
 // TF32 rounding on the way.
 __global__ void transpose_kernel(const float *__restrict__ src, long long so, int sld,
@@ -92,6 +120,16 @@ int pack_conv_weights(const float *w, int cout, int cin, int taps, const float *
   const long long total = static_cast<long long>(cout_rows) * ldb;
   pack_kernel<<<grid_for(total, 256), 256, 0, s>>>(w, cout, cin, taps, w_sc, w_sc ? sc_cin : 0,
                                                    dst, cout_rows, ldb, round_up32(cin));
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(1);
+  return VAE_OK;
+}
+
+int pack_upsample_weights(const float *w, int cout, int cin, float *dst, cudaStream_t s) {
+  if (!w || !dst || cout <= 0 || cin <= 0) return VAE_EINVAL;
+  const int ldb = upsample_ldb(cin);
+  pack_upsample_kernel<<<grid_for(4ll * cout * ldb, 256), 256, 0, s>>>(w, cout, cin, dst, ldb,
+                                                                      round_up32(cin));
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(1);
   return VAE_OK;

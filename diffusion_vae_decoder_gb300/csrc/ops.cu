@@ -58,6 +58,9 @@ struct ConvWs {
 };
 
 // out_scale: output pixels per input pixel (4 for the upsample conv).
+// The upsample conv's packed weights (4 parities x 2x2 taps) take the room of
+// a 16-tap pack.
+constexpr int kUpsamplePackTaps = 16;
 ConvWs carve_conv(Carver &cv, int n, int cin, long long spatial, int layout, int cout, int taps,
                   int sc_cin, int out_scale = 1) {
   ConvWs w{};
@@ -309,7 +312,7 @@ int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout, const f
 size_t vae_upsample_conv_workspace_size(int n, int cin, int h, int w, int layout, int cout) {
   if (n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0) return 0;
   Carver cv(nullptr, 0);
-  carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout, 9, 0, 4);
+  carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout, kUpsamplePackTaps, 0, 4);
   return cv.used;
 }
 
@@ -325,10 +328,10 @@ int vae_upsample_conv(const float *x, int n, int cin, int h, int w, int layout,
   if (layout == VAE_NHWC && cout % 4) return VAE_EUNSUPPORTED;
   const long long spatial = static_cast<long long>(h) * w;
   Carver cv(ws, ws_bytes);
-  ConvWs cw = carve_conv(cv, n, cin, spatial, layout, cout, 9, 0, 4);
+  ConvWs cw = carve_conv(cv, n, cin, spatial, layout, cout, kUpsamplePackTaps, 0, 4);
   if (!cv.ok()) return VAE_EWORKSPACE;
-  const int ldb = packed_ldb(cin, 9, 0);
-  VAE_TRY(pack_conv_weights(weight, cout, cin, 9, nullptr, 0, cw.packed, cout, ldb, s));
+  const int ldb = upsample_ldb(cin);
+  VAE_TRY(pack_upsample_weights(weight, cout, cin, cw.packed, s));
   const float *xa = nullptr;
   VAE_TRY(stage_nhwc(x, n, cin, spatial, layout, cw.xs, round_up32(cin), 1.f, 0.f, 0, &xa, s));
   IgemmDesc d;
