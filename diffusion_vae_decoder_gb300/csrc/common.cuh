@@ -145,8 +145,8 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
                    float *y, void *ws, cudaStream_t s, const float *residual = nullptr);
 
 // GroupNorm(+SiLU) of NHWC x whose statistics were produced by the conv
-// epilogue (float partials [n][groups][slots][3]); ws holds scale/shift.
-size_t groupnorm_partials_ws_bytes(int n, int c);
+// epilogue (float partials [n][groups][slots][3]); ws: groupnorm_ws_bytes(n,
+// c, ., groups) bytes (holds the compacted partials when slots > 64).
 int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int groups,
                             float eps, const float *gamma, const float *beta, int silu,
                             int round_out, const float *part, long long slots, float *y,

@@ -206,8 +206,11 @@ __global__ void gn_finalize(const P *__restrict__ part, long long nblk, int c, i
   }
 }
 
+// SiLU with the fast exponential and division: their few-ulp error sits far
+// below the TF32 rounding applied to the result before the next conv.
+// (v < -88: exp overflows to inf and the quotient is -0, SiLU's limit.)
 __device__ __forceinline__ float act(float v, int silu) {
-  return silu ? v / (1.0f + expf(-v)) : v;
+  return silu ? __fdividef(v, 1.0f + __expf(-v)) : v;
 }
 
 __device__ __forceinline__ float rnd(float v, int round) { return round ? round_tf32(v) : v; }
@@ -271,7 +274,35 @@ __global__ void gn_apply_nchw(const float *__restrict__ x, long long total, int 
 // Finalize and apply in one kernel, for few partials per group: every CTA
 // merges its sample's partials into shared scale/shift, then runs the same
 // vectorised apply loop as gn_apply_nhwc.
-constexpr int kFusedMaxSlots = 64;  // above this, finalize + apply measured faster
+constexpr int kFusedMaxSlots = 64;  // partials merged by each apply block
+constexpr int kCompactThreads = 256;
+
+// Merge each (sample, group)'s `slots` partials down to kFusedMaxSlots: block
+// (b, ng) merges the contiguous slot range b of kFusedMaxSlots equal ranges
+// (fixed order: thread-strided, then a tree) and writes slot b of `out`.
+__global__ void __launch_bounds__(kCompactThreads)
+    gn_compact(const float *__restrict__ part, long long slots, float *__restrict__ out) {
+  __shared__ Triple red[kCompactThreads];
+  const int b = blockIdx.x, ng = blockIdx.y;
+  const long long per = (slots + kFusedMaxSlots - 1) / kFusedMaxSlots;
+  const long long s0 = b * per, s1 = s0 + per < slots ? s0 + per : slots;
+  const float *e = part + static_cast<long long>(ng) * slots * 3;
+  Triple acc{0.f, 0.f, 0.f};
+  for (long long sl = s0 + threadIdx.x; sl < s1; sl += kCompactThreads)
+    acc = merge(acc, Triple{e[3 * sl], e[3 * sl + 1], e[3 * sl + 2]});
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = kCompactThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] = merge(red[threadIdx.x], red[threadIdx.x + w]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    float *o = out + (static_cast<long long>(ng) * kFusedMaxSlots + b) * 3;
+    o[0] = red[0].n;
+    o[1] = red[0].mean;
+    o[2] = red[0].m2;
+  }
+}
 
 __global__ void __launch_bounds__(256)
     gn_apply_fused_nhwc(const float *__restrict__ x, unsigned per_sample4, int c,
@@ -282,16 +313,33 @@ __global__ void __launch_bounds__(256)
   __shared__ __align__(16) float ssh[1024];
   const int n = blockIdx.y;
   const int cg = c / groups;
-  for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+  // tpg lanes (a power of two <= 32) merge one group's partials: strided
+  // over the slots, then a butterfly over the lanes.
+  int tpg = 1;
+  while (tpg < 32 && tpg * 2 * groups <= 256) tpg *= 2;
+  const int sub = threadIdx.x & (tpg - 1);
+  for (int g0 = 0; g0 < groups; g0 += 256 / tpg) {
+    const int g = g0 + threadIdx.x / tpg;  // uniform across each tpg-lane set
     Triple acc{0.f, 0.f, 0.f};
-    const float *e = part + (static_cast<size_t>(n) * groups + g) * slots * 3;
-    for (int sl = 0; sl < slots; ++sl) acc = merge(acc, Triple{e[3 * sl], e[3 * sl + 1], e[3 * sl + 2]});
-    const float var = acc.n > 0.f ? acc.m2 / acc.n : 0.f;
-    const float rstd = rsqrtf(var + eps);
-    for (int ch = g * cg; ch < (g + 1) * cg; ++ch) {
-      const float a = rstd * gamma[ch];
-      ssc[ch] = a;
-      ssh[ch] = beta[ch] - acc.mean * a;
+    if (g < groups) {
+      const float *e = part + (static_cast<size_t>(n) * groups + g) * slots * 3;
+      for (int sl = sub; sl < slots; sl += tpg)
+        acc = merge(acc, Triple{e[3 * sl], e[3 * sl + 1], e[3 * sl + 2]});
+    }
+    for (int o = 1; o < tpg; o <<= 1) {
+      const Triple other{__shfl_xor_sync(0xffffffffu, acc.n, o),
+                         __shfl_xor_sync(0xffffffffu, acc.mean, o),
+                         __shfl_xor_sync(0xffffffffu, acc.m2, o)};
+      acc = (threadIdx.x & o) ? merge(other, acc) : merge(acc, other);
+    }
+    if (g < groups && sub == 0) {
+      const float var = acc.n > 0.f ? acc.m2 / acc.n : 0.f;
+      const float rstd = rsqrtf(var + eps);
+      for (int ch = g * cg; ch < (g + 1) * cg; ++ch) {
+        const float a = rstd * gamma[ch];
+        ssc[ch] = a;
+        ssh[ch] = beta[ch] - acc.mean * a;
+      }
     }
   }
   __syncthreads();
@@ -448,13 +496,6 @@ int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int g
   return VAE_OK;
 }
 
-size_t groupnorm_partials_ws_bytes(int n, int c) {
-  Carver cv(nullptr, 0);
-  cv.take<float>(static_cast<size_t>(n) * c);
-  cv.take<float>(static_cast<size_t>(n) * c);
-  return cv.used;
-}
-
 int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int groups,
                             float eps, const float *gamma, const float *beta, int silu,
                             int round_out, const float *part, long long slots, float *y,
@@ -463,26 +504,33 @@ int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int
       groups <= 0 || slots <= 0)
     return VAE_EINVAL;
   if (c % groups || c % 4 || c > 1024) return VAE_EUNSUPPORTED;
+  Carver cv(ws, ~size_t(0));
   if (slots <= kFusedMaxSlots) {
+    // Few partials: every apply block merges them itself (one launch).
     const long long per4 = spatial * c / 4;
     if (per4 > 0xffffffffll / 2) return VAE_EUNSUPPORTED;
     const long long g = apply_blocks(per4, c, n);
     if ((g * 1024) % c != 0) return VAE_EUNSUPPORTED;
     gn_apply_fused_nhwc<<<dim3(static_cast<unsigned>(g), n), 256, 0, s>>>(
-        x, static_cast<unsigned>(per4), c, part, static_cast<int>(slots), groups, eps, gamma, beta,
-        silu, round_out, residual, y);
+        x, static_cast<unsigned>(per4), c, part, static_cast<int>(slots), groups, eps, gamma,
+        beta, silu, round_out, residual, y);
     if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
     count_launches(1);
     return VAE_OK;
   }
-  Carver cv(ws, ~size_t(0));
+  // Many partials: compact them with all SMs busy, merge the few left into
+  // scale/shift once, then the plain apply pass.
   float *scale = cv.take<float>(static_cast<size_t>(n) * c);
   float *shift = cv.take<float>(static_cast<size_t>(n) * c);
-  gn_finalize<float><<<n * groups, kFinalizeThreads, 0, s>>>(part, slots, c, groups, eps, gamma,
-                                                             beta, scale, shift);
+  float *compact = cv.take<float>(static_cast<size_t>(n) * groups * kFusedMaxSlots * 3);
+  gn_compact<<<dim3(kFusedMaxSlots, static_cast<unsigned>(n * groups)), kCompactThreads, 0, s>>>(
+      part, slots, compact);
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  gn_finalize<float><<<n * groups, kFinalizeThreads, 0, s>>>(compact, kFusedMaxSlots, c, groups,
+                                                             eps, gamma, beta, scale, shift);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   VAE_TRY(launch_apply_nhwc(x, n, c, spatial, scale, shift, silu, round_out, residual, y, s));
-  count_launches(2);
+  count_launches(3);
   return VAE_OK;
 }
 
