@@ -52,8 +52,10 @@ void count_launches(int n);
 long long launch_count();
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+// swizzle128 = false: plain row-major boxes in shared memory.
 int encode_tiled(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                 const uint64_t *strides_bytes /* rank-1 entries */, const uint32_t *box);
+                 const uint64_t *strides_bytes /* rank-1 entries */, const uint32_t *box,
+                 bool swizzle128 = true);
 
 // ------------------------------------------------------------------ kernels
 // Implicit-GEMM convolution / GEMM on tcgen05 (igemm.cu).

@@ -5,12 +5,14 @@
 //
 // With 3 output channels the conv does 2*9*C*3 FLOP per pixel while reading
 // 4*C bytes: far below the tensor cores' ridge, so it runs on the CUDA cores
-// in FP32 and is bounded by reading the last activation once. Each CTA
-// normalises a (TH+2) x (TW+2) halo tile of 16 channels at a time on its way
-// into shared memory (zeros outside the image: the conv's padding applies
-// after the normalisation); every thread accumulates four adjacent output
-// pixels, reading the halo with 16-byte loads and each weight once for all
-// four. The RGB result is written NCHW.
+// in FP32 and is bounded by reading the last activation once. Each CTA works
+// on a (TH+2) x (TW+2) halo tile, 8 channels at a time: a TMA box brings the
+// raw channels of chunk i+1 into shared memory while chunk i is convolved;
+// the GroupNorm affine and SiLU are applied on the way from that box into
+// channel planes (zeros outside the image: the conv's padding applies after
+// the normalisation). Every thread accumulates eight output pixels of one row
+// (two runs of four, 64 pixels apart), reading the planes with 16-byte loads
+// and each weight once for all eight. The RGB result is written NCHW.
 #include <mutex>
 
 #include "common.cuh"
@@ -20,97 +22,88 @@ namespace vae {
 
 namespace {
 
-// Output tile TH rows x 128 pixels (TH = 8); thread (ty, tx) computes pixels
-// 4*tx .. 4*tx+3 of row ty. Channels are staged 16 at a time.
-constexpr int kTW = 128, kCC = 16;
-constexpr int kHW = kTW + 2;  // halo width 130
-constexpr int kRow = 132;     // padded halo row (16-byte aligned rows)
-constexpr int kBatch = 7;
-template <int TH>
-struct HeadCfg {
-  static constexpr int kHH = TH + 2;                   // halo rows
-  static constexpr int kChan = kHH * kRow;             // floats per staged channel
-  static constexpr int kThr = TH * 32;                 // threads
-  static constexpr size_t kSmem = (kCC * kChan) * sizeof(float) + 9 * kCC * sizeof(float4);
-  static constexpr int kItems = kHH * kHW * (kCC / 4);  // float4 halo loads per chunk
-  static constexpr int kPer = (kItems + kThr - 1) / kThr;
-};
+// Output tile TH = 8 rows x TW = 128 pixels; thread (ty, tx), tx < 16,
+// computes pixels 4*tx .. 4*tx+3 and 64+4*tx .. 64+4*tx+3 of row ty.
+constexpr int kTH = 8, kTW = 128, kCC = 8;  // 4-channel chunks measured slower
+constexpr int kThr = kTH * 16;     // 128 threads
+constexpr int kHH = kTH + 2;       // halo rows
+constexpr int kHW = kTW + 2;       // halo width 130
+constexpr int kRow = 132;          // padded plane row (16-byte aligned rows)
+constexpr int kChan = kHH * kRow;  // floats per channel plane
+constexpr int kItems = kHH * kHW;  // halo pixels per chunk
+constexpr uint32_t kRawBytes = kItems * kCC * sizeof(float);  // one TMA box
+constexpr size_t kSmem = 1024 + kRawBytes + kCC * kChan * sizeof(float) +
+                         9 * kCC * sizeof(float4) + 16;
 
 // wpk: [C/32][9 taps][32 channels] x float4 (output channels padded to 4);
-// CO output channels are accumulated (CO <= 4).
-template <int CO, int TH>
-__global__ void __launch_bounds__(TH * 32)
-    head_kernel(const float *__restrict__ x, int H, int W, int C, const float *__restrict__ scale,
-                const float *__restrict__ shift, const float4 *__restrict__ wpk,
-                const float *__restrict__ bias, float *__restrict__ y) {
-  constexpr int cout = CO;
-  using HC = HeadCfg<TH>;
-  constexpr int kHH = HC::kHH, kChan = HC::kChan, kItems = HC::kItems, kPer = HC::kPer;
-  constexpr int kThr = HC::kThr;
-  extern __shared__ float4 head_smem[];
-  float *hal = reinterpret_cast<float *>(head_smem);
+// CO output channels are accumulated (CO <= 4). tmX: the NHWC activation,
+// box (8 channels, 130 pixels, 10 rows, 1 image), no swizzle.
+template <int CO>
+__global__ void __launch_bounds__(kThr)
+    head_kernel(const __grid_constant__ CUtensorMap tmX, int H, int W, int C,
+                const float *__restrict__ scale, const float *__restrict__ shift,
+                const float4 *__restrict__ wpk, const float *__restrict__ bias,
+                float *__restrict__ y, int *err) {
+  extern __shared__ uint8_t head_smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(head_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float *raw = reinterpret_cast<float *>(base);  // [10][130][8]
+  float *hal = raw + kItems * kCC;                // [8][10][132]
   float4 *wsm = reinterpret_cast<float4 *>(hal + kCC * kChan);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(wsm + 9 * kCC);
+  volatile uint32_t *abort = reinterpret_cast<uint32_t *>(bar + 1);
   const int n = blockIdx.z;
-  const int x0 = blockIdx.x * kTW, y0 = blockIdx.y * TH;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  float acc[4][4];  // [pixel][output channel]
-#pragma unroll
-  for (int o = 0; o < 4; ++o) {
-    const float b = (o < cout && bias) ? bias[o] : 0.f;
-#pragma unroll
-    for (int px = 0; px < 4; ++px) acc[px][o] = b;
+  const int x0 = blockIdx.x * kTW, y0 = blockIdx.y * kTH;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort = 0u;
+    fence_mbarrier_init();
   }
-  const float *xn = x + static_cast<size_t>(n) * H * W * C;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmX);
+    mbar_arrive_expect_tx(bar, kRawBytes);
+    tma_load_4d(raw, &tmX, bar, 0, x0 - 1, y0 - 1, n);
+  }
+  float acc[2][4][CO];  // [run][pixel][output channel]
+#pragma unroll
+  for (int o = 0; o < CO; ++o) {
+    const float b = bias ? bias[o] : 0.f;
+#pragma unroll
+    for (int px = 0; px < 4; ++px) acc[0][px][o] = acc[1][px][o] = b;
+  }
   const float *sc = scale + static_cast<size_t>(n) * C;
   const float *sh = shift + static_cast<size_t>(n) * C;
+  uint32_t phase = 0;
   for (int c0 = 0; c0 < C; c0 += kCC) {
-    __syncthreads();
-    // Halo: four lanes per pixel read its 16 channels (64 contiguous bytes),
-    // eight pixels per warp, kBatch independent loads in flight per thread.
-    // Each lane stores its four channels in an order rotated by its quad
-    // index, so the transposing shared stores of a warp hit 32 distinct banks
-    // (one channel plane is 8 banks from the next: kChan = 8 mod 32).
-    const int q4 = threadIdx.x & 3;  // fixed: the item stride (threads) is a multiple of 4
-    const int cq = c0 + q4 * 4;
-    const float4 ga = __ldg(reinterpret_cast<const float4 *>(sc + cq));
-    const float4 gb = __ldg(reinterpret_cast<const float4 *>(sh + cq));
-    float *dq = hal + (q4 * 4) * kChan;
-#pragma unroll 1
-    for (int b0 = 0; b0 < kPer; b0 += kBatch) {
-      float4 v[kBatch];
-      bool in[kBatch];
+    const bool ok = mbar_wait(bar, phase, abort);
+    if (__syncthreads_or(!ok)) {  // the box never landed: report, leave
+      if (threadIdx.x == 0) atomicCAS(err, 0, static_cast<int>(VAE_EDEVICE_TIMEOUT));
+      return;
+    }
+    phase ^= 1u;
+    // raw box -> normalised channel planes
+    const float4 ga = __ldg(reinterpret_cast<const float4 *>(sc + c0));
+    const float4 gb = __ldg(reinterpret_cast<const float4 *>(sc + c0 + 4));
+    const float4 ha = __ldg(reinterpret_cast<const float4 *>(sh + c0));
+    const float4 hb = __ldg(reinterpret_cast<const float4 *>(sh + c0 + 4));
+    const float gs[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+    const float hs[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+    const float4 *raw4 = reinterpret_cast<const float4 *>(raw);
+#pragma unroll 2
+    for (int l = threadIdx.x; l < kItems; l += kThr) {
+      const int hy = l / kHW, hx = l % kHW;
+      const int gy = y0 - 1 + hy, gx = x0 - 1 + hx;
+      const bool in = gy >= 0 && gy < H && gx >= 0 && gx < W;
+      const float4 v0 = raw4[2 * l], v1 = raw4[2 * l + 1];
+      const float t[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      float *d = hal + hy * kRow + hx;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int l = threadIdx.x + (b0 + u) * kThr;
-        const int pix = l >> 2;
-        const int gy = y0 + pix / kHW - 1, gx = x0 + pix % kHW - 1;
-        in[u] = l < kItems && gy >= 0 && gy < H && gx >= 0 && gx < W;
-        v[u] = in[u] ? __ldg(reinterpret_cast<const float4 *>(
-                           xn + (static_cast<size_t>(gy) * W + gx) * C + cq))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int l = threadIdx.x + (b0 + u) * kThr;
-        if (l >= kItems) break;
-        const int pix = l >> 2;
-        float4 t = v[u];
-        if (in[u]) {
-          t.x = fmaf(t.x, ga.x, gb.x);
-          t.y = fmaf(t.y, ga.y, gb.y);
-          t.z = fmaf(t.z, ga.z, gb.z);
-          t.w = fmaf(t.w, ga.w, gb.w);
-          t.x = __fdividef(t.x, 1.0f + __expf(-t.x));  // SiLU, fast intrinsics
-          t.y = __fdividef(t.y, 1.0f + __expf(-t.y));
-          t.z = __fdividef(t.z, 1.0f + __expf(-t.z));
-          t.w = __fdividef(t.w, 1.0f + __expf(-t.w));
-        }
-        float *d = dq + (pix / kHW) * kRow + pix % kHW;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int jj = (j + q4) & 3;
-          d[jj * kChan] = jj == 0 ? t.x : jj == 1 ? t.y : jj == 2 ? t.z : t.w;
-        }
+      for (int j = 0; j < 8; ++j) {
+        float r = fmaf(t[j], gs[j], hs[j]);
+        r = __fdividef(r, 1.0f + __expf(-r));  // SiLU, fast intrinsics
+        d[j * kChan] = in ? r : 0.f;
       }
     }
     for (int l = threadIdx.x; l < 9 * kCC; l += kThr) {
@@ -118,42 +111,53 @@ __global__ void __launch_bounds__(TH * 32)
       const int cg = c0 + c;
       wsm[l] = wpk[(cg / 32) * 288 + tap * 32 + (cg % 32)];
     }
-    __syncthreads();
+    __syncthreads();  // box consumed; planes and weights ready
+    if (threadIdx.x == 0 && c0 + kCC < C) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, kRawBytes);
+      tma_load_4d(raw, &tmX, bar, c0 + kCC, x0 - 1, y0 - 1, n);
+    }
 #pragma unroll 2
     for (int c = 0; c < kCC; ++c) {
 #pragma unroll
       for (int ky = 0; ky < 3; ++ky) {
         const float4 *rowp =
-            reinterpret_cast<const float4 *>(hal + c * kChan + (ty + ky) * kRow + 4 * tx);
-        const float4 a = rowp[0], b = rowp[1];
-        const float xs[6] = {a.x, a.y, a.z, a.w, b.x, b.y};
+            reinterpret_cast<const float4 *>(hal + c * kChan + (ty + ky) * kRow) + tx;
+        const float4 a0 = rowp[0], a1 = rowp[1], b0v = rowp[16], b1v = rowp[17];
+        const float xs[2][6] = {{a0.x, a0.y, a0.z, a0.w, a1.x, a1.y},
+                                {b0v.x, b0v.y, b0v.z, b0v.w, b1v.x, b1v.y}};
 #pragma unroll
         for (int kx = 0; kx < 3; ++kx) {
           const float4 w = wsm[(ky * 3 + kx) * kCC + c];
+          const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int px = 0; px < 4; ++px) {
-            const float xv = xs[px + kx];
-            acc[px][0] = fmaf(xv, w.x, acc[px][0]);
-            if (CO > 1) acc[px][1] = fmaf(xv, w.y, acc[px][1]);
-            if (CO > 2) acc[px][2] = fmaf(xv, w.z, acc[px][2]);
-            if (CO > 3) acc[px][3] = fmaf(xv, w.w, acc[px][3]);
-          }
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int px = 0; px < 4; ++px)
+#pragma unroll
+              for (int o = 0; o < CO; ++o)
+                acc[r][px][o] = fmaf(xs[r][px + kx], wv[o], acc[r][px][o]);
         }
       }
     }
+    __syncthreads();  // planes read before the next chunk overwrites them
   }
-  const int gy = y0 + ty, gx = x0 + 4 * tx;
+  const int gy = y0 + ty;
   if (gy >= H) return;
 #pragma unroll
-  for (int o = 0; o < 4; ++o) {
-    if (o >= cout) break;
-    float *dst = y + (static_cast<size_t>(n * cout + o) * H + gy) * W + gx;
-    if (gx + 3 < W && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-      *reinterpret_cast<float4 *>(dst) = make_float4(acc[0][o], acc[1][o], acc[2][o], acc[3][o]);
-    } else {
+  for (int r = 0; r < 2; ++r) {
+    const int gx = x0 + r * 64 + 4 * tx;
 #pragma unroll
-      for (int px = 0; px < 4; ++px)
-        if (gx + px < W) dst[px] = acc[px][o];
+    for (int o = 0; o < CO; ++o) {
+      float *dst = y + (static_cast<size_t>(n * CO + o) * H + gy) * W + gx;
+      if (gx + 3 < W && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        *reinterpret_cast<float4 *>(dst) =
+            make_float4(acc[r][0][o], acc[r][1][o], acc[r][2][o], acc[r][3][o]);
+      } else {
+#pragma unroll
+        for (int px = 0; px < 4; ++px)
+          if (gx + px < W) dst[px] = acc[r][px][o];
+      }
     }
   }
 }
@@ -188,34 +192,21 @@ int head_pack_weights(const float *w, int cout, int cin, float *dst, cudaStream_
 
 namespace {
 
-template <int CO, int TH>
-int launch_head(const float *x, int n, int h, int w, int c, const float *scale,
-                const float *shift, const float4 *wv, const float *bias, float *y,
+template <int CO>
+int launch_head(const CUtensorMap &tm, int n, int h, int w, int c, const float *scale,
+                const float *shift, const float4 *wv, const float *bias, float *y, int *err,
                 cudaStream_t s) {
-  using HC = HeadCfg<TH>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(head_kernel<CO, TH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(HC::kSmem));
+    attr = cudaFuncSetAttribute(head_kernel<CO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmem));
   });
   if (attr != cudaSuccess) return VAE_ECUDA;
-  if ((h + TH - 1) / TH > 65535) return VAE_EUNSUPPORTED;
-  dim3 grid((w + kTW - 1) / kTW, (h + TH - 1) / TH, n);
-  head_kernel<CO, TH><<<grid, HC::kThr, HC::kSmem, s>>>(x, h, w, c, scale, shift, wv, bias, y);
+  if ((h + kTH - 1) / kTH > 65535) return VAE_EUNSUPPORTED;
+  dim3 grid((w + kTW - 1) / kTW, (h + kTH - 1) / kTH, n);
+  head_kernel<CO><<<grid, kThr, kSmem, s>>>(tm, h, w, c, scale, shift, wv, bias, y, err);
   return cudaGetLastError() == cudaSuccess ? VAE_OK : VAE_ECUDA;
-}
-
-template <int TH>
-int launch_head_co(int cout, const float *x, int n, int h, int w, int c, const float *scale,
-                   const float *shift, const float4 *wv, const float *bias, float *y,
-                   cudaStream_t s) {
-  switch (cout) {
-    case 1: return launch_head<1, TH>(x, n, h, w, c, scale, shift, wv, bias, y, s);
-    case 2: return launch_head<2, TH>(x, n, h, w, c, scale, shift, wv, bias, y, s);
-    case 3: return launch_head<3, TH>(x, n, h, w, c, scale, shift, wv, bias, y, s);
-    default: return launch_head<4, TH>(x, n, h, w, c, scale, shift, wv, bias, y, s);
-  }
 }
 
 }  // namespace
@@ -225,10 +216,24 @@ int head_gn_silu_conv(const float *x, int n, int h, int w, int c, const float *s
                       float *y, cudaStream_t s) {
   if (!x || !scale || !shift || !wpk || !y || n <= 0 || h <= 0 || w <= 0) return VAE_EINVAL;
   if (c % 32 || cout < 1 || cout > 4 || n > 65535) return VAE_EUNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(x) & 15) return VAE_EINVAL;
   const float4 *wv = reinterpret_cast<const float4 *>(wpk);
-  // 8-row tiles (2-row tiles measured slower even on small images: the halo
-  // overhead outweighs the extra CTAs)
-  const int rc = launch_head_co<8>(cout, x, n, h, w, c, scale, shift, wv, bias, y, s);
+  int *err = device_error_word();
+  if (!err) return VAE_ECUDA;
+  CUtensorMap tm{};
+  const uint64_t dims[4] = {static_cast<uint64_t>(c), static_cast<uint64_t>(w),
+                            static_cast<uint64_t>(h), static_cast<uint64_t>(n)};
+  const uint64_t str[3] = {static_cast<uint64_t>(c) * 4, static_cast<uint64_t>(w) * c * 4,
+                           static_cast<uint64_t>(h) * w * c * 4};
+  const uint32_t box[4] = {kCC, kHW, kHH, 1};
+  VAE_TRY(encode_tiled(&tm, x, 4, dims, str, box, false));
+  int rc;
+  switch (cout) {
+    case 1: rc = launch_head<1>(tm, n, h, w, c, scale, shift, wv, bias, y, err, s); break;
+    case 2: rc = launch_head<2>(tm, n, h, w, c, scale, shift, wv, bias, y, err, s); break;
+    case 3: rc = launch_head<3>(tm, n, h, w, c, scale, shift, wv, bias, y, err, s); break;
+    default: rc = launch_head<4>(tm, n, h, w, c, scale, shift, wv, bias, y, err, s); break;
+  }
   if (rc == VAE_OK) count_launches(1);
   return rc;
 }

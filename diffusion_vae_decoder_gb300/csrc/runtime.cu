@@ -63,7 +63,7 @@ void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed);
 long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 int encode_tiled(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                 const uint64_t *strides_bytes, const uint32_t *box) {
+                 const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128) {
   auto fn = encode_fn();
   if (!fn) return VAE_ECUDA;
   cuuint64_t gd[5], gs[4];
@@ -77,7 +77,8 @@ int encode_tiled(CUtensorMap *map, const void *base, int rank, const uint64_t *d
   const CUresult r =
       fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<cuuint32_t>(rank),
          const_cast<void *>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? VAE_OK : VAE_EUNSUPPORTED;
 }
