@@ -33,34 +33,73 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float *sh) {
   return v;
 }
 
-// Row length L <= kThreads * kPerThread: the row lives in registers.
+// Row length ld <= kThreads * kPerThread (ld a multiple of 4): the row lives
+// in registers, read and written with 16-byte accesses. One block reduction
+// of per-thread (max, sum of exp) pairs replaces separate max and sum passes:
+// each thread keeps exp(v - its own max) and rescales by exp(own max - row
+// max) at the end.
 __global__ void __launch_bounds__(kThreads) softmax_reg(float *s, int L, int ld, float scale) {
-  __shared__ float sh[32];
-  float *row = s + static_cast<long long>(blockIdx.x) * ld;
+  __shared__ float shm[32], shs[32];
+  constexpr int kVec = kPerThread / 4;
+  float4 *row = reinterpret_cast<float4 *>(s + static_cast<long long>(blockIdx.x) * ld);
+  const int ld4 = ld >> 2;
   float v[kPerThread];
   float mx = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < kPerThread; ++i) {
-    const int j = threadIdx.x + i * kThreads;
-    v[i] = j < L ? row[j] * scale : -INFINITY;
-    mx = fmaxf(mx, v[i]);
+  for (int i = 0; i < kVec; ++i) {
+    const int q = threadIdx.x + i * kThreads;
+    const float4 x = q < ld4 ? row[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[4 * i + k] = 4 * q + k < L ? e[k] * scale : -INFINITY;
+      mx = fmaxf(mx, v[4 * i + k]);
+    }
   }
-  mx = block_reduce(mx, true, sh);
   float sum = 0.f;
 #pragma unroll
   for (int i = 0; i < kPerThread; ++i) {
-    v[i] = expf(v[i] - mx);  // exp(-inf) = 0 for the padding slots
+    v[i] = mx == -INFINITY ? 0.f : __expf(v[i] - mx);  // exp(-inf) = 0 for the padding
     sum += v[i];
   }
-  sum = block_reduce(sum, false, sh);
-  const float inv = 1.0f / sum;
+  // (max, sum) merge: warp butterfly, then across warps
+  float m = mx, t = sum;
 #pragma unroll
-  for (int i = 0; i < kPerThread; ++i) {
-    const int j = threadIdx.x + i * kThreads;
-    if (j < L)
-      row[j] = round_tf32(v[i] * inv);
-    else if (j < ld)
-      row[j] = 0.f;
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
+    const float mm = fmaxf(m, m2);
+    t = (m == -INFINITY ? 0.f : t * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : t2 * __expf(m2 - mm));
+    m = mm;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    shm[warp] = m;
+    shs[warp] = t;
+  }
+  __syncthreads();
+  m = lane < (kThreads >> 5) ? shm[lane] : -INFINITY;
+  t = lane < (kThreads >> 5) ? shs[lane] : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float t2 = __shfl_xor_sync(0xffffffffu, t, o);
+    const float mm = fmaxf(m, m2);
+    t = (m == -INFINITY ? 0.f : t * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : t2 * __expf(m2 - mm));
+    m = mm;
+  }
+  const float f = (mx == -INFINITY ? 0.f : __expf(mx - m)) / t;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const int q = threadIdx.x + i * kThreads;
+    if (q < ld4) {
+      float4 o;  // padding columns: v = 0 there, so they store exact zeros
+      o.x = round_tf32(v[4 * i] * f);
+      o.y = round_tf32(v[4 * i + 1] * f);
+      o.z = round_tf32(v[4 * i + 2] * f);
+      o.w = round_tf32(v[4 * i + 3] * f);
+      row[q] = o;
+    }
   }
 }
 
@@ -85,7 +124,8 @@ __global__ void __launch_bounds__(kThreads) softmax_long(float *s, int L, int ld
 int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st) {
   if (!s || rows <= 0 || L <= 0 || ld < L) return VAE_EINVAL;
   if (rows > 0x7fffffffll) return VAE_EUNSUPPORTED;
-  if (ld <= kThreads * kPerThread)
+  if (ld <= kThreads * kPerThread && ld % 4 == 0 &&
+      (reinterpret_cast<uintptr_t>(s) & 15) == 0)
     softmax_reg<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale);
   else
     softmax_long<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale);
