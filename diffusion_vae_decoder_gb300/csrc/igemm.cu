@@ -43,6 +43,7 @@
 //             256 pixels; per 32-channel chunk and kx one band of bh + 2
 //             rows serves the three ky taps (views from row ky * bw). The
 //             epilogue transposes each 32 x 32 block into pixel-major rows.
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -88,7 +89,66 @@ struct KParams {
   int stat_cg;       // channels per group (power of two dividing 32)
   int stat_groups;   // groups over cout
   int stat_slots;    // slots per (sample, group)
+  // Stream-K (when whole tiles would leave the last round of SMs mostly
+  // idle): CTA c runs units [c * sk_total / G, (c + 1) * sk_total / G) of the
+  // flattened (tile, reduction unit) space, sk_units units per tile (a unit
+  // is one reduction step, or one 32-channel chunk in MODE 3). A tile cut
+  // between two CTAs: the CTA holding its later part (the tail, at the start
+  // of its range) writes the raw sums to its slot of sk_part and raises its
+  // flags; the CTA holding the head (at the end of its range) adds them in
+  // its epilogue. Fixed split points: deterministic.
+  int sk;
+  int sk_units;
+  long long sk_total;
+  float *sk_part;
+  int *sk_flag;  // [G][4]: one per epilogue warp, zeroed before the launch
   int *err;
+};
+
+// One work item of a CTA: a tile and the range [k0, k1) of its reduction
+// units (reduction steps; 32-channel chunks in MODE 3).
+struct Work {
+  int tile, k0, k1;
+  bool head, tail;  // stream-K: the tile's first part here and the rest on the next CTA / the reverse
+};
+
+// The CTA's work items, identical in the producer, MMA and epilogue roles.
+template <int MODE>
+struct WorkIter {
+  long long u, end;
+  int tile;
+  __device__ explicit WorkIter(const KParams &p) : u(0), end(0), tile(blockIdx.x) {
+    if (p.sk) {
+      u = p.sk_total * blockIdx.x / gridDim.x;
+      end = p.sk_total * (blockIdx.x + 1) / gridDim.x;
+    }
+  }
+  __device__ bool next(const KParams &p, Work &w) {
+    if (p.sk) {
+      if (u >= end) return false;
+      w.tile = static_cast<int>(u / p.sk_units);
+      w.k0 = static_cast<int>(u % p.sk_units);
+      const long long left = end - u;
+      w.k1 = left < p.sk_units - w.k0 ? w.k0 + static_cast<int>(left) : p.sk_units;
+      w.tail = w.k0 > 0;
+      w.head = w.k0 == 0 && w.k1 < p.sk_units;
+      u += w.k1 - w.k0;
+      return true;
+    }
+    if (tile >= p.total_tiles) return false;
+    w.tile = tile;
+    if (MODE == 3) {
+      w.k0 = 0;
+      w.k1 = p.cin_chunks;
+    } else {
+      const int split = tile / (p.m_tiles * p.n_tiles);
+      w.k0 = split * p.ks_per;
+      w.k1 = min(w.k0 + p.ks_per, p.k_stages);
+    }
+    w.head = w.tail = false;
+    tile += gridDim.x;
+    return true;
+  }
 };
 
 // BN: output channels per tile (MMA N; MMA M in MODE 4). MS: 128-row M sub-tiles per tile
@@ -285,12 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t abuf = 0, aphase = 0;       // MODE 3 halo buffer ring
       uint32_t a_pending = 0, a_par = 0;
       bool failed = false;
-      for (int tile = blockIdx.x; tile < p.total_tiles && !failed; tile += gridDim.x) {
+      WorkIter<MODE> it(p);
+      Work w;
+      while (!failed && it.next(p, w)) {
+        const int tile = w.tile;
         const int mn = tile % (p.m_tiles * p.n_tiles);
-        const int split = tile / (p.m_tiles * p.n_tiles);
         const int mt = mn / p.n_tiles;
         const int n0 = (mn % p.n_tiles) * BN;
-        const int ks0 = split * p.ks_per, ks1 = min(ks0 + p.ks_per, p.k_stages);
+        const int ks0 = w.k0, ks1 = w.k1;
         int img = 0, ty = 0, tx = 0, par = 0;
         if (MODE != 2) {
           const int per_img = p.tiles_x * p.tiles_y * (MODE == 1 ? 4 : 1);
@@ -307,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (MODE == 3) {
           // One halo tile per 32-channel chunk, then one weight stage per tap
           // (no appended shortcut in this mode).
-          for (int cc = 0; cc < p.cin_chunks && !failed; ++cc) {
+          for (int cc = ks0; cc < ks1 && !failed; ++cc) {
             if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort)) {
               raise_error(p, abort);
               failed = true;
@@ -453,22 +515,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t abuf = 0, aphase = 0;
       int local = 0;
       bool failed = false, issued = false;
-      for (int tile = blockIdx.x; tile < p.total_tiles && !failed; tile += gridDim.x, ++local) {
-        const int buf = local & 1;
-        const uint32_t aph = (local >> 1) & 1;
+      WorkIter<MODE> it(p);
+      Work w;
+      while (!failed && it.next(p, w)) {
+        const int cur = local++;
+        const int buf = cur & 1;
+        const uint32_t aph = (cur >> 1) & 1;
         if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort)) {
           raise_error(p, abort);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS;
-        const int split = tile / (p.m_tiles * p.n_tiles);
-        const int ks0 = split * p.ks_per, ks1 = min(ks0 + p.ks_per, p.k_stages);
+        const int ks0 = w.k0, ks1 = w.k1;
         if constexpr (MODE == 3) {
           // Tap (ky, kx) of output sub-tile `sub` reads the 128 halo pixels
           // starting at halo row sub + ky, column kx: a row offset into the
           // swizzled halo buffer.
-          for (int cc = 0; cc < p.cin_chunks && !failed; ++cc) {
+          for (int cc = ks0; cc < ks1 && !failed; ++cc) {
             if (!mbar_wait(&a_full[abuf], aphase, abort)) {
               raise_error(p, abort);
               failed = true;
@@ -489,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                   umma_tf32(d_tmem + sub * BN, ad + 2 * k, bd + 2 * k, IDESC,
-                            (cc != 0) || (tap != 0) || (k != 0));
+                            (cc != ks0) || (tap != 0) || (k != 0));
               }
               issued = true;
               umma_commit(&empty[stage]);
@@ -598,10 +662,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t res_phase = 0;
     bool failed = false;
     int local = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles && !failed;
-         tile += gridDim.x, ++local) {
-      const int buf = local & 1;
-      const uint32_t aph = (local >> 1) & 1;
+    WorkIter<MODE> it(p);
+    Work w;
+    while (!failed && it.next(p, w)) {
+      const int tile = w.tile;
+      const int cur = local++;
+      const int buf = cur & 1;
+      const uint32_t aph = (cur >> 1) & 1;
       bool ok = mbar_wait(&acc_full[buf], aph, abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -725,6 +792,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
         continue;
       }
+      // Stream-K: this warp's rows of a tile split with the next CTA. The
+      // tail's raw sums are in that CTA's slot once its flag for this warp
+      // is up (set long before: the tail was its first work item).
+      const size_t sk_slot_f4 = static_cast<size_t>(MS) * BN * 32;  // float4 per slot
+      if (w.head) {
+        bool ok = true;
+        if (lane == 0) {
+          const int *f = p.sk_flag + (blockIdx.x + 1) * 4 + q;
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire_gpu(f) == 0) {
+            if (*abort || global_timer_ns() - t0 > kWaitTimeoutNs) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) {
+          if (lane == 0) raise_error(p, abort);
+          failed = true;
+          break;
+        }
+        __syncwarp();
+        __threadfence();
+      }
       for (int sub = 0; sub < MS; ++sub) {
       const int msub = sub * 128 + m;  // row of the (MS x 128)-row tile
       bool valid;
@@ -782,6 +874,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32cols(taddr, v);
         else
           tmem_ld_16cols(taddr, v);
+        if (C::CH == 32 && (w.tail || w.head)) {
+          // slot layout [sub][chunk][j][128 rows] of float4: a warp's 32
+          // lanes touch 32 consecutive float4 per access
+          const size_t off = static_cast<size_t>((sub * (BN / 32) + c) * 8) * 128 + q * 32 + lane;
+          if (w.tail) {
+            float4 *dst = reinterpret_cast<float4 *>(p.sk_part) + blockIdx.x * sk_slot_f4 + off;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              __stcg(dst + j * 128, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            continue;
+          }
+          const float4 *src =
+              reinterpret_cast<const float4 *>(p.sk_part) + (blockIdx.x + 1) * sk_slot_f4 + off;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 t = __ldcg(src + j * 128);
+            v[4 * j] += t.x;
+            v[4 * j + 1] += t.y;
+            v[4 * j + 2] += t.z;
+            v[4 * j + 3] += t.w;
+          }
+        }
         const int col0 = n0 + c * C::CH;
         if (col0 >= p.cout) continue;  // warp-uniform
         const int ncols = min(C::CH, p.cout - col0);
@@ -937,6 +1051,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (failed) break;
       }  // sub-tiles
+      if (w.tail && !failed) {  // this warp's raw sums are out: raise its flag
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.sk_flag + blockIdx.x * 4 + q, 1);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && !failed) mbar_arrive(&acc_empty[buf]);
@@ -976,7 +1095,21 @@ int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap
   });
   if (attr_err != cudaSuccess) return VAE_ECUDA;
   const int grid = std::min(kp.total_tiles, num_sms());
-  igemm_kernel<BN, MODE, MS><<<grid, kThreads, C::SMEM, stream>>>(ta, tb, ts, to, tr, kp);
+  // Stream-K CTAs wait on their neighbour's flags: a cooperative launch
+  // guarantees that the whole grid is resident.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute coop[1];
+  coop[0].id = cudaLaunchAttributeCooperative;
+  coop[0].val.cooperative = 1;
+  cfg.attrs = coop;
+  cfg.numAttrs = kp.sk ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, igemm_kernel<BN, MODE, MS>, ta, tb, ts, to, tr, kp) !=
+      cudaSuccess)
+    return VAE_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(1);
   return VAE_OK;
@@ -1282,6 +1415,30 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
                              static_cast<uint64_t>(d.hin) * d.win * d.a_c * 4};
     const uint32_t box[4] = {32, 130, static_cast<uint32_t>(kp.bh + 2), 1};
     VAE_TRY(encode_tiled(&ta, d.a, 4, dims, str, box));
+  }
+
+  // Stream-K for convs whose whole tiles would leave the last round of SMs
+  // mostly idle (e.g. 256 tiles on 152 SMs: 1.68 rounds run as 2).
+  kp.sk = 0;
+  if (d.mode == AMode::Conv && !swap && kp.splits == 1 && d.split_ws && bn >= 32) {
+    const int sms = num_sms();
+    const long long tiles = total;
+    const int units = halo ? kp.cin_chunks : kp.k_stages;
+    const double rounds = static_cast<double>(tiles) / sms;
+    const double eff = rounds / std::ceil(rounds);
+    const int ms = halo ? 1 : (bn == 128 ? 2 : 1);
+    const size_t slot = static_cast<size_t>(ms) * bn * kBM;
+    const size_t need = static_cast<size_t>(sms) * slot + static_cast<size_t>(sms) * 4;
+    if (tiles >= sms && eff < 0.9 && units >= 4 && need <= d.split_ws_floats) {
+      kp.sk = 1;
+      kp.sk_units = units;
+      kp.sk_total = tiles * units;
+      kp.sk_part = d.split_ws;
+      kp.sk_flag = reinterpret_cast<int *>(d.split_ws + static_cast<size_t>(sms) * slot);
+      if (cudaMemsetAsync(kp.sk_flag, 0, static_cast<size_t>(sms) * 4 * sizeof(int), stream) !=
+          cudaSuccess)
+        return VAE_ECUDA;
+    }
   }
 
   int rc;

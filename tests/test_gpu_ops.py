@@ -248,6 +248,36 @@ def test_conv2d_channel_major_float_parity():
     assert_layer_parity(got, ref, "conv2d channel-major c=128")
 
 
+# Stream-K: 256 tiles of 128 pixels (one image row each) on a 152-SM part
+# would run as 1.68 rounds; the reduction is split at fixed points between
+# neighbouring CTAs (tail written raw and flagged, head adds it). Halo mode
+# (no shortcut) and per-tap mode (with an appended shortcut); integer data
+# keeps every partial sum exact.
+@pytest.mark.parametrize("with_sc", [False, True])
+def test_conv2d_stream_k_exact_integer(with_sc):
+    n, cin, cout, h, w = 1, 128, 256, 256, 128
+    lay = pkg().VAE_NHWC
+    x = S.integer_tensor((n, cin, h, w), 61, -3, 3)
+    wt = S.integer_tensor((cout, cin, 3, 3), 62, -2, 2)
+    b = S.integer_tensor((cout,), 63, -8, 8)
+    ref = O.conv2d(x, wt, b)
+    kw = {}
+    if with_sc:
+        sx = S.integer_tensor((n, 64, h, w), 64, -3, 3)
+        sw = S.integer_tensor((cout, 64, 1, 1), 65, -2, 2)
+        ref = ref + O.conv2d(sx, sw, None)
+        kw = dict(sc_x=dev(to_layout(sx, lay)), sc_w=dev(sw))
+    y = sentinel_like(out_shape(ref.shape, lay))
+    pkg().vae_conv2d(dev(to_layout(x, lay)), dev(wt), dev(b), layout=lay, out=y, **kw)
+    got = from_layout(y.cpu().numpy(), lay)
+    assert_all_written(got, "conv2d stream-K")
+    np.testing.assert_array_equal(got, ref)
+    # a second call on the same workspace layout gives the same bits
+    y2 = sentinel_like(out_shape(ref.shape, lay))
+    pkg().vae_conv2d(dev(to_layout(x, lay)), dev(wt), dev(b), layout=lay, out=y2, **kw)
+    np.testing.assert_array_equal(from_layout(y2.cpu().numpy(), lay), ref)
+
+
 _FORCED_TAPS = """
 import sys
 sys.path.insert(0, {root!r})
