@@ -167,6 +167,8 @@ struct Cfg {
   static constexpr uint32_t HALO_BYTES =
       HALO ? ((MS + 2) * 130 * 128 + 1023) / 1024 * 1024 : SWAP ? 65536 : 0;
   static constexpr int HALO_BUFS = (HALO || SWAP) ? 2 : 0;
+  // MODE 4: appended-shortcut tiles (MS x 128 rows each) sharing one A buffer.
+  static constexpr int SC_PER_BUF = SWAP ? static_cast<int>(HALO_BYTES / (MS * kABytes)) : 1;
   static constexpr uint32_t A_BYTES = (HALO || SWAP) ? 0 : MS * kABytes;
   static constexpr uint32_t B_BYTES = BN * 128;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -405,11 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (MODE == 4) {
           // Per 32-channel chunk and kx: one band of bh + 2 rows shifted by
-          // kx - 1 serves the three ky taps; then the shortcut chunks, one
-          // plain tile each.
-          const int chunks = p.cin_chunks + p.sc_chunks;
+          // kx - 1 serves the three ky taps; then the shortcut chunks, their
+          // plain tiles SC_PER_BUF to an A buffer.
+          const int chunks = p.cin_chunks + (p.sc_chunks + C::SC_PER_BUF - 1) / C::SC_PER_BUF;
           for (int cc = 0; cc < chunks && !failed; ++cc) {
             const bool is_sc = cc >= p.cin_chunks;
+            const int sc0 = (cc - p.cin_chunks) * C::SC_PER_BUF;
+            const int nsc = is_sc ? min(C::SC_PER_BUF, p.sc_chunks - sc0) : 0;
             const int nkx = is_sc ? 1 : 3;
             for (int kx = 0; kx < nkx && !failed; ++kx) {
               if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort)) {
@@ -423,9 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(a_dst, &tmA, &a_full[abuf], cc * 32, tx * p.bw + kx - 1,
                             ty * p.bh - 1, img);
               } else {
-                mbar_arrive_expect_tx(&a_full[abuf], p.bh * p.bw * 128);
-                tma_load_4d(a_dst, &tmS, &a_full[abuf], (cc - p.cin_chunks) * 32, tx * p.bw,
-                            ty * p.bh, img);
+                mbar_arrive_expect_tx(&a_full[abuf], nsc * p.bh * p.bw * 128);
+                for (int i = 0; i < nsc; ++i)
+                  tma_load_4d(a_dst + i * p.bh * p.bw * 128, &tmS, &a_full[abuf], (sc0 + i) * 32,
+                              tx * p.bw, ty * p.bh, img);
               }
               a_pending |= 1u << abuf;
               a_par = (a_par & ~(1u << abuf)) | (aphase << abuf);
@@ -433,14 +438,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 abuf = 0;
                 aphase ^= 1u;
               }
-              const int nky = is_sc ? 1 : 3;
+              const int nky = is_sc ? nsc : 3;
               for (int ky = 0; ky < nky; ++ky) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
                   raise_error(p, abort);
                   failed = true;
                   break;
                 }
-                const int kcol = is_sc ? p.taps * p.cin_pad + (cc - p.cin_chunks) * 32
+                const int kcol = is_sc ? p.taps * p.cin_pad + (sc0 + ky) * 32
                                        : (ky * 3 + kx) * p.cin_pad + cc * 32;
                 mbar_arrive_expect_tx(&full[stage], STAGE_TX);
                 tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kcol, n0);
@@ -576,10 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // D[channel][pixel] += W[channel][k] . X[pixel][k]: the weight
           // stage is the 128-row M operand, the pixel band the 256-row N
           // operand, viewed from row ky * bw.
-          const int chunks = p.cin_chunks + p.sc_chunks;
+          const int chunks = p.cin_chunks + (p.sc_chunks + C::SC_PER_BUF - 1) / C::SC_PER_BUF;
           bool first = true;
           for (int cc = 0; cc < chunks && !failed; ++cc) {
             const bool is_sc = cc >= p.cin_chunks;
+            const int nsc =
+                is_sc ? min(C::SC_PER_BUF, p.sc_chunks - (cc - p.cin_chunks) * C::SC_PER_BUF) : 0;
             const int nkx = is_sc ? 1 : 3;
             for (int kx = 0; kx < nkx && !failed; ++kx) {
               if (!mbar_wait(&a_full[abuf], aphase, abort)) {
@@ -588,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               const uint32_t abase = smem_u32(sH + abuf * C::HALO_BYTES);
-              const int nky = is_sc ? 1 : 3;
+              const int nky = is_sc ? nsc : 3;
               for (int ky = 0; ky < nky; ++ky) {
                 if (!mbar_wait(&full[stage], phase, abort)) {
                   raise_error(p, abort);
@@ -597,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint64_t wd = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
-                const uint64_t xd = sw128_kmajor_desc_row(abase, ky * p.bw);
+                // band view from row ky * bw, or the ky-th shortcut tile
+                const uint64_t xd = sw128_kmajor_desc_row(abase, ky * (is_sc ? p.bh * p.bw : p.bw));
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                   umma_tf32(d_tmem, wd + 2 * k, xd + 2 * k, IDESC_SWAP, !first || (k != 0));
@@ -1386,8 +1394,8 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // instead of 48 KB, while the MMAs read 48 KB from it; with the two near
   // its bandwidth, that is 7-12% per conv on GB300. Measured slower (so left
   // to the per-tap path): 128-channel tiles (two 128-row sub-tiles), and
-  // convs with an appended shortcut (its chunks get only the two halo
-  // buffers of prefetch).
+  // convs with an appended shortcut (with its tiles one or three to an A
+  // buffer alike: 0.537 -> 0.607 ms on 512 -> 256 channels at 512^2).
   const bool halo = d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 && kp.bw == 128 &&
                     kp.splits == 1 && bn == 256 && kp.sc_chunks == 0 && buffered_a_enabled();
   // Channel-major tiles for 3x3 single-frame convs with 65-128 output

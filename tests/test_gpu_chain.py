@@ -75,6 +75,27 @@ def test_tiny_decoder_batch_and_ragged_latent():
         assert mb["cos"] >= COS_MIN, (b, mb)
 
 
+@pytest.mark.parametrize("cout", [1, 2, 4, 5])
+def test_tiny_decoder_other_output_widths(cout):
+    """conv_out widths other than RGB: the fused norm_out + conv_out head has
+    one kernel instantiation per width up to 4; wider outputs take the
+    implicit-GEMM conv after a separate GroupNorm+SiLU."""
+    import diffusion_vae_decoder_gb300 as pkg
+    seed = S.seed_of("tiny_decoder")
+    w = dict(S.make_decoder_weights("tiny", seed))
+    cin = w["conv_out.weight"].shape[1]
+    w["conv_out.weight"], w["conv_out.bias"] = S.make_conv_params(cout, cin, 3, seed + 7)
+    z = S.make_latent((1, 16, 8, 8), seed)
+    chain = pkg.VaeChain(w, n_up_blocks=4)
+    out = torch.full((1, cout, 64, 64), SENTINEL, dtype=torch.float32, device="cuda")
+    chain.decode(torch.from_numpy(z).cuda(), out=out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    chain.close()
+    ref = O.decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
+    _check(got, ref, f"tiny, {cout} output channels")
+
+
 def test_decoder_256_parity():
     seed = S.seed_of("decoder_256")
     w, z, got = _decode("flux", (1, 16, 32, 32), seed)

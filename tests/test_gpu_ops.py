@@ -146,11 +146,12 @@ def test_conv2d_halo_exact_integer(layout, n, cin, cout, h, w):
     np.testing.assert_array_equal(got, ref)
 
 
-@pytest.mark.parametrize("cout", [128, 256])
-def test_conv2d_halo_shortcut_and_residual_exact(cout):
-    """At halo-eligible widths: the conv with an appended 1x1 shortcut (per-tap
-    staging) and the in-place identity skip (halo staging when cout = 256)."""
-    n, cin, sc_c, h, w = 2, 32, 64, 5, 150
+@pytest.mark.parametrize("cout,sc_c", [(128, 64), (256, 64), (256, 128)])
+def test_conv2d_halo_shortcut_and_residual_exact(cout, sc_c):
+    """At halo-eligible widths: the conv with an appended 1x1 shortcut
+    (per-tap staging: the shortcut keeps a conv off the halo path) and the
+    in-place identity skip (halo staging when cout = 256)."""
+    n, cin, h, w = 2, 32, 5, 150
     lay = pkg().VAE_NHWC
     x = S.integer_tensor((n, cin, h, w), 24, -3, 3)
     wt = S.integer_tensor((cout, cin, 3, 3), 25, -2, 2)
@@ -209,11 +210,12 @@ def test_conv2d_channel_major_exact_integer(n, cin, cout, h, w):
     np.testing.assert_array_equal(got, ref)
 
 
-@pytest.mark.parametrize("cout", [128, 80])
-def test_conv2d_channel_major_shortcut_and_residual_exact(cout):
-    """Channel-major tiles with appended 1x1 shortcut chunks, and with the
-    in-place identity skip (residual read through the transposing staging)."""
-    n, cin, sc_c, h, w = 2, 32, 64, 5, 150
+@pytest.mark.parametrize("cout,sc_c", [(128, 64), (80, 64), (128, 96)])
+def test_conv2d_channel_major_shortcut_and_residual_exact(cout, sc_c):
+    """Channel-major tiles with appended 1x1 shortcut chunks (two tiles to an
+    A buffer; 3 chunks leave the second buffer half used), and with the
+    in-place identity skip."""
+    n, cin, h, w = 2, 32, 5, 150
     lay = pkg().VAE_NHWC
     x = S.integer_tensor((n, cin, h, w), 44, -3, 3)
     wt = S.integer_tensor((cout, cin, 3, 3), 45, -2, 2)
