@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sH = smem;  // A buffers (MODES 3 and 4)
   uint8_t *sA = smem + C::HALO_BUFS * C::HALO_BYTES;
   uint8_t *sB = sA + STAGES * C::A_BYTES;
+  const uint32_t sB_u32 = smem_u32(sB);
   float *staging = reinterpret_cast<float *>(sB + STAGES * C::B_BYTES);  // 1024-aligned
   uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_BYTES + C::STAGING);
   uint64_t *empty = full + STAGES;
@@ -543,24 +544,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               failed = true;
               break;
             }
-            const uint32_t hbase = smem_u32(sH + abuf * C::HALO_BYTES);
-            for (int tap = 0; tap < p.taps; ++tap) {
+            // The nine views differ from the buffer's descriptor only in the
+            // start-address field (row * 128 bytes >> 4; no carry: shared
+            // addresses stay below 256 KB), so they are compile-time offsets.
+            const uint64_t hdesc = sw128_kmajor_desc(smem_u32(sH + abuf * C::HALO_BYTES));
+            const bool acc0 = cc != ks0;
+            issued = true;
+#pragma unroll
+            for (int tap = 0; tap < 9; ++tap) {
               if (!mbar_wait(&full[stage], phase, abort)) {
                 raise_error(p, abort);
                 failed = true;
                 break;
               }
               tc_fence_after();
-              const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
+              const uint64_t bd = sw128_kmajor_desc(sB_u32 + stage * C::B_BYTES);
 #pragma unroll
               for (int sub = 0; sub < MS; ++sub) {
-                const uint64_t ad = sw128_kmajor_desc_row(hbase, (sub + tap / 3) * 130 + tap % 3);
+                const uint64_t ad =
+                    hdesc + static_cast<uint64_t>(((sub + tap / 3) * 130 + tap % 3) * 8);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                   umma_tf32(d_tmem + sub * BN, ad + 2 * k, bd + 2 * k, IDESC,
-                            (cc != ks0) || (tap != 0) || (k != 0));
+                            acc0 || (tap != 0) || (k != 0));
               }
-              issued = true;
               umma_commit(&empty[stage]);
               if (++stage == STAGES) {
                 stage = 0;
@@ -1426,7 +1433,10 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   }
 
   // Stream-K for convs whose whole tiles would leave the last round of SMs
-  // mostly idle (e.g. 256 tiles on 152 SMs: 1.68 rounds run as 2).
+  // mostly idle (e.g. 256 tiles on 152 SMs: 1.68 rounds run as 2). Not for
+  // the attention GEMMs (measured slower): their n-tiles of one row block
+  // share a large A operand through L2 only while they run side by side,
+  // which the stream-K ranges undo.
   kp.sk = 0;
   if (d.mode == AMode::Conv && !swap && kp.splits == 1 && d.split_ws && bn >= 32) {
     const int sms = num_sms();
@@ -1434,10 +1444,14 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
     const int units = halo ? kp.cin_chunks : kp.k_stages;
     const double rounds = static_cast<double>(tiles) / sms;
     const double eff = rounds / std::ceil(rounds);
-    const int ms = halo ? 1 : (bn == 128 ? 2 : 1);
+    const int ms = (!halo && bn == 128) ? 2 : 1;
     const size_t slot = static_cast<size_t>(ms) * bn * kBM;
     const size_t need = static_cast<size_t>(sms) * slot + static_cast<size_t>(sms) * 4;
-    if (tiles >= sms && eff < 0.9 && units >= 4 && need <= d.split_ws_floats) {
+    // Only long reductions: on short ones the tail/head partials would cost
+    // more than the idle round.
+    const int steps = halo ? kp.cin_chunks * 9 : kp.k_stages;
+    if (tiles >= sms && eff < 0.9 && units >= 4 && steps >= 64 &&
+        need <= d.split_ws_floats) {
       kp.sk = 1;
       kp.sk_units = units;
       kp.sk_total = tiles * units;
