@@ -111,7 +111,6 @@ int splitk_reduce(const float *part, int splits, long long split_stride, int sam
                   int stat_groups, long long *stat_slots, cudaStream_t s);
 // Split-K workspace that always suffices for one conv (floats).
 constexpr size_t kSplitWsFloats = 160ull * 65536;
-size_t igemm_smem_bytes(int bn);
 long long igemm_stat_slots(const IgemmDesc &d);
 int igemm_launch(const IgemmDesc &d, cudaStream_t stream);
 

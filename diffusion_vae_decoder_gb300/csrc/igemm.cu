@@ -43,6 +43,12 @@
 //             256 pixels; per 32-channel chunk and kx one band of bh + 2
 //             rows serves the three ky taps (views from row ky * bw). The
 //             epilogue transposes each 32 x 32 block into pixel-major rows.
+//
+// Work distribution: whole tiles strided over the persistent CTAs; split-K
+// slices when the tiles alone fill few SMs; stream-K ranges (a tile may be
+// cut between two neighbouring CTAs, the tail's raw sums handed over through
+// a workspace slot and a flag) when whole tiles would leave the last round
+// of SMs mostly idle.
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -1179,16 +1185,6 @@ long long igemm_stat_slots(const IgemmDesc &d) {
     return 0;
   }
   return static_cast<long long>(d.t > 0 ? d.t : 1) * tiles * ms * 4;
-}
-
-size_t igemm_smem_bytes(int bn) {
-  switch (bn) {
-    case 256: return Cfg<256, 1>::SMEM;
-    case 128: return Cfg<128, 2>::SMEM;
-    case 64: return Cfg<64, 1>::SMEM;
-    case 32: return Cfg<32, 1>::SMEM;
-    default: return Cfg<16, 1>::SMEM;
-  }
 }
 
 int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
