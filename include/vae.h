@@ -84,8 +84,10 @@ VAE_API int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout,
  * vae_upsample_conv -- nearest-2x upsample followed by a 3x3 stride-1 pad-1
  * convolution (cortiq-engine "Module vae", struct VaeUpRef):
  *   u[n,c,i,j] = x[n,c,i/2,j/2];  y = conv3x3(u) + bias
- * The upsampled tensor is never stored: the convolution gathers its operand
- * tiles straight from the low-resolution x.
+ * The upsampled tensor is never stored: per output parity (py, px) the 3x3
+ * taps land on 2x2 distinct low-resolution pixels, so the weights are summed
+ * (then rounded to TF32) into four 2x2 kernels applied to x directly; the
+ * result equals the definition up to where the rounding happens.
  *   x [n,cin,h,w]; weight [cout,cin,3,3]; bias [cout] or NULL; y [n,cout,2h,2w]
  */
 VAE_API size_t vae_upsample_conv_workspace_size(int n, int cin, int h, int w, int layout, int cout);
@@ -258,8 +260,10 @@ VAE_API int vae_chain_destroy(void *handle);
  * after replays returns the last replay's times. */
 typedef enum {
   VAE_PROF_CONV3X3 = 0,        /* 3x3 conv (flops: 2*cin*cout*9 per output pixel, + shortcut) */
-  VAE_PROF_UPSAMPLE_CONV = 1,  /* nearest-2x upsample + 3x3 conv (same per output pixel)     */
-  VAE_PROF_GROUPNORM = 2,      /* GroupNorm(+SiLU) (bytes: 12 per element: read, read, write) */
+  VAE_PROF_UPSAMPLE_CONV = 1,  /* nearest-2x upsample + 3x3 conv (flops executed: 2*cin*cout*4
+                                  per output pixel, four parity 2x2 kernels)                  */
+  VAE_PROF_GROUPNORM = 2,      /* GroupNorm(+SiLU) (bytes: 8 per element, read + write, when
+                                  the producing conv supplied the statistics; 12 otherwise)    */
   VAE_PROF_ATTENTION = 3,      /* mid attention block (flops: 4*L*L*c + 8*L*c*c per image)   */
   VAE_PROF_LAYOUT = 4,         /* latent de-normalisation / layout staging (bytes)           */
   VAE_PROF_HEAD = 5            /* norm_out GroupNorm+SiLU fused into conv_out (CUDA cores):
