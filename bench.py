@@ -434,24 +434,30 @@ def run_ours(args):
     return 0
 
 
-def run_op(args):
+SWEEP = [(128, 512), (256, 256), (512, 128), (512, 64)]  # (channels, input side)
+
+
+def time_op(op, c, hw, steps, warmup):
     """One op of the single-op sweep (batch 1, NHWC, the chain's internal layout;
-    inputs N(0,1), weights N(0, 1/(Cin*9))), timed with CUDA events."""
+    inputs N(0,1), weights N(0, 1/(Cin*9))), timed with CUDA events.
+
+    Every timed iteration is preceded by a 256 MB write that evicts L2; the
+    iterations are queued back to back (one synchronize at the end), so the
+    host enqueues the op while the GPU is still busy with the flush and the
+    events time the op's kernels, not the host's launch latency."""
     import torch
 
     import diffusion_vae_decoder_gb300 as pkg
 
-    torch.cuda.set_device(0)
-    c, hw = args.c, args.hw
     x = torch.from_numpy(S.make_normal((1, hw, hw, c), 31)).cuda()
     wt, b = S.make_conv_params(c, c, 3, 32)
     wt, b = torch.from_numpy(wt).cuda(), torch.from_numpy(b).cuda()
     g, be = (torch.from_numpy(a).cuda() for a in S.make_norm_params(c, 33))
-    if args.op == "conv":
+    if op == "conv":
         out = torch.empty_like(x)
         fn = lambda: pkg.vae_conv2d(x, wt, b, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
         work, unit = 2.0 * c * c * 9 * hw * hw, "TFLOP/s"
-    elif args.op == "upsample_conv":
+    elif op == "upsample_conv":
         out = torch.empty((1, 2 * hw, 2 * hw, c), device="cuda")
         fn = lambda: pkg.vae_upsample_conv(x, wt, b, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
         # executed work: four parity 2x2 convs, 4 taps per output pixel
@@ -460,28 +466,43 @@ def run_op(args):
         out = torch.empty_like(x)
         fn = lambda: pkg.vae_groupnorm_silu(x, g, be, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
         work, unit = 12.0 * c * hw * hw, "GB/s"
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    times = []
-    for _ in range(args.steps):
+    events = []
+    for _ in range(steps):
         flush.zero_()  # evict L2 between timed iterations
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
         e1.record()
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
+        events.append((e0, e1))
+    torch.cuda.synchronize()
+    times = [e0.elapsed_time(e1) for e0, e1 in events]
     assert pkg.vae_device_error() == 0
     ms = statistics.median(times)
     rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
     peaks, src = load_peaks()
     peak = (peaks["bf16_tflops"] * TF32_OVER_BF16 if unit == "TFLOP/s" else peaks["hbm_gbs"])
-    print(json.dumps({"op": args.op, "c": c, "hw": hw, "layout": "NHWC", "ms_median": ms,
-                      "ms_min": min(times), "rate": rate, "unit": unit, "peak": peak,
-                      "frac": rate / peak, "peak_source": src + " burst",
-                      "l2": "flushed between iterations"}), flush=True)
+    return {"op": op, "c": c, "hw": hw, "layout": "NHWC", "ms_median": ms,
+            "ms_min": min(times), "rate": rate, "unit": unit, "peak": peak,
+            "frac": rate / peak, "peak_source": src + " burst",
+            "l2": "flushed between iterations"}
+
+
+def run_op(args):
+    """`--op conv|upsample_conv|groupnorm`: one op at --c / --hw; `--op sweep`:
+    every op at every shape of the single-op sweep, one JSON line each."""
+    import torch
+
+    torch.cuda.set_device(0)
+    if args.op == "sweep":
+        for op in ("conv", "upsample_conv", "groupnorm"):
+            for c, hw in SWEEP:
+                print(json.dumps(time_op(op, c, hw, args.steps, args.warmup)), flush=True)
+        return 0
+    print(json.dumps(time_op(args.op, args.c, args.hw, args.steps, args.warmup)), flush=True)
     return 0
 
 
@@ -495,8 +516,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--detail", action="store_true",
                     help="also print every profiled step of one decode (stderr)")
-    ap.add_argument("--op", choices=["conv", "upsample_conv", "groupnorm"], default=None,
-                    help="time one op of the single-op sweep instead of the decoder")
+    ap.add_argument("--op", choices=["conv", "upsample_conv", "groupnorm", "sweep"], default=None,
+                    help="time one op of the single-op sweep (or all of them: sweep) "
+                         "instead of the decoder")
     ap.add_argument("--c", type=int, default=128)
     ap.add_argument("--hw", type=int, default=512)
     args = ap.parse_args(argv)

@@ -308,6 +308,7 @@ struct DecodeWs {
   float *ss;    // GroupNorm scale / shift for the fused head
   float *part;  // GroupNorm partials written by the producer conv's epilogue
   float *split; // split-K partial sums of the low-resolution convs
+  unsigned *gn_cnt;  // per-(sample, group) arrival counters of the GroupNorm finalize
   AttnScratch attn;
   void *gn;
 };
@@ -331,6 +332,7 @@ DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, 
   // slots: the largest tile-based count, and at least the 1024 CTAs a split-K
   // reduce may use
   d.part = cv.take<float>(static_cast<size_t>(n) * ch.groups * std::max(1024ll, p.max_slots) * 3);
+  d.gn_cnt = cv.take<unsigned>(static_cast<size_t>(n) * ch.groups);
   const size_t nl = static_cast<size_t>(n) * p.attn_l;
   const size_t lp = static_cast<size_t>(round_up32(p.attn_l));
   const int c = p.attn_c;
@@ -413,7 +415,7 @@ int run_gn(Chain &ch, const NormW &nw, const float *in, int n, long long sp, flo
   Step step(ch.prof, VAE_PROF_GROUPNORM, 0, (stats.ready ? 8.0 : 12.0) * n * sp * nw.c, s);
   if (stats.ready)
     return groupnorm_from_partials(in, n, nw.c, sp, ch.groups, ch.eps, nw.g, nw.b, 1, 1, ws.part,
-                                   stats.slots, out, ws.gn, s);
+                                   stats.slots, out, ws.gn, s, nullptr, ws.gn_cnt);
   return groupnorm_silu(in, n, nw.c, sp, 1, ch.groups, ch.eps, nw.g, nw.b, 1, 1, out, ws.gn, s);
 }
 
@@ -526,6 +528,12 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
   DecodeWs d = carve_decode(cv, *ch, p, n, h, w);
   if (!cv.ok()) return VAE_EWORKSPACE;
 
+  // The GroupNorm finalize counters start every decode at zero (each
+  // finalize leaves them at zero; this also clears what an aborted decode
+  // may have left).
+  if (cudaMemsetAsync(d.gn_cnt, 0, static_cast<size_t>(n) * ch->groups * sizeof(unsigned), s) !=
+      cudaSuccess)
+    return VAE_ECUDA;
   // z / scaling_factor + shift_factor, NCHW -> NHWC (channels padded to 32).
   const float *lat = nullptr;
   {
@@ -576,7 +584,7 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
     float *scale = d.ss, *shift = d.ss + static_cast<size_t>(n) * c;
     VAE_TRY(groupnorm_scale_shift(cur, n, c, hw, ch->groups, ch->eps, ch->norm_out.g,
                                   ch->norm_out.b, st.ready ? d.part : nullptr, st.slots, scale,
-                                  shift, d.gn, s));
+                                  shift, d.gn, s, d.gn_cnt));
     return head_gn_silu_conv(cur, n, hh, ww, c, scale, shift, ch->head_w, ch->conv_out.b, co, rgb,
                              s);
   }

@@ -148,17 +148,24 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
 // GroupNorm(+SiLU) of NHWC x whose statistics were produced by the conv
 // epilogue (float partials [n][groups][slots][3]); ws: groupnorm_ws_bytes(n,
 // c, ., groups) bytes (holds the compacted partials when slots > 64).
+// With more than 64 partials per group, `counters` (n * groups unsigned ints,
+// zero on entry and again on return) is required: the compaction's last
+// block per group finalizes the statistics.
 int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int groups,
                             float eps, const float *gamma, const float *beta, int silu,
                             int round_out, const float *part, long long slots, float *y,
-                            void *ws, cudaStream_t s, const float *residual = nullptr);
+                            void *ws, cudaStream_t s, const float *residual = nullptr,
+                            unsigned *counters = nullptr);
 
 // Only the per-(sample, channel) affine of GroupNorm: y = x * scale + shift
 // (from fused partials when `part` is given, else from a statistics pass over
-// NHWC x using ws as groupnorm_ws_bytes describes).
+// NHWC x using ws as groupnorm_ws_bytes describes). `counters` as above: with
+// them (and more than 64 partials) the partials are compacted and finalized
+// in one launch, using ws for the compacted slots.
 int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int groups, float eps,
                           const float *gamma, const float *beta, const float *part,
-                          long long slots, float *scale, float *shift, void *ws, cudaStream_t s);
+                          long long slots, float *scale, float *shift, void *ws, cudaStream_t s,
+                          unsigned *counters = nullptr);
 
 // Fused norm_out GroupNorm+SiLU + conv_out (3x3, cout <= 4) on the CUDA cores
 // (head.cu): x NHWC [n][h][w][c], y NCHW [n][cout][h][w].

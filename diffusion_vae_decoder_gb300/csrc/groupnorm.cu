@@ -271,39 +271,100 @@ __global__ void gn_apply_nchw(const float *__restrict__ x, long long total, int 
   }
 }
 
-// Finalize and apply in one kernel, for few partials per group: every CTA
-// merges its sample's partials into shared scale/shift, then runs the same
-// vectorised apply loop as gn_apply_nhwc.
-constexpr int kFusedMaxSlots = 64;  // partials merged by each apply block
+// Partials per group up to which every apply block merges them itself.
+constexpr int kFusedMaxSlots = 64;
 constexpr int kCompactThreads = 256;
 
-// Merge each (sample, group)'s `slots` partials down to kFusedMaxSlots: block
-// (b, ng) merges the contiguous slot range b of kFusedMaxSlots equal ranges
-// (fixed order: thread-strided, then a tree) and writes slot b of `out`.
+// Fixed-order merge of the 32 lanes' triples (xor butterfly: at each level a
+// lane merges the lower-lane operand first); every lane returns the total,
+// bit-identical to lane 0's.
+__device__ __forceinline__ Triple warp_merge(Triple acc) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const Triple other{__shfl_xor_sync(0xffffffffu, acc.n, o),
+                       __shfl_xor_sync(0xffffffffu, acc.mean, o),
+                       __shfl_xor_sync(0xffffffffu, acc.m2, o)};
+    acc = (threadIdx.x & o) ? merge(other, acc) : merge(acc, other);
+  }
+  return acc;
+}
+
+// Compacted slots per (sample, group) in gn_compact_finalize: one block each,
+// so a 32-group sample takes 512 blocks, a single wave on the SMs.
+constexpr int kCompactSlots = 16;
+
+// Merge each (sample, group)'s `slots` partials in two levels within one
+// launch. Block (b, ng) merges the contiguous slot range b of kCompactSlots
+// equal ranges (fixed order: thread-strided, a warp butterfly, then the
+// block's warps in order) into compacted slot b, then counts itself in on
+// its (sample, group)'s counter; the block that arrives last merges the
+// kCompactSlots compacted slots in a fixed order (so the result does not
+// depend on which block is last), writes the group's per-channel affine and
+// puts the counter back to zero for the next launch. `cnt` [n * groups] must
+// be zero on entry.
 __global__ void __launch_bounds__(kCompactThreads)
-    gn_compact(const float *__restrict__ part, long long slots, float *__restrict__ out) {
-  __shared__ Triple red[kCompactThreads];
+    gn_compact_finalize(const float *__restrict__ part, long long slots, float *compact,
+                        unsigned *cnt, int c, int groups, float eps,
+                        const float *__restrict__ gamma, const float *__restrict__ beta,
+                        float *__restrict__ scale, float *__restrict__ shift) {
+  constexpr int kWarps = kCompactThreads / 32;
+  __shared__ Triple red[kWarps];
+  __shared__ int last;
   const int b = blockIdx.x, ng = blockIdx.y;
-  const long long per = (slots + kFusedMaxSlots - 1) / kFusedMaxSlots;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long per = (slots + kCompactSlots - 1) / kCompactSlots;
   const long long s0 = b * per, s1 = s0 + per < slots ? s0 + per : slots;
   const float *e = part + static_cast<long long>(ng) * slots * 3;
   Triple acc{0.f, 0.f, 0.f};
   for (long long sl = s0 + threadIdx.x; sl < s1; sl += kCompactThreads)
     acc = merge(acc, Triple{e[3 * sl], e[3 * sl + 1], e[3 * sl + 2]});
-  red[threadIdx.x] = acc;
+  acc = warp_merge(acc);
+  if (lane == 0) red[warp] = acc;
   __syncthreads();
-  for (int w = kCompactThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] = merge(red[threadIdx.x], red[threadIdx.x + w]);
-    __syncthreads();
-  }
+  float *mine = compact + static_cast<long long>(ng) * kCompactSlots * 3;
   if (threadIdx.x == 0) {
-    float *o = out + (static_cast<long long>(ng) * kFusedMaxSlots + b) * 3;
-    o[0] = red[0].n;
-    o[1] = red[0].mean;
-    o[2] = red[0].m2;
+    Triple t = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) t = merge(t, red[w]);
+    mine[3 * b] = t.n;
+    mine[3 * b + 1] = t.mean;
+    mine[3 * b + 2] = t.m2;
+    __threadfence();  // the slot is visible device-wide before the count
+    const unsigned seen = atomicAdd(cnt + ng, 1u);
+    last = seen == kCompactSlots - 1;
+    if (last) __threadfence();  // every other block's slot is visible to this one
   }
+  __syncthreads();
+  if (!last) return;
+  // the last block: warp 0 merges the compacted slots
+  if (warp == 0) {
+    Triple t{0.f, 0.f, 0.f};
+    if (lane < kCompactSlots)
+      t = Triple{__ldcg(mine + 3 * lane), __ldcg(mine + 3 * lane + 1),
+                 __ldcg(mine + 3 * lane + 2)};
+    t = warp_merge(t);
+    if (lane == 0) red[0] = t;
+  }
+  __syncthreads();
+  const int cg = c / groups;
+  const int n = ng / groups, g = ng % groups;
+  for (int i = threadIdx.x; i < cg; i += kCompactThreads) {
+    // FP64 only on the cg threads that write a channel (FP64 is slow here)
+    const double cntv = red[0].n;
+    const double mean = red[0].mean;
+    const double var = cntv > 0 ? red[0].m2 / cntv : 0.0;
+    const double rstd = 1.0 / sqrt(var + static_cast<double>(eps));
+    const int ch = g * cg + i;
+    const double a = rstd * gamma[ch];
+    scale[n * c + ch] = static_cast<float>(a);
+    shift[n * c + ch] = static_cast<float>(beta[ch] - mean * a);
+  }
+  if (threadIdx.x == 0) cnt[ng] = 0u;
 }
 
+// Finalize and apply in one kernel, for few partials per group: every CTA
+// merges its sample's partials into shared scale/shift, then runs the same
+// vectorised apply loop as gn_apply_nhwc.
 __global__ void __launch_bounds__(256)
     gn_apply_fused_nhwc(const float *__restrict__ x, unsigned per_sample4, int c,
                         const float *__restrict__ part, int slots, int groups, float eps,
@@ -469,11 +530,22 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
 int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int groups, float eps,
                           const float *gamma, const float *beta, const float *part,
                           long long slots, float *scale, float *shift, void *ws,
-                          cudaStream_t s) {
+                          cudaStream_t s, unsigned *counters) {
   if (!x || !gamma || !beta || !scale || !shift || n <= 0 || c <= 0 || spatial <= 0 ||
       groups <= 0)
     return VAE_EINVAL;
   if (c % groups || c % 4 || c > 1024) return VAE_EUNSUPPORTED;
+  if (part && counters && slots > kFusedMaxSlots) {
+    if (!ws) return VAE_EINVAL;
+    Carver cv(ws, ~size_t(0));
+    float *compact = cv.take<float>(static_cast<size_t>(n) * groups * kCompactSlots * 3);
+    gn_compact_finalize<<<dim3(kCompactSlots, static_cast<unsigned>(n * groups)),
+                          kCompactThreads, 0, s>>>(part, slots, compact, counters, c, groups,
+                                                   eps, gamma, beta, scale, shift);
+    if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+    count_launches(1);
+    return VAE_OK;
+  }
   if (part) {
     gn_finalize<float><<<n * groups, kFinalizeThreads, 0, s>>>(part, slots, c, groups, eps, gamma, beta,
                                                   scale, shift);
@@ -499,7 +571,8 @@ int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int g
 int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int groups,
                             float eps, const float *gamma, const float *beta, int silu,
                             int round_out, const float *part, long long slots, float *y,
-                            void *ws, cudaStream_t s, const float *residual) {
+                            void *ws, cudaStream_t s, const float *residual,
+                            unsigned *counters) {
   if (!x || !y || !gamma || !beta || !ws || !part || n <= 0 || c <= 0 || spatial <= 0 ||
       groups <= 0 || slots <= 0)
     return VAE_EINVAL;
@@ -518,19 +591,18 @@ int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int
     count_launches(1);
     return VAE_OK;
   }
-  // Many partials: compact them with all SMs busy, merge the few left into
-  // scale/shift once, then the plain apply pass.
+  // Many partials: compact them with all SMs busy and merge the compacted
+  // slots into scale/shift in the same launch, then the plain apply pass.
   float *scale = cv.take<float>(static_cast<size_t>(n) * c);
   float *shift = cv.take<float>(static_cast<size_t>(n) * c);
-  float *compact = cv.take<float>(static_cast<size_t>(n) * groups * kFusedMaxSlots * 3);
-  gn_compact<<<dim3(kFusedMaxSlots, static_cast<unsigned>(n * groups)), kCompactThreads, 0, s>>>(
-      part, slots, compact);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
-  gn_finalize<float><<<n * groups, kFinalizeThreads, 0, s>>>(compact, kFusedMaxSlots, c, groups,
-                                                             eps, gamma, beta, scale, shift);
+  float *compact = cv.take<float>(static_cast<size_t>(n) * groups * kCompactSlots * 3);
+  if (!counters) return VAE_EINVAL;
+  gn_compact_finalize<<<dim3(kCompactSlots, static_cast<unsigned>(n * groups)),
+                        kCompactThreads, 0, s>>>(part, slots, compact, counters, c, groups, eps,
+                                                 gamma, beta, scale, shift);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   VAE_TRY(launch_apply_nhwc(x, n, c, spatial, scale, shift, silu, round_out, residual, y, s));
-  count_launches(3);
+  count_launches(2);
   return VAE_OK;
 }
 

@@ -10,9 +10,11 @@
 // raw channels of chunk i+1 into shared memory while chunk i is convolved;
 // the GroupNorm affine and SiLU are applied on the way from that box into
 // channel planes (zeros outside the image: the conv's padding applies after
-// the normalisation). Every thread accumulates eight output pixels of one row
-// (two runs of four, 64 pixels apart), reading the planes with 16-byte loads
-// and each weight once for all eight. The RGB result is written NCHW.
+// the normalisation). Every thread accumulates four adjacent output pixels
+// of one row, reading the planes with 16-byte loads and each weight once for
+// all four; a warp covers one row of the tile, so the loads of a warp are
+// consecutive 16-byte words. The chunk's weights and affine are fetched
+// before its box is waited for. The RGB result is written NCHW.
 #include <mutex>
 
 #include "common.cuh"
@@ -22,10 +24,11 @@ namespace vae {
 
 namespace {
 
-// Output tile TH = 8 rows x TW = 128 pixels; thread (ty, tx), tx < 16,
-// computes pixels 4*tx .. 4*tx+3 and 64+4*tx .. 64+4*tx+3 of row ty.
+// Output tile TH = 8 rows x TW = 128 pixels; thread (ty, tx), tx < 32,
+// computes pixels 4*tx .. 4*tx+3 of row ty (256 threads: with two CTAs per
+// SM, as shared memory allows, 16 warps hide the latencies).
 constexpr int kTH = 8, kTW = 128, kCC = 8;  // 4-channel chunks measured slower
-constexpr int kThr = kTH * 16;     // 128 threads
+constexpr int kThr = kTH * 32;     // 256 threads
 constexpr int kHH = kTH + 2;       // halo rows
 constexpr int kHW = kTW + 2;       // halo width 130
 constexpr int kRow = 132;          // padded plane row (16-byte aligned rows)
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(kThr)
   volatile uint32_t *abort = reinterpret_cast<uint32_t *>(bar + 1);
   const int n = blockIdx.z;
   const int x0 = blockIdx.x * kTW, y0 = blockIdx.y * kTH;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     *abort = 0u;
@@ -66,17 +69,27 @@ __global__ void __launch_bounds__(kThr)
     mbar_arrive_expect_tx(bar, kRawBytes);
     tma_load_4d(raw, &tmX, bar, 0, x0 - 1, y0 - 1, n);
   }
-  float acc[2][4][CO];  // [run][pixel][output channel]
+  float acc[4][CO];  // [pixel][output channel]
 #pragma unroll
   for (int o = 0; o < CO; ++o) {
     const float b = bias ? bias[o] : 0.f;
 #pragma unroll
-    for (int px = 0; px < 4; ++px) acc[0][px][o] = acc[1][px][o] = b;
+    for (int px = 0; px < 4; ++px) acc[px][o] = b;
   }
   const float *sc = scale + static_cast<size_t>(n) * C;
   const float *sh = shift + static_cast<size_t>(n) * C;
   uint32_t phase = 0;
   for (int c0 = 0; c0 < C; c0 += kCC) {
+    // this chunk's weights and affine, in flight while the box is awaited
+    float4 wreg = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x < 9 * kCC) {
+      const int tap = threadIdx.x / kCC, cg = c0 + threadIdx.x % kCC;
+      wreg = __ldg(wpk + (cg / 32) * 288 + tap * 32 + (cg % 32));
+    }
+    const float4 ga = __ldg(reinterpret_cast<const float4 *>(sc + c0));
+    const float4 gb = __ldg(reinterpret_cast<const float4 *>(sc + c0 + 4));
+    const float4 ha = __ldg(reinterpret_cast<const float4 *>(sh + c0));
+    const float4 hb = __ldg(reinterpret_cast<const float4 *>(sh + c0 + 4));
     const bool ok = mbar_wait(bar, phase, abort);
     if (__syncthreads_or(!ok)) {  // the box never landed: report, leave
       if (threadIdx.x == 0) atomicCAS(err, 0, static_cast<int>(VAE_EDEVICE_TIMEOUT));
@@ -84,10 +97,6 @@ __global__ void __launch_bounds__(kThr)
     }
     phase ^= 1u;
     // raw box -> normalised channel planes
-    const float4 ga = __ldg(reinterpret_cast<const float4 *>(sc + c0));
-    const float4 gb = __ldg(reinterpret_cast<const float4 *>(sc + c0 + 4));
-    const float4 ha = __ldg(reinterpret_cast<const float4 *>(sh + c0));
-    const float4 hb = __ldg(reinterpret_cast<const float4 *>(sh + c0 + 4));
     const float gs[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
     const float hs[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
     const float4 *raw4 = reinterpret_cast<const float4 *>(raw);
@@ -106,11 +115,7 @@ __global__ void __launch_bounds__(kThr)
         d[j * kChan] = in ? r : 0.f;
       }
     }
-    for (int l = threadIdx.x; l < 9 * kCC; l += kThr) {
-      const int tap = l / kCC, c = l % kCC;
-      const int cg = c0 + c;
-      wsm[l] = wpk[(cg / 32) * 288 + tap * 32 + (cg % 32)];
-    }
+    if (threadIdx.x < 9 * kCC) wsm[threadIdx.x] = wreg;
     __syncthreads();  // box consumed; planes and weights ready
     if (threadIdx.x == 0 && c0 + kCC < C) {
       fence_proxy_async_smem();
@@ -123,20 +128,16 @@ __global__ void __launch_bounds__(kThr)
       for (int ky = 0; ky < 3; ++ky) {
         const float4 *rowp =
             reinterpret_cast<const float4 *>(hal + c * kChan + (ty + ky) * kRow) + tx;
-        const float4 a0 = rowp[0], a1 = rowp[1], b0v = rowp[16], b1v = rowp[17];
-        const float xs[2][6] = {{a0.x, a0.y, a0.z, a0.w, a1.x, a1.y},
-                                {b0v.x, b0v.y, b0v.z, b0v.w, b1v.x, b1v.y}};
+        const float4 a0 = rowp[0], a1 = rowp[1];
+        const float xs[6] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y};
 #pragma unroll
         for (int kx = 0; kx < 3; ++kx) {
           const float4 w = wsm[(ky * 3 + kx) * kCC + c];
           const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int r = 0; r < 2; ++r)
+          for (int px = 0; px < 4; ++px)
 #pragma unroll
-            for (int px = 0; px < 4; ++px)
-#pragma unroll
-              for (int o = 0; o < CO; ++o)
-                acc[r][px][o] = fmaf(xs[r][px + kx], wv[o], acc[r][px][o]);
+            for (int o = 0; o < CO; ++o) acc[px][o] = fmaf(xs[px + kx], wv[o], acc[px][o]);
         }
       }
     }
@@ -144,20 +145,16 @@ __global__ void __launch_bounds__(kThr)
   }
   const int gy = y0 + ty;
   if (gy >= H) return;
+  const int gx = x0 + 4 * tx;
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int gx = x0 + r * 64 + 4 * tx;
+  for (int o = 0; o < CO; ++o) {
+    float *dst = y + (static_cast<size_t>(n * CO + o) * H + gy) * W + gx;
+    if (gx + 3 < W && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+      *reinterpret_cast<float4 *>(dst) = make_float4(acc[0][o], acc[1][o], acc[2][o], acc[3][o]);
+    } else {
 #pragma unroll
-    for (int o = 0; o < CO; ++o) {
-      float *dst = y + (static_cast<size_t>(n * CO + o) * H + gy) * W + gx;
-      if (gx + 3 < W && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-        *reinterpret_cast<float4 *>(dst) =
-            make_float4(acc[r][0][o], acc[r][1][o], acc[r][2][o], acc[r][3][o]);
-      } else {
-#pragma unroll
-        for (int px = 0; px < 4; ++px)
-          if (gx + px < W) dst[px] = acc[r][px][o];
-      }
+      for (int px = 0; px < 4; ++px)
+        if (gx + px < W) dst[px] = acc[px][o];
     }
   }
 }
