@@ -245,7 +245,11 @@ VAE_API int vae_chain_prepare(const vae_chain_args *args, void **handle, vae_str
  * 0 for a null handle. */
 VAE_API size_t vae_chain_workspace_size(const void *handle, int n, int h, int w);
 /*   z   [n,latent_channels,h,w] NCHW (not yet de-normalised)
- *   rgb [n,3,8h,8w] NCHW (raw decoder output, not clamped) */
+ *   rgb [n,3,8h,8w] NCHW (raw decoder output, not clamped)
+ * The workspace needs no initialisation (the decode clears the counters and
+ * flags it relies on) and holds one decode's intermediate state, so decodes
+ * that may overlap on the GPU need workspaces of their own. Every reduction
+ * has a fixed order: the same inputs give the same bits. */
 VAE_API int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *rgb, void *ws,
                      size_t ws_bytes, vae_stream_t stream);
 VAE_API int vae_chain_destroy(void *handle);
