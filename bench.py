@@ -401,9 +401,12 @@ def run_ours(args):
                              "beyond the 129 MB L2"},
             "roofline": {"bound": "tensor", "kernel": "igemm_kernel (3x3 / upsample conv)",
                          "achieved": conv_tflops, "peak": tf32_peak, "unit": "TFLOP/s",
-                         "frac": conv_tflops / tf32_peak, "traffic": traffic,
-                         "traffic_per": "decode: sum over the igemm conv launches of one decode "
-                                        f"({traffic_launches} launches), ncu dram bytes read+write",
+                         "frac": conv_tflops / tf32_peak,
+                         "traffic": traffic / traffic_launches if traffic else None,
+                         "traffic_per": "launch: ncu dram bytes read+write of the igemm conv "
+                                        "launches of one decode, averaged over its "
+                                        f"{traffic_launches} launches",
+                         "traffic_per_decode": traffic,
                          "peak_source": f"{peak_src} bf16 sustained x {TF32_OVER_BF16:.4f} "
                                         "(nominal TF32/BF16 dense ratio)",
                          "share_of_step": conv_ms / n_prof / ms_profiled,
