@@ -211,6 +211,18 @@ def _attn_torch(x, p, groups=32):
     return (xt + o.transpose(1, 2).reshape(n, c, h, w)).numpy()
 
 
+def test_attention_hand_golden(golden_dir):
+    """Two tokens, two channels, worked by hand (the fixture states the
+    steps): pins GroupNorm before the projections, the out x in orientation of
+    every Linear, the biases, the 1/sqrt(c) scale and the residual add."""
+    g = _load(golden_dir, "attention_hand.json")
+    a = {k: np.array(v, dtype=np.float64) for k, v in g.items() if k not in ("source",)}
+    p = {"group_norm": (a["gamma"], a["beta"]), "to_q": (a["wq"], a["bq"]),
+         "to_k": (a["wk"], a["bk"]), "to_v": (a["wv"], a["bv"]), "to_out": (a["wo"], a["bo"])}
+    y = O.mid_attention(a["x"], p, groups=int(g["groups"]), eps=float(g["eps"]))
+    np.testing.assert_allclose(y, a["y"], rtol=0, atol=1e-13)
+
+
 @pytest.mark.parametrize("shape", [(1, 64, 4, 5), (2, 32, 3, 3)])
 def test_attention_vs_torch_sdpa(shape):
     x = _rng(9).standard_normal(shape)
