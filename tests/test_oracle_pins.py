@@ -410,6 +410,18 @@ def _decode_torch(z, w, sf, sh, n_up):
     return conv(x, "conv_out").numpy()
 
 
+def test_denormalize_closed_forms():
+    """z / scaling_factor + shift_factor, elementwise: z = s maps to 1 + t,
+    z = 0 to t, and z = -t*s to 0 (it undoes the encoder-side (x - t) * s); a
+    swapped order (z + t) / s or a product z * s + t fails every case."""
+    s, t = 0.3611, 0.1159
+    z = np.array([[[[s, 0.0], [-t * s, 2.0 * s]]]])
+    want = np.array([[[[1.0 + t, t], [0.0, 2.0 + t]]]])
+    np.testing.assert_allclose(O.denormalize(z, s, t), want, rtol=0, atol=1e-15)
+    x = _rng(21).standard_normal((2, 16, 3, 5))
+    np.testing.assert_allclose(O.denormalize((x - t) * s, s, t), x, rtol=0, atol=1e-14)
+
+
 def test_tiny_decoder_vs_torch_restatement():
     w = S.make_decoder_weights("tiny", seed=1000)
     z = S.make_latent((1, 16, 4, 4), seed=1000)
