@@ -16,7 +16,9 @@
 //         place: conv2's epilogue adds the skip element by element)
 //   T     GroupNorm+SiLU output (TF32-rounded: it is the next conv's operand)
 //   H     conv1 output
-// plus the latent staging buffer and the attention scratch.
+// plus the latent staging buffer, the GroupNorm partials that conv epilogues
+// write with the per-group arrival counters of their finalize (zeroed at the
+// start of every decode), the split-K area and the attention scratch.
 #include <cmath>
 #include <vector>
 
