@@ -26,6 +26,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
+
 import vae_synth as S  # noqa: E402
 
 WORKLOADS = {
@@ -43,8 +45,8 @@ WORKLOADS = {
                                 "[4,3,512,512], random init"),
 }
 METRIC = "VAE decode Mpix/s"
-# Nominal dense tensor rates (PFLOP/s): TF32 1.1 vs BF16 2.25; the TF32 peak is
-# the measured BF16 peak scaled by this ratio.
+# Nominal dense tensor rates (PFLOP/s): TF32 1.1 vs BF16 2.25 (context only: the
+# roofline fraction is taken against the TF32 MMA rate measured in the run).
 TF32_OVER_BF16 = 1.1 / 2.25
 FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
 
@@ -159,26 +161,27 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
-def conv_traffic_from_profile(workload):
-    """DRAM bytes per decode of the implicit-GEMM conv launches, from the
-    committed ncu summary of this workload -- None when that summary is
-    missing or was taken on a different igemm.cu (the kernel has changed)."""
+def conv_traffic_from_profile(workload, path=None):
+    """DRAM bytes per launch of the implicit-GEMM conv in this workload, from
+    the committed machine-readable ncu summary (profiles/igemm_traffic.json:
+    dram__bytes_read.sum + dram__bytes_write.sum of one conv launch, with the
+    scale to this workload's average conv launch) -- None when the summary is
+    missing, has no entry for the workload, or was taken on a different
+    igemm.cu (the kernel has changed since the counters were read)."""
     import hashlib
-    import re
-    path = os.path.join(ROOT, "profiles", f"launch_list_{workload}.md")
+    path = path or os.path.join(ROOT, "profiles", "igemm_traffic.json")
     src = os.path.join(ROOT, "diffusion_vae_decoder_gb300", "csrc", "igemm.cu")
     if not os.path.exists(path):
         return None, None
-    text = open(path).read()
-    sha = re.search(r"igemm\.cu sha256 at capture: ([0-9a-f]{64})", text)
-    nbytes = re.search(r"igemm conv DRAM bytes per decode \(read \+ write\): (\d+)", text)
-    nlaunch = re.search(r"igemm conv launches per decode: (\d+)", text)
-    if not (sha and nbytes and nlaunch):
-        return None, None
+    with open(path) as f:
+        data = json.load(f)
     with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != sha.group(1):
+        if hashlib.sha256(f.read()).hexdigest() != data.get("igemm_cu_sha256"):
             return None, None
-    return float(nbytes.group(1)), int(nlaunch.group(1))
+    entry = data.get("workloads", {}).get(workload)
+    if not entry:
+        return None, None
+    return float(entry["bytes_per_launch"]), entry
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -192,6 +195,15 @@ def time_oracle_decode(latent, seed, repeats=1):
         oracle.decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
     dt = (time.perf_counter() - t0) / repeats
     return dt, out_pixels(latent) / 1e6
+
+
+def measure_tf32_peak(pkg, seconds=0.3):
+    """TF32 tensor-pipe rate of this GPU (TFLOP/s) from the library's MMA-loop
+    microkernel, with the SM clock sampled while it runs."""
+    pkg.vae_measure_tf32_mma(2000)  # warm-up / calibration
+    tf, ms, _ = pkg.vae_measure_tf32_mma(20000)
+    iters = max(20000, int(20000 * seconds * 1e3 / max(ms, 1e-3)))
+    return tf, iters
 
 
 def host_cores():
@@ -321,9 +333,16 @@ def run_ours(args):
     value = world * mpix / (ms_max / 1e3)
     n_prof = 1  # one decode's worth of step records
 
-    # ---- roofline of the dominant kernel (the implicit-GEMM conv) and of GroupNorm
+    # ---- roofline of the dominant kernel (the implicit-GEMM conv) and of
+    # GroupNorm. The conv's denominator is this GPU's TF32 tensor-pipe rate,
+    # measured right here by the library's MMA-loop microkernel with the SM
+    # clock sampled while it runs (the timed decode's clock is sampled above).
     peaks, peak_src = load_peaks()
-    tf32_peak = peaks["bf16_tflops_sustained"] * TF32_OVER_BF16
+    with ClockSampler(gpu_index) as psampler:
+        _, iters = measure_tf32_peak(pkg)
+        tf32_peak, tf32_ms, _ = pkg.vae_measure_tf32_mma(iters)
+    tf32_clocks = psampler.summary()
+    bf16_derived = peaks["bf16_tflops"] * TF32_OVER_BF16
     conv = [r for r in recs if r["kind"] in ("conv3x3", "upsample_conv")]
     gn = [r for r in recs if r["kind"] == "groupnorm"]
     conv_ms = sum(r["ms"] for r in conv)  # per decode
@@ -379,7 +398,10 @@ def run_ours(args):
     barrier(dist)
     e2e_value = world * mpix / (e2e_ms / 1e3)
 
-    traffic, traffic_launches = conv_traffic_from_profile(args.workload)
+    traffic, traffic_entry = conv_traffic_from_profile(args.workload)
+    extras = None
+    if rank == 0 and world == 1 and not args.no_extras:
+        extras = run_extras(pkg, tf32_peak, gpu_index)
     line = None
     if rank == 0:
         cpu = None
@@ -402,13 +424,14 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "kernel": "igemm_kernel (3x3 / upsample conv)",
                          "achieved": conv_tflops, "peak": tf32_peak, "unit": "TFLOP/s",
                          "frac": conv_tflops / tf32_peak,
-                         "traffic": traffic / traffic_launches if traffic else None,
-                         "traffic_per": "launch: ncu dram bytes read+write of the igemm conv "
-                                        "launches of one decode, averaged over its "
-                                        f"{traffic_launches} launches",
-                         "traffic_per_decode": traffic,
-                         "peak_source": f"{peak_src} bf16 sustained x {TF32_OVER_BF16:.4f} "
-                                        "(nominal TF32/BF16 dense ratio)",
+                         "traffic": traffic,
+                         "traffic_source": traffic_entry,
+                         "peak_source": "measured in this run: tcgen05 kind::tf32 MMA loop on "
+                                        "every SM, operands resident in shared memory "
+                                        f"({tf32_ms:.0f} ms; SM clock median "
+                                        f"{tf32_clocks.get('sm_mhz')} MHz)",
+                         "frac_vs_bf16_burst_derived": conv_tflops / bf16_derived,
+                         "bf16_burst_derived_peak": bf16_derived,
                          "share_of_step": conv_ms / n_prof / ms_profiled,
                          "measured": "CUDA events around every conv step inside the profiled "
                                      "capture of the decode, last of the K profiled replays run "
@@ -429,12 +452,102 @@ def run_ours(args):
             "gpu_launches": int(launches),
             "launches_per_decode": int(launches_per_decode),
             "clocks": sampler.summary(),
+            "extra_workloads": extras,
         }
         print(json.dumps(line), flush=True)
     chain.close()
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def _graph_decode_stats(pkg, arch, latent, seed, steps):
+    """Device time per decode of one latent (CUDA-graph replays, CUDA events)
+    and the conv steps' TFLOP/s from a profiled capture."""
+    import torch
+    chain = pkg.VaeChain(S.make_decoder_weights(arch, seed), n_up_blocks=4)
+    n, _, h, w = latent
+    z = torch.from_numpy(S.make_latent(latent, seed)).cuda()
+    out = torch.empty((n, 3, 8 * h, 8 * w), device="cuda")
+    ws = torch.empty(chain.workspace_size(n, h, w), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        chain.decode(z, out=out, ws=ws)
+    graph = chain.capture_graph(z, out, ws)
+    chain.profile(True)
+    pgraph = chain.capture_graph(z, out, ws)
+    chain.profile(False)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    pgraph.replay()
+    torch.cuda.synchronize()
+    recs = chain.profile_read()
+    chain.close()
+    assert pkg.vae_device_error() == 0
+    conv = [r for r in recs if r["kind"] in ("conv3x3", "upsample_conv")]
+    conv_ms = sum(r["ms"] for r in conv)
+    return ms, sum(r["flops"] for r in conv) / (conv_ms / 1e3) / 1e12, conv_ms
+
+
+def run_extras(pkg, tf32_peak, gpu_index):
+    """The other configured workloads, each on its own (rank 0, one GPU):
+    the 256^2 decode (Mpix/s), the tiny decoder (latency), the 3-D causal
+    conv stack [1,128,17,128,128] (conv TFLOP/s)."""
+    import torch
+    out = {}
+    ms, conv_tf, conv_ms = _graph_decode_stats(pkg, "flux", (1, 16, 32, 32),
+                                               S.seed_of("decoder_256"), 200)
+    out["decoder_256"] = {"value": out_pixels((1, 16, 32, 32)) / 1e6 / (ms / 1e3),
+                          "unit": "Mpix/s", "ms_per_step": ms, "steps": 200,
+                          "conv_tflops": conv_tf, "conv_frac": conv_tf / tf32_peak,
+                          "conv_ms_per_step": conv_ms}
+    ms, conv_tf, _ = _graph_decode_stats(pkg, "tiny", (1, 16, 8, 8), S.seed_of("tiny_decoder"),
+                                         500)
+    out["tiny_decoder"] = {"latency_ms": ms, "value": out_pixels((1, 16, 8, 8)) / 1e6 / (ms / 1e3),
+                           "unit": "Mpix/s", "steps": 500}
+    # 3-D causal conv stack, NDHWC (the kernels' layout): five 3x3x3 convs with
+    # GroupNorm+SiLU and the residual every two layers.
+    shape = S.WORKLOADS["causal3d_stack"]["shape"]
+    x, layers = S.make_causal_stack(shape, 5, S.seed_of("causal3d_stack"))
+    xd = torch.from_numpy(np.ascontiguousarray(np.moveaxis(x, 1, -1))).cuda()
+    dl = [{k: torch.from_numpy(v).cuda() for k, v in L.items()} for L in layers]
+    y = torch.empty_like(xd)
+    n, c, t, h, w = shape
+    flops_conv = 2.0 * c * c * 27 * n * t * h * w
+    for _ in range(3):
+        pkg.vae_causal_stack(xd, dl, layout=pkg.VAE_NHWC, out=y)
+    one = torch.empty_like(xd)
+    for _ in range(3):
+        pkg.vae_conv3d_causal(xd, dl[0]["weight"], dl[0]["bias"], layout=pkg.VAE_NHWC, out=one)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record()
+    for _ in range(5):
+        pkg.vae_causal_stack(xd, dl, layout=pkg.VAE_NHWC, out=y)
+    ev[1].record()
+    ev[2].record()
+    for _ in range(10):
+        pkg.vae_conv3d_causal(xd, dl[0]["weight"], dl[0]["bias"], layout=pkg.VAE_NHWC, out=one)
+    ev[3].record()
+    torch.cuda.synchronize()
+    assert pkg.vae_device_error() == 0
+    stack_ms = ev[0].elapsed_time(ev[1]) / 5
+    conv_ms = ev[2].elapsed_time(ev[3]) / 10
+    out["causal3d_stack"] = {
+        "shape": list(shape), "stack_ms": stack_ms,
+        "stack_conv_tflops": 5 * flops_conv / (stack_ms / 1e3) / 1e12,
+        "conv_ms": conv_ms, "conv_tflops": flops_conv / (conv_ms / 1e3) / 1e12,
+        "conv_frac": flops_conv / (conv_ms / 1e3) / 1e12 / tf32_peak,
+        "note": "stack = five convs + five GroupNorm+SiLU (+ weight packing), NDHWC; conv = one "
+                "vae_conv3d_causal call (its weight packing included)"}
+    return out
 
 
 SWEEP = [(128, 512), (256, 256), (512, 128), (512, 64)]  # (channels, input side)
@@ -517,6 +630,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decoder_1024")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other workloads (256^2 decode, tiny decoder, 3-D stack)")
     ap.add_argument("--detail", action="store_true",
                     help="also print every profiled step of one decode (stderr)")
     ap.add_argument("--op", choices=["conv", "upsample_conv", "groupnorm", "sweep"], default=None,

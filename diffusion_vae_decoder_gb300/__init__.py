@@ -75,6 +75,17 @@ class ProfRecord(ctypes.Structure):
 PROF_KINDS = {0: "conv3x3", 1: "upsample_conv", 2: "groupnorm", 3: "attention", 4: "layout",
               5: "head"}
 
+
+class TracePoint(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("c", ctypes.c_int), ("h", ctypes.c_int),
+                ("w", ctypes.c_int), ("input", ctypes.c_int), ("skip", ctypes.c_int),
+                ("bytes", ctypes.c_size_t)]
+
+
+TRACE_KINDS = {0: "latent", 1: "conv", 2: "groupnorm", 3: "resnet", 4: "attention",
+               5: "upsample", 6: "rgb"}
+INJECT_WITHHOLD_STREAMK_FLAG = 1
+
 _I, _LL, _F, _SZ = ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
     "vae_conv2d_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
@@ -103,6 +114,15 @@ _SIGS = {
     "vae_chain_profile": (_I, [_P, _I]),
     "vae_chain_profile_read": (_I, [_P, ctypes.POINTER(ProfRecord), _I, ctypes.POINTER(_I)]),
     "vae_kernel_launch_count": (_LL, []),
+    "vae_chain_trace_points": (_I, [_P, _I, _I, _I, ctypes.POINTER(TracePoint), _I,
+                                    ctypes.POINTER(_I)]),
+    "vae_decode_chain_traced": (_I, [_P, _P, _I, _I, _I, _P, _P, _SZ, ctypes.POINTER(_P), _I,
+                                     _P]),
+    "vae_measure_tf32_mma": (_I, [_I, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_float), _P]),
+    "vae_debug_set_wait_limit": (_I, [ctypes.c_ulonglong]),
+    "vae_debug_inject": (_I, [_I]),
+    "vae_debug_fail_allocation": (_I, [_I]),
 }
 
 
@@ -318,6 +338,26 @@ def vae_causal_stack(x, layers, groups=32, eps=1e-6, layout=VAE_NCHW, out=None, 
     return out
 
 
+def vae_measure_tf32_mma(iters, stream=None):
+    """(TFLOP/s, ms, flops) of the tensor-pipe TF32 MMA loop (vae_measure_tf32_mma)."""
+    flops, ms = ctypes.c_double(0), ctypes.c_float(0)
+    _check("vae_measure_tf32_mma", load_library().vae_measure_tf32_mma(
+        int(iters), ctypes.byref(flops), ctypes.byref(ms), _stream(stream)))
+    return flops.value / (ms.value / 1e3) / 1e12, ms.value, flops.value
+
+
+def vae_debug_set_wait_limit(ns):
+    _check("vae_debug_set_wait_limit", load_library().vae_debug_set_wait_limit(int(ns)))
+
+
+def vae_debug_inject(bits):
+    _check("vae_debug_inject", load_library().vae_debug_inject(int(bits)))
+
+
+def vae_debug_fail_allocation(nth):
+    _check("vae_debug_fail_allocation", load_library().vae_debug_fail_allocation(int(nth)))
+
+
 def vae_device_error(stream=None):
     lib = load_library()
     code = ctypes.c_int(0)
@@ -410,6 +450,37 @@ class VaeChain:
             ws = _ws(self.workspace_size(n, h, w), z.device)
         _check("vae_decode_chain", lib.vae_decode_chain(
             self.handle, _ptr(z), n, h, w, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+        return out
+
+    def trace_points(self, n, h, w):
+        """The decode's trace points (vae_chain_trace_points) as dicts."""
+        lib = load_library()
+        cnt = ctypes.c_int(0)
+        _check("vae_chain_trace_points", lib.vae_chain_trace_points(
+            self.handle, n, h, w, None, 0, ctypes.byref(cnt)))
+        arr = (TracePoint * max(1, cnt.value))()
+        _check("vae_chain_trace_points", lib.vae_chain_trace_points(
+            self.handle, n, h, w, arr, cnt.value, ctypes.byref(cnt)))
+        return [dict(kind=TRACE_KINDS[p.kind], c=p.c, h=p.h, w=p.w, input=p.input, skip=p.skip,
+                     bytes=p.bytes) for p in arr[:cnt.value]]
+
+    def decode_traced(self, z, trace, out=None, ws=None, stream=None):
+        """vae_decode_chain_traced: ``trace`` is a list with one CUDA tensor
+        (or None) per trace point, receiving that step's output."""
+        lib = load_library()
+        _need(z, "z")
+        n, c, h, w = z.shape
+        if out is None:
+            import torch
+            f = self.up_factor
+            out = torch.empty((n, self.out_channels, f * h, f * w), dtype=torch.float32,
+                              device=z.device)
+        if ws is None:
+            ws = _ws(self.workspace_size(n, h, w), z.device)
+        bufs = (_P * max(1, len(trace)))(*[None if t is None else t.data_ptr() for t in trace])
+        _check("vae_decode_chain_traced", lib.vae_decode_chain_traced(
+            self.handle, _ptr(z), n, h, w, _ptr(out), _ptr(ws), ws.numel(), bufs, len(trace),
+            _stream(stream)))
         return out
 
     def capture_graph(self, z, out, ws):

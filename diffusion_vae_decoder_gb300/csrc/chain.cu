@@ -20,6 +20,8 @@
 // write with the per-group arrival counters of their finalize (zeroed at the
 // start of every decode), the split-K area and the attention scratch.
 #include <cmath>
+#include <mutex>
+#include <unordered_set>
 #include <vector>
 
 #include "common.cuh"
@@ -29,7 +31,31 @@ namespace vae {
 
 namespace {
 
-constexpr uint32_t kMagic = 0x56414543u;  // "VAEC"
+// Registry of live handles: entry points check a handle here instead of
+// reading through it, so a destroyed handle is rejected without touching
+// freed memory.
+std::mutex g_live_mu;
+std::unordered_set<const void *> g_live;
+
+bool is_live(const void *h) {
+  if (!h) return false;
+  std::lock_guard<std::mutex> lk(g_live_mu);
+  return g_live.count(h) != 0;
+}
+
+// Copies each step's output into the caller's trace buffers (in order).
+struct Tracer {
+  float *const *bufs = nullptr;
+  int n = 0;
+  int idx = 0;
+  int status = VAE_OK;
+  void emit(const void *src, size_t bytes, cudaStream_t s) {
+    if (idx < n && bufs[idx] &&
+        cudaMemcpyAsync(bufs[idx], src, bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      status = VAE_ECUDA;
+    ++idx;
+  }
+};
 
 struct ConvW {
   float *w = nullptr, *b = nullptr;
@@ -106,8 +132,8 @@ struct Profiler {
 };
 
 struct Chain {
-  uint32_t magic = kMagic;
   Profiler prof;
+  Tracer *tr = nullptr;  // set for the duration of a traced decode
   int device = 0;
   int latent_c = 0, groups = 32;
   float eps = 1e-6f, sf = 1.f, sh = 0.f;
@@ -130,7 +156,8 @@ struct Builder {
   T *dev(size_t count) {
     void *p = nullptr;
     if (status != VAE_OK) return nullptr;
-    if (cudaMalloc(&p, std::max<size_t>(count, 1) * sizeof(T)) != cudaSuccess) {
+    if (take_alloc_failure() ||
+        cudaMalloc(&p, std::max<size_t>(count, 1) * sizeof(T)) != cudaSuccess) {
       status = VAE_ENOMEM;
       return nullptr;
     }
@@ -144,7 +171,7 @@ struct Builder {
       status = VAE_EINVAL;
       return nullptr;
     }
-    if (cudaMalloc(&p, count * sizeof(float)) != cudaSuccess) {
+    if (take_alloc_failure() || cudaMalloc(&p, count * sizeof(float)) != cudaSuccess) {
       status = VAE_ENOMEM;
       return nullptr;
     }
@@ -426,15 +453,62 @@ int run_gn(Chain &ch, const NormW &nw, const float *in, int n, long long sp, flo
 int run_resnet(Chain &ch, const ResW &r, const float *in, float *out, const DecodeWs &ws, int n,
                int h, int w, int round_out, Stats &st, cudaStream_t s) {
   const long long sp = static_cast<long long>(h) * w;
+  const size_t in_bytes = 4ull * n * sp * r.c1.cin, out_bytes = 4ull * n * sp * r.c1.cout;
   VAE_TRY(run_gn(ch, r.n1, in, n, sp, ws.T, ws, st, s));
+  if (ch.tr) ch.tr->emit(ws.T, in_bytes, s);
   VAE_TRY(run_conv(ch.prof, r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s, false, false, &st,
                    ws.part, ch.groups, ws.split));
+  if (ch.tr) ch.tr->emit(ws.H, out_bytes, s);
   VAE_TRY(run_gn(ch, r.n2, ws.H, n, sp, ws.T, ws, st, s));
+  if (ch.tr) ch.tr->emit(ws.T, out_bytes, s);
   if (r.c2.sc_cin)
-    return run_conv(ch.prof, r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s, false, false,
-                    &st, ws.part, ch.groups, ws.split);
-  return run_conv(ch.prof, r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s, false, false,
-                  &st, ws.part, ch.groups, ws.split);
+    VAE_TRY(run_conv(ch.prof, r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s, false, false,
+                     &st, ws.part, ch.groups, ws.split));
+  else
+    VAE_TRY(run_conv(ch.prof, r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s, false, false,
+                     &st, ws.part, ch.groups, ws.split));
+  if (ch.tr) ch.tr->emit(out, out_bytes, s);
+  return VAE_OK;
+}
+
+// The trace points of a decode, in the order decode_impl emits them.
+std::vector<vae_trace_point> trace_points(const Chain &ch, int n, int h, int w) {
+  std::vector<vae_trace_point> pts;
+  auto add = [&](int kind, int c, int hh, int ww, int input, int skip) {
+    vae_trace_point p{};
+    p.kind = kind;
+    p.c = c;
+    p.h = hh;
+    p.w = ww;
+    p.input = input;
+    p.skip = skip;
+    p.bytes = 4ull * n * hh * ww * c;
+    pts.push_back(p);
+    return static_cast<int>(pts.size()) - 1;
+  };
+  auto resnet = [&](const ResW &r, int x, int hh, int ww) {
+    const int g1 = add(VAE_TRACE_GROUPNORM, r.c1.cin, hh, ww, x, -1);
+    const int c1 = add(VAE_TRACE_CONV, r.c1.cout, hh, ww, g1, -1);
+    const int g2 = add(VAE_TRACE_GROUPNORM, r.c1.cout, hh, ww, c1, -1);
+    return add(VAE_TRACE_RESNET, r.c1.cout, hh, ww, g2, x);
+  };
+  int cur = add(VAE_TRACE_LATENT, round_up32(ch.latent_c), h, w, -1, -1);
+  cur = add(VAE_TRACE_CONV, ch.conv_in.cout, h, w, cur, -1);
+  cur = resnet(ch.mid1, cur, h, w);
+  cur = add(VAE_TRACE_ATTENTION, ch.attn.c, h, w, cur, -1);
+  cur = resnet(ch.mid2, cur, h, w);
+  int hh = h, ww = w;
+  for (const UpW &u : ch.ups) {
+    for (const ResW &r : u.res) cur = resnet(r, cur, hh, ww);
+    if (u.has_up) {
+      hh *= 2;
+      ww *= 2;
+      cur = add(VAE_TRACE_UPSAMPLE, u.up.cout, hh, ww, cur, -1);
+    }
+  }
+  if (!ch.head_w) cur = add(VAE_TRACE_GROUPNORM, ch.norm_out.c, hh, ww, cur, -1);
+  add(VAE_TRACE_RGB, ch.conv_out.cout, hh, ww, cur, -1);
+  return pts;
 }
 
 }  // namespace
@@ -497,34 +571,39 @@ int vae_chain_prepare(const vae_chain_args *a, void **handle, vae_stream_t strea
   for (void *p : b.temps) cudaFree(p);
   if (b.status != VAE_OK) {
     for (void *p : ch->allocs) cudaFree(p);
-    ch->magic = 0;
     delete ch;
     return b.status;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    g_live.insert(ch);
   }
   *handle = ch;
   return VAE_OK;
 }
 
 size_t vae_chain_workspace_size(const void *handle, int n, int h, int w) {
+  if (!is_live(handle) || n <= 0 || h <= 0 || w <= 0) return 0;
   const Chain *ch = static_cast<const Chain *>(handle);
-  if (!ch || ch->magic != kMagic || n <= 0 || h <= 0 || w <= 0) return 0;
   const Plan p = make_plan(*ch, n, h, w);
   Carver cv(nullptr, 0);
   carve_decode(cv, *ch, p, n, h, w);
   return cv.used;
 }
 
-int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *rgb, void *ws,
-                     size_t ws_bytes, vae_stream_t stream) {
-  Chain *ch = static_cast<Chain *>(handle);
-  if (!ch || ch->magic != kMagic) return VAE_ENOTPREPARED;
+}  // extern "C"
+
+namespace vae {
+namespace {
+
+int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void *ws,
+                size_t ws_bytes, cudaStream_t s) {
   if (!z || !rgb || !ws || n <= 0 || h <= 0 || w <= 0) return VAE_EINVAL;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != ch->device) return VAE_EINVAL;
   if ((reinterpret_cast<uintptr_t>(z) | reinterpret_cast<uintptr_t>(rgb)) & 15) return VAE_EINVAL;
   const long long L = static_cast<long long>(h) * w;
   if (L > 65536 || static_cast<long long>(n) * L > 0x7fffffffll) return VAE_EUNSUPPORTED;
-  auto s = reinterpret_cast<cudaStream_t>(stream);
   const Plan p = make_plan(*ch, n, h, w);
   Carver cv(ws, ws_bytes);
   DecodeWs d = carve_decode(cv, *ch, p, n, h, w);
@@ -543,12 +622,14 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
     Step st(ch->prof, VAE_PROF_LAYOUT, 0, 4.0 * n * L * (ch->latent_c + cp), s);
     VAE_TRY(stage_nhwc(z, n, ch->latent_c, L, VAE_NCHW, d.lat, cp, 1.0f / ch->sf, ch->sh, 1,
                        &lat, s));
+    if (ch->tr) ch->tr->emit(lat, 4ull * n * L * cp, s);
   }
   float *cur = d.X, *other = d.Y;
   int hh = h, ww = w;
   Stats st;
   VAE_TRY(run_conv(ch->prof, ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s, false,
                    false, &st, d.part, ch->groups, d.split));
+  if (ch->tr) ch->tr->emit(cur, 4ull * n * L * ch->conv_in.cout, s);
   VAE_TRY(run_resnet(*ch, ch->mid1, cur, cur, d, n, hh, ww, 0, st, s));
   {
     const double c = ch->attn.c;
@@ -557,6 +638,7 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
                            ch->attn.n.g, ch->attn.n.b, ch->attn.wqkv, ch->attn.bqkv, ch->attn.wo,
                            ch->attn.bo, cur, d.attn, s));
   }
+  if (ch->tr) ch->tr->emit(cur, 4ull * n * L * ch->attn.c, s);
   st.ready = false;  // the attention changed `cur`
   VAE_TRY(run_resnet(*ch, ch->mid2, cur, cur, d, n, hh, ww, 0, st, s));
   for (const UpW &u : ch->ups) {
@@ -576,6 +658,7 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
       std::swap(cur, other);
       hh *= 2;
       ww *= 2;
+      if (ch->tr) ch->tr->emit(cur, 4ull * n * hh * ww * u.up.cout, s);
     }
   }
   const long long hw = static_cast<long long>(hh) * ww;
@@ -587,25 +670,70 @@ int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *r
     VAE_TRY(groupnorm_scale_shift(cur, n, c, hw, ch->groups, ch->eps, ch->norm_out.g,
                                   ch->norm_out.b, st.ready ? d.part : nullptr, st.slots, scale,
                                   shift, d.gn, s, d.gn_cnt));
-    return head_gn_silu_conv(cur, n, hh, ww, c, scale, shift, ch->head_w, ch->conv_out.b, co, rgb,
-                             s);
+    VAE_TRY(head_gn_silu_conv(cur, n, hh, ww, c, scale, shift, ch->head_w, ch->conv_out.b, co,
+                              rgb, s));
+    if (ch->tr) ch->tr->emit(rgb, 4ull * n * hw * co, s);
+    return VAE_OK;
   }
   VAE_TRY(run_gn(*ch, ch->norm_out, cur, n, hw, d.T, d, st, s));
-  return run_conv(ch->prof, ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, rgb, 0, s, false,
-                  true);
+  if (ch->tr) ch->tr->emit(d.T, 4ull * n * hw * ch->norm_out.c, s);
+  VAE_TRY(run_conv(ch->prof, ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, rgb, 0, s, false,
+                   true));
+  if (ch->tr) ch->tr->emit(rgb, 4ull * n * hw * ch->conv_out.cout, s);
+  return VAE_OK;
+}
+
+}  // namespace
+}  // namespace vae
+
+extern "C" {
+
+int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *rgb, void *ws,
+                     size_t ws_bytes, vae_stream_t stream) {
+  if (!is_live(handle)) return VAE_ENOTPREPARED;
+  Chain *ch = static_cast<Chain *>(handle);
+  ch->tr = nullptr;
+  return decode_impl(ch, z, n, h, w, rgb, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int vae_chain_trace_points(const void *handle, int n, int h, int w, vae_trace_point *out,
+                           int capacity, int *count) {
+  if (!is_live(handle)) return VAE_ENOTPREPARED;
+  if (!count || n <= 0 || h <= 0 || w <= 0 || (capacity > 0 && !out)) return VAE_EINVAL;
+  const std::vector<vae_trace_point> pts =
+      trace_points(*static_cast<const Chain *>(handle), n, h, w);
+  *count = static_cast<int>(pts.size());
+  for (int i = 0; i < capacity && i < *count; ++i) out[i] = pts[i];
+  return VAE_OK;
+}
+
+int vae_decode_chain_traced(void *handle, const float *z, int n, int h, int w, float *rgb,
+                            void *ws, size_t ws_bytes, float *const *trace, int n_trace,
+                            vae_stream_t stream) {
+  if (!is_live(handle)) return VAE_ENOTPREPARED;
+  if (n_trace < 0 || (n_trace > 0 && !trace)) return VAE_EINVAL;
+  Chain *ch = static_cast<Chain *>(handle);
+  Tracer tr;
+  tr.bufs = trace;
+  tr.n = n_trace;
+  ch->tr = &tr;
+  const int rc =
+      decode_impl(ch, z, n, h, w, rgb, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+  ch->tr = nullptr;
+  return rc != VAE_OK ? rc : tr.status;
 }
 
 int vae_chain_profile(void *handle, int enable) {
+  if (!is_live(handle)) return VAE_ENOTPREPARED;
   Chain *ch = static_cast<Chain *>(handle);
-  if (!ch || ch->magic != kMagic) return VAE_ENOTPREPARED;
   ch->prof.on = enable != 0;
   if (ch->prof.on) ch->prof.reset();
   return VAE_OK;
 }
 
 int vae_chain_profile_read(void *handle, vae_prof_record *out, int capacity, int *count) {
+  if (!is_live(handle)) return VAE_ENOTPREPARED;
   Chain *ch = static_cast<Chain *>(handle);
-  if (!ch || ch->magic != kMagic) return VAE_ENOTPREPARED;
   if (!count || (capacity > 0 && !out)) return VAE_EINVAL;
   Profiler &p = ch->prof;
   const int n = static_cast<int>(p.recs.size());
@@ -624,10 +752,12 @@ int vae_chain_profile_read(void *handle, vae_prof_record *out, int capacity, int
 }
 
 int vae_chain_destroy(void *handle) {
+  {
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    if (!handle || g_live.erase(handle) == 0) return VAE_ENOTPREPARED;
+  }
   Chain *ch = static_cast<Chain *>(handle);
-  if (!ch || ch->magic != kMagic) return VAE_ENOTPREPARED;
   for (void *p : ch->allocs) cudaFree(p);
-  ch->magic = 0;
   delete ch;
   return VAE_OK;
 }

@@ -44,8 +44,17 @@ struct Carver {
 };
 
 // Device error word of the current device (int), via the library's
-// __device__ symbol; resolved once per device.
+// __device__ symbol; resolved once per device and context.
 int *device_error_word();
+// The CUDA context current on this thread (CUcontext), or nullptr.
+void *current_context();
+// Limit of the kernels' device-side waits (vae_debug_set_wait_limit).
+constexpr uint64_t kDefaultWaitNs = 4000000000ull;
+uint64_t wait_limit_ns();
+// VAE_INJECT_* bits set by vae_debug_inject (0 in normal operation).
+int injected_faults();
+// True when the allocation about to be made should fail (vae_debug_fail_allocation).
+bool take_alloc_failure();
 int num_sms();
 // Every kernel launch of the library bumps this process-wide counter.
 void count_launches(int n);

@@ -109,6 +109,8 @@ struct KParams {
   float *sk_part;
   int *sk_flag;  // [G][4]: one per epilogue warp, zeroed before the launch
   int *err;
+  uint64_t wait_ns;  // limit of every device-side wait (normally kWaitTimeoutNs)
+  int inject;        // test hook: VAE_INJECT_* bits (0 in normal operation)
 };
 
 // One work item of a CTA: a tile and the range [k0, k1) of its reduction
@@ -269,10 +271,11 @@ __device__ __forceinline__ void raise_error(const KParams &p, volatile uint32_t 
 }
 
 // Unbounded-by-abort wait used only while draining after an abort.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
+                                                uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   return true;
 }
 
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // One halo tile per 32-channel chunk, then one weight stage per tap
           // (no appended shortcut in this mode).
           for (int cc = ks0; cc < ks1 && !failed; ++cc) {
-            if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort)) {
+            if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort, p.wait_ns)) {
               raise_error(p, abort);
               failed = true;
               break;
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               aphase ^= 1u;
             }
             for (int tap = 0; tap < p.taps; ++tap) {
-              if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+              if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.wait_ns)) {
                 raise_error(p, abort);
                 failed = true;
                 break;
@@ -423,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nsc = is_sc ? min(C::SC_PER_BUF, p.sc_chunks - sc0) : 0;
             const int nkx = is_sc ? 1 : 3;
             for (int kx = 0; kx < nkx && !failed; ++kx) {
-              if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort)) {
+              if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort, p.wait_ns)) {
                 raise_error(p, abort);
                 failed = true;
                 break;
@@ -447,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               const int nky = is_sc ? nsc : 3;
               for (int ky = 0; ky < nky; ++ky) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.wait_ns)) {
                   raise_error(p, abort);
                   failed = true;
                   break;
@@ -468,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         for (int ks = ks0; ks < ks1; ++ks) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.wait_ns)) {
             raise_error(p, abort);
             failed = true;
             break;
@@ -515,9 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort) {
         // Let every copy this thread issued land before the CTA exits.
         for (int s = 0; s < STAGES; ++s)
-          if (pending & (1u << s)) mbar_wait_drain(&full[s], (pend_par >> s) & 1u);
+          if (pending & (1u << s)) mbar_wait_drain(&full[s], (pend_par >> s) & 1u, p.wait_ns);
         for (int b = 0; b < 2; ++b)
-          if (a_pending & (1u << b)) mbar_wait_drain(&a_full[b], (a_par >> b) & 1u);
+          if (a_pending & (1u << b)) mbar_wait_drain(&a_full[b], (a_par >> b) & 1u, p.wait_ns);
       }
     }
   } else if (warp == 1) {
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cur = local++;
         const int buf = cur & 1;
         const uint32_t aph = (cur >> 1) & 1;
-        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort)) {
+        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort, p.wait_ns)) {
           raise_error(p, abort);
           break;
         }
@@ -545,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // starting at halo row sub + ky, column kx: a row offset into the
           // swizzled halo buffer.
           for (int cc = ks0; cc < ks1 && !failed; ++cc) {
-            if (!mbar_wait(&a_full[abuf], aphase, abort)) {
+            if (!mbar_wait(&a_full[abuf], aphase, abort, p.wait_ns)) {
               raise_error(p, abort);
               failed = true;
               break;
@@ -558,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued = true;
 #pragma unroll
             for (int tap = 0; tap < 9; ++tap) {
-              if (!mbar_wait(&full[stage], phase, abort)) {
+              if (!mbar_wait(&full[stage], phase, abort, p.wait_ns)) {
                 raise_error(p, abort);
                 failed = true;
                 break;
@@ -602,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 is_sc ? min(C::SC_PER_BUF, p.sc_chunks - (cc - p.cin_chunks) * C::SC_PER_BUF) : 0;
             const int nkx = is_sc ? 1 : 3;
             for (int kx = 0; kx < nkx && !failed; ++kx) {
-              if (!mbar_wait(&a_full[abuf], aphase, abort)) {
+              if (!mbar_wait(&a_full[abuf], aphase, abort, p.wait_ns)) {
                 raise_error(p, abort);
                 failed = true;
                 break;
@@ -610,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t abase = smem_u32(sH + abuf * C::HALO_BYTES);
               const int nky = is_sc ? nsc : 3;
               for (int ky = 0; ky < nky; ++ky) {
-                if (!mbar_wait(&full[stage], phase, abort)) {
+                if (!mbar_wait(&full[stage], phase, abort, p.wait_ns)) {
                   raise_error(p, abort);
                   failed = true;
                   break;
@@ -642,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         for (int ks = ks0; ks < ks1; ++ks) {
-          if (!mbar_wait(&full[stage], phase, abort)) {
+          if (!mbar_wait(&full[stage], phase, abort, p.wait_ns)) {
             raise_error(p, abort);
             failed = true;
             break;
@@ -671,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Wait for the MMAs still reading shared memory / writing TMEM before
         // the CTA frees TMEM and exits.
         umma_commit(drain);
-        mbar_wait_drain(drain, 0);
+        mbar_wait_drain(drain, 0, p.wait_ns);
       }
     }
   } else {
@@ -690,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cur = local++;
       const int buf = cur & 1;
       const uint32_t aph = (cur >> 1) & 1;
-      bool ok = mbar_wait(&acc_full[buf], aph, abort);
+      bool ok = mbar_wait(&acc_full[buf], aph, abort, p.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         if (lane == 0) raise_error(p, abort);
@@ -823,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int *f = p.sk_flag + (blockIdx.x + 1) * 4 + q;
           const uint64_t t0 = global_timer_ns();
           while (ld_acquire_gpu(f) == 0) {
-            if (*abort || global_timer_ns() - t0 > kWaitTimeoutNs) {
+            if (*abort || global_timer_ns() - t0 > p.wait_ns) {
               ok = false;
               break;
             }
@@ -955,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               else
                 tma_load_5d(sb, &tmR, &res_bar[q], col0, bc1, bc2, bc3, bc4);
             }
-            bool rok = mbar_wait(&res_bar[q], res_phase, abort);
+            bool rok = mbar_wait(&res_bar[q], res_phase, abort, p.wait_ns);
             rok = __all_sync(0xffffffffu, rok);
             res_phase ^= 1u;
             if (!rok) {
@@ -1075,7 +1078,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.tail && !failed) {  // this warp's raw sums are out: raise its flag
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(p.sk_flag + blockIdx.x * 4 + q, 1);
+        // (The test hook withholds the flag so that the head's bounded wait
+        // runs out; nothing else differs.)
+        if (lane == 0 && !(p.inject & VAE_INJECT_WITHHOLD_STREAMK_FLAG))
+          st_release_gpu(p.sk_flag + blockIdx.x * 4 + q, 1);
       }
       tc_fence_before();
       __syncwarp();
@@ -1198,6 +1204,8 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   KParams kp{};
   kp.err = device_error_word();
   if (!kp.err) return VAE_ECUDA;
+  kp.wait_ns = wait_limit_ns();
+  kp.inject = injected_faults();
   kp.cout = d.cout;
   kp.out = d.out;
   kp.ldo = d.ldo;

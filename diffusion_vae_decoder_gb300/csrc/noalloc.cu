@@ -12,8 +12,9 @@
 // The array lives in device global memory of every GPU that loads the
 // library, for the life of the process. Host code must not hand the array's
 // name to a kernel (on the host side it is only a stand-in symbol); its device
-// address is fetched once per device with cudaGetSymbolAddress, with that
-// device current, on the first call made on that device.
+// address is fetched with cudaGetSymbolAddress, with that device current, on
+// the first call made on that device, and again after the device's context
+// was replaced (cudaDeviceReset gives the array a new address).
 #include <mutex>
 
 #include "common.cuh"
@@ -30,15 +31,18 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void *g_noalloc_addr[kMaxDevices] = {};
+void *g_noalloc_ctx[kMaxDevices] = {};  // context the cached address belongs to
 
 int noalloc_scratch(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VAE_ECUDA;
+  void *ctx = current_context();
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  if (!g_noalloc_addr[dev] || g_noalloc_ctx[dev] != ctx) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return VAE_ECUDA;
     g_noalloc_addr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
   *out = g_noalloc_addr[dev];
   return VAE_OK;

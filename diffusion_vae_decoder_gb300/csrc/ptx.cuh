@@ -55,10 +55,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase of `bar` with parity `parity` to complete.
-// Returns false when it gave up: either the time limit passed or another role
-// of the CTA already raised `*abort`.
+// Returns false when it gave up: either `limit_ns` passed or another role of
+// the CTA already raised `*abort`.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile uint32_t *abort) {
+                                          volatile uint32_t *abort,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -66,7 +67,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -16,8 +16,29 @@ __device__ int g_vae_error_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int *g_err_addr[kMaxDevices] = {};
+void *g_err_ctx[kMaxDevices] = {};  // context the cached address belongs to
 int g_sms[kMaxDevices] = {};
 std::atomic<long long> g_launches{0};
+// Test hooks (see vae_debug_*): device-wait limit, injected faults, and a
+// countdown to an allocation failure inside vae_chain_prepare.
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_inject{0};
+std::atomic<int> g_alloc_countdown{0};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -34,16 +55,39 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
+void *current_context() {
+  CUcontext ctx = nullptr;
+  auto fn = ctx_get_current_fn();
+  if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
+
 int *device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  void *ctx = current_context();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_addr[dev]) {
+  // Re-resolved when the context changed (e.g. after cudaDeviceReset, the
+  // symbol lives at a new address; before the first runtime call no context
+  // is current yet and the lookup creates it).
+  if (!g_err_addr[dev] || g_err_ctx[dev] != ctx) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_vae_error_word) != cudaSuccess) return nullptr;
     g_err_addr[dev] = static_cast<int *>(p);
+    g_err_ctx[dev] = ctx;
   }
   return g_err_addr[dev];
+}
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int injected_faults() { return g_inject.load(std::memory_order_relaxed); }
+
+bool take_alloc_failure() {
+  int v = g_alloc_countdown.load();
+  while (v > 0) {
+    if (g_alloc_countdown.compare_exchange_weak(v, v - 1)) return v == 1;
+  }
+  return false;
 }
 
 int num_sms() {
@@ -116,6 +160,23 @@ int vae_device_error(vae_stream_t stream, int *code) {
 }
 
 int vae_num_sms(void) { return vae::num_sms(); }
+
+int vae_debug_set_wait_limit(unsigned long long ns) {
+  vae::g_wait_ns.store(ns ? ns : vae::kDefaultWaitNs);
+  return VAE_OK;
+}
+
+int vae_debug_inject(int bits) {
+  if (bits & ~VAE_INJECT_WITHHOLD_STREAMK_FLAG) return VAE_EINVAL;
+  vae::g_inject.store(bits);
+  return VAE_OK;
+}
+
+int vae_debug_fail_allocation(int nth) {
+  if (nth < 0) return VAE_EINVAL;
+  vae::g_alloc_countdown.store(nth);
+  return VAE_OK;
+}
 
 long long vae_kernel_launch_count(void) { return vae::launch_count(); }
 

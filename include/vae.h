@@ -122,8 +122,10 @@ VAE_API int vae_groupnorm_silu(const float *x, int n, int c, long long spatial, 
  * (held in the global memory of every GPU that loads the library until the
  * process exits): enough for up to 10 samples at 32 groups; larger requests
  * return VAE_EUNSUPPORTED before anything is launched. The first call on a
- * device looks up the array's device address for that device (make that
- * first call before any stream capture). All calls share the array, so calls
+ * device looks up the array's device address for that device, and so does
+ * the first call after the device's context was replaced (cudaDeviceReset
+ * moves the array); make that first call before any stream capture. All
+ * calls share the array, so calls
  * that overlap on the GPU (e.g. on two streams at once) race; calls on one
  * stream are ordered and safe. No part of the array needs clearing between
  * calls. Allocates nothing. */
@@ -252,7 +254,55 @@ VAE_API size_t vae_chain_workspace_size(const void *handle, int n, int h, int w)
  * has a fixed order: the same inputs give the same bits. */
 VAE_API int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *rgb, void *ws,
                      size_t ws_bytes, vae_stream_t stream);
+/* Frees the handle's device memory. Handles are tracked in a registry of live
+ * handles: every entry point given a destroyed (or never prepared) handle
+ * returns VAE_ENOTPREPARED without touching it. */
 VAE_API int vae_chain_destroy(void *handle);
+
+/* ------------------------------------------------------------------------
+ * Layer trace of one decode, for per-layer parity checks: the same decode as
+ * vae_decode_chain (identical kernels and arithmetic) that also copies each
+ * step's output tensor, right after the step, into caller buffers. The
+ * points follow the chain's execution order ("Module vae", VaeChainArgs):
+ *   LATENT     de-normalised latent, NHWC with channels padded to 32
+ *   CONV       3x3 conv output: conv_in, a resnet's conv1
+ *   GROUPNORM  GroupNorm+SiLU output: a resnet's norm1 / norm2, and norm_out
+ *              when conv_out does not take the fused head
+ *   RESNET     resnet output: conv2 + bias + skip (identity or 1x1 shortcut)
+ *   ATTENTION  mid attention block output: x + out-projection
+ *   UPSAMPLE   nearest-2x upsample + conv output
+ *   RGB        decoder output, NCHW: conv_out of the GroupNorm point before
+ *              it, or norm_out + SiLU + conv_out (fused head) of the point
+ *              before it when that point is not a GROUPNORM
+ * Activations are NHWC [n][h][w][c] float32, stored as the next step reads
+ * them (operands of a tensor-core product are TF32-rounded values). */
+typedef enum {
+  VAE_TRACE_LATENT = 0,
+  VAE_TRACE_CONV = 1,
+  VAE_TRACE_GROUPNORM = 2,
+  VAE_TRACE_RESNET = 3,
+  VAE_TRACE_ATTENTION = 4,
+  VAE_TRACE_UPSAMPLE = 5,
+  VAE_TRACE_RGB = 6
+} vae_trace_kind;
+
+typedef struct {
+  int kind;     /* vae_trace_kind */
+  int c, h, w;  /* tensor channels and spatial size (per image) */
+  int input;    /* index of the point holding this step's input (-1: none) */
+  int skip;     /* RESNET: index of the point holding the resnet's input */
+  size_t bytes; /* n * h * w * c * 4 */
+} vae_trace_point;
+
+/* Describes the trace points of a decode of a [n,latent_channels,h,w]
+ * latent: copies min(capacity, total) of them to `out`, *count = total. */
+VAE_API int vae_chain_trace_points(const void *handle, int n, int h, int w, vae_trace_point *out,
+                                   int capacity, int *count);
+/* vae_decode_chain plus the trace: trace[i] (device, bytes of point i) or
+ * NULL to skip point i; n_trace may be smaller than the point count. */
+VAE_API int vae_decode_chain_traced(void *handle, const float *z, int n, int h, int w,
+                                    float *rgb, void *ws, size_t ws_bytes, float *const *trace,
+                                    int n_trace, vae_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Step profiler of the chain: when enabled, vae_decode_chain brackets every
@@ -296,6 +346,32 @@ VAE_API const char *vae_status_string(int status);
 VAE_API int vae_device_error(vae_stream_t stream, int *code);
 /* Number of SMs the kernels size their persistent grids for (current device). */
 VAE_API int vae_num_sms(void);
+/* Measures this GPU's tcgen05 kind::tf32 tensor-pipe rate, the denominator of
+ * the convolution's roofline fraction: one CTA per SM issues iters x 4
+ * MMAs of M = 128, N = 256, K = 8 on operands resident in shared memory
+ * (no global-memory traffic), accumulating in TMEM. *flops receives the
+ * floating-point operations executed, *ms their device time (CUDA events on
+ * `stream`, synchronised before returning). */
+VAE_API int vae_measure_tf32_mma(int iters, double *flops, float *ms, vae_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Test hooks for the failure paths; none of them faults, traps or hangs a
+ * GPU. Process-wide settings, read when a kernel is launched.
+ *
+ * vae_debug_set_wait_limit: every device-side wait of the implicit-GEMM conv
+ * gives up after `ns` nanoseconds (0 restores the default, 4 s) and records
+ * VAE_EDEVICE_TIMEOUT, drains its own copies and MMAs, frees its TMEM and
+ * returns.
+ * vae_debug_inject: VAE_INJECT_WITHHOLD_STREAMK_FLAG makes the conv's
+ * stream-K CTAs skip the flag that hands a tile's tail over to the CTA that
+ * finishes it, so that CTA's bounded wait runs out (0 clears).
+ * vae_debug_fail_allocation: the nth device allocation vae_chain_prepare
+ * makes from now on (1 = the next) fails as if the device were out of
+ * memory: prepare frees what it allocated and returns VAE_ENOMEM (0 clears). */
+typedef enum { VAE_INJECT_WITHHOLD_STREAMK_FLAG = 1 } vae_inject_bits;
+VAE_API int vae_debug_set_wait_limit(unsigned long long ns);
+VAE_API int vae_debug_inject(int bits);
+VAE_API int vae_debug_fail_allocation(int nth);
 
 #ifdef __cplusplus
 }

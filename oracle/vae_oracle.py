@@ -28,6 +28,7 @@ __all__ = [
     "denormalize", "conv2d", "group_norm", "silu", "group_norm_silu",
     "upsample_nearest2x", "upsample_conv", "resnet", "softmax_rows",
     "mid_attention", "up_block", "decode", "conv3d_causal", "causal_stack",
+    "conv2d_at", "upsample_conv_at", "mid_attention_at",
 ]
 
 
@@ -70,6 +71,45 @@ def conv2d(x, weight, bias=None):
     if bias is not None:
         y += _f64(bias)[None, :, None, None]
     return y
+
+
+def conv2d_at(x, weight, bias, pixels, upsample=False):
+    """The conv2d definition evaluated at chosen output pixels only (for
+    outputs too large to compute whole): ``pixels`` is an int array [S, 3] of
+    (image, row, col); returns [S, cout].
+
+    y[o] = b[o] + sum_{c,ky,kx} w[o,c,ky,kx] * u[c, i+ky-p, j+kx-p], zero
+    outside the image, where u is x itself, or with ``upsample`` the
+    nearest-2x upsample of x ([vae] VaeUpRef: u[c,i,j] = x[c,i//2,j//2] on the
+    doubled grid). ``x`` is NCHW (any array that supports numpy indexing,
+    e.g. a transposed view); only the gathered taps are widened to float64."""
+    w = _f64(weight)
+    cout, cin, k, _ = w.shape
+    p = k // 2
+    pix = np.asarray(pixels, dtype=np.int64)
+    b_idx, i_idx, j_idx = pix[:, 0], pix[:, 1], pix[:, 2]
+    h, wd = x.shape[2], x.shape[3]
+    if upsample:
+        h, wd = 2 * h, 2 * wd
+    y = np.zeros((len(pix), cout))
+    for ky in range(k):
+        for kx in range(k):
+            r = i_idx + ky - p
+            c = j_idx + kx - p
+            inside = (r >= 0) & (r < h) & (c >= 0) & (c < wd)
+            rs, cs = np.where(inside, r, 0), np.where(inside, c, 0)
+            if upsample:
+                rs, cs = rs // 2, cs // 2
+            taps = _f64(x[b_idx, :, rs, cs]) * inside[:, None]  # [S, cin]
+            y += taps @ w[:, :, ky, kx].T
+    if bias is not None:
+        y += _f64(bias)[None, :]
+    return y
+
+
+def upsample_conv_at(x, weight, bias, pixels):
+    """upsample_conv at chosen output pixels of the doubled grid ([S, cout])."""
+    return conv2d_at(x, weight, bias, pixels, upsample=True)
 
 
 def group_norm(x, gamma, beta, groups=32, eps=1e-6):
@@ -155,6 +195,27 @@ def mid_attention(x, p, groups=32, eps=1e-6):
         a = softmax_rows(q @ k.T / np.sqrt(c)) @ v
         o = a @ _f64(p["to_out"][0]).T + _f64(p["to_out"][1])
         y[b] = x[b] + o.T.reshape(c, h, w)
+    return y
+
+
+def mid_attention_at(x, p, tokens, groups=32, eps=1e-6):
+    """mid_attention evaluated for chosen query tokens only: the GroupNorm,
+    k and v of every token, q and the softmax rows of the chosen tokens.
+    ``tokens`` index i * W + j; returns [n, c, len(tokens)] (block output
+    x + out-projection at those tokens)."""
+    x = _f64(x)
+    n, c, h, w = x.shape
+    tokens = np.asarray(tokens, dtype=np.int64)
+    t = group_norm(x, *p["group_norm"], groups, eps)
+    y = np.empty((n, c, len(tokens)))
+    for b in range(n):
+        tok = t[b].reshape(c, h * w).T  # [HW, c]
+        q = tok[tokens] @ _f64(p["to_q"][0]).T + _f64(p["to_q"][1])
+        k = tok @ _f64(p["to_k"][0]).T + _f64(p["to_k"][1])
+        v = tok @ _f64(p["to_v"][0]).T + _f64(p["to_v"][1])
+        a = softmax_rows(q @ k.T / np.sqrt(c)) @ v
+        o = a @ _f64(p["to_out"][0]).T + _f64(p["to_out"][1])
+        y[b] = x[b].reshape(c, h * w)[:, tokens] + o.T
     return y
 
 

@@ -54,8 +54,9 @@ PROBE = r"""
 #define O(T, f) printf(#T "." #f " %zu\n", offsetof(T, f));
 int main(void) {
   P(vae_conv_ref) P(vae_norm_ref) P(vae_resnet_ref) P(vae_attn_ref) P(vae_up_ref)
-  P(vae_chain_args) P(vae_prof_record)
+  P(vae_chain_args) P(vae_prof_record) P(vae_trace_point)
   O(vae_prof_record, flops) O(vae_prof_record, ms)
+  O(vae_trace_point, skip) O(vae_trace_point, bytes)
   O(vae_conv_ref, k) O(vae_resnet_ref, shortcut) O(vae_attn_ref, out)
   O(vae_up_ref, resnets) O(vae_up_ref, upsample_conv)
   O(vae_chain_args, eps) O(vae_chain_args, conv_in) O(vae_chain_args, mid_attn)
@@ -77,7 +78,7 @@ def test_ctypes_struct_layout_matches_c(tmp_path):
     m = {"vae_conv_ref": pkg.ConvRef, "vae_norm_ref": pkg.NormRef,
          "vae_resnet_ref": pkg.ResnetRef, "vae_attn_ref": pkg.AttnRef,
          "vae_up_ref": pkg.UpRef, "vae_chain_args": pkg.ChainArgs,
-         "vae_prof_record": pkg.ProfRecord}
+         "vae_prof_record": pkg.ProfRecord, "vae_trace_point": pkg.TracePoint}
     for key, val in got.items():
         if "." in key:
             t, f = key.split(".")
@@ -113,6 +114,30 @@ def test_argument_checks_reject_before_any_launch(lib):
                                   1 << 20, None) == -1
     assert lib.vae_mid_attn(fake, 1, 48, 4, 4, 0, 16, 1e-6, *([fake] * 11), fake, 1 << 20,
                             None) == -2
+
+
+def test_unknown_handles_are_rejected_without_being_read(lib):
+    """Handles are checked against the registry of live handles, never read
+    through: a pointer that vae_chain_prepare did not return (here an address
+    that would fault if dereferenced) is refused by every handle entry point."""
+    bogus = ctypes.c_void_p(0x10)
+    fake = ctypes.c_void_p(16)
+    cnt = ctypes.c_int(-1)
+    assert lib.vae_chain_destroy(bogus) == -5
+    assert lib.vae_decode_chain(bogus, fake, 1, 8, 8, fake, fake, 1, None) == -5
+    assert lib.vae_decode_chain_traced(bogus, fake, 1, 8, 8, fake, fake, 1, None, 0, None) == -5
+    assert lib.vae_chain_trace_points(bogus, 1, 8, 8, None, 0, ctypes.byref(cnt)) == -5
+    assert lib.vae_chain_workspace_size(bogus, 1, 8, 8) == 0
+    assert lib.vae_chain_profile(bogus, 1) == -5
+    assert lib.vae_chain_profile_read(bogus, None, 0, ctypes.byref(cnt)) == -5
+
+
+def test_debug_hooks_validate_their_arguments(lib):
+    assert lib.vae_debug_inject(2) == -1
+    assert lib.vae_debug_inject(0) == 0
+    assert lib.vae_debug_fail_allocation(-1) == -1
+    assert lib.vae_debug_fail_allocation(0) == 0
+    assert lib.vae_debug_set_wait_limit(0) == 0
 
 
 def test_workspace_sizes_are_positive_and_monotone(lib):

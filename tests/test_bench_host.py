@@ -61,21 +61,23 @@ def test_reference_arm_prints_one_json_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0
 
 
-def test_conv_traffic_comes_from_the_committed_launch_list():
-    """The roofline's DRAM traffic is read from the committed ncu summary of
-    the workload, and only while igemm.cu is the file that summary was taken
-    on (its sha256 is recorded there); other workloads have none."""
+def test_conv_traffic_is_read_only_for_the_kernel_it_was_captured_on(tmp_path):
+    """The roofline's DRAM traffic comes from a machine-readable ncu summary
+    that records the sha256 of igemm.cu at capture: it is used only while
+    igemm.cu is that file, and only for the workloads it lists."""
     import hashlib
-    import re
     sys.path.insert(0, ROOT)
     import bench
-    text = open(os.path.join(ROOT, "profiles", "launch_list_decoder_1024.md")).read()
-    sha = re.search(r"igemm\.cu sha256 at capture: ([0-9a-f]{64})", text).group(1)
     src = os.path.join(ROOT, "diffusion_vae_decoder_gb300", "csrc", "igemm.cu")
     current = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    nbytes, nlaunch = bench.conv_traffic_from_profile("decoder_1024")
-    if current == sha:
-        assert nlaunch == 32 and nbytes > 1e10
-    else:
-        assert (nbytes, nlaunch) == (None, None)
-    assert bench.conv_traffic_from_profile("decoder_256") == (None, None)
+    entry = {"bytes_per_launch": 5.5e8, "capture": "one launch"}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps({"igemm_cu_sha256": current,
+                                "workloads": {"decoder_1024": entry}}))
+    assert bench.conv_traffic_from_profile("decoder_1024", str(path)) == (5.5e8, entry)
+    assert bench.conv_traffic_from_profile("decoder_256", str(path)) == (None, None)
+    path.write_text(json.dumps({"igemm_cu_sha256": "0" * 64,
+                                "workloads": {"decoder_1024": entry}}))
+    assert bench.conv_traffic_from_profile("decoder_1024", str(path)) == (None, None)
+    assert bench.conv_traffic_from_profile("decoder_1024", str(tmp_path / "none.json")) == \
+        (None, None)

@@ -481,3 +481,44 @@ def test_fused_attention_forced_on_wide_heads():
     r = subprocess.run([sys.executable, "-c", _FORCED_FLASH.format(root=root)], env=env,
                        cwd=root, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+_LONG_ROWS = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, {root!r})
+import oracle as O, vae_synth as S
+import diffusion_vae_decoder_gb300 as pkg
+from tests._parity import metrics
+n, c, h, w = 1, 32, 132, 132   # 17424 tokens: score rows longer than 16384
+x = S.make_normal((n, c, h, w), 35)
+wt = S.make_attn_params(c, 36)
+p = {{k: (wt[k + ".weight"], wt[k + ".bias"]) for k in
+     ("group_norm", "to_q", "to_k", "to_v", "to_out")}}
+pd = {{k: (torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()) for k, (a, b) in p.items()}}
+got = pkg.vae_mid_attn(torch.from_numpy(x).cuda(), pd).cpu().numpy().reshape(n, c, h * w)
+tokens = np.unique(np.concatenate([[0, 1, h * w - 1],
+                                   np.random.default_rng(37).integers(0, h * w, 300)]))
+ref = O.mid_attention_at(x, p, tokens)
+g = got[:, :, tokens]
+xt = x.reshape(n, c, h * w)[:, :, tokens]
+for a, b in ((g, ref), (g - xt, ref - xt)):
+    m = metrics(a, b)
+    assert m["cos"] >= 0.99999 and m["rel_l2"] <= 1e-3, m
+assert pkg.vae_device_error() == 0
+print("ok")
+"""
+
+
+def test_score_rows_longer_than_16384_take_the_long_softmax():
+    """Decodes above 1024^2 have more than 16384 latent tokens: on the
+    score-matrix path (forced with VAE_ATTN=unfused in a child process) their
+    rows exceed what the register-resident softmax holds and the three-sweep
+    kernel runs. Checked at sampled query tokens against the oracle."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, VAE_ATTN="unfused")
+    r = subprocess.run([sys.executable, "-c", _LONG_ROWS.format(root=root)], env=env,
+                       cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr

@@ -446,3 +446,50 @@ def test_decoder_weight_plan_shapes():
     rev, plan = S.decoder_layout("flux")
     assert rev == [512, 512, 256, 128]
     assert plan == [(512, 512, True), (512, 512, True), (512, 256, True), (256, 128, False)]
+
+
+# ------------------------------------------------------------------ sampled outputs
+# The full-size parity tests evaluate the definitions at sampled outputs only;
+# these pins hold the sampled forms to library routines and brute force.
+
+@pytest.mark.parametrize("k", [1, 3])
+def test_conv2d_at_every_pixel_matches_torch_and_brute_force(k):
+    r = _rng(40 + k)
+    x = r.standard_normal((2, 3, 5, 7))
+    w, b = r.standard_normal((4, 3, k, k)), r.standard_normal(4)
+    pix = np.array(list(itertools.product(range(2), range(5), range(7))))
+    got = O.conv2d_at(x, w, b, pix)
+    ref = F.conv2d(_t(x), _t(w), _t(b), padding=k // 2).numpy()
+    np.testing.assert_allclose(got, ref[pix[:, 0], :, pix[:, 1], pix[:, 2]], atol=1e-12)
+    brute = _conv_brute(x, w, b)
+    np.testing.assert_allclose(got, brute[pix[:, 0], :, pix[:, 1], pix[:, 2]], atol=1e-12)
+
+
+def test_conv2d_at_reads_a_channels_last_view():
+    """The tests hand it NHWC activations as an NCHW view (no copy)."""
+    r = _rng(44)
+    x = r.standard_normal((1, 6, 4, 8)).astype(np.float32)
+    w, b = r.standard_normal((5, 6, 3, 3)), r.standard_normal(5)
+    nhwc = np.ascontiguousarray(np.moveaxis(x, 1, -1))
+    pix = np.array([[0, 0, 0], [0, 3, 7], [0, 1, 4], [0, 2, 0]])
+    np.testing.assert_array_equal(O.conv2d_at(np.moveaxis(nhwc, -1, 1), w, b, pix),
+                                  O.conv2d_at(x, w, b, pix))
+
+
+def test_upsample_conv_at_matches_torch():
+    r = _rng(45)
+    x = r.standard_normal((2, 4, 3, 5))
+    w, b = r.standard_normal((3, 4, 3, 3)), r.standard_normal(3)
+    ref = F.conv2d(F.interpolate(_t(x), scale_factor=2, mode="nearest"), _t(w), _t(b),
+                   padding=1).numpy()
+    pix = np.array(list(itertools.product(range(2), range(6), range(10))))
+    np.testing.assert_allclose(O.upsample_conv_at(x, w, b, pix),
+                               ref[pix[:, 0], :, pix[:, 1], pix[:, 2]], atol=1e-11)
+
+
+def test_mid_attention_at_matches_torch_sdpa():
+    x = _rng(46).standard_normal((2, 64, 4, 5))
+    p = _attn_params(64, 46)
+    tokens = np.array([0, 7, 19, 3])
+    ref = _attn_torch(x, p).reshape(2, 64, 20)[:, :, tokens]
+    np.testing.assert_allclose(O.mid_attention_at(x, p, tokens), ref, atol=1e-11)

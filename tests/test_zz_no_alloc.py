@@ -6,14 +6,16 @@ the library instead of a caller workspace.
 Checked through the C ABI against the workspace entry point,
 vae_groupnorm_silu, with the tolerance the GroupNorm parity tests use, on two
 calls in a row with different shapes and layouts (the shared scratch keeps
-the previous call's contents), plus the size limit. This file is collected
-last on purpose so that a run stopping at the first failure has run every
-other test before it."""
+the previous call's contents), against the float64 oracle's GroupNorm(+SiLU)
+on both, plus the size limit. This file is collected last on purpose so
+that a run stopping at the first failure has run every other test before
+it."""
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle as O
 import vae_synth as S
 from tests._parity import metrics
 
@@ -64,6 +66,16 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
         assert not (got == -12345.0).any()
         m = metrics(got, ref)
         assert m["rel_l2"] < 2e-6 and m["max_abs"] < 2e-5, (shape, m)
+        # and against the oracle itself (NCHW view of the input)
+        xh = x.cpu().numpy()
+        xn = xh if layout == 0 else np.moveaxis(xh, -1, 1)
+        gh, bh = g.cpu().numpy(), b.cpu().numpy()
+        want = O.group_norm_silu(xn, gh, bh, 32, 1e-6) if silu else \
+            O.group_norm(xn, gh, bh, 32, 1e-6)
+        if layout == 1:
+            want = np.moveaxis(want, 1, -1)
+        mo = metrics(got, want)
+        assert mo["rel_l2"] < 2e-6 and mo["cos"] >= 0.99999, (shape, mo)
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(lib):
