@@ -82,6 +82,7 @@ def _nchw(t_nhwc):
 def _check(got, ref, what, results):
     m = metrics(got, ref)
     results.append((what, m))
+    print(f"{what:60s} rel_l2 {m['rel_l2']:.2e} cos {m['cos']:.8f} max {m['max_abs']:.2e}")
     assert np.isfinite(got).all(), what
     assert m["cos"] >= COS_MIN and m["rel_l2"] <= REL_L2_MAX, (what, m)
     return m
@@ -162,7 +163,12 @@ def run_layer_parity(latent, seed, arch="flux"):
                 skip = xin[pix[:, 0], :, pix[:, 1], pix[:, 2]].astype(np.float64)
             got = get(i)[pix[:, 0], pix[:, 1], pix[:, 2]].astype(np.float64)
             _check(got, branch + skip, what, results)
-            if pre + ".conv_shortcut.weight" not in w:
+            # The branch alone, where the output is stored unrounded: an
+            # up-block's last resnet feeds the upsample conv's MMA and is
+            # stored TF32-rounded, a rounding of the whole output (skip
+            # included) that is not the branch's arithmetic.
+            rounded = i + 1 < len(steps) and steps[i + 1][0] == "upsample"
+            if pre + ".conv_shortcut.weight" not in w and not rounded:
                 _check(got - skip, branch, what + " branch", results)
             continue
         if kind == "attention":
@@ -195,8 +201,6 @@ def run_layer_parity(latent, seed, arch="flux"):
             assert torch.equal(bufs[i].view_as(rgb), rgb)
             continue
         raise AssertionError(kind)
-    for what, m in results:
-        print(f"{what:60s} rel_l2 {m['rel_l2']:.2e} cos {m['cos']:.8f} max {m['max_abs']:.2e}")
     return results
 
 
