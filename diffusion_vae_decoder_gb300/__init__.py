@@ -64,7 +64,11 @@ class ChainArgs(ctypes.Structure):
                 ("shift_factor", ctypes.c_float), ("groups", ctypes.c_int),
                 ("eps", ctypes.c_float), ("conv_in", ConvRef), ("mid_res1", ResnetRef),
                 ("mid_attn", AttnRef), ("mid_res2", ResnetRef), ("n_ups", ctypes.c_int),
-                ("ups", ctypes.POINTER(UpRef)), ("norm_out", NormRef), ("conv_out", ConvRef)]
+                ("ups", ctypes.POINTER(UpRef)), ("norm_out", NormRef), ("conv_out", ConvRef),
+                ("precision", ctypes.c_int)]
+
+
+PRECISION_AUTO, PRECISION_TF32, PRECISION_SPLIT_TF32 = 0, 1, 2
 
 
 class ProfRecord(ctypes.Structure):
@@ -397,10 +401,13 @@ class VaeChain:
 
     ``weights`` maps diffusers-style names (conv_in.weight, mid.resnets.0...,
     mid.attentions.0.to_q.weight, up_blocks.{i}.resnets.{j}..., ...,
-    conv_norm_out.weight, conv_out.weight) to host float32 arrays."""
+    conv_norm_out.weight, conv_out.weight) to host float32 arrays.
+    ``precision``: PRECISION_AUTO (split-TF32 products for decodes with little
+    conv work, TF32 otherwise), PRECISION_TF32 or PRECISION_SPLIT_TF32."""
 
     def __init__(self, weights, n_up_blocks, resnets_per_block=3, latent_channels=16,
-                 scaling_factor=0.3611, shift_factor=0.1159, groups=32, eps=1e-6, stream=None):
+                 scaling_factor=0.3611, shift_factor=0.1159, groups=32, eps=1e-6, stream=None,
+                 precision=PRECISION_AUTO):
         lib = load_library()
         keep = []
         ups = []
@@ -424,7 +431,7 @@ class VaeChain:
                          _resnet_ref(weights, "mid.resnets.0", keep), attn,
                          _resnet_ref(weights, "mid.resnets.1", keep), n_up_blocks, ups_arr,
                          _norm_ref(weights, "conv_norm_out", keep),
-                         _conv_ref(weights, "conv_out", keep))
+                         _conv_ref(weights, "conv_out", keep), int(precision))
         h = ctypes.c_void_p()
         _check("vae_chain_prepare", lib.vae_chain_prepare(ctypes.byref(args), ctypes.byref(h),
                                                           _stream(stream)))

@@ -7,9 +7,12 @@
 // z / scaling_factor + shift_factor. "VAE decode -> GPU handoff", step 3:
 // activations stay on the device and only the RGB image comes back.
 //
-// vae_chain_prepare packs every weight once into GEMM layout (TF32-rounded;
-// each resnet's 1x1 shortcut appended to conv2's reduction with the summed
-// bias) and returns the handle that plays the role of that key.
+// vae_chain_prepare packs every weight once into GEMM layout (TF32-rounded,
+// and unrounded as well unless the chain is TF32-only; each resnet's 1x1
+// shortcut appended to conv2's reduction with the summed bias) and returns
+// the handle that plays the role of that key. A decode whose products are
+// split-TF32 (vae_precision) keeps its activations in FP32 instead of storing
+// the MMA operands TF32-rounded.
 // vae_decode_chain then walks the chain on the caller's stream with no host
 // synchronisation, ping-ponging NHWC activations through the workspace:
 //   X, Y  the residual stream (a resnet without a shortcut updates it in
@@ -59,6 +62,7 @@ struct Tracer {
 
 struct ConvW {
   float *w = nullptr, *b = nullptr;
+  float *w_exact = nullptr;  // the same pack unrounded (split-TF32 products)
   int cin = 0, cout = 0, k = 0, ldb = 0, sc_cin = 0;
 };
 struct NormW {
@@ -72,6 +76,7 @@ struct ResW {
 struct AttnW {
   NormW n;
   float *wqkv = nullptr, *bqkv = nullptr, *wo = nullptr, *bo = nullptr;
+  float *wqkv_exact = nullptr, *wo_exact = nullptr;  // unrounded (split-TF32)
   int c = 0;
 };
 struct UpW {
@@ -134,6 +139,8 @@ struct Profiler {
 struct Chain {
   Profiler prof;
   Tracer *tr = nullptr;  // set for the duration of a traced decode
+  int precision = VAE_PRECISION_TF32;
+  bool exact = false;  // this decode forms split-TF32 products (set per decode)
   int device = 0;
   int latent_c = 0, groups = 32;
   float eps = 1e-6f, sf = 1.f, sh = 0.f;
@@ -219,8 +226,13 @@ struct Builder {
     const float *wsc = has_sc ? upload_tmp(sc->weight, static_cast<size_t>(cout) * c.sc_cin)
                               : nullptr;
     c.w = dev<float>(static_cast<size_t>(cout) * c.ldb);
+    if (ch->precision != VAE_PRECISION_TF32)
+      c.w_exact = dev<float>(static_cast<size_t>(cout) * c.ldb);
     if (status != VAE_OK) return c;
     fail(pack_conv_weights(wt, cout, cin, r.k * r.k, wsc, c.sc_cin, c.w, cout, c.ldb, s));
+    if (c.w_exact)
+      fail(pack_conv_weights(wt, cout, cin, r.k * r.k, wsc, c.sc_cin, c.w_exact, cout, c.ldb, s,
+                             0));
     if (has_sc) {
       const float *b1 = r.bias ? upload_tmp(r.bias, cout) : nullptr;
       const float *b2 = sc->bias ? upload_tmp(sc->bias, cout) : nullptr;
@@ -243,8 +255,10 @@ struct Builder {
     c.ldb = upsample_ldb(cin);
     const float *wt = upload_tmp(r.weight, static_cast<size_t>(cout) * cin * 9);
     c.w = dev<float>(4ull * cout * c.ldb);
+    if (ch->precision != VAE_PRECISION_TF32) c.w_exact = dev<float>(4ull * cout * c.ldb);
     if (status != VAE_OK) return c;
     fail(pack_upsample_weights(wt, cout, cin, c.w, s));
+    if (c.w_exact) fail(pack_upsample_weights(wt, cout, cin, c.w_exact, s, 0));
     if (r.bias) c.b = upload(r.bias, cout);
     return c;
   }
@@ -265,7 +279,9 @@ struct Builder {
     if (c % 32) fail(VAE_EUNSUPPORTED);
     a.n = norm(r.norm, c);
     const vae_conv_ref *p[3] = {&r.q, &r.k, &r.v};
+    const bool exact = ch->precision != VAE_PRECISION_TF32;
     a.wqkv = dev<float>(3ull * c * c);
+    if (exact) a.wqkv_exact = dev<float>(3ull * c * c);
     a.bqkv = dev<float>(3ull * c);
     for (int i = 0; i < 3 && status == VAE_OK; ++i) {
       if (p[i]->cin != c || p[i]->cout != c || p[i]->k != 1) fail(VAE_EINVAL);
@@ -273,6 +289,9 @@ struct Builder {
       if (status != VAE_OK) break;
       fail(pack_conv_weights(wt, c, c, 1, nullptr, 0, a.wqkv + static_cast<size_t>(i) * c * c,
                              c, c, s));
+      if (exact)
+        fail(pack_conv_weights(wt, c, c, 1, nullptr, 0,
+                               a.wqkv_exact + static_cast<size_t>(i) * c * c, c, c, s, 0));
       if (!p[i]->bias) fail(VAE_EINVAL);
       if (status == VAE_OK &&
           cudaMemcpyAsync(a.bqkv + i * c, p[i]->bias, c * 4, cudaMemcpyDefault, s) != cudaSuccess)
@@ -281,7 +300,10 @@ struct Builder {
     if (r.out.cin != c || r.out.cout != c || r.out.k != 1) fail(VAE_EINVAL);
     const float *wo = upload_tmp(r.out.weight, static_cast<size_t>(c) * c);
     a.wo = dev<float>(static_cast<size_t>(c) * c);
+    if (exact) a.wo_exact = dev<float>(static_cast<size_t>(c) * c);
     if (status == VAE_OK) fail(pack_conv_weights(wo, c, c, 1, nullptr, 0, a.wo, c, c, s));
+    if (status == VAE_OK && exact)
+      fail(pack_conv_weights(wo, c, c, 1, nullptr, 0, a.wo_exact, c, c, s, 0));
     a.bo = upload(r.out.bias, c);
     return a;
   }
@@ -389,14 +411,14 @@ double conv_flops(const ConvW &c, long long out_pixels) {
   return 2.0 * out_pixels * c.cout * (static_cast<double>(c.cin) * c.k * c.k + c.sc_cin);
 }
 
-int run_conv(Profiler &prof, const ConvW &c, const float *in, int n, int h, int w,
+int run_conv(Chain &ch, const ConvW &c, const float *in, int n, int h, int w,
              const float *sc_in, const float *residual, float *out, int round_out,
              cudaStream_t s, bool upsample = false, bool nchw_out = false,
              Stats *st = nullptr, float *part = nullptr, int groups = 0,
              float *split = nullptr) {
   const long long out_px = static_cast<long long>(n) * h * w * (upsample ? 4 : 1);
-  Step step(prof, upsample ? VAE_PROF_UPSAMPLE_CONV : VAE_PROF_CONV3X3, conv_flops(c, out_px),
-            0, s);
+  Step step(ch.prof, upsample ? VAE_PROF_UPSAMPLE_CONV : VAE_PROF_CONV3X3,
+            conv_flops(c, out_px), 0, s);
   IgemmDesc d;
   d.mode = upsample ? AMode::Upsample : AMode::Conv;
   d.a = in;
@@ -407,7 +429,8 @@ int run_conv(Profiler &prof, const ConvW &c, const float *in, int n, int h, int 
   d.k = c.k;
   d.sc = c.sc_cin ? sc_in : nullptr;
   d.sc_c = c.sc_cin ? round_up32(c.sc_cin) : 0;
-  d.b = c.w;
+  d.b = ch.exact ? c.w_exact : c.w;
+  d.precise = ch.exact ? 1 : 0;
   d.ldb = c.ldb;
   d.cout = c.cout;
   d.out = out;
@@ -415,7 +438,7 @@ int run_conv(Profiler &prof, const ConvW &c, const float *in, int n, int h, int 
   d.out_nchw = nchw_out;
   d.bias = c.b;
   d.residual = residual;
-  d.round_out = round_out;
+  d.round_out = ch.exact ? 0 : round_out;  // split-TF32 operands stay FP32
   d.split_ws = split;
   d.split_ws_floats = split ? kSplitWsFloats : 0;
   int fused = 0;
@@ -443,9 +466,11 @@ int run_gn(Chain &ch, const NormW &nw, const float *in, int n, long long sp, flo
            const DecodeWs &ws, const Stats &stats, cudaStream_t s) {
   Step step(ch.prof, VAE_PROF_GROUPNORM, 0, (stats.ready ? 8.0 : 12.0) * n * sp * nw.c, s);
   if (stats.ready)
-    return groupnorm_from_partials(in, n, nw.c, sp, ch.groups, ch.eps, nw.g, nw.b, 1, 1, ws.part,
+    return groupnorm_from_partials(in, n, nw.c, sp, ch.groups, ch.eps, nw.g, nw.b, 1, !ch.exact,
+                                   ws.part,
                                    stats.slots, out, ws.gn, s, nullptr, ws.gn_cnt);
-  return groupnorm_silu(in, n, nw.c, sp, 1, ch.groups, ch.eps, nw.g, nw.b, 1, 1, out, ws.gn, s);
+  return groupnorm_silu(in, n, nw.c, sp, 1, ch.groups, ch.eps, nw.g, nw.b, 1, !ch.exact, out,
+                        ws.gn, s);
 }
 
 // One resnet on NHWC data; `st` holds the statistics of `in` on entry and
@@ -456,16 +481,16 @@ int run_resnet(Chain &ch, const ResW &r, const float *in, float *out, const Deco
   const size_t in_bytes = 4ull * n * sp * r.c1.cin, out_bytes = 4ull * n * sp * r.c1.cout;
   VAE_TRY(run_gn(ch, r.n1, in, n, sp, ws.T, ws, st, s));
   if (ch.tr) ch.tr->emit(ws.T, in_bytes, s);
-  VAE_TRY(run_conv(ch.prof, r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s, false, false, &st,
+  VAE_TRY(run_conv(ch, r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s, false, false, &st,
                    ws.part, ch.groups, ws.split));
   if (ch.tr) ch.tr->emit(ws.H, out_bytes, s);
   VAE_TRY(run_gn(ch, r.n2, ws.H, n, sp, ws.T, ws, st, s));
   if (ch.tr) ch.tr->emit(ws.T, out_bytes, s);
   if (r.c2.sc_cin)
-    VAE_TRY(run_conv(ch.prof, r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s, false, false,
+    VAE_TRY(run_conv(ch, r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s, false, false,
                      &st, ws.part, ch.groups, ws.split));
   else
-    VAE_TRY(run_conv(ch.prof, r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s, false, false,
+    VAE_TRY(run_conv(ch, r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s, false, false,
                      &st, ws.part, ch.groups, ws.split));
   if (ch.tr) ch.tr->emit(out, out_bytes, s);
   return VAE_OK;
@@ -533,6 +558,11 @@ int vae_chain_prepare(const vae_chain_args *a, void **handle, vae_stream_t strea
   ch->eps = a->eps;
   ch->sf = a->scaling_factor;
   ch->sh = a->shift_factor;
+  if (a->precision < VAE_PRECISION_AUTO || a->precision > VAE_PRECISION_SPLIT_TF32) {
+    delete ch;
+    return VAE_EINVAL;
+  }
+  ch->precision = a->precision;
   Builder b{ch, s};
   const int c0 = a->conv_in.cout;
   ch->conv_in = b.conv(a->conv_in, a->latent_channels, c0);
@@ -596,6 +626,24 @@ size_t vae_chain_workspace_size(const void *handle, int n, int h, int w) {
 namespace vae {
 namespace {
 
+// Conv work of one decode (GFLOP, 2 per multiply-add at the definition's tap
+// count), which the AUTO precision compares with VAE_SPLIT_AUTO_GFLOP.
+double decode_conv_gflops(const Chain &ch, int n, int h, int w) {
+  auto conv = [&](const ConvW &c, double px) {
+    return 2.0 * px * c.cout * (static_cast<double>(c.cin) * (c.k == 2 ? 9 : c.k * c.k) + c.sc_cin);
+  };
+  double px = static_cast<double>(n) * h * w, f = conv(ch.conv_in, px);
+  for (const ResW *r : {&ch.mid1, &ch.mid2}) f += conv(r->c1, px) + conv(r->c2, px);
+  for (const UpW &u : ch.ups) {
+    for (const ResW &r : u.res) f += conv(r.c1, px) + conv(r.c2, px);
+    if (u.has_up) {
+      px *= 4;
+      f += conv(u.up, px);
+    }
+  }
+  return (f + conv(ch.conv_out, px)) / 1e9;
+}
+
 int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void *ws,
                 size_t ws_bytes, cudaStream_t s) {
   if (!z || !rgb || !ws || n <= 0 || h <= 0 || w <= 0) return VAE_EINVAL;
@@ -608,6 +656,9 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
   Carver cv(ws, ws_bytes);
   DecodeWs d = carve_decode(cv, *ch, p, n, h, w);
   if (!cv.ok()) return VAE_EWORKSPACE;
+  ch->exact = ch->precision == VAE_PRECISION_SPLIT_TF32 ||
+              (ch->precision == VAE_PRECISION_AUTO &&
+               decode_conv_gflops(*ch, n, h, w) <= VAE_SPLIT_AUTO_GFLOP);
 
   // The GroupNorm finalize counters start every decode at zero (each
   // finalize leaves them at zero; this also clears what an aborted decode
@@ -620,23 +671,24 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
   {
     const int cp = round_up32(ch->latent_c);
     Step st(ch->prof, VAE_PROF_LAYOUT, 0, 4.0 * n * L * (ch->latent_c + cp), s);
-    VAE_TRY(stage_nhwc(z, n, ch->latent_c, L, VAE_NCHW, d.lat, cp, 1.0f / ch->sf, ch->sh, 1,
-                       &lat, s));
+    VAE_TRY(stage_nhwc(z, n, ch->latent_c, L, VAE_NCHW, d.lat, cp, 1.0f / ch->sf, ch->sh,
+                       !ch->exact, &lat, s));
     if (ch->tr) ch->tr->emit(lat, 4ull * n * L * cp, s);
   }
   float *cur = d.X, *other = d.Y;
   int hh = h, ww = w;
   Stats st;
-  VAE_TRY(run_conv(ch->prof, ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s, false,
+  VAE_TRY(run_conv(*ch, ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s, false,
                    false, &st, d.part, ch->groups, d.split));
   if (ch->tr) ch->tr->emit(cur, 4ull * n * L * ch->conv_in.cout, s);
   VAE_TRY(run_resnet(*ch, ch->mid1, cur, cur, d, n, hh, ww, 0, st, s));
   {
     const double c = ch->attn.c;
     Step st(ch->prof, VAE_PROF_ATTENTION, n * (4.0 * L * L * c + 8.0 * L * c * c), 0, s);
-    VAE_TRY(attention_nhwc(cur, n, ch->attn.c, static_cast<int>(L), ch->groups, ch->eps,
-                           ch->attn.n.g, ch->attn.n.b, ch->attn.wqkv, ch->attn.bqkv, ch->attn.wo,
-                           ch->attn.bo, cur, d.attn, s));
+    const AttnW &a = ch->attn;
+    VAE_TRY(attention_nhwc(cur, n, a.c, static_cast<int>(L), ch->groups, ch->eps, a.n.g, a.n.b,
+                           ch->exact ? a.wqkv_exact : a.wqkv, a.bqkv,
+                           ch->exact ? a.wo_exact : a.wo, a.bo, cur, d.attn, s, ch->exact));
   }
   if (ch->tr) ch->tr->emit(cur, 4ull * n * L * ch->attn.c, s);
   st.ready = false;  // the attention changed `cur`
@@ -653,7 +705,7 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
     }
     if (u.has_up) {
       // Output rounded: the next resnet may read it through its shortcut MMA.
-      VAE_TRY(run_conv(ch->prof, u.up, cur, n, hh, ww, nullptr, nullptr, other, 1, s, true,
+      VAE_TRY(run_conv(*ch, u.up, cur, n, hh, ww, nullptr, nullptr, other, 1, s, true,
                        false, &st, d.part, ch->groups, d.split));
       std::swap(cur, other);
       hh *= 2;
@@ -677,7 +729,7 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
   }
   VAE_TRY(run_gn(*ch, ch->norm_out, cur, n, hw, d.T, d, st, s));
   if (ch->tr) ch->tr->emit(d.T, 4ull * n * hw * ch->norm_out.c, s);
-  VAE_TRY(run_conv(ch->prof, ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, rgb, 0, s, false,
+  VAE_TRY(run_conv(*ch, ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, rgb, 0, s, false,
                    true));
   if (ch->tr) ch->tr->emit(rgb, 4ull * n * hw * ch->conv_out.cout, s);
   return VAE_OK;

@@ -110,6 +110,10 @@ struct IgemmDesc {
   // when the output tiles alone would leave most SMs idle.
   float *split_ws = nullptr;
   size_t split_ws_floats = 0;
+  // Split-TF32 products (Conv / Upsample / Gemm): A and B are FP32 and every
+  // product is formed as a_hi b_hi + a_lo b_hi + a_hi b_lo with each part
+  // rounded to TF32 (three MMAs per step, about FP32 accuracy).
+  int precise = 0;
 };
 // Split-K reduce (splitk.cu): out = alpha * sum of the partials + bias
 // (+ residual), rounded on request; GroupNorm partials [samples][groups][slots]
@@ -126,8 +130,10 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream);
 // Weight packing (layout.cu): w [cout][cin][taps] (+ shortcut [cout][sc_cin])
 // -> dst [cout_rows][ldb] with K index tap * cin_pad + c, TF32-rounded, zeros in
 // the padding.
+// round = 0 keeps the FP32 values (split-TF32 products split them in the kernel).
 int pack_conv_weights(const float *w, int cout, int cin, int taps, const float *w_sc,
-                      int sc_cin, float *dst, int cout_rows, int ldb, cudaStream_t s);
+                      int sc_cin, float *dst, int cout_rows, int ldb, cudaStream_t s,
+                      int round = 1);
 inline int packed_ldb(int cin, int taps, int sc_cin) {
   return taps * round_up32(cin) + (sc_cin ? round_up32(sc_cin) : 0);
 }
@@ -135,7 +141,8 @@ inline int packed_ldb(int cin, int taps, int sc_cin) {
 // w [cout][cin][3][3] -> dst [4 parities][cout][upsample_ldb(cin)], K index
 // (a * 2 + b) * cin_pad + c, parity = py * 2 + px.
 inline int upsample_ldb(int cin) { return 4 * round_up32(cin); }
-int pack_upsample_weights(const float *w, int cout, int cin, float *dst, cudaStream_t s);
+int pack_upsample_weights(const float *w, int cout, int cin, float *dst, cudaStream_t s,
+                          int round = 1);
 
 // Layout transforms (layout.cu). src [outer][rows][cols] (row stride src_ld)
 // -> dst [outer][cols][rows] (row stride dst_ld), dst = src * alpha + beta,
@@ -191,7 +198,9 @@ bool flash_supported(int d);
 int flash_attention(const float *q, const float *k, int ld, const float *vt, int ldv, int L, int d,
                     float scale, float *out, int ldo, cudaStream_t s);
 
-// Row softmax in place: s[r][:L] <- softmax(scale * s[r][:L]), TF32-rounded.
-int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st);
+// Row softmax in place: s[r][:L] <- softmax(scale * s[r][:L]), TF32-rounded
+// unless round == 0.
+int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st,
+                 int round = 1);
 
 }  // namespace vae

@@ -56,1090 +56,19 @@
 #include <mutex>
 
 #include "common.cuh"
-#include "ptx.cuh"
+#include "igemm_kernel.cuh"
 
 namespace vae {
 
+using namespace igk;
+
 namespace {
-
-constexpr int kBM = 128;
-constexpr int kThreads = 192;
-constexpr uint32_t kABytes = kBM * 128;
-
-struct KParams {
-  int imgs, t, hin, win, hout, wout;
-  int bh, bw;  // tile rows / cols (Conv: output pixels; Upsample: low-res pixels)
-  int tiles_x, tiles_y;
-  int m_tiles, n_tiles, total_tiles;
-  int M;
-  int k, kt, taps;
-  int cin_chunks, sc_chunks, k_stages, cin_pad;
-  // split-K: tile index = (split, m tile, n tile); split s covers reduction
-  // steps [s * ks_per, min((s + 1) * ks_per, k_stages)) and writes its raw
-  // partial sums at out + s * split_stride.
-  int splits, ks_per;
-  long long split_stride;
-  int cout;
-  float *out;
-  int ldo, out_nchw;
-  const float *bias;
-  int bias_per_row;
-  const float *residual;
-  float alpha;
-  int round_out;
-  int epi_tma;  // 1: rows leave through shared staging + TMA stores (NHWC / GEMM)
-  int has_res;  // residual present (TMA-loaded into the staging buffer when epi_tma)
-  // GroupNorm statistics of the output (optional): per (sample, group, slot)
-  // partial (count, mean, M2); slot = (frame, tile, sub-tile, warp).
-  float *stat_part;
-  int stat_cg;       // channels per group (power of two dividing 32)
-  int stat_groups;   // groups over cout
-  int stat_slots;    // slots per (sample, group)
-  // Stream-K (when whole tiles would leave the last round of SMs mostly
-  // idle): CTA c runs units [c * sk_total / G, (c + 1) * sk_total / G) of the
-  // flattened (tile, reduction unit) space, sk_units units per tile (a unit
-  // is one reduction step, or one 32-channel chunk in MODE 3). A tile cut
-  // between two CTAs: the CTA holding its later part (the tail, at the start
-  // of its range) writes the raw sums to its slot of sk_part and raises its
-  // flags; the CTA holding the head (at the end of its range) adds them in
-  // its epilogue. Fixed split points: deterministic.
-  int sk;
-  int sk_units;
-  long long sk_total;
-  float *sk_part;
-  int *sk_flag;  // [G][4]: one per epilogue warp, zeroed before the launch
-  int *err;
-  uint64_t wait_ns;  // limit of every device-side wait (normally kWaitTimeoutNs)
-  int inject;        // test hook: VAE_INJECT_* bits (0 in normal operation)
-};
-
-// One work item of a CTA: a tile and the range [k0, k1) of its reduction
-// units (reduction steps; 32-channel chunks in MODE 3).
-struct Work {
-  int tile, k0, k1;
-  bool head, tail;  // stream-K: the tile's first part here and the rest on the next CTA / the reverse
-};
-
-// The CTA's work items, identical in the producer, MMA and epilogue roles.
-template <int MODE>
-struct WorkIter {
-  long long u, end;
-  int tile;
-  __device__ explicit WorkIter(const KParams &p) : u(0), end(0), tile(blockIdx.x) {
-    if (p.sk) {
-      u = p.sk_total * blockIdx.x / gridDim.x;
-      end = p.sk_total * (blockIdx.x + 1) / gridDim.x;
-    }
-  }
-  __device__ bool next(const KParams &p, Work &w) {
-    if (p.sk) {
-      if (u >= end) return false;
-      w.tile = static_cast<int>(u / p.sk_units);
-      w.k0 = static_cast<int>(u % p.sk_units);
-      const long long left = end - u;
-      w.k1 = left < p.sk_units - w.k0 ? w.k0 + static_cast<int>(left) : p.sk_units;
-      w.tail = w.k0 > 0;
-      w.head = w.k0 == 0 && w.k1 < p.sk_units;
-      u += w.k1 - w.k0;
-      return true;
-    }
-    if (tile >= p.total_tiles) return false;
-    w.tile = tile;
-    if (MODE == 3) {
-      w.k0 = 0;
-      w.k1 = p.cin_chunks;
-    } else {
-      const int split = tile / (p.m_tiles * p.n_tiles);
-      w.k0 = split * p.ks_per;
-      w.k1 = min(w.k0 + p.ks_per, p.k_stages);
-    }
-    w.head = w.tail = false;
-    tile += gridDim.x;
-    return true;
-  }
-};
-
-// BN: output channels per tile (MMA N; MMA M in MODE 4). MS: 128-row M sub-tiles per tile
-// sharing each B stage (1, or 2 for 128-channel convs: a 256-pixel tile keeps
-// the operand bytes per FLOP of a 128 x 256 tile). MODE 3 (halo conv): the
-// input tile of a 32-channel chunk is staged once, with a one-pixel halo
-// ((MS + 2) rows x 130 pixels, two buffers), and serves all nine taps; the
-// ring stages then carry weights only.
-template <int BN, int MS, int MODE = 0>
-struct Cfg {
-  static constexpr bool HALO = MODE == 3;
-  static constexpr bool SWAP = MODE == 4;
-  // Separately buffered A operand (MODES 3 and 4): two buffers, each serving
-  // several reduction steps. MODE 4 holds (bh + 2) rows x bw pixels with
-  // bh * bw = 256, at most 64 KB (bw <= 128).
-  static constexpr uint32_t HALO_BYTES =
-      HALO ? ((MS + 2) * 130 * 128 + 1023) / 1024 * 1024 : SWAP ? 65536 : 0;
-  static constexpr int HALO_BUFS = (HALO || SWAP) ? 2 : 0;
-  // MODE 4: appended-shortcut tiles (MS x 128 rows each) sharing one A buffer.
-  static constexpr int SC_PER_BUF = SWAP ? static_cast<int>(HALO_BYTES / (MS * kABytes)) : 1;
-  static constexpr uint32_t A_BYTES = (HALO || SWAP) ? 0 : MS * kABytes;
-  static constexpr uint32_t B_BYTES = BN * 128;
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  // Epilogue staging: 4 warps x NSTG buffers x (32 rows x 128 bytes).
-  static constexpr int NSTG = HALO ? 1 : 2;
-  static constexpr uint32_t STAGING = 4 * NSTG * 4096;
-  static constexpr int FIT =
-      (232448 - 1024 - STAGING - 1024 - HALO_BUFS * HALO_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
-  static constexpr uint32_t ACC_COLS = BN * MS;  // TMEM columns of one accumulator set
-  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
-  static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
-  static constexpr size_t SMEM = 1024 + HALO_BUFS * HALO_BYTES + STAGES * STAGE_BYTES + STAGING +
-                                 (2 * STAGES + 13) * sizeof(uint64_t) + 16;
-  static_assert(!(HALO || SWAP) || STAGES >= 3, "buffered-A modes need a weight ring");
-  static_assert(!SWAP || (BN == 128 && MS == 2), "MODE 4 tiles are 128 channels x 256 pixels");
-  static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
-  static_assert(SMEM <= 232448, "shared memory budget");
-};
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Sum each of NG per-lane values over the warp with a reduce-scatter
-// butterfly: every step sends half of the remaining values to the partner
-// lane, so NG - 1 + (5 - log2 NG) shuffles replace NG * 5. On return a[0]
-// holds, in every lane, the total of group (lane >> (5 - log2 NG)).
-template <int NG>
-__device__ __forceinline__ void warp_reduce_scatter(float (&a)[NG], int lane) {
-#pragma unroll
-  for (int half = NG / 2, o = 16; half >= 1; half /= 2, o /= 2) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? a[i] : a[half + i];
-      const float keep = upper ? a[half + i] : a[i];
-      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-  constexpr int kLog = NG >= 32 ? 5 : NG >= 16 ? 4 : NG >= 8 ? 3 : NG >= 4 ? 2 : NG >= 2 ? 1 : 0;
-#pragma unroll
-  for (int o = 16 >> kLog; o >= 1; o /= 2) a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
-}
-
-// Exact two-pass (count, mean, M2) of each CG-channel group of a warp's 32
-// rows x 32 channels (invalid rows excluded). The lanes holding a group's
-// totals write its partial; successive groups are `gstride` floats apart.
-template <int CG>
-__device__ __forceinline__ void emit_group_stats(const float *v, bool valid, float nrows,
-                                                 float *out, long long gstride, int lane) {
-  constexpr int NG = 32 / CG;
-  constexpr int kShift = NG >= 32 ? 0 : NG >= 16 ? 1 : NG >= 8 ? 2 : NG >= 4 ? 3 : NG >= 2 ? 4 : 5;
-  const float cnt = nrows * CG;
-  const float inv = cnt > 0.f ? __fdividef(1.0f, cnt) : 0.f;
-  float a[NG];
-#pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    float sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < CG; ++j) sum += v[g * CG + j];
-    a[g] = valid ? sum : 0.f;
-  }
-  warp_reduce_scatter<NG>(a, lane);
-  const float my_mean = a[0] * inv;  // mean of group (lane >> kShift)
-  float m2[NG];
-#pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    const float mean = __shfl_sync(0xffffffffu, my_mean, g << kShift);
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < CG; ++j) {
-      const float d = v[g * CG + j] - mean;
-      acc = fmaf(d, d, acc);
-    }
-    m2[g] = valid ? acc : 0.f;
-  }
-  warp_reduce_scatter<NG>(m2, lane);
-  if ((lane & ((1 << kShift) - 1)) == 0) {
-    float *o = out + (lane >> kShift) * gstride;
-    o[0] = cnt;
-    o[1] = my_mean;
-    o[2] = m2[0];
-  }
-}
-
-__device__ __forceinline__ void raise_error(const KParams &p, volatile uint32_t *abort) {
-  *abort = 1u;
-  atomicCAS(p.err, 0, static_cast<int>(VAE_EDEVICE_TIMEOUT));
-}
-
-// Unbounded-by-abort wait used only while draining after an abort.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
-                                                uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  return true;
-}
-
-template <int BN, int MODE, int MS>
-__global__ void __launch_bounds__(kThreads, 1)
-    igemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmO,
-                 const __grid_constant__ CUtensorMap tmR, const KParams p) {
-  using C = Cfg<BN, MS, MODE>;
-  constexpr int STAGES = C::STAGES;
-  constexpr bool kConv = MODE == 0 || MODE == 3 || MODE == 4;  // conv tiles (epilogue geometry)
-  constexpr uint32_t STAGE_TX = C::STAGE_BYTES;
-  constexpr uint32_t IDESC = idesc_tf32(kBM, BN);
-  constexpr uint32_t IDESC_SWAP = idesc_tf32(kBM, 256);  // MODE 4: M = channels, N = pixels
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *sH = smem;  // A buffers (MODES 3 and 4)
-  uint8_t *sA = smem + C::HALO_BUFS * C::HALO_BYTES;
-  uint8_t *sB = sA + STAGES * C::A_BYTES;
-  const uint32_t sB_u32 = smem_u32(sB);
-  float *staging = reinterpret_cast<float *>(sB + STAGES * C::B_BYTES);  // 1024-aligned
-  uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_BYTES + C::STAGING);
-  uint64_t *empty = full + STAGES;
-  uint64_t *acc_full = empty + STAGES;
-  uint64_t *acc_empty = acc_full + 2;
-  uint64_t *drain = acc_empty + 2;  // used only after an abort
-  uint64_t *res_bar = drain + 1;    // one per epilogue warp: residual box landed
-  uint64_t *a_full = res_bar + 4;   // MODES 3, 4: A buffer landed / free
-  uint64_t *a_empty = a_full + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(a_empty + 2);
-  volatile uint32_t *abort = tmem_slot + 1;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
-    }
-    mbar_init(drain, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&res_bar[q], 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&a_full[b], 1);
-      mbar_init(&a_empty[b], 1);
-    }
-    *abort = 0u;
-    fence_mbarrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-    if (kConv && p.sc_chunks > 0) prefetch_tmap(&tmS);
-    if (p.epi_tma) {
-      prefetch_tmap(&tmO);
-      if (p.has_res) prefetch_tmap(&tmR);
-    }
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      uint32_t pending = 0, pend_par = 0;  // stages with a copy issued, and its parity
-      uint32_t abuf = 0, aphase = 0;       // MODE 3 halo buffer ring
-      uint32_t a_pending = 0, a_par = 0;
-      bool failed = false;
-      WorkIter<MODE> it(p);
-      Work w;
-      while (!failed && it.next(p, w)) {
-        const int tile = w.tile;
-        const int mn = tile % (p.m_tiles * p.n_tiles);
-        const int mt = mn / p.n_tiles;
-        const int n0 = (mn % p.n_tiles) * BN;
-        const int ks0 = w.k0, ks1 = w.k1;
-        int img = 0, ty = 0, tx = 0, par = 0;
-        if (MODE != 2) {
-          const int per_img = p.tiles_x * p.tiles_y * (MODE == 1 ? 4 : 1);
-          img = mt / per_img;
-          int rem = mt % per_img;
-          if (MODE == 1) {  // the four output parities of a low-res tile are adjacent tiles
-            par = rem & 3;
-            rem >>= 2;
-          }
-          ty = rem / p.tiles_x;
-          tx = rem % p.tiles_x;
-        }
-        const int n_idx = img / p.t, t_idx = img % p.t;
-        if constexpr (MODE == 3) {
-          // One halo tile per 32-channel chunk, then one weight stage per tap
-          // (no appended shortcut in this mode).
-          for (int cc = ks0; cc < ks1 && !failed; ++cc) {
-            if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort, p.wait_ns)) {
-              raise_error(p, abort);
-              failed = true;
-              break;
-            }
-            mbar_arrive_expect_tx(&a_full[abuf], (MS + 2) * 130 * 128);
-            tma_load_4d(sH + abuf * C::HALO_BYTES, &tmA, &a_full[abuf], cc * 32, tx * p.bw - 1,
-                        ty * p.bh - 1, img);
-            a_pending |= 1u << abuf;
-            a_par = (a_par & ~(1u << abuf)) | (aphase << abuf);
-            if (++abuf == 2) {
-              abuf = 0;
-              aphase ^= 1u;
-            }
-            for (int tap = 0; tap < p.taps; ++tap) {
-              if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.wait_ns)) {
-                raise_error(p, abort);
-                failed = true;
-                break;
-              }
-              mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-              tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], tap * p.cin_pad + cc * 32,
-                          n0);
-              pending |= 1u << stage;
-              pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-              if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1u;
-              }
-            }
-          }
-          continue;
-        }
-        if constexpr (MODE == 4) {
-          // Per 32-channel chunk and kx: one band of bh + 2 rows shifted by
-          // kx - 1 serves the three ky taps; then the shortcut chunks, their
-          // plain tiles SC_PER_BUF to an A buffer.
-          const int chunks = p.cin_chunks + (p.sc_chunks + C::SC_PER_BUF - 1) / C::SC_PER_BUF;
-          for (int cc = 0; cc < chunks && !failed; ++cc) {
-            const bool is_sc = cc >= p.cin_chunks;
-            const int sc0 = (cc - p.cin_chunks) * C::SC_PER_BUF;
-            const int nsc = is_sc ? min(C::SC_PER_BUF, p.sc_chunks - sc0) : 0;
-            const int nkx = is_sc ? 1 : 3;
-            for (int kx = 0; kx < nkx && !failed; ++kx) {
-              if (!mbar_wait(&a_empty[abuf], aphase ^ 1u, abort, p.wait_ns)) {
-                raise_error(p, abort);
-                failed = true;
-                break;
-              }
-              uint8_t *a_dst = sH + abuf * C::HALO_BYTES;
-              if (!is_sc) {
-                mbar_arrive_expect_tx(&a_full[abuf], (p.bh + 2) * p.bw * 128);
-                tma_load_4d(a_dst, &tmA, &a_full[abuf], cc * 32, tx * p.bw + kx - 1,
-                            ty * p.bh - 1, img);
-              } else {
-                mbar_arrive_expect_tx(&a_full[abuf], nsc * p.bh * p.bw * 128);
-                for (int i = 0; i < nsc; ++i)
-                  tma_load_4d(a_dst + i * p.bh * p.bw * 128, &tmS, &a_full[abuf], (sc0 + i) * 32,
-                              tx * p.bw, ty * p.bh, img);
-              }
-              a_pending |= 1u << abuf;
-              a_par = (a_par & ~(1u << abuf)) | (aphase << abuf);
-              if (++abuf == 2) {
-                abuf = 0;
-                aphase ^= 1u;
-              }
-              const int nky = is_sc ? nsc : 3;
-              for (int ky = 0; ky < nky; ++ky) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.wait_ns)) {
-                  raise_error(p, abort);
-                  failed = true;
-                  break;
-                }
-                const int kcol = is_sc ? p.taps * p.cin_pad + (sc0 + ky) * 32
-                                       : (ky * 3 + kx) * p.cin_pad + cc * 32;
-                mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-                tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kcol, n0);
-                pending |= 1u << stage;
-                pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-                if (++stage == STAGES) {
-                  stage = 0;
-                  phase ^= 1u;
-                }
-              }
-            }
-          }
-          continue;
-        }
-        for (int ks = ks0; ks < ks1; ++ks) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort, p.wait_ns)) {
-            raise_error(p, abort);
-            failed = true;
-            break;
-          }
-          uint8_t *a_dst = sA + stage * C::A_BYTES;
-          uint8_t *b_dst = sB + stage * C::B_BYTES;
-          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-          if (MODE == 0) {
-            const int main_steps = p.taps * p.cin_chunks;
-            if (ks < main_steps) {
-              const int tap = ks / p.cin_chunks, cc = ks % p.cin_chunks;
-              const int kk = p.k * p.k;
-              const int ktap = tap / kk, sp = tap % kk;
-              const int dy = sp / p.k - p.k / 2, dx = sp % p.k - p.k / 2;
-              int ft = t_idx + ktap - (p.kt - 1);
-              ft = ft < 0 ? 0 : ft;  // causal padding repeats the first frame
-              tma_load_4d(a_dst, &tmA, &full[stage], cc * 32, tx * p.bw + dx, ty * p.bh + dy,
-                          n_idx * p.t + ft);
-              tma_load_2d(b_dst, &tmB, &full[stage], tap * p.cin_pad + cc * 32, n0);
-            } else {
-              const int cc = ks - main_steps;
-              tma_load_4d(a_dst, &tmS, &full[stage], cc * 32, tx * p.bw, ty * p.bh, img);
-              tma_load_2d(b_dst, &tmB, &full[stage], p.taps * p.cin_pad + cc * 32, n0);
-            }
-          } else if (MODE == 1) {
-            // 2x2 tap (a, b) of parity (py, px) reads the low-res tile shifted
-            // by (py - 1 + a, px - 1 + b); weights of that parity's kernel.
-            const int tap = ks / p.cin_chunks, cc = ks % p.cin_chunks;
-            tma_load_4d(a_dst, &tmA, &full[stage], cc * 32, tx * p.bw + (par & 1) - 1 + (tap & 1),
-                        ty * p.bh + (par >> 1) - 1 + (tap >> 1), img);
-            tma_load_2d(b_dst, &tmB, &full[stage], tap * p.cin_pad + cc * 32, par * p.cout + n0);
-          } else {
-            tma_load_2d(a_dst, &tmA, &full[stage], ks * 32, mt * kBM);
-            tma_load_2d(b_dst, &tmB, &full[stage], ks * 32, n0);
-          }
-          pending |= 1u << stage;
-          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (*abort) {
-        // Let every copy this thread issued land before the CTA exits.
-        for (int s = 0; s < STAGES; ++s)
-          if (pending & (1u << s)) mbar_wait_drain(&full[s], (pend_par >> s) & 1u, p.wait_ns);
-        for (int b = 0; b < 2; ++b)
-          if (a_pending & (1u << b)) mbar_wait_drain(&a_full[b], (a_par >> b) & 1u, p.wait_ns);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      uint32_t abuf = 0, aphase = 0;
-      int local = 0;
-      bool failed = false, issued = false;
-      WorkIter<MODE> it(p);
-      Work w;
-      while (!failed && it.next(p, w)) {
-        const int cur = local++;
-        const int buf = cur & 1;
-        const uint32_t aph = (cur >> 1) & 1;
-        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort, p.wait_ns)) {
-          raise_error(p, abort);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS;
-        const int ks0 = w.k0, ks1 = w.k1;
-        if constexpr (MODE == 3) {
-          // Tap (ky, kx) of output sub-tile `sub` reads the 128 halo pixels
-          // starting at halo row sub + ky, column kx: a row offset into the
-          // swizzled halo buffer.
-          for (int cc = ks0; cc < ks1 && !failed; ++cc) {
-            if (!mbar_wait(&a_full[abuf], aphase, abort, p.wait_ns)) {
-              raise_error(p, abort);
-              failed = true;
-              break;
-            }
-            // The nine views differ from the buffer's descriptor only in the
-            // start-address field (row * 128 bytes >> 4; no carry: shared
-            // addresses stay below 256 KB), so they are compile-time offsets.
-            const uint64_t hdesc = sw128_kmajor_desc(smem_u32(sH + abuf * C::HALO_BYTES));
-            const bool acc0 = cc != ks0;
-            issued = true;
-#pragma unroll
-            for (int tap = 0; tap < 9; ++tap) {
-              if (!mbar_wait(&full[stage], phase, abort, p.wait_ns)) {
-                raise_error(p, abort);
-                failed = true;
-                break;
-              }
-              tc_fence_after();
-              const uint64_t bd = sw128_kmajor_desc(sB_u32 + stage * C::B_BYTES);
-#pragma unroll
-              for (int sub = 0; sub < MS; ++sub) {
-                const uint64_t ad =
-                    hdesc + static_cast<uint64_t>(((sub + tap / 3) * 130 + tap % 3) * 8);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  umma_tf32(d_tmem + sub * BN, ad + 2 * k, bd + 2 * k, IDESC,
-                            acc0 || (tap != 0) || (k != 0));
-              }
-              umma_commit(&empty[stage]);
-              if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1u;
-              }
-            }
-            if (failed) break;
-            umma_commit(&a_empty[abuf]);
-            if (++abuf == 2) {
-              abuf = 0;
-              aphase ^= 1u;
-            }
-          }
-          if (!failed) umma_commit(&acc_full[buf]);
-          continue;
-        }
-        if constexpr (MODE == 4) {
-          // D[channel][pixel] += W[channel][k] . X[pixel][k]: the weight
-          // stage is the 128-row M operand, the pixel band the 256-row N
-          // operand, viewed from row ky * bw.
-          const int chunks = p.cin_chunks + (p.sc_chunks + C::SC_PER_BUF - 1) / C::SC_PER_BUF;
-          bool first = true;
-          for (int cc = 0; cc < chunks && !failed; ++cc) {
-            const bool is_sc = cc >= p.cin_chunks;
-            const int nsc =
-                is_sc ? min(C::SC_PER_BUF, p.sc_chunks - (cc - p.cin_chunks) * C::SC_PER_BUF) : 0;
-            const int nkx = is_sc ? 1 : 3;
-            for (int kx = 0; kx < nkx && !failed; ++kx) {
-              if (!mbar_wait(&a_full[abuf], aphase, abort, p.wait_ns)) {
-                raise_error(p, abort);
-                failed = true;
-                break;
-              }
-              const uint32_t abase = smem_u32(sH + abuf * C::HALO_BYTES);
-              const int nky = is_sc ? nsc : 3;
-              for (int ky = 0; ky < nky; ++ky) {
-                if (!mbar_wait(&full[stage], phase, abort, p.wait_ns)) {
-                  raise_error(p, abort);
-                  failed = true;
-                  break;
-                }
-                tc_fence_after();
-                const uint64_t wd = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
-                // band view from row ky * bw, or the ky-th shortcut tile
-                const uint64_t xd = sw128_kmajor_desc_row(abase, ky * (is_sc ? p.bh * p.bw : p.bw));
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  umma_tf32(d_tmem, wd + 2 * k, xd + 2 * k, IDESC_SWAP, !first || (k != 0));
-                first = false;
-                issued = true;
-                umma_commit(&empty[stage]);
-                if (++stage == STAGES) {
-                  stage = 0;
-                  phase ^= 1u;
-                }
-              }
-              if (failed) break;
-              umma_commit(&a_empty[abuf]);
-              if (++abuf == 2) {
-                abuf = 0;
-                aphase ^= 1u;
-              }
-            }
-          }
-          if (!failed) umma_commit(&acc_full[buf]);
-          continue;
-        }
-        for (int ks = ks0; ks < ks1; ++ks) {
-          if (!mbar_wait(&full[stage], phase, abort, p.wait_ns)) {
-            raise_error(p, abort);
-            failed = true;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
-#pragma unroll
-          for (int sub = 0; sub < MS; ++sub) {
-            const uint64_t ad =
-                sw128_kmajor_desc(smem_u32(sA + stage * C::A_BYTES + sub * kABytes));
-#pragma unroll
-            for (int k = 0; k < 4; ++k)  // 4 x K=8 TF32 steps = 32 channels (128 bytes)
-              umma_tf32(d_tmem + sub * BN, ad + 2 * k, bd + 2 * k, IDESC,
-                        (ks != ks0) || (k != 0));
-          }
-          issued = true;
-          umma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!failed) umma_commit(&acc_full[buf]);
-      }
-      if (*abort && issued) {
-        // Wait for the MMAs still reading shared memory / writing TMEM before
-        // the CTA frees TMEM and exits.
-        umma_commit(drain);
-        mbar_wait_drain(drain, 0, p.wait_ns);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int m = q * 32 + lane;
-    float *stg = staging + q * C::NSTG * 1024;  // this warp's 4 KB staging buffer(s)
-    int sbuf = 0;
-    uint32_t res_phase = 0;
-    bool failed = false;
-    int local = 0;
-    WorkIter<MODE> it(p);
-    Work w;
-    while (!failed && it.next(p, w)) {
-      const int tile = w.tile;
-      const int cur = local++;
-      const int buf = cur & 1;
-      const uint32_t aph = (cur >> 1) & 1;
-      bool ok = mbar_wait(&acc_full[buf], aph, abort, p.wait_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        if (lane == 0) raise_error(p, abort);
-        break;
-      }
-      tc_fence_after();
-
-      const int mn = tile % (p.m_tiles * p.n_tiles);
-      const int split = tile / (p.m_tiles * p.n_tiles);
-      const int mt = mn / p.n_tiles;
-      const int n0 = (mn % p.n_tiles) * BN;
-      float *const obase = p.out + split * p.split_stride;
-      if constexpr (MODE == 4) {
-        // Accumulator lanes are output channels, columns pixels: each lane
-        // owns one channel and reads 32 pixels at a time, transposing into
-        // the pixel-major staging block on its way to the TMA store.
-        const int per_img = p.tiles_x * p.tiles_y;
-        const int img = mt / per_img;
-        const int rem = mt % per_img;
-        const int ty = rem / p.tiles_x, tx = rem % p.tiles_x;
-        const int c0 = n0 + q * 32;  // this warp's first channel (warp-uniform)
-        const int ch = c0 + lane;
-        const bool ch_ok = ch < p.cout;
-        const float bch = (p.bias && ch_ok) ? __ldg(p.bias + ch) : 0.f;
-        const int lbw = __ffs(p.bw) - 1;  // bw is a power of two
-        // In-image mask of a 32-pixel chunk: lane j tests pixel j.
-        auto chunk_mask = [&](int mp0) -> uint32_t {
-          const int py = ty * p.bh + ((mp0 + lane) >> lbw);
-          const int px = tx * p.bw + ((mp0 + lane) & (p.bw - 1));
-          return __ballot_sync(0xffffffffu, py < p.hout && px < p.wout);
-        };
-        // Residual of a chunk: for pixel j the 32 lanes read 32 adjacent
-        // channels (one 128-byte line), so plain loads are coalesced; they
-        // are issued one chunk ahead of their use.
-        const float *rcol = (p.has_res && ch_ok)
-                                ? p.residual + static_cast<long long>(img) * p.hout * p.wout * p.ldo + ch
-                                : nullptr;
-        auto load_res = [&](int mp0, uint32_t mask, float(&dst)[32]) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int y = ty * p.bh + ((mp0 + j) >> lbw);
-            const int x = tx * p.bw + ((mp0 + j) & (p.bw - 1));
-            dst[j] = (rcol && ((mask >> j) & 1u))
-                         ? __ldcg(rcol + (static_cast<long long>(y) * p.wout + x) * p.ldo)
-                         : 0.f;
-          }
-        };
-        float rnext[32], rcur[32];
-        uint32_t mnext = chunk_mask(0);
-        if (p.has_res) load_res(0, mnext, rnext);
-        for (int pc = 0; pc < 8 && c0 < p.cout; ++pc) {
-          const uint32_t vmask = mnext;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) rcur[j] = rnext[j];
-          if (pc + 1 < 8) {
-            mnext = chunk_mask((pc + 1) * 32);
-            if (p.has_res) load_res((pc + 1) * 32, mnext, rnext);
-          }
-          float v[32];
-          tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(buf * C::ACC_COLS + pc * 32),
-                         v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], p.alpha, bch);
-          const int mp0 = pc * 32;  // first pixel of the chunk within the tile
-          const int bx = tx * p.bw + (mp0 & (p.bw - 1)), by = ty * p.bh + (mp0 >> lbw);
-          float *sb = stg + sbuf * 1024;
-          if (lane == 0) bulk_wait_read<1>();  // the store that used sb last is done
-          __syncwarp();
-          // Pixel j is row j of the block, this lane's channel its column;
-          // the 128-byte swizzle puts 16-byte chunk (lane / 4) at
-          // (lane / 4) ^ (j % 8), so each row's 32 stores hit 32 banks.
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int idx = j * 32 + ((((lane >> 2) ^ (j & 7)) << 2) | (lane & 3));
-            float val = p.has_res ? v[j] + rcur[j] : v[j];
-            if (p.round_out) val = round_tf32(val);
-            sb[idx] = val;
-            v[j] = val;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_4d(&tmO, sb, c0, bx, by, img);
-            bulk_commit();
-          }
-          sbuf ^= 1;
-          if (p.stat_part) {
-            // (count, mean, M2) of each group (stat_cg adjacent lanes) over
-            // the chunk's in-image pixels; slot = (frame, tile, chunk).
-            const int nv = __popc(vmask);
-            float sum = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sum += ((vmask >> j) & 1u) ? v[j] : 0.f;
-            for (int o = 1; o < p.stat_cg; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            const float cnt = static_cast<float>(nv * p.stat_cg);
-            const float mean = cnt > 0.f ? __fdividef(sum, cnt) : 0.f;
-            float m2 = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float d = v[j] - mean;
-              m2 = ((vmask >> j) & 1u) ? fmaf(d, d, m2) : m2;
-            }
-            for (int o = 1; o < p.stat_cg; o <<= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
-            if (ch_ok && (lane & (p.stat_cg - 1)) == 0) {
-              const long long slot =
-                  (static_cast<long long>(img % p.t) * per_img + rem) * 8 + pc;
-              float *o = p.stat_part +
-                         ((static_cast<long long>(img / p.t) * p.stat_groups + ch / p.stat_cg) *
-                              p.stat_slots + slot) * 3;
-              o[0] = cnt;
-              o[1] = mean;
-              o[2] = m2;
-            }
-          }
-        }
-        if (failed) break;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        continue;
-      }
-      // Stream-K: this warp's rows of a tile split with the next CTA. The
-      // tail's raw sums are in that CTA's slot once its flag for this warp
-      // is up (set long before: the tail was its first work item).
-      const size_t sk_slot_f4 = static_cast<size_t>(MS) * BN * 32;  // float4 per slot
-      if (w.head) {
-        bool ok = true;
-        if (lane == 0) {
-          const int *f = p.sk_flag + (blockIdx.x + 1) * 4 + q;
-          const uint64_t t0 = global_timer_ns();
-          while (ld_acquire_gpu(f) == 0) {
-            if (*abort || global_timer_ns() - t0 > p.wait_ns) {
-              ok = false;
-              break;
-            }
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) {
-          if (lane == 0) raise_error(p, abort);
-          failed = true;
-          break;
-        }
-        __syncwarp();
-        __threadfence();
-      }
-      for (int sub = 0; sub < MS; ++sub) {
-      const int msub = sub * 128 + m;  // row of the (MS x 128)-row tile
-      bool valid;
-      long long row;          // NHWC / GEMM row index
-      long long nchw0 = 0;    // NCHW: offset of channel 0 for this pixel
-      long long cstride = 0;  // NCHW: distance between channels
-      int bc1 = 0, bc2 = 0, bc3 = 0, bc4 = 0;  // this warp's TMA box coordinates
-      if (MODE == 2) {
-        row = static_cast<long long>(mt) * kBM + msub;
-        valid = row < p.M;
-        bc1 = mt * kBM + q * 32;
-      } else {
-        const int per_img = p.tiles_x * p.tiles_y * (MODE == 1 ? 4 : 1);
-        const int img = mt / per_img;
-        int rem = mt % per_img;
-        const int par = MODE == 1 ? (rem & 3) : 0;
-        if (MODE == 1) rem >>= 2;
-        const int ty = rem / p.tiles_x, tx = rem % p.tiles_x;
-        int y, x;
-        if (kConv) {
-          y = ty * p.bh + msub / p.bw;
-          x = tx * p.bw + msub % p.bw;
-          valid = y < p.hout && x < p.wout;
-          bc1 = tx * p.bw + (sub * 128 + q * 32) % p.bw;
-          bc2 = ty * p.bh + (sub * 128 + q * 32) / p.bw;
-          bc3 = img;
-        } else {
-          // rows are low-res pixels of the tile; all share the parity par
-          const int yl = ty * p.bh + msub / p.bw, xl = tx * p.bw + msub % p.bw;
-          y = 2 * yl + (par >> 1);
-          x = 2 * xl + (par & 1);
-          valid = yl < p.hin && xl < p.win;
-          const int r0 = sub * 128 + q * 32;  // this warp's first row
-          bc1 = par & 1;                      // px
-          bc2 = tx * p.bw + r0 % p.bw;        // xl
-          bc3 = par >> 1;                     // py
-          bc4 = img * p.hin + ty * p.bh + r0 / p.bw;
-        }
-        row = (static_cast<long long>(img) * p.hout + y) * p.wout + x;
-        const long long hw = static_cast<long long>(p.hout) * p.wout;
-        const int n_idx = img / p.t, t_idx = img % p.t;
-        cstride = hw * p.t;
-        nchw0 = static_cast<long long>(n_idx) * p.cout * cstride + t_idx * hw +
-                static_cast<long long>(y) * p.wout + x;
-      }
-      const float rbias = (MODE == 2 && p.bias_per_row && p.bias && valid) ? p.bias[row] : 0.f;
-
-#pragma unroll 1
-      for (int c = 0; c < BN / C::CH; ++c) {
-        float v[C::CH];
-        const uint32_t taddr =
-            tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-            static_cast<uint32_t>(buf * C::ACC_COLS + sub * BN + c * C::CH);
-        if (C::CH == 32)
-          tmem_ld_32cols(taddr, v);
-        else
-          tmem_ld_16cols(taddr, v);
-        if (C::CH == 32 && (w.tail || w.head)) {
-          // slot layout [sub][chunk][j][128 rows] of float4: a warp's 32
-          // lanes touch 32 consecutive float4 per access
-          const size_t off = static_cast<size_t>((sub * (BN / 32) + c) * 8) * 128 + q * 32 + lane;
-          if (w.tail) {
-            float4 *dst = reinterpret_cast<float4 *>(p.sk_part) + blockIdx.x * sk_slot_f4 + off;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              __stcg(dst + j * 128, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-            continue;
-          }
-          const float4 *src =
-              reinterpret_cast<const float4 *>(p.sk_part) + (blockIdx.x + 1) * sk_slot_f4 + off;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 t = __ldcg(src + j * 128);
-            v[4 * j] += t.x;
-            v[4 * j + 1] += t.y;
-            v[4 * j + 2] += t.z;
-            v[4 * j + 3] += t.w;
-          }
-        }
-        const int col0 = n0 + c * C::CH;
-        if (col0 >= p.cout) continue;  // warp-uniform
-        const int ncols = min(C::CH, p.cout - col0);
-        // bias + scale (vector loads when the whole chunk is in range)
-        if (!p.bias_per_row && p.bias && ncols == C::CH) {
-#pragma unroll
-          for (int i = 0; i < C::CH; i += 4) {
-            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(p.bias + col0 + i));
-            v[i] = fmaf(v[i], p.alpha, b4.x);
-            v[i + 1] = fmaf(v[i + 1], p.alpha, b4.y);
-            v[i + 2] = fmaf(v[i + 2], p.alpha, b4.z);
-            v[i + 3] = fmaf(v[i + 3], p.alpha, b4.w);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < C::CH; ++i) {
-            float b = rbias;
-            if (!p.bias_per_row && p.bias && i < ncols) b = __ldg(p.bias + col0 + i);
-            v[i] = fmaf(v[i], p.alpha, b);
-          }
-        }
-        if (C::CH == 32 && p.epi_tma) {
-          // Stage the warp's 32 x 32 block in the 128-byte-swizzled layout the
-          // TMA store reads (row r, 16-byte chunk j at j ^ (r % 8)); rows and
-          // channels outside the tensor are clipped by the store.
-          float *sb = stg + sbuf * 1024;
-          if (lane == 0) bulk_wait_read<C::NSTG - 1>();  // the store that used sb last is done
-          __syncwarp();
-          if (p.has_res) {
-            if (lane == 0) {
-              mbar_arrive_expect_tx(&res_bar[q], 4096);
-              if (MODE == 2)
-                tma_load_2d(sb, &tmR, &res_bar[q], col0, bc1);
-              else if (kConv)
-                tma_load_4d(sb, &tmR, &res_bar[q], col0, bc1, bc2, bc3);
-              else
-                tma_load_5d(sb, &tmR, &res_bar[q], col0, bc1, bc2, bc3, bc4);
-            }
-            bool rok = mbar_wait(&res_bar[q], res_phase, abort, p.wait_ns);
-            rok = __all_sync(0xffffffffu, rok);
-            res_phase ^= 1u;
-            if (!rok) {
-              if (lane == 0) raise_error(p, abort);
-              failed = true;
-              break;
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float4 *slot = reinterpret_cast<float4 *>(sb + lane * 32 + ((j ^ (lane & 7)) * 4));
-            float4 val = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-            if (p.has_res) {
-              const float4 rv = *slot;
-              val.x += rv.x;
-              val.y += rv.y;
-              val.z += rv.z;
-              val.w += rv.w;
-            }
-            if (p.round_out) {
-              val.x = round_tf32(val.x);
-              val.y = round_tf32(val.y);
-              val.z = round_tf32(val.z);
-              val.w = round_tf32(val.w);
-            }
-            *slot = val;
-            v[4 * j] = val.x;  // keep the stored values for the statistics
-            v[4 * j + 1] = val.y;
-            v[4 * j + 2] = val.z;
-            v[4 * j + 3] = val.w;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if (MODE == 2)
-              tma_store_2d(&tmO, sb, col0, bc1);
-            else if (kConv)
-              tma_store_4d(&tmO, sb, col0, bc1, bc2, bc3);
-            else
-              tma_store_5d(&tmO, sb, col0, bc1, bc2, bc3, bc4);
-            bulk_commit();
-          }
-          if (C::NSTG == 2) sbuf ^= 1;
-          if (MODE != 2 && p.stat_part) {
-            const int per_img = p.tiles_x * p.tiles_y * (MODE == 1 ? 4 : 1);
-            const int img = mt / per_img;
-            const long long slot =
-                ((static_cast<long long>(img % p.t) * per_img + mt % per_img) * MS + sub) * 4 + q;
-            const int gbase = col0 / p.stat_cg;
-            float *out = p.stat_part +
-                         ((static_cast<long long>(img / p.t) * p.stat_groups + gbase) *
-                              p.stat_slots + slot) * 3;
-            const long long gs = static_cast<long long>(p.stat_slots) * 3;
-            const float nrows = static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid)));
-            switch (p.stat_cg) {
-              case 1: emit_group_stats<1>(v, valid, nrows, out, gs, lane); break;
-              case 2: emit_group_stats<2>(v, valid, nrows, out, gs, lane); break;
-              case 4: emit_group_stats<4>(v, valid, nrows, out, gs, lane); break;
-              case 8: emit_group_stats<8>(v, valid, nrows, out, gs, lane); break;
-              case 16: emit_group_stats<16>(v, valid, nrows, out, gs, lane); break;
-              default: emit_group_stats<32>(v, valid, nrows, out, gs, lane); break;
-            }
-          }
-          continue;
-        }
-        if (!valid) continue;
-        if (p.out_nchw) {
-          float *o = obase + nchw0 + static_cast<long long>(col0) * cstride;
-          const float *r = p.residual ? p.residual + nchw0 + static_cast<long long>(col0) * cstride
-                                      : nullptr;
-#pragma unroll
-          for (int i = 0; i < C::CH; ++i) {
-            if (i < ncols) {
-              float val = v[i];
-              if (r) val += r[i * cstride];
-              if (p.round_out) val = round_tf32(val);
-              o[i * cstride] = val;
-            }
-          }
-        } else {
-          float *o = obase + row * p.ldo + col0;
-          const float *r = p.residual ? p.residual + row * p.ldo + col0 : nullptr;
-          if (ncols == C::CH) {
-#pragma unroll
-            for (int i = 0; i < C::CH; i += 4) {
-              float4 val = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-              if (r) {
-                const float4 rv = *reinterpret_cast<const float4 *>(r + i);
-                val.x += rv.x;
-                val.y += rv.y;
-                val.z += rv.z;
-                val.w += rv.w;
-              }
-              if (p.round_out) {
-                val.x = round_tf32(val.x);
-                val.y = round_tf32(val.y);
-                val.z = round_tf32(val.z);
-                val.w = round_tf32(val.w);
-              }
-              *reinterpret_cast<float4 *>(o + i) = val;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < C::CH; ++i) {
-              if (i < ncols) {
-                float val = v[i];
-                if (r) val += r[i];
-                if (p.round_out) val = round_tf32(val);
-                o[i] = val;
-              }
-            }
-          }
-        }
-      }
-      if (failed) break;
-      }  // sub-tiles
-      if (w.tail && !failed) {  // this warp's raw sums are out: raise its flag
-        __threadfence();
-        __syncwarp();
-        // (The test hook withholds the flag so that the head's bounded wait
-        // runs out; nothing else differs.)
-        if (lane == 0 && !(p.inject & VAE_INJECT_WITHHOLD_STREAMK_FLAG))
-          st_release_gpu(p.sk_flag + blockIdx.x * 4 + q, 1);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && !failed) mbar_arrive(&acc_empty[buf]);
-    }
-    // Every TMA store of this warp must finish reading shared memory (and
-    // land) before the CTA exits.
-    if (lane == 0 && p.epi_tma) bulk_wait_all();
-  }
-
-  // ------------------------------------------------------------ teardown
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
-  }
-}
 
 // ---------------------------------------------------------------- host side
 int pow2_at_least(int v) {
   int r = 1;
   while (r < v) r <<= 1;
   return r;
-}
-
-template <int BN, int MODE, int MS>
-int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ts,
-                 const CUtensorMap &to, const CUtensorMap &tr, const KParams &kp,
-                 cudaStream_t stream) {
-  using C = Cfg<BN, MS, MODE>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(igemm_kernel<BN, MODE, MS>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(C::SMEM));
-  });
-  if (attr_err != cudaSuccess) return VAE_ECUDA;
-  const int grid = std::min(kp.total_tiles, num_sms());
-  // Stream-K CTAs wait on their neighbour's flags: a cooperative launch
-  // guarantees that the whole grid is resident.
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = stream;
-  cudaLaunchAttribute coop[1];
-  coop[0].id = cudaLaunchAttributeCooperative;
-  coop[0].val.cooperative = 1;
-  cfg.attrs = coop;
-  cfg.numAttrs = kp.sk ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, igemm_kernel<BN, MODE, MS>, ta, tb, ts, to, tr, kp) !=
-      cudaSuccess)
-    return VAE_ECUDA;
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
-  count_launches(1);
-  return VAE_OK;
 }
 
 template <int MODE>
@@ -1175,22 +104,74 @@ int pick_bn(int cout) {
   return 16;
 }
 
+// VAE_SPLIT=force forms every product in split-TF32 (tests of that path on
+// the single-op entry points).
+bool split_forced() {
+  static const bool v = [] {
+    const char *e = std::getenv("VAE_SPLIT");
+    return e && std::strcmp(e, "force") == 0;
+  }();
+  return v;
+}
+
+// VAE_PAIR=off keeps every conv on 1-SM tiles, VAE_PAIR=force pairs every conv
+// that can be paired (comparisons and tests); default: by the estimate below.
+int pair_setting() {
+  static const int v = [] {
+    const char *e = std::getenv("VAE_PAIR");
+    if (e && std::strcmp(e, "off") == 0) return 0;
+    if (e && std::strcmp(e, "force") == 0) return 2;
+    return 1;
+  }();
+  return v;
+}
+
+// Output tiles per image of a conv / upsample conv whose tiles hold `rows`
+// pixel rows (per output parity tile for the upsample conv).
+long long tiles_per_image(const IgemmDesc &d, int rows) {
+  const int bw = std::min(128, pow2_at_least(d.win));
+  const int bh = rows / bw;
+  long long t = static_cast<long long>(ceil_div(d.win, bw)) * ceil_div(d.hin, bh);
+  if (d.mode == AMode::Upsample) t *= 4;  // one tile per output parity
+  return t;
+}
+
+// Whether a conv runs as paired-CTA tiles (Cfg, PAIR): 256-channel tiles of
+// the pixel-major modes, outside the split-K regime, when the pairs'
+// 256-row tiles (about 0.8 of a 1-SM tile's time each: shared memory stops
+// being the bound) finish sooner than 1-SM 128-row tiles, counting the
+// stream-K balance the 1-SM path would get.
+bool use_pair(const IgemmDesc &d) {
+  const int setting = pair_setting();
+  if (setting == 0) return false;
+  if (!(d.mode == AMode::Conv || d.mode == AMode::Upsample) || pick_bn(d.cout) != 256) return false;
+  const int sms = num_sms();
+  if (sms < 2) return false;
+  if (setting == 2) return true;
+  const int t = d.t > 0 ? d.t : 1;
+  const long long n_tiles = ceil_div(d.cout, 256);
+  const long long tiles1 = static_cast<long long>(d.imgs) * tiles_per_image(d, kBM) * n_tiles;
+  const long long tiles2 = static_cast<long long>(d.imgs) * tiles_per_image(d, 2 * kBM) * n_tiles;
+  (void)t;
+  if (tiles1 * 5 < static_cast<long long>(sms) * 3) return false;  // split-K regime
+  const double r1 = static_cast<double>(tiles1) / sms;
+  const double est1 = r1 / std::ceil(r1) < 0.9 ? r1 : std::ceil(r1);  // stream-K or whole rounds
+  const double est2 = 0.8 * std::ceil(static_cast<double>(tiles2) / (sms / 2));
+  return est2 <= est1;
+}
+
+long long stat_slots_for(const IgemmDesc &d, bool pair) {
+  if (!(d.mode == AMode::Conv || d.mode == AMode::Upsample)) return 0;
+  const int ms = (pair || pick_bn(d.cout) == 128) ? 2 : 1;
+  return static_cast<long long>(d.t > 0 ? d.t : 1) * tiles_per_image(d, ms * kBM) * ms * 4;
+}
+
 }  // namespace
 
+// Upper bound over the tile geometries a launch may take (callers size the
+// partials buffer with it; the launch reports the stride it used).
 long long igemm_stat_slots(const IgemmDesc &d) {
-  const int bn = pick_bn(d.cout);
-  long long tiles;
-  int ms = 1;
-  if (d.mode == AMode::Conv || d.mode == AMode::Upsample) {
-    ms = bn == 128 ? 2 : 1;
-    const int bw = std::min(128, pow2_at_least(d.win));
-    const int bh = ms * kBM / bw;
-    tiles = static_cast<long long>(ceil_div(d.win, bw)) * ceil_div(d.hin, bh);
-    if (d.mode == AMode::Upsample) tiles *= 4;  // one tile per output parity
-  } else {
-    return 0;
-  }
-  return static_cast<long long>(d.t > 0 ? d.t : 1) * tiles * ms * 4;
+  return std::max(stat_slots_for(d, false), stat_slots_for(d, true));
 }
 
 int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
@@ -1201,6 +182,11 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
     return VAE_EINVAL;
 
   const int bn = pick_bn(d.cout);
+  // Paired-CTA tiles (256 pixel rows across a CTA pair; see Cfg).
+  // Split-TF32 products (split_setting: VAE_SPLIT=force makes every launch
+  // split, for tests); they run on per-step A and B stages only.
+  const bool split = d.precise || split_forced();
+  const bool pair = !split && use_pair(d);
   KParams kp{};
   kp.err = device_error_word();
   if (!kp.err) return VAE_ECUDA;
@@ -1248,7 +234,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
       kp.taps = d.k * d.k * d.kt;
       kp.hout = d.hin;
       kp.wout = d.win;
-      const int rows = (bn == 128 ? 2 : 1) * kBM;  // M sub-tiles (see Cfg)
+      const int rows = (bn == 128 || pair ? 2 : 1) * kBM;  // M sub-tiles (see Cfg)
       kp.bw = std::min(128, pow2_at_least(d.win));
       kp.bh = rows / kp.bw;
       kp.tiles_x = ceil_div(d.win, kp.bw);
@@ -1257,7 +243,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
       if (d.sc && (d.sc_c <= 0 || d.sc_c % 32)) return VAE_EINVAL;
       box[0] = 32;
       box[1] = kp.bw;
-      box[2] = kp.bh;
+      box[2] = pair ? kp.bh / 2 : kp.bh;  // a paired CTA loads its own 128 rows
       box[3] = 1;
     } else {
       // Nearest-2x upsample + 3x3 conv as four parity-specific 2x2 convs of
@@ -1266,14 +252,14 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
       kp.taps = 4;
       kp.hout = 2 * d.hin;
       kp.wout = 2 * d.win;
-      const int rows = (bn == 128 ? 2 : 1) * kBM;
+      const int rows = (bn == 128 || pair ? 2 : 1) * kBM;
       kp.bw = std::min(128, pow2_at_least(d.win));
       kp.bh = rows / kp.bw;
       kp.tiles_x = ceil_div(d.win, kp.bw);
       kp.tiles_y = ceil_div(d.hin, kp.bh);
       box[0] = 32;
       box[1] = kp.bw;
-      box[2] = kp.bh;
+      box[2] = pair ? kp.bh / 2 : kp.bh;
       box[3] = 1;
     }
     kp.m_tiles = d.imgs * kp.tiles_x * kp.tiles_y * (d.mode == AMode::Upsample ? 4 : 1);
@@ -1302,7 +288,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
     const uint64_t brows = static_cast<uint64_t>(d.cout) * (d.mode == AMode::Upsample ? 4 : 1);
     const uint64_t dims[2] = {static_cast<uint64_t>(bkdim), brows};
     const uint64_t str[1] = {static_cast<uint64_t>(d.ldb) * 4};
-    const uint32_t box[2] = {32, static_cast<uint32_t>(bn)};
+    const uint32_t box[2] = {32, static_cast<uint32_t>(pair ? bn / 2 : bn)};  // paired: a half
     VAE_TRY(encode_tiled(&tb, d.b, 2, dims, str, box));
   }
   const long long total = static_cast<long long>(kp.m_tiles) * kp.n_tiles;
@@ -1317,7 +303,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   const long long rows_total = d.mode == AMode::Gemm
                                    ? static_cast<long long>(d.M)
                                    : static_cast<long long>(d.imgs) * kp.hout * kp.wout;
-  if (d.split_ws && d.mode != AMode::Gemm && !d.out_nchw && d.cout % 4 == 0 &&
+  if (!pair && d.split_ws && d.mode != AMode::Gemm && !d.out_nchw && d.cout % 4 == 0 &&
       d.ldo == d.cout && !d.bias_per_row) {
     const int sms = num_sms();
     if (total * 5 < static_cast<long long>(sms) * 3) {
@@ -1386,7 +372,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // inside one 32-channel chunk; otherwise the caller computes them itself.
   if (d.stat_part) {
     const int cg = d.stat_groups > 0 ? d.cout / d.stat_groups : 0;
-    const long long slots = igemm_stat_slots(d);
+    const long long slots = stat_slots_for(d, pair);
     if (epi && d.mode != AMode::Gemm && d.cout % 32 == 0 && d.stat_groups > 0 &&
         d.cout % d.stat_groups == 0 && cg >= 1 && cg <= 32 && (cg & (cg - 1)) == 0 &&
         slots > 0 && slots < (1ll << 31)) {
@@ -1407,14 +393,15 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // to the per-tap path): 128-channel tiles (two 128-row sub-tiles), and
   // convs with an appended shortcut (with its tiles one or three to an A
   // buffer alike: 0.537 -> 0.607 ms on 512 -> 256 channels at 512^2).
-  const bool halo = d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 && kp.bw == 128 &&
+  const bool halo = !split && d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 && kp.bw == 128 &&
                     kp.splits == 1 && bn == 256 && kp.sc_chunks == 0 && buffered_a_enabled();
   // Channel-major tiles for 3x3 single-frame convs with 65-128 output
   // channels: the MMA runs M = 128 channels x N = 256 pixels (one wide
   // instruction where the pixel-major tile needs two 128 x 128 ones that both
   // read the weights), and per 32-channel chunk one band of bh + 2 rows per
   // kx serves the three ky taps. Needs the staged epilogue (it transposes).
-  const bool swap = !halo && d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 && bn == 128 &&
+  const bool swap = !split && !halo && d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 &&
+                    bn == 128 &&
                     kp.splits == 1 && epi && kp.bw >= 2 && buffered_a_enabled();
   if (swap) {
     const uint64_t dims[4] = {static_cast<uint64_t>(d.a_c), static_cast<uint64_t>(d.win),
@@ -1432,7 +419,8 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
     const uint64_t str[3] = {static_cast<uint64_t>(d.a_c) * 4,
                              static_cast<uint64_t>(d.win) * d.a_c * 4,
                              static_cast<uint64_t>(d.hin) * d.win * d.a_c * 4};
-    const uint32_t box[4] = {32, 130, static_cast<uint32_t>(kp.bh + 2), 1};
+    // (paired: each CTA stages its own row with its one-pixel border)
+    const uint32_t box[4] = {32, 130, static_cast<uint32_t>((pair ? kp.bh / 2 : kp.bh) + 2), 1};
     VAE_TRY(encode_tiled(&ta, d.a, 4, dims, str, box));
   }
 
@@ -1442,7 +430,8 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // share a large A operand through L2 only while they run side by side,
   // which the stream-K ranges undo.
   kp.sk = 0;
-  if (d.mode == AMode::Conv && !swap && kp.splits == 1 && d.split_ws && bn >= 32) {
+  if (!pair && !split && d.mode == AMode::Conv && !swap && kp.splits == 1 && d.split_ws &&
+      bn >= 32) {
     const int sms = num_sms();
     const long long tiles = total;
     const int units = halo ? kp.cin_chunks : kp.k_stages;
@@ -1468,13 +457,22 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   }
 
   int rc;
-  switch (d.mode) {
+  if (split) {
+    rc = launch_split(static_cast<int>(d.mode), bn, ta, tb, ts, to, tr, kp, stream);
+  } else switch (d.mode) {
     case AMode::Conv:
-      rc = halo   ? launch_typed<256, 3, 1>(ta, tb, ts, to, tr, kp, stream)
-           : swap ? launch_typed<128, 4, 2>(ta, tb, ts, to, tr, kp, stream)
-                  : launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream);
+      if (pair)
+        rc = halo ? launch_typed<256, 3, 1, true>(ta, tb, ts, to, tr, kp, stream)
+                  : launch_typed<256, 0, 1, true>(ta, tb, ts, to, tr, kp, stream);
+      else
+        rc = halo   ? launch_typed<256, 3, 1>(ta, tb, ts, to, tr, kp, stream)
+             : swap ? launch_typed<128, 4, 2>(ta, tb, ts, to, tr, kp, stream)
+                    : launch_mode<0>(bn, ta, tb, ts, to, tr, kp, stream);
       break;
-    case AMode::Upsample: rc = launch_mode<1>(bn, ta, tb, ts, to, tr, kp, stream); break;
+    case AMode::Upsample:
+      rc = pair ? launch_typed<256, 1, 1, true>(ta, tb, ts, to, tr, kp, stream)
+                : launch_mode<1>(bn, ta, tb, ts, to, tr, kp, stream);
+      break;
     default: rc = launch_mode<2>(bn, ta, tb, ts, to, tr, kp, stream); break;
   }
   if (rc != VAE_OK || kp.splits == 1) return rc;

@@ -9,11 +9,12 @@ namespace vae {
 
 namespace {
 
-// dst[o][tap * cin_pad + c] = tf32(w[o][c][tap]); shortcut columns follow at
-// taps * cin_pad + c; zero in every padding slot and padding row.
+// dst[o][tap * cin_pad + c] = tf32(w[o][c][tap]) (unrounded when !round);
+// shortcut columns follow at taps * cin_pad + c; zero in every padding slot
+// and padding row.
 __global__ void pack_kernel(const float *__restrict__ w, int cout, int cin, int taps,
                             const float *__restrict__ wsc, int sc_cin, float *__restrict__ dst,
-                            int rows, int ldb, int cin_pad) {
+                            int rows, int ldb, int cin_pad, int round) {
   const long long total = static_cast<long long>(rows) * ldb;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -30,7 +31,7 @@ __global__ void pack_kernel(const float *__restrict__ w, int cout, int cin, int 
         if (c < sc_cin) v = wsc[static_cast<long long>(o) * sc_cin + c];
       }
     }
-    dst[i] = round_tf32(v);
+    dst[i] = round ? round_tf32(v) : v;
   }
 }
 
@@ -38,9 +39,10 @@ __global__ void pack_kernel(const float *__restrict__ w, int cout, int cin, int 
 // taps ky that land on low-res row offset py - 1 + a (a = 0, 1) are those with
 // floor((py + ky - 1) / 2) = py - 1 + a, and likewise for kx. Their weights
 // act on the same input pixel, so they are summed into a 2x2 kernel:
-// dst[par][o][(a * 2 + b) * cin_pad + c], par = py * 2 + px, TF32-rounded.
+// dst[par][o][(a * 2 + b) * cin_pad + c], par = py * 2 + px, TF32-rounded
+// (unless !round).
 __global__ void pack_upsample_kernel(const float *__restrict__ w, int cout, int cin,
-                                     float *__restrict__ dst, int ldb, int cin_pad) {
+                                     float *__restrict__ dst, int ldb, int cin_pad, int round) {
   const long long total = 4ll * cout * ldb;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -58,7 +60,7 @@ __global__ void pack_upsample_kernel(const float *__restrict__ w, int cout, int 
           if (((px + kx + 1) >> 1) - px == b) v += wc[ky * 3 + kx];
       }
     }
-    dst[i] = round_tf32(v);
+    dst[i] = round ? round_tf32(v) : v;
   }
 }
 
@@ -114,22 +116,24 @@ int grid_for(long long n, int threads) {
 }  // namespace
 
 int pack_conv_weights(const float *w, int cout, int cin, int taps, const float *w_sc,
-                      int sc_cin, float *dst, int cout_rows, int ldb, cudaStream_t s) {
+                      int sc_cin, float *dst, int cout_rows, int ldb, cudaStream_t s,
+                      int round) {
   if (!w || !dst || cout <= 0 || cin <= 0 || cout_rows < cout) return VAE_EINVAL;
   if (ldb != packed_ldb(cin, taps, w_sc ? sc_cin : 0)) return VAE_EINVAL;
   const long long total = static_cast<long long>(cout_rows) * ldb;
   pack_kernel<<<grid_for(total, 256), 256, 0, s>>>(w, cout, cin, taps, w_sc, w_sc ? sc_cin : 0,
-                                                   dst, cout_rows, ldb, round_up32(cin));
+                                                   dst, cout_rows, ldb, round_up32(cin), round);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(1);
   return VAE_OK;
 }
 
-int pack_upsample_weights(const float *w, int cout, int cin, float *dst, cudaStream_t s) {
+int pack_upsample_weights(const float *w, int cout, int cin, float *dst, cudaStream_t s,
+                          int round) {
   if (!w || !dst || cout <= 0 || cin <= 0) return VAE_EINVAL;
   const int ldb = upsample_ldb(cin);
   pack_upsample_kernel<<<grid_for(4ll * cout * ldb, 256), 256, 0, s>>>(w, cout, cin, dst, ldb,
-                                                                      round_up32(cin));
+                                                                      round_up32(cin), round);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(1);
   return VAE_OK;

@@ -152,10 +152,11 @@ bool use_fused_attention(int c) {
 int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
                    const float *gn_w, const float *gn_b, const float *wqkv, const float *bqkv,
                    const float *wo, const float *bo, float *y, const AttnScratch &sc,
-                   cudaStream_t s) {
+                   cudaStream_t s, bool exact) {
   const int lp = round_up32(L);
+  const int rnd = exact ? 0 : 1;  // MMA operands are stored TF32-rounded unless split
   // t = GroupNorm(x), no SiLU; TF32-rounded because it is an MMA operand.
-  VAE_TRY(groupnorm_silu(x, n, c, L, 1, groups, eps, gn_w, gn_b, 0, 1, sc.t, sc.gn, s));
+  VAE_TRY(groupnorm_silu(x, n, c, L, 1, groups, eps, gn_w, gn_b, 0, rnd, sc.t, sc.gn, s));
   // [q | k | v] = t [Wq; Wk; Wv]^T + [bq; bk; bv], one GEMM for all images.
   {
     IgemmDesc d;
@@ -170,11 +171,12 @@ int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
     d.out = sc.qkv;
     d.ldo = 3 * c;
     d.bias = bqkv;
-    d.round_out = 1;
+    d.round_out = rnd;
+    d.precise = exact;
     VAE_TRY(igemm_launch(d, s));
   }
   if (lp != L) VAE_CUDA_TRY(cudaMemsetAsync(sc.vt, 0, static_cast<size_t>(c) * lp * 4, s));
-  const bool fused = use_fused_attention(c);
+  const bool fused = !exact && use_fused_attention(c);
   for (int b = 0; b < n; ++b) {
     const float *qkv_b = sc.qkv + static_cast<size_t>(b) * L * 3 * c;
     // V^T [c][L] (row stride lp): the K-major B operand of P.V.
@@ -198,9 +200,10 @@ int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
       d.cout = L;
       d.out = sc.s;
       d.ldo = lp;
+      d.precise = exact;
       VAE_TRY(igemm_launch(d, s));
     }
-    VAE_TRY(softmax_rows(sc.s, L, L, lp, 1.0f / std::sqrt(static_cast<float>(c)), s));
+    VAE_TRY(softmax_rows(sc.s, L, L, lp, 1.0f / std::sqrt(static_cast<float>(c)), s, rnd));
     // o = P V
     {
       IgemmDesc d;
@@ -214,7 +217,8 @@ int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
       d.cout = c;
       d.out = sc.o + static_cast<size_t>(b) * L * c;
       d.ldo = c;
-      d.round_out = 1;
+      d.round_out = rnd;
+      d.precise = exact;
       VAE_TRY(igemm_launch(d, s));
     }
   }
@@ -232,6 +236,7 @@ int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
   d.ldo = c;
   d.bias = bo;
   d.residual = x;
+  d.precise = exact;
   return igemm_launch(d, s);
 }
 

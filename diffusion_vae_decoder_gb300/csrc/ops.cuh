@@ -18,9 +18,11 @@ struct AttnScratch {
   void *gn;
 };
 size_t attn_ws_bytes(int n, int c, int L, int layout);
+// exact: split-TF32 products on FP32 operands (weights packed unrounded),
+// through the score-matrix path.
 int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
                    const float *gn_w, const float *gn_b, const float *wqkv, const float *bqkv,
                    const float *wo, const float *bo, float *y, const AttnScratch &sc,
-                   cudaStream_t s);
+                   cudaStream_t s, bool exact = false);
 
 }  // namespace vae

@@ -3,7 +3,8 @@
 // cortiq-engine "Module vae", struct VaeAttnRef: softmax(q k^T / sqrt(c));
 // the row softmax subtracts the row maximum, exponentiates and divides by the
 // sum (vae3d.rs fn softmax_inplace). Rows are written back in place, rounded
-// to TF32 because they are the A operand of the P.V tensor-core product; the
+// to TF32 because they are the A operand of the P.V tensor-core product (or
+// left in FP32 for the split-TF32 product, which splits them itself); the
 // padding columns [L, ld) are set to zero so that the padded reduction of P.V
 // adds exact zeros.
 #include "common.cuh"
@@ -38,7 +39,8 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float *sh) {
 // of per-thread (max, sum of exp) pairs replaces separate max and sum passes:
 // each thread keeps exp(v - its own max) and rescales by exp(own max - row
 // max) at the end.
-__global__ void __launch_bounds__(kThreads) softmax_reg(float *s, int L, int ld, float scale) {
+__global__ void __launch_bounds__(kThreads) softmax_reg(float *s, int L, int ld, float scale,
+                                                        int round) {
   __shared__ float shm[32], shs[32];
   constexpr int kVec = kPerThread / 4;
   float4 *row = reinterpret_cast<float4 *>(s + static_cast<long long>(blockIdx.x) * ld);
@@ -94,17 +96,24 @@ __global__ void __launch_bounds__(kThreads) softmax_reg(float *s, int L, int ld,
     const int q = threadIdx.x + i * kThreads;
     if (q < ld4) {
       float4 o;  // padding columns: v = 0 there, so they store exact zeros
-      o.x = round_tf32(v[4 * i] * f);
-      o.y = round_tf32(v[4 * i + 1] * f);
-      o.z = round_tf32(v[4 * i + 2] * f);
-      o.w = round_tf32(v[4 * i + 3] * f);
+      o.x = v[4 * i] * f;
+      o.y = v[4 * i + 1] * f;
+      o.z = v[4 * i + 2] * f;
+      o.w = v[4 * i + 3] * f;
+      if (round) {
+        o.x = round_tf32(o.x);
+        o.y = round_tf32(o.y);
+        o.z = round_tf32(o.z);
+        o.w = round_tf32(o.w);
+      }
       row[q] = o;
     }
   }
 }
 
 // Any row length: three sweeps over global memory.
-__global__ void __launch_bounds__(kThreads) softmax_long(float *s, int L, int ld, float scale) {
+__global__ void __launch_bounds__(kThreads) softmax_long(float *s, int L, int ld, float scale,
+                                                         int round) {
   __shared__ float sh[32];
   float *row = s + static_cast<long long>(blockIdx.x) * ld;
   float mx = -INFINITY;
@@ -114,21 +123,24 @@ __global__ void __launch_bounds__(kThreads) softmax_long(float *s, int L, int ld
   for (int j = threadIdx.x; j < L; j += kThreads) sum += expf(row[j] * scale - mx);
   sum = block_reduce(sum, false, sh);
   const float inv = 1.0f / sum;
-  for (int j = threadIdx.x; j < L; j += kThreads)
-    row[j] = round_tf32(expf(row[j] * scale - mx) * inv);
+  for (int j = threadIdx.x; j < L; j += kThreads) {
+    const float v = expf(row[j] * scale - mx) * inv;
+    row[j] = round ? round_tf32(v) : v;
+  }
   for (int j = L + threadIdx.x; j < ld; j += kThreads) row[j] = 0.f;
 }
 
 }  // namespace
 
-int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st) {
+int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st,
+                 int round) {
   if (!s || rows <= 0 || L <= 0 || ld < L) return VAE_EINVAL;
   if (rows > 0x7fffffffll) return VAE_EUNSUPPORTED;
   if (ld <= kThreads * kPerThread && ld % 4 == 0 &&
       (reinterpret_cast<uintptr_t>(s) & 15) == 0)
-    softmax_reg<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale);
+    softmax_reg<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale, round);
   else
-    softmax_long<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale);
+    softmax_long<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale, round);
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(1);
   return VAE_OK;

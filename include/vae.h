@@ -21,7 +21,8 @@
  *     the attention products run on the tcgen05 tensor cores with TF32
  *     operands and FP32 accumulation; weights are rounded to TF32
  *     (round-to-nearest) when packed; normalisation, softmax and epilogues are
- *     FP32.
+ *     FP32. The chain can instead form every product in split-TF32 (see
+ *     vae_precision).
  *   - Outputs may not alias inputs, except y == residual (vae_conv2d,
  *     vae_conv3d_causal) and y == x (vae_groupnorm_silu).
  *   - Device-side waits are bounded: a kernel that gives up records
@@ -224,6 +225,21 @@ typedef struct {
   vae_conv_ref upsample_conv; /* weight NULL: no upsample */
 } vae_up_ref;
 
+/* Arithmetic of the chain's tensor-core products.
+ *   TF32        TF32 operands (rounded to nearest), FP32 accumulation.
+ *   SPLIT_TF32  every operand split into two TF32 parts, hi + lo, and each
+ *               product formed as hi*hi + lo*hi + hi*lo (three MMAs), FP32
+ *               accumulation: about FP32 accuracy at three times the MMA work.
+ *   AUTO        SPLIT_TF32 for a decode whose conv work is at most
+ *               VAE_SPLIT_AUTO_GFLOP (small, low-channel decoders, where the
+ *               extra products cost next to nothing), TF32 otherwise. */
+typedef enum {
+  VAE_PRECISION_AUTO = 0,
+  VAE_PRECISION_TF32 = 1,
+  VAE_PRECISION_SPLIT_TF32 = 2
+} vae_precision;
+#define VAE_SPLIT_AUTO_GFLOP 20.0
+
 typedef struct {
   int latent_channels;
   float scaling_factor, shift_factor;
@@ -237,6 +253,7 @@ typedef struct {
   const vae_up_ref *ups;
   vae_norm_ref norm_out;
   vae_conv_ref conv_out;
+  int precision; /* vae_precision */
 } vae_chain_args;
 
 /* Packs every weight once (TF32-rounded, GEMM layout) into device memory owned

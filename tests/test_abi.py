@@ -61,6 +61,7 @@ int main(void) {
   O(vae_up_ref, resnets) O(vae_up_ref, upsample_conv)
   O(vae_chain_args, eps) O(vae_chain_args, conv_in) O(vae_chain_args, mid_attn)
   O(vae_chain_args, n_ups) O(vae_chain_args, ups) O(vae_chain_args, conv_out)
+  O(vae_chain_args, precision)
   return 0;
 }
 """

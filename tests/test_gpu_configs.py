@@ -125,4 +125,4 @@ def test_decoder_full_size(workload):
     m = metrics(got, ref)
     print(workload, m)
     assert m["cos"] >= COS_MIN and m["max_abs"] <= RGB_MAXABS, (workload, m)
-    assert m["rel_l2"] <= 2 * REL_L2_MAX, (workload, m)
+    assert m["rel_l2"] <= REL_L2_MAX, (workload, m)

@@ -321,7 +321,8 @@ def test_conv2d_per_tap_staging_forced():
 # ------------------------------------------------------------------ upsample + conv
 @pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("n,cin,cout,h,w", [(1, 32, 32, 4, 4), (2, 64, 80, 9, 37),
-                                            (1, 32, 16, 1, 1), (1, 128, 128, 16, 64)])
+                                            (1, 32, 16, 1, 1), (1, 128, 128, 16, 64),
+                                            (2, 32, 256, 3, 70), (1, 64, 160, 5, 37)])
 def test_upsample_conv_exact_integer(layout, n, cin, cout, h, w):
     x = S.integer_tensor((n, cin, h, w), 13, -3, 3)
     wt = S.integer_tensor((cout, cin, 3, 3), 14, -2, 2)
