@@ -134,7 +134,7 @@ template <int BN, int MS, int MODE = 0, bool PAIR = false, bool SPLIT = false>
 struct Cfg {
   static constexpr bool HALO = MODE == 3;
   static constexpr bool SWAP = MODE == 4;
-  static_assert(!PAIR || (BN == 256 && MS == 1 && (MODE == 0 || MODE == 1 || MODE == 3)),
+  static_assert(!PAIR || (MS == 1 && BN == 256 && (MODE == 0 || MODE == 1 || MODE == 3)),
                 "paired tiles: 256 channels, pixel-major conv modes");
   static_assert(!SPLIT || (!PAIR && MODE <= 2), "split products: per-step A and B stages");
   static constexpr int THREADS = SPLIT ? kThreads + 128 : kThreads;
@@ -152,18 +152,21 @@ struct Cfg {
   static constexpr uint32_t B_BYTES = B_LOAD * (SPLIT ? 2 : 1);
   static constexpr uint32_t STAGE_TX = A_LOAD + B_LOAD;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  // Epilogue staging: 4 warps x NSTG buffers x (32 rows x 128 bytes).
+  // Epilogue staging: 4 warps x NSTG buffers x (32 rows x 128 bytes). Two
+  // buffers let a block's store drain (and the next block's residual land)
+  // while the warp works on the current one; the halo modes keep one so that
+  // their shared memory holds more weight stages (measured faster on GB300).
   static constexpr int NSTG = HALO ? 1 : 2;
   static constexpr uint32_t STAGING = 4 * NSTG * 4096;
   static constexpr int FIT =
       (232448 - 1024 - STAGING - 1024 - HALO_BUFS * HALO_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
   static constexpr uint32_t ACC_COLS = BN * MS;  // TMEM columns of one accumulator set
-  static constexpr int ROWS = PAIR ? 2 : MS;      // 128-row sub-tiles of a (pair) tile
+  static constexpr int ROWS = PAIR ? 2 : MS;  // 128-row sub-tiles of a (pair) tile
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
   static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
   static constexpr size_t SMEM = 1024 + HALO_BUFS * HALO_BYTES + STAGES * STAGE_BYTES + STAGING +
-                                 ((SPLIT ? 3 : 2) * STAGES + 13) * sizeof(uint64_t) + 16;
+                                 ((SPLIT ? 3 : 2) * STAGES + 17) * sizeof(uint64_t) + 16;
   static_assert(STAGES >= 2, "at least double-buffered stages");
   static_assert(!(HALO || SWAP) || STAGES >= 3, "buffered-A modes need a weight ring");
   static_assert(!SWAP || (BN == 128 && MS == 2), "MODE 4 tiles are 128 channels x 256 pixels");
@@ -278,8 +281,8 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
   uint64_t *acc_full = empty + STAGES;
   uint64_t *acc_empty = acc_full + 2;
   uint64_t *drain = acc_empty + 2;  // used only after an abort
-  uint64_t *res_bar = drain + 1;    // one per epilogue warp: residual box landed
-  uint64_t *a_full = res_bar + 4;   // MODES 3, 4: A buffer landed / free
+  uint64_t *res_bar = drain + 1;    // per epilogue warp and staging buffer: residual landed
+  uint64_t *a_full = res_bar + 8;   // MODES 3, 4: A buffer landed / free
   uint64_t *a_empty = a_full + 2;
   uint64_t *xfull = a_empty + 2;    // SPLIT: stage split into hi / lo parts
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfull + (SPLIT ? STAGES : 0));
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
       mbar_init(&acc_empty[b], PAIR ? 8 : 4);  // every epilogue warp of the pair
     }
     mbar_init(drain, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&res_bar[q], 1);
+    for (int q = 0; q < 8; ++q) mbar_init(&res_bar[q], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&a_full[b], 1);
       mbar_init(&a_empty[b], 1);
@@ -740,7 +743,8 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
     const int m = q * 32 + lane;
     float *stg = staging + q * C::NSTG * 1024;  // this warp's 4 KB staging buffer(s)
     int sbuf = 0;
-    uint32_t res_phase = 0;
+    uint32_t res_phase = 0;    // bit b: phase of this warp's residual barrier b
+    uint32_t res_pending = 0;  // bit b: a residual load into buffer b not yet waited for
     bool failed = false;
     int local = 0;
     // PAIR: this CTA's accumulator rows are sub-tile `rank` of the pair's
@@ -903,7 +907,8 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
         __threadfence();
       }
       for (int sub = 0; sub < MS; ++sub) {
-      const int sg = PAIR ? static_cast<int>(rank) : sub;  // 128-row sub-tile of the tile
+      // 128-row sub-tile of the (pair) tile this warp's rows belong to
+      const int sg = PAIR ? static_cast<int>(rank) : sub;
       const int msub = sg * 128 + m;  // row of the (ROWS x 128)-row tile
       bool valid;
       long long row;          // NHWC / GEMM row index
@@ -1008,26 +1013,49 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
           // TMA store reads (row r, 16-byte chunk j at j ^ (r % 8)); rows and
           // channels outside the tensor are clipped by the store.
           float *sb = stg + sbuf * 1024;
-          if (lane == 0) bulk_wait_read<C::NSTG - 1>();  // the store that used sb last is done
-          __syncwarp();
+          // The residual block of channels from c0 lands in staging buffer b
+          // (its 4 KB box, clipped rows and channels read as zero).
+          auto load_res = [&](int b, int c0) {
+            uint64_t *bar = &res_bar[q * 2 + b];
+            mbar_arrive_expect_tx(bar, 4096);
+            float *dst = stg + b * 1024;
+            if (MODE == 2)
+              tma_load_2d(dst, &tmR, bar, c0, bc1);
+            else if (kConv)
+              tma_load_4d(dst, &tmR, bar, c0, bc1, bc2, bc3);
+            else
+              tma_load_5d(dst, &tmR, bar, c0, bc1, bc2, bc3, bc4);
+          };
           if (p.has_res) {
+            // With two buffers the next block's residual is requested before
+            // this one is processed, so its latency overlaps this block.
             if (lane == 0) {
-              mbar_arrive_expect_tx(&res_bar[q], 4096);
-              if (MODE == 2)
-                tma_load_2d(sb, &tmR, &res_bar[q], col0, bc1);
-              else if (kConv)
-                tma_load_4d(sb, &tmR, &res_bar[q], col0, bc1, bc2, bc3);
-              else
-                tma_load_5d(sb, &tmR, &res_bar[q], col0, bc1, bc2, bc3, bc4);
+              if (!(res_pending & (1u << sbuf))) {  // first block of the row range
+                bulk_wait_read<0>();
+                load_res(sbuf, col0);
+              }
+              if (C::NSTG == 2 && c + 1 < BN / C::CH && col0 + C::CH < p.cout) {
+                bulk_wait_read<0>();  // the store from the other buffer has read it
+                load_res(sbuf ^ 1, col0 + C::CH);
+              }
             }
-            bool rok = mbar_wait(&res_bar[q], res_phase, abort, p.wait_ns);
+            res_pending |= 1u << sbuf;
+            if (C::NSTG == 2 && c + 1 < BN / C::CH && col0 + C::CH < p.cout)
+              res_pending |= 1u << (sbuf ^ 1);
+            __syncwarp();
+            bool rok = mbar_wait(&res_bar[q * 2 + sbuf], (res_phase >> sbuf) & 1u, abort,
+                                 p.wait_ns);
             rok = __all_sync(0xffffffffu, rok);
-            res_phase ^= 1u;
+            res_phase ^= 1u << sbuf;
+            res_pending &= ~(1u << sbuf);
             if (!rok) {
               if (lane == 0) raise_error(p, abort);
               failed = true;
               break;
             }
+          } else {
+            if (lane == 0) bulk_wait_read<C::NSTG - 1>();  // the store that used sb last is done
+            __syncwarp();
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -1156,8 +1184,12 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
       }
     }
     // Every TMA store of this warp must finish reading shared memory (and
-    // land) before the CTA exits.
+    // land), and a residual load still in flight after an abort must land,
+    // before the CTA exits.
     if (lane == 0 && p.epi_tma) bulk_wait_all();
+    for (int b = 0; b < 2; ++b)
+      if (lane == 0 && (res_pending & (1u << b)))
+        mbar_wait_drain(&res_bar[q * 2 + b], (res_phase >> b) & 1u, p.wait_ns);
   } else {
     // ------------------------------------------------------------ split (SPLIT)
     // Each landed stage, in place: v -> hi = tf32(v), and lo = tf32(v - hi)
