@@ -122,6 +122,8 @@ _SIGS = {
                                     ctypes.POINTER(_I)]),
     "vae_decode_chain_traced": (_I, [_P, _P, _I, _I, _I, _P, _P, _SZ, ctypes.POINTER(_P), _I,
                                      _P]),
+    "vae_chain_tiled_workspace_size": (_SZ, [_P, _I, _I, _I, _I, _I, _I]),
+    "vae_decode_chain_tiled": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "vae_measure_tf32_mma": (_I, [_I, ctypes.POINTER(ctypes.c_double),
                                   ctypes.POINTER(ctypes.c_float), _P]),
     "vae_debug_set_wait_limit": (_I, [ctypes.c_ulonglong]),
@@ -457,6 +459,29 @@ class VaeChain:
             ws = _ws(self.workspace_size(n, h, w), z.device)
         _check("vae_decode_chain", lib.vae_decode_chain(
             self.handle, _ptr(z), n, h, w, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+        return out
+
+    def decode_tiled(self, z, tile=512, min_overlap=64, tiles_per_batch=0, out=None, ws=None,
+                     stream=None):
+        """vae_decode_chain_tiled: decode in overlapping tiles of ``tile``
+        output pixels, cross-faded over their overlaps."""
+        lib = load_library()
+        _need(z, "z")
+        n, c, h, w = z.shape
+        if out is None:
+            import torch
+            f = self.up_factor
+            out = torch.empty((n, self.out_channels, f * h, f * w), dtype=torch.float32,
+                              device=z.device)
+        if ws is None:
+            nb = lib.vae_chain_tiled_workspace_size(self.handle, n, h, w, tile, min_overlap,
+                                                    tiles_per_batch)
+            if nb == 0:
+                raise VaeError("vae_chain_tiled_workspace_size", -1)
+            ws = _ws(nb, z.device)
+        _check("vae_decode_chain_tiled", lib.vae_decode_chain_tiled(
+            self.handle, _ptr(z), n, h, w, tile, min_overlap, tiles_per_batch, _ptr(out),
+            _ptr(ws), ws.numel(), _stream(stream)))
         return out
 
     def trace_points(self, n, h, w):

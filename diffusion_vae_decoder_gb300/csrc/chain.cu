@@ -735,10 +735,92 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
   return VAE_OK;
 }
 
+// ---------------------------------------------------------------- tiled decode
+int up_factor(const Chain &ch) {
+  int r = 1;
+  for (const UpW &u : ch.ups)
+    if (u.has_up) r *= 2;
+  return r;
+}
+
+// Tile schedule and batch of a tiled decode; tile / min_overlap in output
+// pixels, multiples of the decoder's latent-to-pixel factor.
+int tiled_plan(const Chain &ch, int n, int h, int w, int tile, int min_overlap, int per_batch,
+               TileSchedule *ts, int *batch) {
+  if (n <= 0 || h <= 0 || w <= 0 || tile <= 0 || min_overlap < 0 || min_overlap >= tile)
+    return VAE_EINVAL;
+  const int r = up_factor(ch);
+  if (tile % r || min_overlap % r) return VAE_EINVAL;
+  VAE_TRY(make_tile_schedule(h * r, w * r, r, tile, min_overlap, ts));
+  const long long total = static_cast<long long>(n) * ts->ny * ts->nx;
+  if (total > 0x7fffffffll) return VAE_EUNSUPPORTED;
+  *batch = static_cast<int>(per_batch <= 0 ? total : std::min<long long>(per_batch, total));
+  return VAE_OK;
+}
+
+struct TiledWs {
+  float *lat = nullptr, *tiles = nullptr;
+  void *inner = nullptr;
+  size_t inner_bytes = 0;
+};
+
+TiledWs carve_tiled(Carver &cv, const Chain &ch, int n, const TileSchedule &ts, int batch) {
+  TiledWs t;
+  t.lat = cv.take<float>(static_cast<size_t>(batch) * ch.latent_c * ts.tzh * ts.tzw);
+  t.tiles = cv.take<float>(static_cast<size_t>(n) * ts.ny * ts.nx * ch.conv_out.cout * ts.th *
+                           ts.tw);
+  const Plan p = make_plan(ch, batch, ts.tzh, ts.tzw);
+  Carver inner(nullptr, 0);
+  carve_decode(inner, ch, p, batch, ts.tzh, ts.tzw);
+  t.inner_bytes = inner.used;
+  t.inner = cv.take<char>(t.inner_bytes);
+  return t;
+}
+
 }  // namespace
 }  // namespace vae
 
 extern "C" {
+
+size_t vae_chain_tiled_workspace_size(const void *handle, int n, int h, int w, int tile,
+                                      int min_overlap, int tiles_per_batch) {
+  if (!is_live(handle)) return 0;
+  const Chain &ch = *static_cast<const Chain *>(handle);
+  TileSchedule ts;
+  int batch = 0;
+  if (tiled_plan(ch, n, h, w, tile, min_overlap, tiles_per_batch, &ts, &batch) != VAE_OK) return 0;
+  Carver cv(nullptr, 0);
+  carve_tiled(cv, ch, n, ts, batch);
+  return cv.used;
+}
+
+int vae_decode_chain_tiled(void *handle, const float *z, int n, int h, int w, int tile,
+                           int min_overlap, int tiles_per_batch, float *rgb, void *ws,
+                           size_t ws_bytes, vae_stream_t stream) {
+  if (!is_live(handle)) return VAE_ENOTPREPARED;
+  if (!z || !rgb || !ws) return VAE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(z) | reinterpret_cast<uintptr_t>(rgb)) & 15) return VAE_EINVAL;
+  Chain *ch = static_cast<Chain *>(handle);
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  TileSchedule ts;
+  int batch = 0;
+  VAE_TRY(tiled_plan(*ch, n, h, w, tile, min_overlap, tiles_per_batch, &ts, &batch));
+  Carver cv(ws, ws_bytes);
+  const TiledWs t = carve_tiled(cv, *ch, n, ts, batch);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  const int co = ch->conv_out.cout;
+  const long long total = static_cast<long long>(n) * ts.ny * ts.nx;
+  const size_t tile_floats = static_cast<size_t>(co) * ts.th * ts.tw;
+  ch->tr = nullptr;
+  for (long long t0 = 0; t0 < total; t0 += batch) {
+    const int cnt = static_cast<int>(std::min<long long>(batch, total - t0));
+    VAE_TRY(gather_latent_tiles(z, ch->latent_c, h, w, ts, t0, cnt, t.lat, s));
+    VAE_TRY(decode_impl(ch, t.lat, cnt, ts.tzh, ts.tzw, t.tiles + t0 * tile_floats, t.inner,
+                        t.inner_bytes, s));
+  }
+  const int r = up_factor(*ch);
+  return blend_decoded_tiles(t.tiles, n, co, ts, h * r, w * r, rgb, s);
+}
 
 int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *rgb, void *ws,
                      size_t ws_bytes, vae_stream_t stream) {

@@ -271,6 +271,36 @@ VAE_API size_t vae_chain_workspace_size(const void *handle, int n, int h, int w)
  * has a fixed order: the same inputs give the same bits. */
 VAE_API int vae_decode_chain(void *handle, const float *z, int n, int h, int w, float *rgb, void *ws,
                      size_t ws_bytes, vae_stream_t stream);
+/* ------------------------------------------------------------------------
+ * Tiled decode, for outputs the whole-image decode cannot hold (its
+ * activations and attention grow with the image; a latent above 65536
+ * tokens is refused by vae_decode_chain). The tile schedule and the
+ * cross-fade follow cortiq-engine 0.8.78's vae3d.rs (fn split_tiles,
+ * fn blend, fn crop, VideoVae::decode_clip), written there for another
+ * decoder:
+ *   - along each axis of the output plane (8h x 8w pixels), the fewest
+ *     tiles of `tile` pixels whose overlaps are at least `min_overlap`,
+ *     the slack added to the overlaps one latent cell (8 pixels) at a time,
+ *     round robin; a single tile when the axis fits in one;
+ *   - every tile's latent crop is decoded on its own (GroupNorm statistics
+ *     and attention see only that tile, so the output differs from the
+ *     whole-image decode unless one tile covers the image);
+ *   - in raster order, a tile's first overlap rows are cross-faded with the
+ *     last rows of the tile above as that tile was decoded (weights
+ *     1 - k/e and k/e at row k of the e-row overlap), then its first
+ *     overlap columns likewise with the tile to its left; a tile keeps its
+ *     last overlap rows / columns only if it is the last of its column /
+ *     row (the next tile's cross-fade replaces them).
+ * tile, min_overlap: output pixels, multiples of the latent-to-pixel factor
+ * (8), min_overlap < tile; at most 128 tiles per axis. tiles_per_batch: how
+ * many tiles one pass of the chain decodes (0 = all), which bounds the
+ * workspace. z, rgb as vae_decode_chain. */
+VAE_API size_t vae_chain_tiled_workspace_size(const void *handle, int n, int h, int w, int tile,
+                                              int min_overlap, int tiles_per_batch);
+VAE_API int vae_decode_chain_tiled(void *handle, const float *z, int n, int h, int w, int tile,
+                                   int min_overlap, int tiles_per_batch, float *rgb, void *ws,
+                                   size_t ws_bytes, vae_stream_t stream);
+
 /* Frees the handle's device memory. Handles are tracked in a registry of live
  * handles: every entry point given a destroyed (or never prepared) handle
  * returns VAE_ENOTPREPARED without touching it. */

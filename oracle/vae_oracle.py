@@ -8,6 +8,10 @@ Sources (cited by page title and section):
           struct GroupNorm (apply).
   [hand]  "VAE decode -> GPU handoff (FLUX/LTX render services)": sections
           "The CPU VAE code" and "GPU plan -- im2col + cuBLAS SGEMM".
+  [tile]  cortiq-engine 0.8.78, source of vae3d.rs: fn split_tiles, fn crop,
+          fn blend and VideoVae::decode_clip (the spatial tile schedule and
+          the cross-fade of neighbouring tiles, written there for another
+          decoder and applied here to this one).
 
 Layout: NCHW (NCTHW for the 3-D case), as the pages' decoders store tensors.
 Every input is widened to float64 first; every step is float64. Where a page
@@ -29,6 +33,7 @@ __all__ = [
     "upsample_nearest2x", "upsample_conv", "resnet", "softmax_rows",
     "mid_attention", "up_block", "decode", "conv3d_causal", "causal_stack",
     "conv2d_at", "upsample_conv_at", "mid_attention_at",
+    "split_tiles", "blend_tiles", "tiled_decode",
 ]
 
 
@@ -311,3 +316,96 @@ def causal_stack(x, layers, groups=32, eps=1e-6):
             v = v + u[i - 2]
         u.append(v)
     return u[-1]
+
+
+def split_tiles(length, ratio, tile=256, min_overlap=64):
+    """[tile] fn split_tiles: (starts, lens, overlaps) of one axis in pixels.
+    At or under one tile: a single tile of the whole length. Otherwise the
+    fewest tiles of exactly ``tile`` pixels whose overlaps, all at least
+    ``min_overlap``, cover the length; the slack is then added to the
+    overlaps ``ratio`` pixels at a time, round robin from the first, so that
+    every tile start stays on the latent grid."""
+    if tile >= length:
+        return [0], [length], []
+    n = -(-length // tile)
+    while tile * n < min_overlap * (n - 1) + length:
+        n += 1
+    overlaps = [min_overlap] * (n - 1)
+    slack = tile * n - sum(overlaps) - length
+    for i in range(slack // ratio):
+        overlaps[i % (n - 1)] += ratio
+    starts = [0]
+    for i in range(n - 1):
+        starts.append(starts[i] + tile - overlaps[i])
+    return starts, [tile] * n, overlaps
+
+
+def blend_tiles(tiles, height, width, ys, yo, xs, xo):
+    """[tile] VideoVae::decode_clip's assembly of decoded tiles
+    ``tiles[i][j]`` ([c, th, tw] each) into a [c, height, width] image, in
+    raster order. Tile (i, j): its first yo[i-1] rows are cross-faded with the
+    last yo[i-1] rows of the tile above as that tile was decoded (before its
+    own blending), weights 1 - k/e and k/e at row k (fn blend, dim 2); then
+    its first xo[j-1] columns likewise with the last xo[j-1] columns of the
+    tile to its left as decoded (dim 3); then its last yo[i] rows and xo[j]
+    columns are dropped
+    (fn crop) unless it is the last of its row / column, and what is left is
+    written at the running output position."""
+    c = tiles[0][0].shape[0]
+    out = np.zeros((c, height, width))
+    oy = 0
+    for i in range(len(ys)):
+        ox = 0
+        th = tw = 0
+        for j in range(len(xs)):
+            raw = _f64(tiles[i][j])
+            th, tw = raw.shape[1], raw.shape[2]
+            t = raw.copy()
+            if i > 0:
+                above = _f64(tiles[i - 1][j])
+                e = min(yo[i - 1], above.shape[1], th)
+                for k in range(e):
+                    wb = k / e
+                    t[:, k, :] = above[:, above.shape[1] - e + k, :] * (1 - wb) + t[:, k, :] * wb
+            if j > 0:
+                left = _f64(tiles[i][j - 1])
+                e = min(xo[j - 1], left.shape[2], tw)
+                for k in range(e):
+                    wb = k / e
+                    t[:, :, k] = left[:, :, left.shape[2] - e + k] * (1 - wb) + t[:, :, k] * wb
+            if i + 1 < len(ys):
+                t = t[:, :th - yo[i], :]
+            if j + 1 < len(xs):
+                t = t[:, :, :tw - xo[j]]
+            out[:, oy:oy + t.shape[1], ox:ox + t.shape[2]] = t
+            ox += t.shape[2]
+            th = t.shape[1]
+        oy += th
+    return out
+
+
+def tiled_decode(z, weights, scaling_factor, shift_factor, n_up_blocks, tile=256,
+                 min_overlap=64, n_resnets=3, groups=32, eps=1e-6):
+    """[tile] decode_clip applied to this decoder: split the output plane
+    with split_tiles along each axis (ratio = the decoder's 2^upsamples
+    latent-to-pixel factor), decode each tile's latent crop on its own with
+    ``decode``, and assemble them with blend_tiles. Each tile sees only its
+    own latents (GroupNorm statistics and attention included), so the
+    result differs from the whole-image decode except when one tile covers
+    the image."""
+    z = _f64(z)
+    n, _, zh, zw = z.shape
+    up = [f"up_blocks.{i}.upsamplers.0.conv.weight" in weights for i in range(n_up_blocks)]
+    r = 2 ** sum(up)
+    height, width = zh * r, zw * r
+    ys, yl, yo = split_tiles(height, r, tile, min_overlap)
+    xs, xl, xo = split_tiles(width, r, tile, min_overlap)
+    outs = []
+    for b in range(n):
+        tiles = [[decode(z[b:b + 1, :, ys[i] // r:(ys[i] + yl[i]) // r,
+                           xs[j] // r:(xs[j] + xl[j]) // r],
+                         weights, scaling_factor, shift_factor, n_up_blocks, n_resnets,
+                         groups, eps)[0]
+                  for j in range(len(xs))] for i in range(len(ys))]
+        outs.append(blend_tiles(tiles, height, width, ys, yo, xs, xo))
+    return np.stack(outs)

@@ -493,3 +493,60 @@ def test_mid_attention_at_matches_torch_sdpa():
     tokens = np.array([0, 7, 19, 3])
     ref = _attn_torch(x, p).reshape(2, 64, 20)[:, :, tokens]
     np.testing.assert_allclose(O.mid_attention_at(x, p, tokens), ref, atol=1e-11)
+
+
+# ------------------------------------------------------------------ tiled decode
+
+def test_split_tiles_matches_the_page_values(golden_dir):
+    g = _load(golden_dir, "tile_schedule.json")
+    for case in g["cases"]:
+        s, ln, o = O.split_tiles(case["length"], case["ratio"], g["tile"], g["min_overlap"])
+        assert (s, ln, o) == (case["starts"], case["lens"], case["overlaps"]), case
+
+
+@pytest.mark.parametrize("length,ratio,tile,ov", [(1024, 8, 256, 64), (800, 8, 256, 64),
+                                                  (1000, 8, 512, 64), (264, 8, 256, 64),
+                                                  (4096, 8, 512, 128)])
+def test_split_tiles_cover_the_axis_on_the_latent_grid(length, ratio, tile, ov):
+    s, ln, o = O.split_tiles(length, ratio, tile, ov)
+    assert s[0] == 0 and s[-1] + ln[-1] == length and all(x == tile for x in ln)
+    assert all(x >= ov for x in o) and all(x % ratio == 0 for x in s)
+    assert all(s[i + 1] == s[i] + tile - o[i] for i in range(len(o)))
+
+
+def _crops(img, ys, yl, xs, xl):
+    return [[img[:, ys[i]:ys[i] + yl[i], xs[j]:xs[j] + xl[j]] for j in range(len(xs))]
+            for i in range(len(ys))]
+
+
+def test_blend_of_consistent_crops_rebuilds_the_image():
+    """Tiles cut from one image agree on their overlaps, so every cross-fade
+    returns the shared value: any offset, crop or placement mistake shows."""
+    img = _rng(50).standard_normal((3, 800, 1000))
+    ys, yl, yo = O.split_tiles(800, 8, 256, 64)
+    xs, xl, xo = O.split_tiles(1000, 8, 256, 64)
+    out = O.blend_tiles(_crops(img, ys, yl, xs, xl), 800, 1000, ys, yo, xs, xo)
+    np.testing.assert_allclose(out, img, atol=1e-12)
+
+
+def test_blend_cross_fades_linearly_from_the_earlier_tile():
+    """Two tiles side by side, constant a and b: across the overlap of e
+    columns the result runs a*(1 - k/e) + b*k/e, the earlier tile fading
+    out; outside it each tile's own value."""
+    xs, xl, xo = O.split_tiles(288, 16, 256, 64)  # two tiles, overlap 224
+    a = np.full((1, 4, 256), 2.0)
+    b = np.full((1, 4, 256), -3.0)
+    out = O.blend_tiles([[a, b]], 4, 288, [0], [], xs, xo)
+    e = xo[0]
+    k = np.arange(e)
+    np.testing.assert_allclose(out[0, :, xs[1]:xs[1] + e], np.broadcast_to(
+        2.0 * (1 - k / e) + -3.0 * (k / e), (4, e)), atol=1e-14)
+    assert (out[0, :, :xs[1]] == 2.0).all() and (out[0, :, xs[1] + e:] == -3.0).all()
+
+
+def test_tiled_decode_with_one_tile_is_the_decode():
+    w = S.make_decoder_weights("tiny", 3)
+    z = S.make_latent((1, 16, 6, 7), 3)
+    ref = O.decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
+    got = O.tiled_decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4, tile=64, min_overlap=16)
+    np.testing.assert_array_equal(got, ref)
