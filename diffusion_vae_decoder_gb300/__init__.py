@@ -71,6 +71,15 @@ class ChainArgs(ctypes.Structure):
 PRECISION_AUTO, PRECISION_TF32, PRECISION_SPLIT_TF32 = 0, 1, 2
 
 
+class CausalDecoderArgs(ctypes.Structure):
+    _fields_ = [("latent_channels", ctypes.c_int), ("scaling_factor", ctypes.c_float),
+                ("shift_factor", ctypes.c_float), ("groups", ctypes.c_int),
+                ("eps", ctypes.c_float), ("conv_in", ConvRef), ("n_mid", ctypes.c_int),
+                ("mid", ctypes.POINTER(ResnetRef)), ("n_ups", ctypes.c_int),
+                ("ups", ctypes.POINTER(UpRef)), ("norm_out", NormRef), ("conv_out", ConvRef),
+                ("precision", ctypes.c_int)]
+
+
 class ProfRecord(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("kernels", ctypes.c_int), ("flops", ctypes.c_double),
                 ("bytes", ctypes.c_double), ("ms", ctypes.c_double)]
@@ -122,6 +131,10 @@ _SIGS = {
                                     ctypes.POINTER(_I)]),
     "vae_decode_chain_traced": (_I, [_P, _P, _I, _I, _I, _P, _P, _SZ, ctypes.POINTER(_P), _I,
                                      _P]),
+    "vae_causal_decoder_prepare": (_I, [ctypes.POINTER(CausalDecoderArgs), ctypes.POINTER(_P),
+                                        _P]),
+    "vae_causal_decoder_workspace_size": (_SZ, [_P, _I, _I, _I, _I]),
+    "vae_decode_causal": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "vae_chain_tiled_workspace_size": (_SZ, [_P, _I, _I, _I, _I, _I, _I]),
     "vae_decode_chain_tiled": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "vae_measure_tf32_mma": (_I, [_I, ctypes.POINTER(ctypes.c_double),
@@ -539,6 +552,79 @@ class VaeChain:
                                                                     ctypes.byref(cnt)))
         return [dict(kind=PROF_KINDS.get(r.kind, r.kind), kernels=r.kernels, flops=r.flops,
                      bytes=r.bytes, ms=r.ms) for r in arr[:cnt.value]]
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _check("vae_chain_destroy", load_library().vae_chain_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class VaeCausalDecoder:
+    """Prepared 3-D causal decoder (vae_causal_decoder_prepare /
+    vae_decode_causal / vae_chain_destroy). ``weights`` as
+    vae_synth.make_causal_decoder_weights names them: conv weights
+    [cout, cin, 3, 3, 3], 1x1x1 shortcuts [cout, cin, 1, 1]."""
+
+    def __init__(self, weights, n_up_blocks, n_mid=2, resnets_per_block=2, latent_channels=16,
+                 scaling_factor=0.3611, shift_factor=0.1159, groups=32, eps=1e-6, stream=None,
+                 precision=PRECISION_AUTO):
+        lib = load_library()
+        keep = []
+
+        def conv(name):
+            r = _conv_ref(weights, name, keep)
+            if name + ".weight" in weights and weights[name + ".weight"].ndim == 5:
+                r.k = 3
+            return r
+
+        def res(pre):
+            return ResnetRef(_norm_ref(weights, pre + ".norm1", keep), conv(pre + ".conv1"),
+                             _norm_ref(weights, pre + ".norm2", keep), conv(pre + ".conv2"),
+                             _conv_ref(weights, pre + ".conv_shortcut", keep))
+
+        mid = (ResnetRef * max(1, n_mid))(*[res(f"mid.resnets.{m}") for m in range(n_mid)])
+        ups, self._res_arrays = [], [mid]
+        for i in range(n_up_blocks):
+            arr = (ResnetRef * resnets_per_block)(*[
+                res(f"up_blocks.{i}.resnets.{j}") for j in range(resnets_per_block)])
+            self._res_arrays.append(arr)
+            ups.append(UpRef(resnets_per_block, arr, conv(f"up_blocks.{i}.upsamplers.0.conv")))
+        ups_arr = (UpRef * max(1, n_up_blocks))(*ups)
+        args = CausalDecoderArgs(latent_channels, scaling_factor, shift_factor, groups, eps,
+                                 conv("conv_in"), n_mid, mid, n_up_blocks, ups_arr,
+                                 _norm_ref(weights, "conv_norm_out", keep), conv("conv_out"),
+                                 int(precision))
+        h = ctypes.c_void_p()
+        _check("vae_causal_decoder_prepare", lib.vae_causal_decoder_prepare(
+            ctypes.byref(args), ctypes.byref(h), _stream(stream)))
+        self.handle = h
+        self.out_channels = weights["conv_out.weight"].shape[0]
+        self.up_factor = 2 ** sum(1 for i in range(n_up_blocks)
+                                  if f"up_blocks.{i}.upsamplers.0.conv.weight" in weights)
+
+    def workspace_size(self, n, t, h, w):
+        return load_library().vae_causal_decoder_workspace_size(self.handle, n, t, h, w)
+
+    def decode(self, z, out=None, ws=None, stream=None):
+        lib = load_library()
+        _need(z, "z")
+        n, c, t, h, w = z.shape
+        if out is None:
+            import torch
+            f = self.up_factor
+            out = torch.empty((n, self.out_channels, t, f * h, f * w), dtype=torch.float32,
+                              device=z.device)
+        if ws is None:
+            ws = _ws(self.workspace_size(n, t, h, w), z.device)
+        _check("vae_decode_causal", lib.vae_decode_causal(
+            self.handle, _ptr(z), n, t, h, w, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+        return out
 
     def close(self):
         if getattr(self, "handle", None):

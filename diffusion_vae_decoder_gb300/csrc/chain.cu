@@ -64,6 +64,7 @@ struct ConvW {
   float *w = nullptr, *b = nullptr;
   float *w_exact = nullptr;  // the same pack unrounded (split-TF32 products)
   int cin = 0, cout = 0, k = 0, ldb = 0, sc_cin = 0;
+  int kt = 1;  // time taps: 3 for the causal 3x3x3 convs of the 3-D decoder
 };
 struct NormW {
   float *g = nullptr, *b = nullptr;
@@ -139,6 +140,13 @@ struct Profiler {
 struct Chain {
   Profiler prof;
   Tracer *tr = nullptr;  // set for the duration of a traced decode
+  // 3-D causal decoder (vae_causal_decoder_prepare): causal 3x3x3 convs, no
+  // attention, mid resnets in mid3, nearest-2x spatial upsample materialised
+  // before each upsample conv; `frames` is the current decode's frame count
+  // (1 for the 2-D decoder).
+  bool causal = false;
+  std::vector<ResW> mid3;
+  int frames = 1;
   int precision = VAE_PRECISION_TF32;
   bool exact = false;  // this decode forms split-TF32 products (set per decode)
   int device = 0;
@@ -211,7 +219,9 @@ struct Builder {
     return n;
   }
   // Conv (optionally with the 1x1 shortcut appended to its reduction).
-  ConvW conv(const vae_conv_ref &r, int cin, int cout, const vae_conv_ref *sc = nullptr) {
+  // kt = 3: a causal 3x3x3 conv, weight [cout][cin][3][3][3].
+  ConvW conv(const vae_conv_ref &r, int cin, int cout, const vae_conv_ref *sc = nullptr,
+             int kt = 1) {
     ConvW c;
     if (r.cin != cin || r.cout != cout || !(r.k == 1 || r.k == 3)) fail(VAE_EINVAL);
     const bool has_sc = sc && sc->weight;
@@ -220,19 +230,20 @@ struct Builder {
     c.cin = cin;
     c.cout = cout;
     c.k = r.k;
+    c.kt = kt;
     c.sc_cin = has_sc ? sc->cin : 0;
-    c.ldb = packed_ldb(cin, r.k * r.k, c.sc_cin);
-    const float *wt = upload_tmp(r.weight, static_cast<size_t>(cout) * cin * r.k * r.k);
+    const int taps = r.k * r.k * kt;
+    c.ldb = packed_ldb(cin, taps, c.sc_cin);
+    const float *wt = upload_tmp(r.weight, static_cast<size_t>(cout) * cin * taps);
     const float *wsc = has_sc ? upload_tmp(sc->weight, static_cast<size_t>(cout) * c.sc_cin)
                               : nullptr;
     c.w = dev<float>(static_cast<size_t>(cout) * c.ldb);
     if (ch->precision != VAE_PRECISION_TF32)
       c.w_exact = dev<float>(static_cast<size_t>(cout) * c.ldb);
     if (status != VAE_OK) return c;
-    fail(pack_conv_weights(wt, cout, cin, r.k * r.k, wsc, c.sc_cin, c.w, cout, c.ldb, s));
+    fail(pack_conv_weights(wt, cout, cin, taps, wsc, c.sc_cin, c.w, cout, c.ldb, s));
     if (c.w_exact)
-      fail(pack_conv_weights(wt, cout, cin, r.k * r.k, wsc, c.sc_cin, c.w_exact, cout, c.ldb, s,
-                             0));
+      fail(pack_conv_weights(wt, cout, cin, taps, wsc, c.sc_cin, c.w_exact, cout, c.ldb, s, 0));
     if (has_sc) {
       const float *b1 = r.bias ? upload_tmp(r.bias, cout) : nullptr;
       const float *b2 = sc->bias ? upload_tmp(sc->bias, cout) : nullptr;
@@ -262,13 +273,13 @@ struct Builder {
     if (r.bias) c.b = upload(r.bias, cout);
     return c;
   }
-  ResW resnet(const vae_resnet_ref &r, int cin, int cout) {
+  ResW resnet(const vae_resnet_ref &r, int cin, int cout, int kt = 1) {
     ResW w;
     if ((cin != cout) != (r.shortcut.weight != nullptr)) fail(VAE_EINVAL);
     w.n1 = norm(r.norm1, cin);
-    w.c1 = conv(r.conv1, cin, cout);
+    w.c1 = conv(r.conv1, cin, cout, nullptr, kt);
     w.n2 = norm(r.norm2, cout);
-    w.c2 = conv(r.conv2, cout, cout, &r.shortcut);
+    w.c2 = conv(r.conv2, cout, cout, &r.shortcut, kt);
     if (w.c2.sc_cin && w.c2.sc_cin != cin) fail(VAE_EINVAL);
     if (w.c1.k != 3 || w.c2.k != 3) fail(VAE_EINVAL);
     return w;
@@ -416,13 +427,16 @@ int run_conv(Chain &ch, const ConvW &c, const float *in, int n, int h, int w,
              cudaStream_t s, bool upsample = false, bool nchw_out = false,
              Stats *st = nullptr, float *part = nullptr, int groups = 0,
              float *split = nullptr) {
-  const long long out_px = static_cast<long long>(n) * h * w * (upsample ? 4 : 1);
+  const long long out_px =
+      static_cast<long long>(n) * ch.frames * h * w * (upsample ? 4 : 1);
   Step step(ch.prof, upsample ? VAE_PROF_UPSAMPLE_CONV : VAE_PROF_CONV3X3,
             conv_flops(c, out_px), 0, s);
   IgemmDesc d;
   d.mode = upsample ? AMode::Upsample : AMode::Conv;
   d.a = in;
-  d.imgs = n;
+  d.imgs = n * ch.frames;  // one image per frame
+  d.t = ch.frames;
+  d.kt = c.kt;
   d.hin = h;
   d.win = w;
   d.a_c = round_up32(c.cin);
@@ -477,7 +491,7 @@ int run_gn(Chain &ch, const NormW &nw, const float *in, int n, long long sp, flo
 // those of `out` on return.
 int run_resnet(Chain &ch, const ResW &r, const float *in, float *out, const DecodeWs &ws, int n,
                int h, int w, int round_out, Stats &st, cudaStream_t s) {
-  const long long sp = static_cast<long long>(h) * w;
+  const long long sp = static_cast<long long>(h) * w * ch.frames;  // GroupNorm extent
   const size_t in_bytes = 4ull * n * sp * r.c1.cin, out_bytes = 4ull * n * sp * r.c1.cout;
   VAE_TRY(run_gn(ch, r.n1, in, n, sp, ws.T, ws, st, s));
   if (ch.tr) ch.tr->emit(ws.T, in_bytes, s);
@@ -615,6 +629,7 @@ int vae_chain_prepare(const vae_chain_args *a, void **handle, vae_stream_t strea
 size_t vae_chain_workspace_size(const void *handle, int n, int h, int w) {
   if (!is_live(handle) || n <= 0 || h <= 0 || w <= 0) return 0;
   const Chain *ch = static_cast<const Chain *>(handle);
+  if (ch->causal) return 0;
   const Plan p = make_plan(*ch, n, h, w);
   Carver cv(nullptr, 0);
   carve_decode(cv, *ch, p, n, h, w);
@@ -646,6 +661,8 @@ double decode_conv_gflops(const Chain &ch, int n, int h, int w) {
 
 int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void *ws,
                 size_t ws_bytes, cudaStream_t s) {
+  if (ch->causal) return VAE_EINVAL;  // a 3-D causal decoder: vae_decode_causal
+  ch->frames = 1;
   if (!z || !rgb || !ws || n <= 0 || h <= 0 || w <= 0) return VAE_EINVAL;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != ch->device) return VAE_EINVAL;
@@ -735,6 +752,142 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
   return VAE_OK;
 }
 
+// ---------------------------------------------------------------- 3-D causal decoder
+// Activations NDHWC: [n * t frames][h][w][c], one image per frame for the
+// conv kernel (whose causal taps read frames max(f + kt - 2, 0) of the same
+// sample); GroupNorm statistics over (t, h, w) of each sample.
+struct CausalPlan {
+  size_t max_elems = 0, up_elems = 0;
+  int max_c = 0;
+  long long max_slots = 0;
+};
+
+long long stat_slots_frames(AMode mode, int hin, int win, int cout, int t) {
+  IgemmDesc d;
+  d.mode = mode;
+  d.hin = hin;
+  d.win = win;
+  d.cout = cout;
+  d.t = t;
+  return igemm_stat_slots(d);
+}
+
+CausalPlan make_causal_plan(const Chain &ch, int n, int t, int h, int w) {
+  CausalPlan p;
+  auto see = [&](long long hh, long long ww, int c) {
+    p.max_elems = std::max(p.max_elems, static_cast<size_t>(static_cast<long long>(n) * t * hh *
+                                                            ww * c));
+    p.max_c = std::max(p.max_c, c);
+    p.max_slots = std::max(p.max_slots, stat_slots_frames(AMode::Conv, static_cast<int>(hh),
+                                                          static_cast<int>(ww), c, t));
+  };
+  long long hh = h, ww = w;
+  see(hh, ww, ch.conv_in.cout);
+  for (const UpW &u : ch.ups) {
+    for (const ResW &r : u.res) {
+      see(hh, ww, r.c1.cin);
+      see(hh, ww, r.c1.cout);
+    }
+    if (u.has_up) {
+      p.up_elems = std::max(p.up_elems, static_cast<size_t>(static_cast<long long>(n) * t * 4 *
+                                                            hh * ww * u.up.cin));
+      hh *= 2;
+      ww *= 2;
+      see(hh, ww, u.up.cout);
+    }
+  }
+  return p;
+}
+
+struct CausalWs {
+  float *lat, *X, *Y, *T, *H, *U, *part, *split;
+  unsigned *gn_cnt;
+  void *gn;
+};
+
+CausalWs carve_causal(Carver &cv, const Chain &ch, const CausalPlan &p, int n, int t, int h,
+                      int w) {
+  CausalWs d{};
+  d.lat = cv.take<float>(static_cast<size_t>(n) * t * h * w * round_up32(ch.latent_c));
+  d.X = cv.take<float>(p.max_elems);
+  d.Y = cv.take<float>(p.max_elems);
+  d.T = cv.take<float>(p.max_elems);
+  d.H = cv.take<float>(p.max_elems);
+  d.U = cv.take<float>(std::max<size_t>(p.up_elems, 1));
+  d.split = cv.take<float>(kSplitWsFloats);
+  d.part = cv.take<float>(static_cast<size_t>(n) * ch.groups * std::max(1024ll, p.max_slots) * 3);
+  d.gn_cnt = cv.take<unsigned>(static_cast<size_t>(n) * ch.groups);
+  d.gn = cv.take<char>(groupnorm_ws_bytes(n, std::max(p.max_c, ch.norm_out.c), 1, ch.groups));
+  return d;
+}
+
+int decode_causal_impl(Chain *ch, const float *z, int n, int t, int h, int w, float *out,
+                       void *ws, size_t ws_bytes, cudaStream_t s) {
+  if (!ch->causal) return VAE_EINVAL;
+  if (!z || !out || !ws || n <= 0 || t <= 0 || h <= 0 || w <= 0) return VAE_EINVAL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != ch->device) return VAE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(z) | reinterpret_cast<uintptr_t>(out)) & 15) return VAE_EINVAL;
+  if (static_cast<long long>(n) * t > 65535 || h > 65535 || w > 65535) return VAE_EUNSUPPORTED;
+  const CausalPlan p = make_causal_plan(*ch, n, t, h, w);
+  Carver cv(ws, ws_bytes);
+  CausalWs d = carve_causal(cv, *ch, p, n, t, h, w);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  ch->frames = t;
+  ch->exact = ch->precision == VAE_PRECISION_SPLIT_TF32 ||
+              (ch->precision == VAE_PRECISION_AUTO &&
+               decode_conv_gflops(*ch, n, h, w) * 3.0 * t <= VAE_SPLIT_AUTO_GFLOP);
+  // DecodeWs view of the buffers run_resnet / run_gn use
+  DecodeWs dw{};
+  dw.X = d.X;
+  dw.Y = d.Y;
+  dw.T = d.T;
+  dw.H = d.H;
+  dw.part = d.part;
+  dw.split = d.split;
+  dw.gn_cnt = d.gn_cnt;
+  dw.gn = d.gn;
+  if (cudaMemsetAsync(d.gn_cnt, 0, static_cast<size_t>(n) * ch->groups * sizeof(unsigned), s) !=
+      cudaSuccess)
+    return VAE_ECUDA;
+  const long long vox = static_cast<long long>(t) * h * w;
+  const float *lat = nullptr;
+  {
+    const int cp = round_up32(ch->latent_c);
+    Step st(ch->prof, VAE_PROF_LAYOUT, 0, 4.0 * n * vox * (ch->latent_c + cp), s);
+    VAE_TRY(stage_nhwc(z, n, ch->latent_c, vox, VAE_NCHW, d.lat, cp, 1.0f / ch->sf, ch->sh,
+                       !ch->exact, &lat, s));
+  }
+  float *cur = d.X, *other = d.Y;
+  int hh = h, ww = w;
+  Stats st;
+  VAE_TRY(run_conv(*ch, ch->conv_in, lat, n, hh, ww, nullptr, nullptr, cur, 0, s, false, false,
+                   &st, d.part, ch->groups, d.split));
+  for (const ResW &r : ch->mid3) VAE_TRY(run_resnet(*ch, r, cur, cur, dw, n, hh, ww, 0, st, s));
+  for (const UpW &u : ch->ups) {
+    for (size_t j = 0; j < u.res.size(); ++j) {
+      const ResW &r = u.res[j];
+      const int round = (u.has_up && j + 1 == u.res.size()) ? 1 : 0;
+      float *dst = r.c2.sc_cin ? other : cur;
+      VAE_TRY(run_resnet(*ch, r, cur, dst, dw, n, hh, ww, round, st, s));
+      if (dst != cur) std::swap(cur, other);
+    }
+    if (u.has_up) {
+      // every frame upsampled, then the causal conv at the doubled size
+      VAE_TRY(upsample_nearest2x_nhwc(cur, static_cast<long long>(n) * t, hh, ww, u.up.cin, d.U,
+                                      s));
+      hh *= 2;
+      ww *= 2;
+      VAE_TRY(run_conv(*ch, u.up, d.U, n, hh, ww, nullptr, nullptr, other, 1, s, false, false,
+                       &st, d.part, ch->groups, d.split));
+      std::swap(cur, other);
+    }
+  }
+  const long long sp = static_cast<long long>(t) * hh * ww;
+  VAE_TRY(run_gn(*ch, ch->norm_out, cur, n, sp, d.T, dw, st, s));
+  return run_conv(*ch, ch->conv_out, d.T, n, hh, ww, nullptr, nullptr, out, 0, s, false, true);
+}
+
 // ---------------------------------------------------------------- tiled decode
 int up_factor(const Chain &ch) {
   int r = 1;
@@ -782,10 +935,91 @@ TiledWs carve_tiled(Carver &cv, const Chain &ch, int n, const TileSchedule &ts, 
 
 extern "C" {
 
+int vae_causal_decoder_prepare(const vae_causal_decoder_args *a, void **handle,
+                               vae_stream_t stream) {
+  if (!a || !handle) return VAE_EINVAL;
+  *handle = nullptr;
+  if (a->latent_channels <= 0 || a->groups <= 0 || a->n_ups < 0 || (a->n_ups && !a->ups) ||
+      a->n_mid < 0 || (a->n_mid && !a->mid) || a->scaling_factor == 0.f ||
+      a->precision < VAE_PRECISION_AUTO || a->precision > VAE_PRECISION_SPLIT_TF32)
+    return VAE_EINVAL;
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  Chain *ch = new Chain();
+  cudaGetDevice(&ch->device);
+  ch->causal = true;
+  ch->latent_c = a->latent_channels;
+  ch->groups = a->groups;
+  ch->eps = a->eps;
+  ch->sf = a->scaling_factor;
+  ch->sh = a->shift_factor;
+  ch->precision = a->precision;
+  Builder b{ch, s};
+  const int c0 = a->conv_in.cout;
+  ch->conv_in = b.conv(a->conv_in, a->latent_channels, c0, nullptr, 3);
+  if (ch->conv_in.k != 3) b.fail(VAE_EINVAL);
+  for (int m = 0; m < a->n_mid && b.status == VAE_OK; ++m)
+    ch->mid3.push_back(b.resnet(a->mid[m], c0, c0, 3));
+  int c = c0;
+  for (int i = 0; i < a->n_ups && b.status == VAE_OK; ++i) {
+    const vae_up_ref &u = a->ups[i];
+    UpW uw;
+    if (u.n_resnets <= 0 || !u.resnets) b.fail(VAE_EINVAL);
+    for (int j = 0; j < u.n_resnets && b.status == VAE_OK; ++j) {
+      const int cout = u.resnets[j].conv1.cout;
+      uw.res.push_back(b.resnet(u.resnets[j], c, cout, 3));
+      c = cout;
+    }
+    uw.has_up = u.upsample_conv.weight != nullptr;
+    if (uw.has_up) {
+      uw.up = b.conv(u.upsample_conv, c, u.upsample_conv.cout, nullptr, 3);
+      if (uw.up.k != 3 || c % 4) b.fail(VAE_EINVAL);
+      c = u.upsample_conv.cout;
+    }
+    ch->ups.push_back(std::move(uw));
+  }
+  ch->norm_out = b.norm(a->norm_out, c);
+  ch->conv_out = b.conv(a->conv_out, c, a->conv_out.cout, nullptr, 3);
+  if (ch->conv_out.k != 3 && b.status == VAE_OK) b.fail(VAE_EINVAL);
+  if (b.status == VAE_OK && cudaStreamSynchronize(s) != cudaSuccess) b.fail(VAE_ECUDA);
+  cudaStreamSynchronize(s);
+  for (void *p : b.temps) cudaFree(p);
+  if (b.status != VAE_OK) {
+    for (void *p : ch->allocs) cudaFree(p);
+    delete ch;
+    return b.status;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    g_live.insert(ch);
+  }
+  *handle = ch;
+  return VAE_OK;
+}
+
+size_t vae_causal_decoder_workspace_size(const void *handle, int n, int t, int h, int w) {
+  if (!is_live(handle) || n <= 0 || t <= 0 || h <= 0 || w <= 0) return 0;
+  const Chain &ch = *static_cast<const Chain *>(handle);
+  if (!ch.causal) return 0;
+  const CausalPlan p = make_causal_plan(ch, n, t, h, w);
+  Carver cv(nullptr, 0);
+  carve_causal(cv, ch, p, n, t, h, w);
+  return cv.used;
+}
+
+int vae_decode_causal(void *handle, const float *z, int n, int t, int h, int w, float *out,
+                      void *ws, size_t ws_bytes, vae_stream_t stream) {
+  if (!is_live(handle)) return VAE_ENOTPREPARED;
+  Chain *ch = static_cast<Chain *>(handle);
+  ch->tr = nullptr;
+  return decode_causal_impl(ch, z, n, t, h, w, out, ws, ws_bytes,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t vae_chain_tiled_workspace_size(const void *handle, int n, int h, int w, int tile,
                                       int min_overlap, int tiles_per_batch) {
   if (!is_live(handle)) return 0;
   const Chain &ch = *static_cast<const Chain *>(handle);
+  if (ch.causal) return 0;
   TileSchedule ts;
   int batch = 0;
   if (tiled_plan(ch, n, h, w, tile, min_overlap, tiles_per_batch, &ts, &batch) != VAE_OK) return 0;
@@ -801,6 +1035,7 @@ int vae_decode_chain_tiled(void *handle, const float *z, int n, int h, int w, in
   if (!z || !rgb || !ws) return VAE_EINVAL;
   if ((reinterpret_cast<uintptr_t>(z) | reinterpret_cast<uintptr_t>(rgb)) & 15) return VAE_EINVAL;
   Chain *ch = static_cast<Chain *>(handle);
+  if (ch->causal) return VAE_EINVAL;
   auto s = reinterpret_cast<cudaStream_t>(stream);
   TileSchedule ts;
   int batch = 0;
@@ -834,6 +1069,7 @@ int vae_chain_trace_points(const void *handle, int n, int h, int w, vae_trace_po
                            int capacity, int *count) {
   if (!is_live(handle)) return VAE_ENOTPREPARED;
   if (!count || n <= 0 || h <= 0 || w <= 0 || (capacity > 0 && !out)) return VAE_EINVAL;
+  if (static_cast<const Chain *>(handle)->causal) return VAE_EINVAL;
   const std::vector<vae_trace_point> pts =
       trace_points(*static_cast<const Chain *>(handle), n, h, w);
   *count = static_cast<int>(pts.size());

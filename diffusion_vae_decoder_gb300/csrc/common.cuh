@@ -154,6 +154,9 @@ int transpose(const float *src, long long src_outer_stride, int src_ld, float *d
 int pad_rows(const float *src, long long rows, int cols, float *dst, int dst_cols,
              cudaStream_t s);
 int add_bias(float *dst, const float *a, const float *b, int n, cudaStream_t s);
+// Nearest-2x spatial upsample of NHWC images [imgs][h][w][c] (c % 4 == 0).
+int upsample_nearest2x_nhwc(const float *src, long long imgs, int h, int w, int c, float *dst,
+                            cudaStream_t s);
 
 // GroupNorm (+SiLU) (groupnorm.cu). `x` NHWC [n][spatial][c] or NCHW.
 size_t groupnorm_ws_bytes(int n, int c, long long spatial, int groups);

@@ -107,6 +107,22 @@ __global__ void add_kernel(float *dst, const float *a, const float *b, int n) {
     dst[i] = (a ? a[i] : 0.f) + (b ? b[i] : 0.f);
 }
 
+// Nearest-2x spatial upsample of NHWC images (every frame of a video on its
+// own): dst[img][2y + a][2x + b][c] = src[img][y][x][c], float4 per thread.
+__global__ void upsample2x_nhwc_kernel(const float4 *__restrict__ src, int h, int w, int c4,
+                                       long long total, float4 *__restrict__ dst) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % c4);
+    long long r = i / c4;
+    const int x2 = static_cast<int>(r % (2 * w));
+    r /= 2 * w;
+    const int y2 = static_cast<int>(r % (2 * h));
+    const long long img = r / (2 * h);
+    dst[i] = src[((img * h + (y2 >> 1)) * w + (x2 >> 1)) * c4 + c];
+  }
+}
+
 int grid_for(long long n, int threads) {
   long long g = (n + threads - 1) / threads;
   const long long cap = static_cast<long long>(num_sms()) * 8;
@@ -158,6 +174,17 @@ int transpose(const float *src, long long src_outer_stride, int src_ld, float *d
 int pad_rows(const float *src, long long rows, int cols, float *dst, int dst_cols,
              cudaStream_t s) {
   pad_rows_kernel<<<grid_for(rows * dst_cols, 256), 256, 0, s>>>(src, rows, cols, dst, dst_cols);
+  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  count_launches(1);
+  return VAE_OK;
+}
+
+int upsample_nearest2x_nhwc(const float *src, long long imgs, int h, int w, int c, float *dst,
+                            cudaStream_t s) {
+  if (!src || !dst || imgs <= 0 || h <= 0 || w <= 0 || c <= 0 || c % 4) return VAE_EINVAL;
+  const long long total = imgs * 4ll * h * w * (c / 4);
+  upsample2x_nhwc_kernel<<<grid_for(total, 256), 256, 0, s>>>(
+      reinterpret_cast<const float4 *>(src), h, w, c / 4, total, reinterpret_cast<float4 *>(dst));
   if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
   count_launches(1);
   return VAE_OK;

@@ -352,6 +352,45 @@ VAE_API int vae_decode_chain_traced(void *handle, const float *z, int n, int h, 
                                     int n_trace, vae_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * 3-D causal decoder: an LTX-style video decoder ("VAE decode -> GPU handoff
+ * (FLUX/LTX render services)", "The CPU VAE code": LtxVaeDecoder::decode, a
+ * 3-D causal conv over time x H x W with causal padding on the time axis)
+ * as a structural decoder, since the pages give no LTX architecture
+ * constants: the 2-D decoder's order (VaeChainArgs) with every 3x3 conv a
+ * causal 3x3x3 conv (vae_conv3d_causal's definition: two copies of the
+ * first frame in front, zero spatial padding) and GroupNorm over (t, h, w):
+ *   z / scaling_factor + shift_factor -> conv_in -> mid resnets (no
+ *   attention) -> ups[i]: resnets, then (if upsample_conv.weight) nearest-2x
+ *   upsample of every frame and upsample_conv -> GroupNorm+SiLU -> conv_out.
+ * Frames stay frames (no temporal upsampling).
+ *   conv refs with k = 3: weight [cout][cin][3][3][3]; shortcuts k = 1:
+ *   [cout][cin] (1x1x1); norms as for the chain.
+ *   z   [n, latent_channels, t, h, w] NCDHW; out [n, conv_out.cout, t, f*h,
+ *   f*w] NCDHW, f = 2^(upsampling up-blocks).
+ * The handle is freed with vae_chain_destroy; the 2-D entry points refuse it
+ * (VAE_EINVAL), as vae_decode_causal refuses a 2-D chain. */
+typedef struct {
+  int latent_channels;
+  float scaling_factor, shift_factor;
+  int groups;
+  float eps;
+  vae_conv_ref conv_in;
+  int n_mid;
+  const vae_resnet_ref *mid;
+  int n_ups;
+  const vae_up_ref *ups;
+  vae_norm_ref norm_out;
+  vae_conv_ref conv_out;
+  int precision; /* vae_precision; AUTO compares the decode's conv work */
+} vae_causal_decoder_args;
+
+VAE_API int vae_causal_decoder_prepare(const vae_causal_decoder_args *args, void **handle,
+                                       vae_stream_t stream);
+VAE_API size_t vae_causal_decoder_workspace_size(const void *handle, int n, int t, int h, int w);
+VAE_API int vae_decode_causal(void *handle, const float *z, int n, int t, int h, int w,
+                              float *out, void *ws, size_t ws_bytes, vae_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Step profiler of the chain: when enabled, vae_decode_chain brackets every
  * step (one conv, one GroupNorm+SiLU, the attention block, the latent
  * staging) with CUDA events on the caller's stream and stores the step's

@@ -34,6 +34,7 @@ __all__ = [
     "mid_attention", "up_block", "decode", "conv3d_causal", "causal_stack",
     "conv2d_at", "upsample_conv_at", "mid_attention_at",
     "split_tiles", "blend_tiles", "tiled_decode",
+    "upsample_nearest2x_spatial", "resnet3d", "causal_decode",
 ]
 
 
@@ -409,3 +410,55 @@ def tiled_decode(z, weights, scaling_factor, shift_factor, n_up_blocks, tile=256
                   for j in range(len(xs))] for i in range(len(ys))]
         outs.append(blend_tiles(tiles, height, width, ys, yo, xs, xo))
     return np.stack(outs)
+
+
+def upsample_nearest2x_spatial(x):
+    """Nearest-2x upsample of every frame of a [n, c, t, h, w] video
+    ([vae] VaeUpRef's upsample, per frame; time is kept)."""
+    x = _f64(x)
+    h, w = x.shape[3], x.shape[4]
+    rows = np.arange(2 * h) // 2
+    cols = np.arange(2 * w) // 2
+    return x[:, :, :, rows][:, :, :, :, cols]
+
+
+def resnet3d(x, p, groups=32, eps=1e-6):
+    """resnet with every 3x3 conv a causal 3x3x3 conv (conv3d_causal) and
+    GroupNorm over (t, h, w); the 1x1 shortcut acts on every frame."""
+    x = _f64(x)
+    h = conv3d_causal(group_norm_silu(x, *p["norm1"], groups, eps), *p["conv1"])
+    h = conv3d_causal(group_norm_silu(h, *p["norm2"], groups, eps), *p["conv2"])
+    if "conv_shortcut" in p:
+        w, b = p["conv_shortcut"]
+        w = _f64(w).reshape(w.shape[0], -1)
+        skip = np.einsum("oc,ncthw->nothw", w, x) + _f64(b)[None, :, None, None, None]
+    else:
+        skip = x
+    return skip + h
+
+
+def causal_decode(z, weights, scaling_factor, shift_factor, n_up_blocks, n_mid=2,
+                  n_resnets=2, groups=32, eps=1e-6):
+    """[hand] "The CPU VAE code" (LtxVaeDecoder::decode: a 3-D causal decode,
+    causal padding on the time axis) as a structural decoder: the pages give
+    no LTX architecture constants, so the structure is the 2-D decoder's
+    ([vae] VaeChainArgs order) with every conv a causal 3x3x3 conv and
+    GroupNorm over (t, h, w): de-normalise, conv_in, the mid resnets (no
+    attention), up blocks of resnets each followed (but the last) by a
+    per-frame nearest-2x spatial upsample and a causal conv, GroupNorm+SiLU,
+    conv_out. z [n, c, t, h, w] -> [n, 3, t, 8h, 8w] for three upsamples;
+    frames stay frames (no temporal upsampling is read into the pages)."""
+    x = denormalize(z, scaling_factor, shift_factor)
+    x = conv3d_causal(x, weights["conv_in.weight"], weights["conv_in.bias"])
+    for m in range(n_mid):
+        x = resnet3d(x, _pairs(weights, f"mid.resnets.{m}", _RES), groups, eps)
+    for i in range(n_up_blocks):
+        for j in range(n_resnets):
+            x = resnet3d(x, _pairs(weights, f"up_blocks.{i}.resnets.{j}", _RES), groups, eps)
+        key = f"up_blocks.{i}.upsamplers.0.conv"
+        if key + ".weight" in weights:
+            x = conv3d_causal(upsample_nearest2x_spatial(x), weights[key + ".weight"],
+                              weights[key + ".bias"])
+    x = group_norm_silu(x, weights["conv_norm_out.weight"], weights["conv_norm_out.bias"],
+                        groups, eps)
+    return conv3d_causal(x, weights["conv_out.weight"], weights["conv_out.bias"])

@@ -61,7 +61,9 @@ int main(void) {
   O(vae_up_ref, resnets) O(vae_up_ref, upsample_conv)
   O(vae_chain_args, eps) O(vae_chain_args, conv_in) O(vae_chain_args, mid_attn)
   O(vae_chain_args, n_ups) O(vae_chain_args, ups) O(vae_chain_args, conv_out)
-  O(vae_chain_args, precision)
+  O(vae_chain_args, precision) P(vae_causal_decoder_args)
+  O(vae_causal_decoder_args, mid) O(vae_causal_decoder_args, ups)
+  O(vae_causal_decoder_args, conv_out) O(vae_causal_decoder_args, precision)
   return 0;
 }
 """
@@ -79,7 +81,8 @@ def test_ctypes_struct_layout_matches_c(tmp_path):
     m = {"vae_conv_ref": pkg.ConvRef, "vae_norm_ref": pkg.NormRef,
          "vae_resnet_ref": pkg.ResnetRef, "vae_attn_ref": pkg.AttnRef,
          "vae_up_ref": pkg.UpRef, "vae_chain_args": pkg.ChainArgs,
-         "vae_prof_record": pkg.ProfRecord, "vae_trace_point": pkg.TracePoint}
+         "vae_prof_record": pkg.ProfRecord, "vae_trace_point": pkg.TracePoint,
+         "vae_causal_decoder_args": pkg.CausalDecoderArgs}
     for key, val in got.items():
         if "." in key:
             t, f = key.split(".")

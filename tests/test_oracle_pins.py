@@ -550,3 +550,84 @@ def test_tiled_decode_with_one_tile_is_the_decode():
     ref = O.decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
     got = O.tiled_decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4, tile=64, min_overlap=16)
     np.testing.assert_array_equal(got, ref)
+
+
+# ------------------------------------------------------------------ 3-D causal decoder
+
+def _causal_conv_torch(x, w, b):
+    """torch restatement: replicate frame 0 twice in front, zero-pad space,
+    F.conv3d (cross-correlation)."""
+    xp = torch.cat([x[:, :, :1], x[:, :, :1], x], dim=2)
+    xp = F.pad(xp, (1, 1, 1, 1, 0, 0))
+    return F.conv3d(xp, _t(w), _t(b))
+
+
+def _causal_decode_torch(z, wts, n_up=4, n_mid=2, n_res=2):
+    def gs(x, pre):
+        return F.silu(F.group_norm(x, 32, _t(wts[pre + ".weight"]), _t(wts[pre + ".bias"]),
+                                   eps=1e-6))
+
+    def res(x, pre):
+        h = _causal_conv_torch(gs(x, pre + ".norm1"), wts[pre + ".conv1.weight"],
+                               wts[pre + ".conv1.bias"])
+        h = _causal_conv_torch(gs(h, pre + ".norm2"), wts[pre + ".conv2.weight"],
+                               wts[pre + ".conv2.bias"])
+        if pre + ".conv_shortcut.weight" in wts:
+            sw = _t(wts[pre + ".conv_shortcut.weight"])[:, :, :, :, None]
+            x = F.conv3d(x, sw, _t(wts[pre + ".conv_shortcut.bias"]))
+        return x + h
+
+    x = _t(z) / S.SCALING_FACTOR + S.SHIFT_FACTOR
+    x = _causal_conv_torch(x, wts["conv_in.weight"], wts["conv_in.bias"])
+    for m in range(n_mid):
+        x = res(x, f"mid.resnets.{m}")
+    for i in range(n_up):
+        for j in range(n_res):
+            x = res(x, f"up_blocks.{i}.resnets.{j}")
+        k = f"up_blocks.{i}.upsamplers.0.conv"
+        if k + ".weight" in wts:
+            x = F.interpolate(x, scale_factor=(1, 2, 2), mode="nearest")
+            x = _causal_conv_torch(x, wts[k + ".weight"], wts[k + ".bias"])
+    x = gs(x, "conv_norm_out")
+    return _causal_conv_torch(x, wts["conv_out.weight"], wts["conv_out.bias"]).numpy()
+
+
+def test_causal_decoder_vs_torch_restatement():
+    w = S.make_causal_decoder_weights("causal_tiny", 11)
+    z = S.make_latent((2, 16, 3, 3, 4), 11)
+    got = O.causal_decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
+    assert got.shape == (2, 3, 3, 24, 32)
+    np.testing.assert_allclose(got, _causal_decode_torch(z, w), atol=1e-10)
+
+
+def test_causal_decoder_single_frame_is_the_2d_decoder_with_summed_time_taps():
+    """With one frame every causal conv reads frame 0 through all three time
+    taps, so the decoder is the 2-D decoder (no attention) whose 3x3 kernels
+    are the 3x3x3 kernels summed over time: composed here from the pinned
+    2-D oracle functions."""
+    w = S.make_causal_decoder_weights("causal_tiny", 12)
+    z = S.make_latent((1, 16, 1, 4, 3), 12)
+    got = O.causal_decode(z, w, S.SCALING_FACTOR, S.SHIFT_FACTOR, 4)
+
+    def w2(name):
+        return np.asarray(w[name + ".weight"], np.float64).sum(axis=2), w[name + ".bias"]
+
+    def res2(x, pre):
+        p = {"norm1": (w[pre + ".norm1.weight"], w[pre + ".norm1.bias"]),
+             "norm2": (w[pre + ".norm2.weight"], w[pre + ".norm2.bias"]),
+             "conv1": w2(pre + ".conv1"), "conv2": w2(pre + ".conv2")}
+        if pre + ".conv_shortcut.weight" in w:
+            p["conv_shortcut"] = (w[pre + ".conv_shortcut.weight"], w[pre + ".conv_shortcut.bias"])
+        return O.resnet(x, p)
+
+    x = O.conv2d(O.denormalize(z[:, :, 0], S.SCALING_FACTOR, S.SHIFT_FACTOR), *w2("conv_in"))
+    for m in range(2):
+        x = res2(x, f"mid.resnets.{m}")
+    for i in range(4):
+        for j in range(2):
+            x = res2(x, f"up_blocks.{i}.resnets.{j}")
+        if f"up_blocks.{i}.upsamplers.0.conv.weight" in w:
+            x = O.upsample_conv(x, *w2(f"up_blocks.{i}.upsamplers.0.conv"))
+    x = O.group_norm_silu(x, w["conv_norm_out.weight"], w["conv_norm_out.bias"])
+    ref = O.conv2d(x, *w2("conv_out"))
+    np.testing.assert_allclose(got[:, :, 0], ref, atol=1e-10)

@@ -118,6 +118,62 @@ def make_decoder_weights(arch: str, seed: int) -> dict:
     return w
 
 
+# 3-D causal decoders (LTX-style structure, random init): block_out_channels
+# as for the 2-D decoder; latent channels; resnets in the mid block.
+CAUSAL_ARCHS = {
+    "causal_tiny": dict(channels=(32, 32, 64, 64), latent_channels=16, mid_resnets=2),
+    "causal_small": dict(channels=(64, 128, 256, 256), latent_channels=16, mid_resnets=2),
+}
+
+
+def _conv3(d, out, name, cout, cin):
+    out[name + ".weight"] = d.normal((cout, cin, 3, 3, 3), 1.0 / (cin * 27))
+    out[name + ".bias"] = d.normal((cout,), 0.01)
+
+
+def _resnet3(d, out, name, cin, cout):
+    _norm(d, out, name + ".norm1", cin)
+    _conv3(d, out, name + ".conv1", cout, cin)
+    _norm(d, out, name + ".norm2", cout)
+    _conv3(d, out, name + ".conv2", cout, cout)
+    if cin != cout:
+        _conv(d, out, name + ".conv_shortcut", cout, cin, 1)
+
+
+def causal_decoder_layout(arch: str):
+    """(reversed channels, up-block plan [(cin, cout, has_upsample)], latent
+    channels, mid resnets) of a 3-D causal decoder architecture."""
+    a = CAUSAL_ARCHS[arch]
+    rev = list(reversed(a["channels"]))
+    plan, prev = [], rev[0]
+    for i, c in enumerate(rev):
+        plan.append((prev, c, i < len(rev) - 1))
+        prev = c
+    return rev, plan, a["latent_channels"], a["mid_resnets"]
+
+
+def make_causal_decoder_weights(arch: str, seed: int, resnets_per_block: int = 2) -> dict:
+    """All tensors of a 3-D causal decoder (3x3x3 convs [cout, cin, 3, 3, 3],
+    1x1x1 shortcuts stored [cout, cin, 1, 1]), float32, diffusers-style names,
+    drawn in execution order with the 2-D decoder's init recipe (conv weights
+    N(0, 1/(Cin*27)))."""
+    d = _Drawer([seed, 8])
+    rev, plan, lc, n_mid = causal_decoder_layout(arch)
+    c0 = rev[0]
+    w: dict = {}
+    _conv3(d, w, "conv_in", c0, lc)
+    for m in range(n_mid):
+        _resnet3(d, w, f"mid.resnets.{m}", c0, c0)
+    for i, (cin, cout, up) in enumerate(plan):
+        for j in range(resnets_per_block):
+            _resnet3(d, w, f"up_blocks.{i}.resnets.{j}", cin if j == 0 else cout, cout)
+        if up:
+            _conv3(d, w, f"up_blocks.{i}.upsamplers.0.conv", cout, cout)
+    _norm(d, w, "conv_norm_out", rev[-1])
+    _conv3(d, w, "conv_out", 3, rev[-1])
+    return w
+
+
 def make_latent(shape, seed: int) -> np.ndarray:
     return _Drawer([seed, 1]).normal(shape, 1.0)
 
