@@ -161,27 +161,27 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
-def conv_traffic_from_profile(workload, path=None):
-    """DRAM bytes per launch of the implicit-GEMM conv in this workload, from
-    the committed machine-readable ncu summary (profiles/igemm_traffic.json:
-    dram__bytes_read.sum + dram__bytes_write.sum of one conv launch, with the
-    scale to this workload's average conv launch) -- None when the summary is
-    missing, has no entry for the workload, or was taken on a different
-    igemm.cu (the kernel has changed since the counters were read)."""
+def igemm_source_sha():
     import hashlib
+    src = b"".join(open(os.path.join(ROOT, "diffusion_vae_decoder_gb300", "csrc", f), "rb").read()
+                   for f in ("igemm.cu", "igemm_kernel.cuh"))
+    return hashlib.sha256(src).hexdigest()
+
+
+def conv_traffic_ratio(path=None):
+    """DRAM bytes over algorithmic bytes of the implicit-GEMM conv, from the
+    committed machine-readable ncu summary (profiles/igemm_traffic.json:
+    single launches at single-op sweep shapes) -- (None, None) when the
+    summary is missing or was taken on other kernel source (the kernel has
+    changed since the counters were read)."""
     path = path or os.path.join(ROOT, "profiles", "igemm_traffic.json")
-    src = os.path.join(ROOT, "diffusion_vae_decoder_gb300", "csrc", "igemm.cu")
     if not os.path.exists(path):
         return None, None
     with open(path) as f:
         data = json.load(f)
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != data.get("igemm_cu_sha256"):
-            return None, None
-    entry = data.get("workloads", {}).get(workload)
-    if not entry:
+    if data.get("igemm_sha256") != igemm_source_sha():
         return None, None
-    return float(entry["bytes_per_launch"]), entry
+    return float(data["dram_over_algorithmic"]), data
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -398,7 +398,19 @@ def run_ours(args):
     barrier(dist)
     e2e_value = world * mpix / (e2e_ms / 1e3)
 
-    traffic, traffic_entry = conv_traffic_from_profile(args.workload)
+    # DRAM traffic per conv launch: the decode's algorithmic bytes per conv
+    # launch (input, output, residual, shortcut input once) times the
+    # DRAM/algorithmic ratio ncu measured on single launches of this kernel.
+    ratio, traffic_src = conv_traffic_ratio()
+    conv_launches = sum(r["kernels"] for r in conv)
+    alg_per_launch = sum(r["bytes"] for r in conv) / max(conv_launches, 1)
+    traffic = alg_per_launch * ratio if ratio else None
+    traffic_entry = None
+    if traffic_src:
+        traffic_entry = {"dram_over_algorithmic": ratio,
+                         "algorithmic_bytes_per_launch": alg_per_launch,
+                         "conv_launches_per_decode": conv_launches,
+                         "captures": [c["shape"] for c in traffic_src["captures"]]}
     extras = None
     if rank == 0 and world == 1 and not args.no_extras:
         extras = run_extras(pkg, tf32_peak, gpu_index)

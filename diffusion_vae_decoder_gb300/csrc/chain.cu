@@ -427,10 +427,15 @@ int run_conv(Chain &ch, const ConvW &c, const float *in, int n, int h, int w,
              cudaStream_t s, bool upsample = false, bool nchw_out = false,
              Stats *st = nullptr, float *part = nullptr, int groups = 0,
              float *split = nullptr) {
-  const long long out_px =
-      static_cast<long long>(n) * ch.frames * h * w * (upsample ? 4 : 1);
+  const long long in_px = static_cast<long long>(n) * ch.frames * h * w;
+  const long long out_px = in_px * (upsample ? 4 : 1);
+  // algorithmic bytes: the input, the output, a residual and a shortcut
+  // input, each moved once
+  const double bytes = 4.0 * (static_cast<double>(in_px) * c.cin + out_px * c.cout +
+                              (residual ? static_cast<double>(out_px) * c.cout : 0.0) +
+                              (c.sc_cin ? static_cast<double>(out_px) * c.sc_cin : 0.0));
   Step step(ch.prof, upsample ? VAE_PROF_UPSAMPLE_CONV : VAE_PROF_CONV3X3,
-            conv_flops(c, out_px), 0, s);
+            conv_flops(c, out_px), bytes, s);
   IgemmDesc d;
   d.mode = upsample ? AMode::Upsample : AMode::Conv;
   d.a = in;

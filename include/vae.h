@@ -399,9 +399,11 @@ VAE_API int vae_decode_causal(void *handle, const float *z, int n, int t, int h,
  * event-record nodes of the graph: every replay re-records them, and a read
  * after replays returns the last replay's times. */
 typedef enum {
-  VAE_PROF_CONV3X3 = 0,        /* 3x3 conv (flops: 2*cin*cout*9 per output pixel, + shortcut) */
+  VAE_PROF_CONV3X3 = 0,        /* 3x3 conv (flops: 2*cin*cout*9 per output pixel, + shortcut;
+                                  bytes: input, output, residual and shortcut input once)     */
   VAE_PROF_UPSAMPLE_CONV = 1,  /* nearest-2x upsample + 3x3 conv (flops executed: 2*cin*cout*4
-                                  per output pixel, four parity 2x2 kernels)                  */
+                                  per output pixel, four parity 2x2 kernels; bytes: low-res
+                                  input and output once)                                      */
   VAE_PROF_GROUPNORM = 2,      /* GroupNorm(+SiLU) (bytes: 8 per element, read + write, when
                                   the producing conv supplied the statistics; 12 otherwise)    */
   VAE_PROF_ATTENTION = 3,      /* mid attention block (flops: 4*L*L*c + 8*L*c*c per image)   */

@@ -63,21 +63,15 @@ def test_reference_arm_prints_one_json_line():
 
 def test_conv_traffic_is_read_only_for_the_kernel_it_was_captured_on(tmp_path):
     """The roofline's DRAM traffic comes from a machine-readable ncu summary
-    that records the sha256 of igemm.cu at capture: it is used only while
-    igemm.cu is that file, and only for the workloads it lists."""
-    import hashlib
+    that records the sha256 of the conv kernel's source at capture: it is
+    used only while the source is that file."""
     sys.path.insert(0, ROOT)
     import bench
-    src = os.path.join(ROOT, "diffusion_vae_decoder_gb300", "csrc", "igemm.cu")
-    current = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    entry = {"bytes_per_launch": 5.5e8, "capture": "one launch"}
     path = tmp_path / "traffic.json"
-    path.write_text(json.dumps({"igemm_cu_sha256": current,
-                                "workloads": {"decoder_1024": entry}}))
-    assert bench.conv_traffic_from_profile("decoder_1024", str(path)) == (5.5e8, entry)
-    assert bench.conv_traffic_from_profile("decoder_256", str(path)) == (None, None)
-    path.write_text(json.dumps({"igemm_cu_sha256": "0" * 64,
-                                "workloads": {"decoder_1024": entry}}))
-    assert bench.conv_traffic_from_profile("decoder_1024", str(path)) == (None, None)
-    assert bench.conv_traffic_from_profile("decoder_1024", str(tmp_path / "none.json")) == \
-        (None, None)
+    path.write_text(json.dumps({"igemm_sha256": bench.igemm_source_sha(),
+                                "dram_over_algorithmic": 0.95, "captures": []}))
+    assert bench.conv_traffic_ratio(str(path))[0] == 0.95
+    path.write_text(json.dumps({"igemm_sha256": "0" * 64, "dram_over_algorithmic": 0.95,
+                                "captures": []}))
+    assert bench.conv_traffic_ratio(str(path)) == (None, None)
+    assert bench.conv_traffic_ratio(str(tmp_path / "none.json")) == (None, None)
