@@ -136,26 +136,32 @@ long long tiles_per_image(const IgemmDesc &d, int rows) {
   return t;
 }
 
-// Whether a conv runs as paired-CTA tiles (Cfg, PAIR): 256-channel tiles of
-// the pixel-major modes, outside the split-K regime, when the pairs'
-// 256-row tiles (about 0.8 of a 1-SM tile's time each: shared memory stops
-// being the bound) finish sooner than 1-SM 128-row tiles, counting the
-// stream-K balance the 1-SM path would get. (128-channel convs stay on the
-// 1-SM channel-major tiles: paired halo tiles of 128 channels, one or two
-// rows per CTA, measured 5-10 % slower on the 1024^2 layers.)
+// Whether a launch runs as paired-CTA tiles (Cfg, PAIR): 256-column tiles of
+// the pixel-major conv modes and of the GEMM mode, outside the split-K
+// regime, when the pairs' 256-row tiles (about 0.8 of a 1-SM tile's time
+// each: shared memory stops being the bound) finish sooner than 1-SM
+// 128-row tiles, counting the stream-K balance the 1-SM conv path would get.
+// (128-channel convs stay on the 1-SM channel-major tiles: paired halo tiles
+// of 128 channels, one or two rows per CTA, measured 5-10 % slower on the
+// 1024^2 layers.)
 bool use_pair(const IgemmDesc &d) {
   const int setting = pair_setting();
   if (setting == 0) return false;
-  if (!(d.mode == AMode::Conv || d.mode == AMode::Upsample) || pick_bn(d.cout) != 256) return false;
+  if (pick_bn(d.cout) != 256) return false;
   const int sms = num_sms();
   if (sms < 2) return false;
   if (setting == 2) return true;
   const long long n_tiles = ceil_div(d.cout, 256);
-  const long long tiles1 = static_cast<long long>(d.imgs) * tiles_per_image(d, kBM) * n_tiles;
-  const long long tiles2 = static_cast<long long>(d.imgs) * tiles_per_image(d, 2 * kBM) * n_tiles;
+  const bool gemm = d.mode == AMode::Gemm;
+  const long long tiles1 = gemm ? ceil_div(d.M, kBM) * n_tiles
+                                : static_cast<long long>(d.imgs) * tiles_per_image(d, kBM) * n_tiles;
+  const long long tiles2 = gemm ? ceil_div(d.M, 2 * kBM) * n_tiles
+                                : static_cast<long long>(d.imgs) * tiles_per_image(d, 2 * kBM) *
+                                      n_tiles;
   if (tiles1 * 5 < static_cast<long long>(sms) * 3) return false;  // split-K regime
   const double r1 = static_cast<double>(tiles1) / sms;
-  const double est1 = r1 / std::ceil(r1) < 0.9 ? r1 : std::ceil(r1);  // stream-K or whole rounds
+  // stream-K balance (convs only) or whole rounds
+  const double est1 = !gemm && r1 / std::ceil(r1) < 0.9 ? r1 : std::ceil(r1);
   const double est2 = 0.8 * std::ceil(static_cast<double>(tiles2) / (sms / 2));
   return est2 <= est1;
 }
@@ -210,7 +216,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   if (d.mode == AMode::Gemm) {
     if (d.kdim <= 0 || d.kdim % 32 || d.M <= 0 || d.lda % 4) return VAE_EINVAL;
     kp.M = d.M;
-    kp.m_tiles = ceil_div(d.M, kBM);
+    kp.m_tiles = ceil_div(d.M, pair ? 2 * kBM : kBM);  // paired tiles: 256 rows
     kp.taps = 1;
     kp.cin_chunks = d.kdim / 32;
     kp.cin_pad = d.kdim;
@@ -473,7 +479,10 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
       rc = pair ? launch_typed<256, 1, 1, true>(ta, tb, ts, to, tr, kp, stream)
                 : launch_mode<1>(bn, ta, tb, ts, to, tr, kp, stream);
       break;
-    default: rc = launch_mode<2>(bn, ta, tb, ts, to, tr, kp, stream); break;
+    default:
+      rc = pair ? launch_typed<256, 2, 1, true>(ta, tb, ts, to, tr, kp, stream)
+                : launch_mode<2>(bn, ta, tb, ts, to, tr, kp, stream);
+      break;
   }
   if (rc != VAE_OK || kp.splits == 1) return rc;
   // Split-K: fixed-order reduce + epilogue (+ GroupNorm partials of the output).

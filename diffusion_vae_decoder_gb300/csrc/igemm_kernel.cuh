@@ -134,8 +134,8 @@ template <int BN, int MS, int MODE = 0, bool PAIR = false, bool SPLIT = false>
 struct Cfg {
   static constexpr bool HALO = MODE == 3;
   static constexpr bool SWAP = MODE == 4;
-  static_assert(!PAIR || (MS == 1 && BN == 256 && (MODE == 0 || MODE == 1 || MODE == 3)),
-                "paired tiles: 256 channels, pixel-major conv modes");
+  static_assert(!PAIR || (MS == 1 && BN == 256 && MODE <= 3),
+                "paired tiles: 256 output columns, the pixel-major conv modes and GEMM");
   static_assert(!SPLIT || (!PAIR && MODE <= 2), "split products: per-step A and B stages");
   static constexpr int THREADS = SPLIT ? kThreads + 128 : kThreads;
   // Separately buffered A operand (MODES 3 and 4): two buffers, each serving
@@ -536,8 +536,13 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
                    ty * p.bh + yoff + (par >> 1) - 1 + (tap >> 1), img);
             load_b(b_dst, stage, tap * p.cin_pad + cc * 32, par * p.cout + n0);
           } else {
-            tma_load_2d(a_dst, &tmA, &full[stage], ks * 32, mt * kBM);
-            tma_load_2d(b_dst, &tmB, &full[stage], ks * 32, n0);
+            // (a paired CTA loads its own 128 of the tile's rows)
+            const int arow = mt * C::ROWS * kBM + static_cast<int>(rank) * kBM;
+            if constexpr (PAIR)
+              tma_load_2d_pair(a_dst, &tmA, full_c + stage * 8, ks * 32, arow);
+            else
+              tma_load_2d(a_dst, &tmA, &full[stage], ks * 32, arow);
+            load_b(b_dst, stage, ks * 32, n0);
           }
           pending |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
@@ -916,9 +921,9 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
       long long cstride = 0;  // NCHW: distance between channels
       int bc1 = 0, bc2 = 0, bc3 = 0, bc4 = 0;  // this warp's TMA box coordinates
       if (MODE == 2) {
-        row = static_cast<long long>(mt) * kBM + msub;
+        row = static_cast<long long>(mt) * C::ROWS * kBM + msub;
         valid = row < p.M;
-        bc1 = mt * kBM + q * 32;
+        bc1 = mt * C::ROWS * kBM + sg * kBM + q * 32;
       } else {
         const int per_img = p.tiles_x * p.tiles_y * (MODE == 1 ? 4 : 1);
         const int img = mt / per_img;

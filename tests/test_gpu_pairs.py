@@ -5,8 +5,9 @@ replaces).
 
 The default picks paired tiles by an estimate of which finishes first, so
 the small exact-integer shapes of test_gpu_ops.py run on 1-SM tiles and the
-full-size parity tests on paired ones. Here the exact-integer tests are run
-again with VAE_PAIR=force (every 256-channel conv and upsample conv paired:
+full-size parity tests on paired ones. Here the exact-integer and attention
+tests are run again with VAE_PAIR=force (every 256-column conv, upsample
+conv and attention GEMM paired, ragged GEMM rows included:
 per-tap staging with the appended 1x1 shortcut and the in-place residual,
 halo staging, the upsample parities, ragged rows where one CTA of a pair
 holds only rows outside the image), and the full-size sweep again with
@@ -37,7 +38,8 @@ def _child_pytest(setting, args):
 
 def test_exact_integer_convs_on_forced_pairs():
     _child_pytest("force", ["tests/test_gpu_ops.py", "-k",
-                            "exact_integer or shortcut_and_residual or causal_float"])
+                            "exact_integer or shortcut_and_residual or causal_float or "
+                            "mid_attn_parity or growing_scores"])
 
 
 def test_full_size_sweep_on_single_sm_tiles():
