@@ -104,10 +104,16 @@ struct Profiler {
       if (cudaEventCreate(&e) != cudaSuccess) return -1;
       events.push_back(e);
     }
-    // External record: inside a stream capture this becomes an event-record
-    // node of the graph, so every replay re-records it.
-    if (cudaEventRecordWithFlags(events[next], s, cudaEventRecordExternal) != cudaSuccess)
-      return -1;
+    // Inside a stream capture an external record becomes an event-record
+    // node of the graph, so every replay re-records it; outside one that
+    // flag is refused (and would linger as the thread's last error), so a
+    // plain record.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return -1;
+    const cudaError_t e = cap == cudaStreamCaptureStatusActive
+                              ? cudaEventRecordWithFlags(events[next], s, cudaEventRecordExternal)
+                              : cudaEventRecord(events[next], s);
+    if (e != cudaSuccess) return -1;
     return next++;
   }
   // Opens a step; returns its record index, or -1 when profiling is off.
@@ -403,6 +409,7 @@ DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, 
   d.attn.vt = cv.take<float>(static_cast<size_t>(c) * lp);
   d.attn.s = cv.take<float>(static_cast<size_t>(p.attn_l) * lp);
   d.attn.o = cv.take<float>(nl * c);
+  d.attn.rs = cv.take<float>(attn_rs_floats(p.attn_l));
   d.gn = cv.take<char>(groupnorm_ws_bytes(n, p.max_c, 1, ch.groups));
   d.attn.gn = d.gn;
   return d;
@@ -426,7 +433,8 @@ int run_conv(Chain &ch, const ConvW &c, const float *in, int n, int h, int w,
              const float *sc_in, const float *residual, float *out, int round_out,
              cudaStream_t s, bool upsample = false, bool nchw_out = false,
              Stats *st = nullptr, float *part = nullptr, int groups = 0,
-             float *split = nullptr) {
+             float *split = nullptr, const float *gn_scale = nullptr,
+             const float *gn_shift = nullptr) {
   const long long in_px = static_cast<long long>(n) * ch.frames * h * w;
   const long long out_px = in_px * (upsample ? 4 : 1);
   // algorithmic bytes: the input, the output, a residual and a shortcut
@@ -460,6 +468,8 @@ int run_conv(Chain &ch, const ConvW &c, const float *in, int n, int h, int w,
   d.round_out = ch.exact ? 0 : round_out;  // split-TF32 operands stay FP32
   d.split_ws = split;
   d.split_ws_floats = split ? kSplitWsFloats : 0;
+  d.gn_scale = gn_scale;  // the input's GroupNorm+SiLU, applied in the kernel
+  d.gn_shift = gn_shift;
   int fused = 0;
   long long slots = 0;
   if (st) {
@@ -492,25 +502,75 @@ int run_gn(Chain &ch, const NormW &nw, const float *in, int n, long long sp, flo
                         ws.gn, s);
 }
 
+// Whether conv `c` over w-pixel rows applies its input's GroupNorm+SiLU
+// itself (on the halo it stages; opt-in, see igemm_input_gn_ok), so that
+// only the normalisation's per-(sample, channel) affine is computed
+// beforehand.
+bool gn_folds_into(const Chain &ch, const ConvW &c, int w) {
+  IgemmDesc d;
+  d.mode = AMode::Conv;
+  d.k = c.k;
+  d.kt = c.kt;
+  d.win = w;
+  d.cout = c.cout;
+  d.sc_c = c.sc_cin;
+  d.precise = ch.exact ? 1 : 0;
+  return igemm_input_gn_ok(d);
+}
+
+// The GroupNorm+SiLU of `in` that conv `c` reads: either applied here into
+// ws.T (*act = ws.T), or reduced to its affine in ws.ss for the conv to apply
+// (*act = in; *scale / *shift set). A trace still receives the normalised
+// tensor.
+int run_gn_for(Chain &ch, const NormW &nw, const ConvW &c, const float *in, int n, int w,
+               long long sp, const DecodeWs &ws, const Stats &st, const float **act,
+               const float **scale, const float **shift, cudaStream_t s) {
+  *scale = *shift = nullptr;
+  *act = in;
+  const size_t bytes = 4ull * n * sp * nw.c;
+  if (!gn_folds_into(ch, c, w)) {
+    VAE_TRY(run_gn(ch, nw, in, n, sp, ws.T, ws, st, s));
+    if (ch.tr) ch.tr->emit(ws.T, bytes, s);
+    *act = ws.T;
+    return VAE_OK;
+  }
+  float *sc = ws.ss, *sh = ws.ss + static_cast<size_t>(n) * nw.c;
+  {
+    // bytes: the statistics pass over the input when they were not fused
+    // into its producer, else only the partials
+    Step step(ch.prof, VAE_PROF_GROUPNORM, 0,
+              st.ready ? 12.0 * n * ch.groups * st.slots : 4.0 * n * sp * nw.c, s);
+    VAE_TRY(groupnorm_scale_shift(in, n, nw.c, sp, ch.groups, ch.eps, nw.g, nw.b,
+                                  st.ready ? ws.part : nullptr, st.slots, sc, sh, ws.gn, s,
+                                  ws.gn_cnt));
+  }
+  if (ch.tr) {
+    VAE_TRY(groupnorm_apply(in, n, nw.c, sp, sc, sh, 1, !ch.exact, ws.T, s));
+    ch.tr->emit(ws.T, bytes, s);
+  }
+  *scale = sc;
+  *shift = sh;
+  return VAE_OK;
+}
+
 // One resnet on NHWC data; `st` holds the statistics of `in` on entry and
 // those of `out` on return.
 int run_resnet(Chain &ch, const ResW &r, const float *in, float *out, const DecodeWs &ws, int n,
                int h, int w, int round_out, Stats &st, cudaStream_t s) {
   const long long sp = static_cast<long long>(h) * w * ch.frames;  // GroupNorm extent
-  const size_t in_bytes = 4ull * n * sp * r.c1.cin, out_bytes = 4ull * n * sp * r.c1.cout;
-  VAE_TRY(run_gn(ch, r.n1, in, n, sp, ws.T, ws, st, s));
-  if (ch.tr) ch.tr->emit(ws.T, in_bytes, s);
-  VAE_TRY(run_conv(ch, r.c1, ws.T, n, h, w, nullptr, nullptr, ws.H, 0, s, false, false, &st,
-                   ws.part, ch.groups, ws.split));
+  const size_t out_bytes = 4ull * n * sp * r.c1.cout;
+  const float *a1, *a2, *gsc, *gsh;
+  VAE_TRY(run_gn_for(ch, r.n1, r.c1, in, n, w, sp, ws, st, &a1, &gsc, &gsh, s));
+  VAE_TRY(run_conv(ch, r.c1, a1, n, h, w, nullptr, nullptr, ws.H, 0, s, false, false, &st,
+                   ws.part, ch.groups, ws.split, gsc, gsh));
   if (ch.tr) ch.tr->emit(ws.H, out_bytes, s);
-  VAE_TRY(run_gn(ch, r.n2, ws.H, n, sp, ws.T, ws, st, s));
-  if (ch.tr) ch.tr->emit(ws.T, out_bytes, s);
+  VAE_TRY(run_gn_for(ch, r.n2, r.c2, ws.H, n, w, sp, ws, st, &a2, &gsc, &gsh, s));
   if (r.c2.sc_cin)
-    VAE_TRY(run_conv(ch, r.c2, ws.T, n, h, w, in, nullptr, out, round_out, s, false, false,
-                     &st, ws.part, ch.groups, ws.split));
+    VAE_TRY(run_conv(ch, r.c2, a2, n, h, w, in, nullptr, out, round_out, s, false, false,
+                     &st, ws.part, ch.groups, ws.split, gsc, gsh));
   else
-    VAE_TRY(run_conv(ch, r.c2, ws.T, n, h, w, nullptr, in, out, round_out, s, false, false,
-                     &st, ws.part, ch.groups, ws.split));
+    VAE_TRY(run_conv(ch, r.c2, a2, n, h, w, nullptr, in, out, round_out, s, false, false,
+                     &st, ws.part, ch.groups, ws.split, gsc, gsh));
   if (ch.tr) ch.tr->emit(out, out_bytes, s);
   return VAE_OK;
 }

@@ -11,11 +11,15 @@
 
 namespace vae {
 
-#define VAE_CUDA_TRY(expr)                              \
-  do {                                                  \
-    cudaError_t e__ = (expr);                           \
-    if (e__ != cudaSuccess) return VAE_ECUDA;           \
+// True when e is an error; with VAE_VERBOSE=1 in the environment the error
+// and the call site go to stderr.
+bool cuda_failed(cudaError_t e, const char *file, int line);
+#define VAE_CUDA_TRY(expr)                                         \
+  do {                                                             \
+    if (::vae::cuda_failed((expr), __FILE__, __LINE__)) return VAE_ECUDA; \
   } while (0)
+// After a kernel launch: the launch's own error (configuration, resources).
+#define VAE_LAUNCH_CHECK() VAE_CUDA_TRY(cudaGetLastError())
 
 #define VAE_TRY(expr)                                   \
   do {                                                  \
@@ -114,7 +118,38 @@ struct IgemmDesc {
   // product is formed as a_hi b_hi + a_lo b_hi + a_hi b_lo with each part
   // rounded to TF32 (three MMAs per step, about FP32 accuracy).
   int precise = 0;
+  // Optional GroupNorm (+SiLU) of the A operand applied inside the kernel
+  // (Conv; only where igemm_input_gn_ok(d)): a -> silu(a * gn_scale[s][c] +
+  // gn_shift[s][c]), TF32-rounded, zero padding outside the image, with
+  // s = image / t and [s][a_c] arrays. Replaces a separate normalisation pass
+  // over the conv's input.
+  const float *gn_scale = nullptr, *gn_shift = nullptr;
+  int gn_silu = 1;
+  // Gemm (only where igemm_softmax_a_ok(d)): A holds raw scores s and the MMA
+  // reads the row softmax p = exp(s * sm_scale - sm_m[row]) * sm_inv_l[row],
+  // 0 for columns >= sm_cols.
+  const float *sm_m = nullptr, *sm_inv_l = nullptr;
+  float sm_scale = 1.0f;
+  int sm_cols = 0;
+  // Gemm: per row and column tile of igemm_col_tile(cout) columns, the
+  // softmax statistics of the stored values v (max of v * rs_scale over the
+  // columns < rs_cols, and the sum of exp(v * rs_scale - max)), at
+  // rs_out[row * rs_ld + column tile]; (-inf, 0) for a tile with no valid
+  // column.
+  float2 *rs_out = nullptr;
+  float rs_scale = 1.0f;
+  int rs_cols = 0, rs_ld = 0;
 };
+// Output-channel (column) tile of a launch with `cout` columns.
+int igemm_col_tile(int cout);
+// Whether igemm_launch applies an input GroupNorm (gn_scale) for this
+// descriptor: 3x3 single-frame convs whose 256-channel tiles stage a halo
+// of input rows at least 65 pixels wide, without shortcut operand or
+// split-TF32 products. Both transforms are opt-in (VAE_FUSE=on; slower than
+// the separate passes on GB300) and these return false without it.
+bool igemm_input_gn_ok(const IgemmDesc &d);
+// Whether igemm_launch takes a softmax-normalised A (sm_m) for this GEMM.
+bool igemm_softmax_a_ok(const IgemmDesc &d);
 // Split-K reduce (splitk.cu): out = alpha * sum of the partials + bias
 // (+ residual), rounded on request; GroupNorm partials [samples][groups][slots]
 // of the result when stat_part is given (*stat_slots receives slots, 0 if none).
@@ -186,6 +221,11 @@ int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int g
                           long long slots, float *scale, float *shift, void *ws, cudaStream_t s,
                           unsigned *counters = nullptr);
 
+// y = act(x * scale[s][c] + shift[s][c]) over NHWC x [n][spatial][c]
+// (act = SiLU when silu), TF32-rounded when round_out.
+int groupnorm_apply(const float *x, int n, int c, long long spatial, const float *scale,
+                    const float *shift, int silu, int round_out, float *y, cudaStream_t s);
+
 // Fused norm_out GroupNorm+SiLU + conv_out (3x3, cout <= 4) on the CUDA cores
 // (head.cu): x NHWC [n][h][w][c], y NCHW [n][cout][h][w].
 bool head_supported(int cin, int cout, int k);
@@ -205,5 +245,10 @@ int flash_attention(const float *q, const float *k, int ld, const float *vt, int
 // unless round == 0.
 int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st,
                  int round = 1);
+// Per-row softmax statistics from the per-column-tile pairs a GEMM epilogue
+// wrote (IgemmDesc::rs_out: part[row * ld + tile] = (max, sum of exp(v -
+// max))): m[row] = the row max, inv_l[row] = 1 / the row's sum of exp(v - m).
+int softmax_merge_stats(const float2 *part, int rows, int tiles, int ld, float *m, float *inv_l,
+                        cudaStream_t st);
 
 }  // namespace vae

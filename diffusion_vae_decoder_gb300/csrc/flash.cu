@@ -358,7 +358,7 @@ int launch_flash(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap
   });
   if (attr != cudaSuccess) return VAE_ECUDA;
   flash_kernel<DH><<<dim3(qtiles, slices), kFThreads, kFlashSmem, s>>>(tq, tk, tv, fp);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }

@@ -509,10 +509,10 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
     gn_stats_nchw<<<dim3(nblk, n * groups), kStatThreads, 0, s>>>(x, c, spatial, groups, nblk,
                                                                    part);
   }
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   gn_finalize<double><<<n * groups, kFinalizeThreads, 0, s>>>(part, nblk, c, groups, eps, gamma,
                                                                beta, scale, shift);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   const long long total = static_cast<long long>(n) * c * spatial;
   const int threads = 256;
   if (nhwc) {
@@ -522,7 +522,7 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
     gn_apply_nchw<<<static_cast<int>(g), threads, 0, s>>>(x, total, c, spatial, scale, shift,
                                                           silu, round_out, y);
   }
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(3);
   return VAE_OK;
 }
@@ -542,14 +542,14 @@ int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int g
     gn_compact_finalize<<<dim3(kCompactSlots, static_cast<unsigned>(n * groups)),
                           kCompactThreads, 0, s>>>(part, slots, compact, counters, c, groups,
                                                    eps, gamma, beta, scale, shift);
-    if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+    VAE_LAUNCH_CHECK();
     count_launches(1);
     return VAE_OK;
   }
   if (part) {
     gn_finalize<float><<<n * groups, kFinalizeThreads, 0, s>>>(part, slots, c, groups, eps, gamma, beta,
                                                   scale, shift);
-    if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+    VAE_LAUNCH_CHECK();
     count_launches(1);
     return VAE_OK;
   }
@@ -560,11 +560,21 @@ int groupnorm_scale_shift(const float *x, int n, int c, long long spatial, int g
   const int tpp = c / 4, ppi = kStatThreads / tpp;
   const size_t sm = static_cast<size_t>(ppi) * c * 3 * sizeof(float);
   gn_stats_nhwc<<<dim3(nblk, n), kStatThreads, sm, s>>>(x, c, spatial, groups, nblk, dpart);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   gn_finalize<double><<<n * groups, kFinalizeThreads, 0, s>>>(dpart, nblk, c, groups, eps, gamma, beta,
                                                  scale, shift);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(2);
+  return VAE_OK;
+}
+
+int groupnorm_apply(const float *x, int n, int c, long long spatial, const float *scale,
+                    const float *shift, int silu, int round_out, float *y, cudaStream_t s) {
+  if (!x || !y || !scale || !shift || n <= 0 || c <= 0 || spatial <= 0) return VAE_EINVAL;
+  if (c % 4 || c > 1024) return VAE_EUNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) return VAE_EINVAL;
+  VAE_TRY(launch_apply_nhwc(x, n, c, spatial, scale, shift, silu, round_out, nullptr, y, s));
+  count_launches(1);
   return VAE_OK;
 }
 
@@ -587,7 +597,7 @@ int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int
     gn_apply_fused_nhwc<<<dim3(static_cast<unsigned>(g), n), 256, 0, s>>>(
         x, static_cast<unsigned>(per4), c, part, static_cast<int>(slots), groups, eps, gamma,
         beta, silu, round_out, residual, y);
-    if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+    VAE_LAUNCH_CHECK();
     count_launches(1);
     return VAE_OK;
   }
@@ -600,7 +610,7 @@ int groupnorm_from_partials(const float *x, int n, int c, long long spatial, int
   gn_compact_finalize<<<dim3(kCompactSlots, static_cast<unsigned>(n * groups)),
                         kCompactThreads, 0, s>>>(part, slots, compact, counters, c, groups, eps,
                                                  gamma, beta, scale, shift);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   VAE_TRY(launch_apply_nhwc(x, n, c, spatial, scale, shift, silu, round_out, residual, y, s));
   count_launches(2);
   return VAE_OK;

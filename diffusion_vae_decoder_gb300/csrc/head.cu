@@ -182,7 +182,7 @@ int head_pack_weights(const float *w, int cout, int cin, float *dst, cudaStream_
   if (!head_supported(cin, cout, 3)) return VAE_EUNSUPPORTED;
   const int total = cin * 9 * 4;
   head_pack_kernel<<<(total + 255) / 256, 256, 0, s>>>(w, cout, cin, dst);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }

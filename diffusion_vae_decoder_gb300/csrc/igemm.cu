@@ -174,6 +174,42 @@ long long stat_slots_for(const IgemmDesc &d, bool pair) {
 
 }  // namespace
 
+int igemm_col_tile(int cout) { return pick_bn(cout); }
+
+// The operand transforms (input GroupNorm, softmax A) run only with
+// VAE_FUSE=on. Measured on GB300 they lose to the separate passes: the
+// GroupNorm+SiLU of a halo buffer sits between its copy and the MMAs of a
+// two-buffer ring, so the 128^2 x 512-channel conv goes from 0.103 to 0.218
+// ms (0.113 ms with the transform's arithmetic removed), while the separate
+// apply pass it replaces costs about 0.035 ms; the softmax-normalised P.V
+// GEMM takes 1.2 ms even with an empty transform (0.3 ms plain) and the
+// statistics epilogue adds about 0.25 ms to the score GEMM, against the
+// 0.3 ms row-softmax pass.
+bool operand_transforms_enabled() {
+  static const bool v = [] {
+    const char *e = std::getenv("VAE_FUSE");
+    return e && std::strcmp(e, "on") == 0;
+  }();
+  return v;
+}
+
+// The halo-staged path (see igemm_launch), less its no-split-K condition:
+// a launch with an input GroupNorm never splits K.
+bool halo_candidate(const IgemmDesc &d, bool split) {
+  return !split && d.mode == AMode::Conv && d.k == 3 && d.kt == 1 &&
+         pow2_at_least(d.win) >= 128 && pick_bn(d.cout) == 256 && !d.sc && d.sc_c == 0 &&
+         buffered_a_enabled();
+}
+
+bool igemm_input_gn_ok(const IgemmDesc &d) {
+  return operand_transforms_enabled() && halo_candidate(d, d.precise || split_forced());
+}
+
+bool igemm_softmax_a_ok(const IgemmDesc &d) {
+  return operand_transforms_enabled() && d.mode == AMode::Gemm && !d.precise &&
+         !split_forced() && pick_bn(d.cout) == 256;
+}
+
 // Upper bound over the tile geometries a launch may take (callers size the
 // partials buffer with it; the launch reports the stride it used).
 long long igemm_stat_slots(const IgemmDesc &d) {
@@ -193,6 +229,13 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // split, for tests); they run on per-step A and B stages only.
   const bool split = d.precise || split_forced();
   const bool pair = !split && use_pair(d);
+  // operand transforms: only on the paths that implement them
+  const int xf = d.gn_scale ? 1 : d.sm_m ? 2 : 0;
+  if (d.gn_scale && d.sm_m) return VAE_EINVAL;
+  if (xf == 1 && (!igemm_input_gn_ok(d) || !d.gn_shift)) return VAE_EUNSUPPORTED;
+  if (xf == 2 && (!igemm_softmax_a_ok(d) || !d.sm_inv_l || d.sm_cols <= 0)) return VAE_EUNSUPPORTED;
+  if (d.rs_out && (d.mode != AMode::Gemm || d.rs_ld < ceil_div(d.cout, bn) || d.rs_cols <= 0))
+    return VAE_EINVAL;
   KParams kp{};
   kp.err = device_error_word();
   if (!kp.err) return VAE_ECUDA;
@@ -210,6 +253,19 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   kp.t = d.t > 0 ? d.t : 1;
   kp.imgs = d.imgs;
   kp.n_tiles = ceil_div(d.cout, bn);
+  kp.gn_scale = d.gn_scale;
+  kp.gn_shift = d.gn_shift;
+  kp.gn_silu = d.gn_silu;
+  kp.sm_m = d.sm_m;
+  kp.sm_inv_l = d.sm_inv_l;
+  kp.sm_scale = d.sm_scale;
+  kp.sm_cols = d.sm_cols;
+  kp.rs_out = d.rs_out;
+  kp.rs_scale = d.rs_scale;
+  kp.rs_cols = d.rs_cols;
+  kp.rs_ld = d.rs_ld;
+  if (xf == 1 && ((reinterpret_cast<uintptr_t>(d.gn_scale) | reinterpret_cast<uintptr_t>(d.gn_shift)) & 15))
+    return VAE_EINVAL;
 
   CUtensorMap ta{}, tb{}, ts{};
   int bkdim;
@@ -309,7 +365,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   const long long rows_total = d.mode == AMode::Gemm
                                    ? static_cast<long long>(d.M)
                                    : static_cast<long long>(d.imgs) * kp.hout * kp.wout;
-  if (!pair && d.split_ws && d.mode != AMode::Gemm && !d.out_nchw && d.cout % 4 == 0 &&
+  if (!pair && !xf && d.split_ws && d.mode != AMode::Gemm && !d.out_nchw && d.cout % 4 == 0 &&
       d.ldo == d.cout && !d.bias_per_row) {
     const int sms = num_sms();
     if (total * 5 < static_cast<long long>(sms) * 3) {
@@ -399,8 +455,8 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // to the per-tap path): 128-channel tiles (two 128-row sub-tiles), and
   // convs with an appended shortcut (with its tiles one or three to an A
   // buffer alike: 0.537 -> 0.607 ms on 512 -> 256 channels at 512^2).
-  const bool halo = !split && d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 && kp.bw == 128 &&
-                    kp.splits == 1 && bn == 256 && kp.sc_chunks == 0 && buffered_a_enabled();
+  const bool halo = halo_candidate(d, split) && kp.splits == 1;
+  if (xf == 1 && !halo) return VAE_EUNSUPPORTED;  // (not reached: no split-K with xf)
   // Channel-major tiles for 3x3 single-frame convs with 65-128 output
   // channels: the MMA runs M = 128 channels x N = 256 pixels (one wide
   // instruction where the pixel-major tile needs two 128 x 128 ones that both
@@ -465,6 +521,8 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   int rc;
   if (split) {
     rc = launch_split(static_cast<int>(d.mode), bn, ta, tb, ts, to, tr, kp, stream);
+  } else if (xf) {
+    rc = launch_xf(xf, pair, ta, tb, ts, to, tr, kp, stream);
   } else switch (d.mode) {
     case AMode::Conv:
       if (pair)

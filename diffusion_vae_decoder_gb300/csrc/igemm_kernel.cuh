@@ -64,6 +64,22 @@ struct KParams {
   int *err;
   uint64_t wait_ns;  // limit of every device-side wait (normally kWaitTimeoutNs)
   int inject;        // test hook: VAE_INJECT_* bits (0 in normal operation)
+  // XF = 1: GroupNorm (+SiLU) of the halo-staged input applied in shared
+  // memory before the MMAs: v -> silu(v * gn_scale[s][c] + gn_shift[s][c]),
+  // TF32-rounded, zero outside the image; s = image / t, [s][cin_pad].
+  const float *gn_scale, *gn_shift;
+  int gn_silu;
+  // XF = 2: the A stage holds raw attention scores s; the MMA reads
+  // p = exp(s * sm_scale - sm_m[row]) * sm_inv_l[row] (0 for keys >= sm_cols).
+  const float *sm_m, *sm_inv_l;
+  float sm_scale;
+  int sm_cols;
+  // GEMM epilogue (optional): per row and 256-column tile, the softmax
+  // statistics (max of v * rs_scale over the valid columns, and the sum of
+  // exp(v * rs_scale - max)) of the stored values, at rs_out[row * rs_ld + n tile].
+  float2 *rs_out;
+  float rs_scale;
+  int rs_cols, rs_ld;
 };
 
 // One work item of a CTA: a tile and the range [k0, k1) of its reduction
@@ -130,14 +146,22 @@ struct WorkIter {
 // split it in place into TF32 parts (hi = tf32(v), lo = tf32(v - hi), lo
 // stored beside hi) and the MMA issuer forms a_hi b_hi + a_lo b_hi + a_hi
 // b_lo (three MMAs per step) into the FP32 accumulator.
-template <int BN, int MS, int MODE = 0, bool PAIR = false, bool SPLIT = false>
+// XF: an operand transform by four more warps between the copy and the MMA
+// (1: GroupNorm+SiLU of the halo buffer, MODE 3; 2: softmax normalisation
+// of the GEMM A stage, MODE 2). Each CTA's copy lands on a barrier of its
+// own; the transforming warps of both CTAs of a pair then arrive on the
+// leader's barrier the MMA issuer waits on.
+template <int BN, int MS, int MODE = 0, bool PAIR = false, bool SPLIT = false, int XF = 0>
 struct Cfg {
   static constexpr bool HALO = MODE == 3;
   static constexpr bool SWAP = MODE == 4;
   static_assert(!PAIR || (MS == 1 && BN == 256 && MODE <= 3),
                 "paired tiles: 256 output columns, the pixel-major conv modes and GEMM");
   static_assert(!SPLIT || (!PAIR && MODE <= 2), "split products: per-step A and B stages");
-  static constexpr int THREADS = SPLIT ? kThreads + 128 : kThreads;
+  static_assert(XF == 0 || (!SPLIT && ((XF == 1 && MODE == 3) || (XF == 2 && MODE == 2 && MS == 1))),
+                "operand transforms: GroupNorm on halo buffers, softmax on GEMM A stages");
+  static constexpr int THREADS = (SPLIT || XF) ? kThreads + 128 : kThreads;
+  static constexpr int NCTA = PAIR ? 2 : 1;
   // Separately buffered A operand (MODES 3 and 4): two buffers, each serving
   // several reduction steps. MODE 4 holds (bh + 2) rows x bw pixels with
   // bh * bw = 256, at most 64 KB (bw <= 128).
@@ -150,7 +174,9 @@ struct Cfg {
   static constexpr uint32_t B_LOAD = (PAIR ? BN / 2 : BN) * 128;          // this CTA's weight rows
   static constexpr uint32_t A_BYTES = A_LOAD * (SPLIT ? 2 : 1);  // stage footprint (hi | lo)
   static constexpr uint32_t B_BYTES = B_LOAD * (SPLIT ? 2 : 1);
-  static constexpr uint32_t STAGE_TX = A_LOAD + B_LOAD;
+  // bytes that complete on `full` (XF = 2: the A stage lands on a barrier of
+  // this CTA's own, for its transforming warps)
+  static constexpr uint32_t STAGE_TX = (XF == 2 ? 0 : A_LOAD) + B_LOAD;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   // Epilogue staging: 4 warps x NSTG buffers x (32 rows x 128 bytes). Two
   // buffers let a block's store drain (and the next block's residual land)
@@ -166,7 +192,7 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
   static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
   static constexpr size_t SMEM = 1024 + HALO_BUFS * HALO_BYTES + STAGES * STAGE_BYTES + STAGING +
-                                 ((SPLIT ? 3 : 2) * STAGES + 17) * sizeof(uint64_t) + 16;
+                                 (4 * STAGES + 19) * sizeof(uint64_t) + 16;
   static_assert(STAGES >= 2, "at least double-buffered stages");
   static_assert(!(HALO || SWAP) || STAGES >= 3, "buffered-A modes need a weight ring");
   static_assert(!SWAP || (BN == 128 && MS == 2), "MODE 4 tiles are 128 channels x 256 pixels");
@@ -256,12 +282,12 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity,
   return true;
 }
 
-template <int BN, int MODE, int MS, bool PAIR, bool SPLIT>
-__global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
+template <int BN, int MODE, int MS, bool PAIR, bool SPLIT, int XF>
+__global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1)
     igemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmO,
                  const __grid_constant__ CUtensorMap tmR, const KParams p) {
-  using C = Cfg<BN, MS, MODE, PAIR, SPLIT>;
+  using C = Cfg<BN, MS, MODE, PAIR, SPLIT, XF>;
   constexpr int STAGES = C::STAGES;
   constexpr bool kConv = MODE == 0 || MODE == 3 || MODE == 4;  // conv tiles (epilogue geometry)
   constexpr uint32_t STAGE_TX = C::STAGE_TX;
@@ -284,8 +310,10 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
   uint64_t *res_bar = drain + 1;    // per epilogue warp and staging buffer: residual landed
   uint64_t *a_full = res_bar + 8;   // MODES 3, 4: A buffer landed / free
   uint64_t *a_empty = a_full + 2;
-  uint64_t *xfull = a_empty + 2;    // SPLIT: stage split into hi / lo parts
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfull + (SPLIT ? STAGES : 0));
+  uint64_t *xfull = a_empty + 2;    // SPLIT / XF 2: stage transformed, ready for the MMA
+  uint64_t *xa_full = xfull + STAGES;  // XF 2: this CTA's A stage landed
+  uint64_t *h_full = xa_full + STAGES;  // XF 1: this CTA's halo buffer landed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(h_full + 2);
   volatile uint32_t *abort = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -308,11 +336,16 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
     mbar_init(drain, 1);
     for (int q = 0; q < 8; ++q) mbar_init(&res_bar[q], 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&a_full[b], 1);
+      // XF 1: the transforming warps of every CTA of the pair arrive instead
+      // of a copy completing
+      mbar_init(&a_full[b], XF == 1 ? 4 * C::NCTA : 1);
       mbar_init(&a_empty[b], 1);
+      mbar_init(&h_full[b], 1);
     }
-    if (SPLIT)
-      for (int s = 0; s < STAGES; ++s) mbar_init(&xfull[s], 128);  // every splitting thread
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&xfull[s], SPLIT ? 128 : 4 * C::NCTA);  // splitting threads / transforming warps
+      mbar_init(&xa_full[s], 1);
+    }
     *abort = 0u;
     fence_mbarrier_init();
   }
@@ -356,7 +389,8 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t pending = 0, pend_par = 0;  // stages with a copy issued, and its parity
       uint32_t abuf = 0, aphase = 0;       // MODE 3 halo buffer ring
-      uint32_t a_pending = 0, a_par = 0;
+      uint32_t a_pending = 0, a_par = 0;  // (XF 1: copies onto h_full)
+      uint32_t x_pending = 0, x_par = 0;  // XF 2: A copies onto xa_full
       bool failed = false;
       // PAIR: both CTAs' copies complete on the leader's barriers; this CTA
       // loads its own 128 A rows (tile rows from yoff) and weight rows from
@@ -396,13 +430,20 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
               failed = true;
               break;
             }
-            if (leader) mbar_arrive_expect_tx(&a_full[abuf], tx_mult * (MS + 2) * 130 * 128);
-            if constexpr (PAIR)
+            if constexpr (XF == 1) {
+              // lands on this CTA's own barrier, for its transforming warps
+              mbar_arrive_expect_tx(&h_full[abuf], (MS + 2) * 130 * 128);
+              tma_load_4d(sH + abuf * C::HALO_BYTES, &tmA, &h_full[abuf], cc * 32, tx * p.bw - 1,
+                          ty * p.bh + yoff - 1, img);
+            } else if constexpr (PAIR) {
+              if (leader) mbar_arrive_expect_tx(&a_full[abuf], tx_mult * (MS + 2) * 130 * 128);
               tma_load_4d_pair(sH + abuf * C::HALO_BYTES, &tmA, afull_c + abuf * 8, cc * 32,
                                tx * p.bw - 1, ty * p.bh + yoff - 1, img);
-            else
+            } else {
+              mbar_arrive_expect_tx(&a_full[abuf], (MS + 2) * 130 * 128);
               tma_load_4d(sH + abuf * C::HALO_BYTES, &tmA, &a_full[abuf], cc * 32, tx * p.bw - 1,
                           ty * p.bh - 1, img);
+            }
             a_pending |= 1u << abuf;
             a_par = (a_par & ~(1u << abuf)) | (aphase << abuf);
             if (++abuf == 2) {
@@ -538,10 +579,16 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
           } else {
             // (a paired CTA loads its own 128 of the tile's rows)
             const int arow = mt * C::ROWS * kBM + static_cast<int>(rank) * kBM;
-            if constexpr (PAIR)
+            if constexpr (XF == 2) {  // A lands on this CTA's own barrier
+              mbar_arrive_expect_tx(&xa_full[stage], C::A_LOAD);
+              tma_load_2d(a_dst, &tmA, &xa_full[stage], ks * 32, arow);
+              x_pending |= 1u << stage;
+              x_par = (x_par & ~(1u << stage)) | (phase << stage);
+            } else if constexpr (PAIR) {
               tma_load_2d_pair(a_dst, &tmA, full_c + stage * 8, ks * 32, arow);
-            else
+            } else {
               tma_load_2d(a_dst, &tmA, &full[stage], ks * 32, arow);
+            }
             load_b(b_dst, stage, ks * 32, n0);
           }
           pending |= 1u << stage;
@@ -552,14 +599,25 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
           }
         }
       }
-      if (*abort && leader) {
+      if (*abort) {
         // Let every copy issued land before the CTA exits (under PAIR the
         // leader's barriers count both CTAs' copies; the peer leaves only
-        // after the closing cluster barrier, i.e. after this drain).
-        for (int s = 0; s < STAGES; ++s)
-          if (pending & (1u << s)) mbar_wait_drain(&full[s], (pend_par >> s) & 1u, p.wait_ns);
-        for (int b = 0; b < 2; ++b)
-          if (a_pending & (1u << b)) mbar_wait_drain(&a_full[b], (a_par >> b) & 1u, p.wait_ns);
+        // after the closing cluster barrier, i.e. after this drain). Copies
+        // onto this CTA's own barriers (XF) are drained by each CTA.
+        if (leader) {
+          for (int s = 0; s < STAGES; ++s)
+            if (pending & (1u << s)) mbar_wait_drain(&full[s], (pend_par >> s) & 1u, p.wait_ns);
+          if (XF != 1)
+            for (int b = 0; b < 2; ++b)
+              if (a_pending & (1u << b))
+                mbar_wait_drain(&a_full[b], (a_par >> b) & 1u, p.wait_ns);
+        }
+        if (XF == 1)
+          for (int b = 0; b < 2; ++b)
+            if (a_pending & (1u << b)) mbar_wait_drain(&h_full[b], (a_par >> b) & 1u, p.wait_ns);
+        if (XF == 2)
+          for (int s = 0; s < STAGES; ++s)
+            if (x_pending & (1u << s)) mbar_wait_drain(&xa_full[s], (x_par >> s) & 1u, p.wait_ns);
       }
     }
   } else if (warp == 1) {
@@ -699,7 +757,10 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
           continue;
         }
         for (int ks = ks0; ks < ks1; ++ks) {
-          if (!wait(SPLIT ? &xfull[stage] : &full[stage], phase)) {
+          // (XF 2: the weight halves on `full`, the transformed A stages of
+          // both CTAs on `xfull`)
+          if (!wait(SPLIT ? &xfull[stage] : &full[stage], phase) ||
+              (XF == 2 && !wait(&xfull[stage], phase))) {
             raise_error(p, abort);
             failed = true;
             break;
@@ -742,7 +803,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
         mbar_wait_drain(drain, 0, p.wait_ns);
       }
     }
-  } else if (!SPLIT || warp < 6) {
+  } else if (!(SPLIT || XF) || warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;
@@ -959,6 +1020,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
                 static_cast<long long>(y) * p.wout + x;
       }
       const float rbias = (MODE == 2 && p.bias_per_row && p.bias && valid) ? p.bias[row] : 0.f;
+      float rs_m = -INFINITY, rs_s = 0.f;  // softmax statistics of this row (rs_out)
 
 #pragma unroll 1
       for (int c = 0; c < BN / C::CH; ++c) {
@@ -1011,6 +1073,25 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
             float b = rbias;
             if (!p.bias_per_row && p.bias && i < ncols) b = __ldg(p.bias + col0 + i);
             v[i] = fmaf(v[i], p.alpha, b);
+          }
+        }
+        if (MODE == 2 && p.rs_out) {
+          // running (max, sum of exp) of v * rs_scale over the valid columns
+          float mc = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < C::CH; ++i)
+            if (col0 + i < p.rs_cols) mc = fmaxf(mc, v[i] * p.rs_scale);
+          if (mc != -INFINITY) {
+            float sc = 0.f;
+#pragma unroll
+            for (int i = 0; i < C::CH; ++i)
+              if (col0 + i < p.rs_cols) sc += __expf(v[i] * p.rs_scale - mc);
+            if (mc > rs_m) {
+              rs_s = rs_s * __expf(rs_m - mc) + sc;
+              rs_m = mc;
+            } else {
+              rs_s += sc * __expf(mc - rs_m);
+            }
           }
         }
         if (C::CH == 32 && p.epi_tma) {
@@ -1170,6 +1251,8 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
         }
       }
       if (failed) break;
+      if (MODE == 2 && p.rs_out && valid)
+        p.rs_out[row * p.rs_ld + mn % p.n_tiles] = make_float2(rs_m, rs_s);
       }  // sub-tiles
       if (w.tail && !failed) {  // this warp's raw sums are out: raise its flag
         __threadfence();
@@ -1195,7 +1278,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
     for (int b = 0; b < 2; ++b)
       if (lane == 0 && (res_pending & (1u << b)))
         mbar_wait_drain(&res_bar[q * 2 + b], (res_phase >> b) & 1u, p.wait_ns);
-  } else {
+  } else if constexpr (SPLIT) {
     // ------------------------------------------------------------ split (SPLIT)
     // Each landed stage, in place: v -> hi = tf32(v), and lo = tf32(v - hi)
     // at the same offset in the lo half. The stage's parts then reach the
@@ -1242,6 +1325,158 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
         }
       }
     }
+  } else if constexpr (XF == 1) {
+    // ------------------------------------------------------------ GroupNorm (XF 1)
+    // Each landed halo buffer, in place: v -> silu(v * scale[c] + shift[c])
+    // (the same arithmetic as the separate GroupNorm apply), TF32-rounded
+    // as an MMA operand; pixels outside the image stay 0 (the conv's zero
+    // padding, not silu(shift)). Then the leader's a_full learns that this
+    // CTA's buffer is ready. Thread tt touches the 16-byte words tt + 128 j:
+    // pixel rows (tt >> 3) + 16 j, always the same 4-channel group (the
+    // 128-byte swizzle XORs the word index with the row's low 3 bits, which
+    // 16 j leaves alone), so its scale and shift load once per chunk; the
+    // words go through in batches of kU for independent loads and math.
+    constexpr int kWords = (MS + 2) * 130 * 8;
+    constexpr int kU = 5;
+    constexpr int kBatches = (kWords + 128 * kU - 1) / (128 * kU);
+    const int tt = threadIdx.x - kThreads;  // 0..127
+    const int lc = (tt & 7) ^ ((tt >> 3) & 7);
+    const uint32_t afull_c = PAIR ? mapa_rank(a_full, 0) : 0u;
+    const int yoff = PAIR ? static_cast<int>(rank) * (p.bh >> 1) : 0;
+    uint32_t abuf = 0, aphase = 0;
+    bool failed = false;
+    WorkIter<MODE> it(p, wid, wcount);
+    Work w;
+    while (!failed && it.next(p, w)) {
+      const int mn = w.tile % (p.m_tiles * p.n_tiles);
+      const int mt = mn / p.n_tiles;
+      const int per_img = p.tiles_x * p.tiles_y;
+      const int img = mt / per_img, rem = mt % per_img;
+      const int ty = rem / p.tiles_x, tx = rem % p.tiles_x;
+      const int y0 = ty * p.bh + yoff - 1, x0 = tx * p.bw - 1;
+      const long long ss0 = static_cast<long long>(img / p.t) * p.cin_pad + lc * 4;
+      for (int cc = w.k0; cc < w.k1; ++cc) {
+        const float4 sa = __ldg(reinterpret_cast<const float4 *>(p.gn_scale + ss0 + cc * 32));
+        const float4 sb = __ldg(reinterpret_cast<const float4 *>(p.gn_shift + ss0 + cc * 32));
+        bool ok = mbar_wait(&h_full[abuf], aphase, abort, p.wait_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) raise_error(p, abort);
+          failed = true;
+          break;
+        }
+        float4 *buf = reinterpret_cast<float4 *>(sH + abuf * C::HALO_BYTES);
+#pragma unroll 1
+        for (int bt = 0; bt < kBatches; ++bt) {
+          float4 v[kU];
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int i = tt + 128 * (bt * kU + u);
+            if (i < kWords) v[u] = buf[i];
+          }
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int R = (tt >> 3) + 16 * (bt * kU + u);  // halo pixel
+            const int hr = R / 130, hc = R - hr * 130;
+            const int y = y0 + hr, x = x0 + hc;
+            if (y >= 0 && y < p.hin && x >= 0 && x < p.win) {
+              float e[4] = {fmaf(v[u].x, sa.x, sb.x), fmaf(v[u].y, sa.y, sb.y),
+                            fmaf(v[u].z, sa.z, sb.z), fmaf(v[u].w, sa.w, sb.w)};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                if (p.gn_silu) e[k] = __fdividef(e[k], 1.0f + __expf(-e[k]));
+                e[k] = round_tf32(e[k]);
+              }
+              v[u] = make_float4(e[0], e[1], e[2], e[3]);
+            } else {
+              v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int i = tt + 128 * (bt * kU + u);
+            if (i < kWords) buf[i] = v[u];
+          }
+        }
+        fence_proxy_async_smem();  // generic writes -> the tensor core's reads
+        __syncwarp();
+        if (lane == 0) {
+          if (!PAIR || leader)
+            mbar_arrive(&a_full[abuf]);
+          else
+            mbar_arrive_cluster(afull_c + abuf * 8);
+        }
+        if (++abuf == 2) {
+          abuf = 0;
+          aphase ^= 1u;
+        }
+      }
+    }
+  } else if constexpr (XF == 2) {
+    // ------------------------------------------------------------ softmax (XF 2)
+    // Each landed A stage of raw scores, in place: s -> exp(s * scale -
+    // m[row]) * inv_l[row] (the row softmax, with the row statistics known),
+    // TF32-rounded; keys beyond the valid count read 0. Thread tt touches
+    // the 16-byte words tt + 128 j (j < 8): rows (tt >> 3) + 16 j, always
+    // the same 4 keys of the stage's 32, so the eight rows' statistics load
+    // once per tile.
+    const int tt = threadIdx.x - kThreads;  // 0..127
+    const int lc = (tt & 7) ^ ((tt >> 3) & 7);
+    const uint32_t xfull_c = PAIR ? mapa_rank(xfull, 0) : 0u;
+    static_assert(C::A_LOAD / 16 == 8 * 128, "one 128-row stage: eight words per thread");
+    uint32_t stage = 0, phase = 0;
+    bool failed = false;
+    WorkIter<MODE> it(p, wid, wcount);
+    Work w;
+    while (!failed && it.next(p, w)) {
+      const int mn = w.tile % (p.m_tiles * p.n_tiles);
+      const int mt = mn / p.n_tiles;
+      const int row0 = mt * C::ROWS * kBM + static_cast<int>(rank) * kBM + (tt >> 3);
+      float rm[8], ril[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int row = min(row0 + 16 * j, p.M - 1);
+        rm[j] = __ldg(p.sm_m + row);
+        ril[j] = __ldg(p.sm_inv_l + row);
+      }
+      for (int ks = w.k0; ks < w.k1; ++ks) {
+        bool ok = mbar_wait(&xa_full[stage], phase, abort, p.wait_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) raise_error(p, abort);
+          failed = true;
+          break;
+        }
+        float4 *a = reinterpret_cast<float4 *>(sA + stage * C::A_BYTES);
+        const int key = ks * 32 + lc * 4;
+        const bool k0 = key < p.sm_cols, k1 = key + 1 < p.sm_cols, k2 = key + 2 < p.sm_cols,
+                   k3 = key + 3 < p.sm_cols;
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = a[tt + 128 * j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[j].x = k0 ? round_tf32(__expf(v[j].x * p.sm_scale - rm[j]) * ril[j]) : 0.f;
+          v[j].y = k1 ? round_tf32(__expf(v[j].y * p.sm_scale - rm[j]) * ril[j]) : 0.f;
+          v[j].z = k2 ? round_tf32(__expf(v[j].z * p.sm_scale - rm[j]) * ril[j]) : 0.f;
+          v[j].w = k3 ? round_tf32(__expf(v[j].w * p.sm_scale - rm[j]) * ril[j]) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[tt + 128 * j] = v[j];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (!PAIR || leader)
+            mbar_arrive(&xfull[stage]);
+          else
+            mbar_arrive_cluster(xfull_c + stage * 8);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -1263,19 +1498,19 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT>::THREADS, 1)
   }
 }
 
-template <int BN, int MODE, int MS, bool PAIR = false, bool SPLIT = false>
+template <int BN, int MODE, int MS, bool PAIR = false, bool SPLIT = false, int XF = 0>
 int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ts,
                  const CUtensorMap &to, const CUtensorMap &tr, const KParams &kp,
                  cudaStream_t stream) {
-  using C = Cfg<BN, MS, MODE, PAIR, SPLIT>;
+  using C = Cfg<BN, MS, MODE, PAIR, SPLIT, XF>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(igemm_kernel<BN, MODE, MS, PAIR, SPLIT>,
+    attr_err = cudaFuncSetAttribute(igemm_kernel<BN, MODE, MS, PAIR, SPLIT, XF>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(C::SMEM));
   });
-  if (attr_err != cudaSuccess) return VAE_ECUDA;
+  VAE_CUDA_TRY(attr_err);
   // PAIR: one cluster of two CTAs per SM pair, two CTAs per worker.
   const int workers = PAIR ? num_sms() / 2 : num_sms();
   const int grid = std::min(kp.total_tiles, workers) * (PAIR ? 2 : 1);
@@ -1300,10 +1535,9 @@ int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap
     attrs[0].val.cooperative = 1;
     cfg.numAttrs = 1;
   }
-  if (cudaLaunchKernelEx(&cfg, igemm_kernel<BN, MODE, MS, PAIR, SPLIT>, ta, tb, ts, to, tr, kp) !=
-      cudaSuccess)
-    return VAE_ECUDA;
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_CUDA_TRY(
+      cudaLaunchKernelEx(&cfg, igemm_kernel<BN, MODE, MS, PAIR, SPLIT, XF>, ta, tb, ts, to, tr, kp));
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }
@@ -1313,6 +1547,12 @@ int launch_typed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap
 int launch_split(int mode, int bn, const CUtensorMap &ta, const CUtensorMap &tb,
                  const CUtensorMap &ts, const CUtensorMap &to, const CUtensorMap &tr,
                  const KParams &kp, cudaStream_t s);
+
+// Operand-transform instantiations (igemm_xf.cu): xf 1 (input GroupNorm,
+// halo conv) or 2 (softmax A, GEMM), 256-column tiles, paired or not.
+int launch_xf(int xf, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+              const CUtensorMap &ts, const CUtensorMap &to, const CUtensorMap &tr,
+              const KParams &kp, cudaStream_t s);
 
 }  // namespace igk
 }  // namespace vae

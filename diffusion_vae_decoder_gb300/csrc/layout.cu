@@ -139,7 +139,7 @@ int pack_conv_weights(const float *w, int cout, int cin, int taps, const float *
   const long long total = static_cast<long long>(cout_rows) * ldb;
   pack_kernel<<<grid_for(total, 256), 256, 0, s>>>(w, cout, cin, taps, w_sc, w_sc ? sc_cin : 0,
                                                    dst, cout_rows, ldb, round_up32(cin), round);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }
@@ -150,7 +150,7 @@ int pack_upsample_weights(const float *w, int cout, int cin, float *dst, cudaStr
   const int ldb = upsample_ldb(cin);
   pack_upsample_kernel<<<grid_for(4ll * cout * ldb, 256), 256, 0, s>>>(w, cout, cin, dst, ldb,
                                                                       round_up32(cin), round);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }
@@ -166,7 +166,7 @@ int transpose(const float *src, long long src_outer_stride, int src_ld, float *d
   transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(src, src_outer_stride, src_ld, dst,
                                                  dst_outer_stride, dst_ld, rows, cols, alpha,
                                                  beta, round);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }
@@ -174,7 +174,7 @@ int transpose(const float *src, long long src_outer_stride, int src_ld, float *d
 int pad_rows(const float *src, long long rows, int cols, float *dst, int dst_cols,
              cudaStream_t s) {
   pad_rows_kernel<<<grid_for(rows * dst_cols, 256), 256, 0, s>>>(src, rows, cols, dst, dst_cols);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }
@@ -185,14 +185,14 @@ int upsample_nearest2x_nhwc(const float *src, long long imgs, int h, int w, int 
   const long long total = imgs * 4ll * h * w * (c / 4);
   upsample2x_nhwc_kernel<<<grid_for(total, 256), 256, 0, s>>>(
       reinterpret_cast<const float4 *>(src), h, w, c / 4, total, reinterpret_cast<float4 *>(dst));
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }
 
 int add_bias(float *dst, const float *a, const float *b, int n, cudaStream_t s) {
   add_kernel<<<grid_for(n, 256), 256, 0, s>>>(dst, a, b, n);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }

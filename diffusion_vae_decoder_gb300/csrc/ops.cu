@@ -82,7 +82,7 @@ ConvWs carve_conv(Carver &cv, int n, int cin, long long spatial, int layout, int
 
 // ---------------------------------------------------------------- attention
 struct AttnWs {
-  float *xs, *t, *wqkv, *bqkv, *wo, *qkv, *vt, *s, *o, *y;
+  float *xs, *t, *wqkv, *bqkv, *wo, *qkv, *vt, *s, *o, *y, *rs;
   void *gn;
 };
 
@@ -101,6 +101,7 @@ AttnWs carve_attn(Carver &cv, int n, int c, int L, int layout) {
   w.o = cv.take<float>(nl * c);
   w.y = layout == VAE_NCHW ? cv.take<float>(nl * c) : nullptr;
   w.gn = cv.take<char>(groupnorm_ws_bytes(n, c, L, c));  // groups <= c
+  w.rs = cv.take<float>(attn_rs_floats(L));
   return w;
 }
 
@@ -123,6 +124,11 @@ StackWs carve_stack(Carver &cv, int n, int c, long long vox, int layout, int n_l
 }
 
 }  // namespace
+
+size_t attn_rs_floats(int L) {
+  const size_t tiles = static_cast<size_t>(ceil_div(L, igemm_col_tile(L)));
+  return 2 * static_cast<size_t>(L) * tiles + 2 * static_cast<size_t>(L);
+}
 
 size_t attn_ws_bytes(int n, int c, int L, int layout) {
   Carver cv(nullptr, 0);
@@ -177,17 +183,41 @@ int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
   }
   if (lp != L) VAE_CUDA_TRY(cudaMemsetAsync(sc.vt, 0, static_cast<size_t>(c) * lp * 4, s));
   const bool fused = !exact && use_fused_attention(c);
+  const float scale = 1.0f / std::sqrt(static_cast<float>(c));
   for (int b = 0; b < n; ++b) {
     const float *qkv_b = sc.qkv + static_cast<size_t>(b) * L * 3 * c;
     // V^T [c][L] (row stride lp): the K-major B operand of P.V.
     VAE_TRY(transpose(qkv_b + 2 * c, 0, 3 * c, sc.vt, 0, lp, 1, L, c, 1.0f, 0.0f, 0, s));
     if (fused) {  // scores stay on chip
-      VAE_TRY(flash_attention(qkv_b, qkv_b + c, 3 * c, sc.vt, lp, L, c,
-                              1.0f / std::sqrt(static_cast<float>(c)),
+      VAE_TRY(flash_attention(qkv_b, qkv_b + c, 3 * c, sc.vt, lp, L, c, scale,
                               sc.o + static_cast<size_t>(b) * L * c, c, s));
       continue;
     }
-    // S = q k^T (scale applied inside the softmax).
+    // o = P V with P = softmax(S * scale) row-wise
+    IgemmDesc pv;
+    pv.mode = AMode::Gemm;
+    pv.a = sc.s;
+    pv.lda = lp;
+    pv.M = L;
+    pv.kdim = lp;
+    pv.b = sc.vt;
+    pv.ldb = lp;
+    pv.cout = c;
+    pv.out = sc.o + static_cast<size_t>(b) * L * c;
+    pv.ldo = c;
+    pv.round_out = rnd;
+    pv.precise = exact;
+    // The softmax folded into the two GEMMs when the P.V kernel normalises
+    // its A stages (opt-in, see igemm_softmax_a_ok): the score GEMM's
+    // epilogue gathers each row's
+    // (max, sum of exponentials) per column tile, a merge turns them into the
+    // row's max and 1 / sum, and the P.V kernel reads exp(s * scale - max) /
+    // sum from the raw scores.
+    const bool fold = igemm_softmax_a_ok(pv);
+    const int rs_tiles = ceil_div(L, igemm_col_tile(L));
+    float2 *rs = reinterpret_cast<float2 *>(sc.rs);
+    float *row_m = sc.rs + 2 * static_cast<size_t>(L) * rs_tiles, *row_il = row_m + L;
+    // S = q k^T (scale applied by the softmax).
     {
       IgemmDesc d;
       d.mode = AMode::Gemm;
@@ -201,26 +231,24 @@ int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,
       d.out = sc.s;
       d.ldo = lp;
       d.precise = exact;
+      if (fold) {
+        d.rs_out = rs;
+        d.rs_scale = scale;
+        d.rs_cols = L;
+        d.rs_ld = rs_tiles;
+      }
       VAE_TRY(igemm_launch(d, s));
     }
-    VAE_TRY(softmax_rows(sc.s, L, L, lp, 1.0f / std::sqrt(static_cast<float>(c)), s, rnd));
-    // o = P V
-    {
-      IgemmDesc d;
-      d.mode = AMode::Gemm;
-      d.a = sc.s;
-      d.lda = lp;
-      d.M = L;
-      d.kdim = lp;
-      d.b = sc.vt;
-      d.ldb = lp;
-      d.cout = c;
-      d.out = sc.o + static_cast<size_t>(b) * L * c;
-      d.ldo = c;
-      d.round_out = rnd;
-      d.precise = exact;
-      VAE_TRY(igemm_launch(d, s));
+    if (fold) {
+      VAE_TRY(softmax_merge_stats(rs, L, rs_tiles, rs_tiles, row_m, row_il, s));
+      pv.sm_m = row_m;
+      pv.sm_inv_l = row_il;
+      pv.sm_scale = scale;
+      pv.sm_cols = L;
+    } else {
+      VAE_TRY(softmax_rows(sc.s, L, L, lp, scale, s, rnd));
     }
+    VAE_TRY(igemm_launch(pv, s));
   }
   // y = x + (o Wo^T + bo)
   IgemmDesc d;
@@ -420,7 +448,7 @@ int vae_mid_attn(const float *x, int n, int c, int h, int w, int layout, int gro
     VAE_TRY(stage_nhwc(x, n, c, L, layout, aw.xs, c, 1.f, 0.f, 0, &xa, s));
     ya = aw.y;
   }
-  AttnScratch sc{aw.t, aw.qkv, aw.vt, aw.s, aw.o, aw.gn};
+  AttnScratch sc{aw.t, aw.qkv, aw.vt, aw.s, aw.o, aw.gn, aw.rs};
   VAE_TRY(attention_nhwc(xa, n, c, L, groups, eps, gn_w, gn_b, aw.wqkv, aw.bqkv, aw.wo, bo, ya,
                          sc, s));
   if (layout == VAE_NCHW) VAE_TRY(unstage_nchw(ya, n, c, L, y, s));

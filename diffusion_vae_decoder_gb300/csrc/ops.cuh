@@ -16,8 +16,12 @@ int unstage_nchw(const float *src_nhwc, int n, int c, long long spatial, float *
 struct AttnScratch {
   float *t, *qkv, *vt, *s, *o;
   void *gn;
+  float *rs;  // attn_rs_floats(L): the score rows' softmax statistics
 };
 size_t attn_ws_bytes(int n, int c, int L, int layout);
+// Room for the per-column-tile softmax statistics of L score rows and the
+// merged per-row max and reciprocal sum.
+size_t attn_rs_floats(int L);
 // exact: split-TF32 products on FP32 operands (weights packed unrounded),
 // through the score-matrix path.
 int attention_nhwc(const float *x, int n, int c, int L, int groups, float eps,

@@ -4,6 +4,8 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -54,6 +56,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 }  // namespace
+
+bool cuda_failed(cudaError_t e, const char *file, int line) {
+  if (e == cudaSuccess) return false;
+  static const bool verbose = [] {
+    const char *v = std::getenv("VAE_VERBOSE");
+    return v && v[0] == '1';
+  }();
+  if (verbose) std::fprintf(stderr, "vae: %s at %s:%d\n", cudaGetErrorString(e), file, line);
+  return true;
+}
 
 void *current_context() {
   CUcontext ctx = nullptr;

@@ -130,7 +130,49 @@ __global__ void __launch_bounds__(kThreads) softmax_long(float *s, int L, int ld
   for (int j = L + threadIdx.x; j < ld; j += kThreads) row[j] = 0.f;
 }
 
+// (max, sum of exp(v - max)) pairs merged; a pair with no value is
+// (-inf, 0) and leaves the other unchanged.
+__device__ __forceinline__ float2 merge_stats(float2 a, float2 b) {
+  if (b.x == -INFINITY) return a;
+  if (a.x == -INFINITY) return b;
+  const float mx = fmaxf(a.x, b.x);
+  return make_float2(mx, a.y * __expf(a.x - mx) + b.y * __expf(b.x - mx));
+}
+
+// One warp per row: the row's per-tile statistics merged into its max and
+// the reciprocal of its sum of exponentials.
+__global__ void __launch_bounds__(256) softmax_stats_merge(const float2 *__restrict__ part,
+                                                           int rows, int tiles, int ld,
+                                                           float *__restrict__ m,
+                                                           float *__restrict__ inv_l) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float2 acc = make_float2(-INFINITY, 0.f);
+  for (int t = lane; t < tiles; t += 32)
+    acc = merge_stats(acc, part[static_cast<long long>(row) * ld + t]);
+  for (int o = 16; o > 0; o >>= 1) {
+    const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, acc.x, o),
+                                     __shfl_xor_sync(0xffffffffu, acc.y, o));
+    acc = merge_stats(acc, other);
+  }
+  if (lane == 0) {
+    m[row] = acc.x;
+    inv_l[row] = 1.0f / acc.y;
+  }
+}
+
 }  // namespace
+
+int softmax_merge_stats(const float2 *part, int rows, int tiles, int ld, float *m, float *inv_l,
+                        cudaStream_t st) {
+  if (!part || !m || !inv_l || rows <= 0 || tiles <= 0 || ld < tiles) return VAE_EINVAL;
+  softmax_stats_merge<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(part, rows, tiles,
+                                                                            ld, m, inv_l);
+  VAE_LAUNCH_CHECK();
+  count_launches(1);
+  return VAE_OK;
+}
 
 int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStream_t st,
                  int round) {
@@ -141,7 +183,7 @@ int softmax_rows(float *s, long long rows, int L, int ld, float scale, cudaStrea
     softmax_reg<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale, round);
   else
     softmax_long<<<static_cast<unsigned>(rows), kThreads, 0, st>>>(s, L, ld, scale, round);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }

@@ -155,7 +155,7 @@ int splitk_reduce(const float *part, int splits, long long split_stride, int sam
       reinterpret_cast<const float4 *>(part), splits, split_stride / 4,
       static_cast<unsigned>(per4), cout, bias, alpha, reinterpret_cast<const float4 *>(residual),
       round, reinterpret_cast<float4 *>(out), stats ? stat_part : nullptr, stat_groups);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   if (stat_slots) *stat_slots = stats ? blocks : 0;
   return VAE_OK;

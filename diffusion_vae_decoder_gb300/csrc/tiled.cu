@@ -138,7 +138,7 @@ int gather_latent_tiles(const float *z, int c, int zh, int zw, const TileSchedul
   const long long blocks = std::min<long long>((total + 255) / 256, 8ll * num_sms());
   gather_tiles_kernel<<<static_cast<unsigned>(std::max<long long>(blocks, 1)), 256, 0, s>>>(
       z, c, zh, zw, ts, t0, count, dst);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }
@@ -150,7 +150,7 @@ int blend_decoded_tiles(const float *tiles, int n, int co, const TileSchedule &t
   const dim3 grid(static_cast<unsigned>(bands), static_cast<unsigned>(ts.ny * ts.nx),
                   static_cast<unsigned>(n));
   blend_tiles_kernel<<<grid, 256, 0, s>>>(tiles, co, ts, height, width, out);
-  if (cudaGetLastError() != cudaSuccess) return VAE_ECUDA;
+  VAE_LAUNCH_CHECK();
   count_launches(1);
   return VAE_OK;
 }

@@ -35,17 +35,18 @@ def pkg():
 
 
 def _conv_case():
-    """512 -> 512 channels at 128 x 128, NHWC: 256 output tiles on the SMs,
-    which the conv runs with stream-K ranges (a tile cut between two CTAs)."""
-    x = S.make_normal((1, 128, 128, 512), 61)
-    w, b = S.make_conv_params(512, 512, 3, 62)
+    """256 -> 64 channels at 192 x 128, NHWC: 192 one-SM output tiles of 64
+    channels (1.26 rounds of the SMs) and 72 reduction steps each, which the
+    conv runs with stream-K ranges (a tile cut between two CTAs)."""
+    x = S.make_normal((1, 192, 128, 256), 61)
+    w, b = S.make_conv_params(64, 256, 3, 62)
     return x, w, b
 
 
 def test_expired_device_wait_reports_timeout_and_recovers(pkg):
     x, w, b = _conv_case()
     xd, wd, bd = (torch.from_numpy(a).cuda() for a in (x, w, b))
-    y = torch.empty_like(xd)
+    y = torch.empty((1, 192, 128, 64), device="cuda")
     assert pkg.vae_device_error() == 0
     pkg.vae_debug_set_wait_limit(2_000_000)  # 2 ms
     pkg.vae_debug_inject(pkg.INJECT_WITHHOLD_STREAMK_FLAG)
@@ -62,9 +63,10 @@ def test_expired_device_wait_reports_timeout_and_recovers(pkg):
     torch.cuda.synchronize()
     assert pkg.vae_device_error() == 0
     got = np.moveaxis(y.cpu().numpy(), -1, 1)
-    pix = np.array([[0, i, j] for i in (0, 1, 63, 127) for j in (0, 5, 64, 127)] +
+    r = np.random.default_rng(3)
+    pix = np.array([[0, i, j] for i in (0, 1, 95, 191) for j in (0, 5, 64, 127)] +
                    [[0, int(i), int(j)] for i, j in
-                    np.random.default_rng(3).integers(0, 128, (400, 2))])
+                    zip(r.integers(0, 192, 400), r.integers(0, 128, 400))])
     ref = O.conv2d_at(np.moveaxis(x, -1, 1), w, b, pix)
     assert_layer_parity(got[0][:, pix[:, 1], pix[:, 2]].T, ref, "conv after a timeout")
 
