@@ -572,7 +572,11 @@ def time_op(op, c, hw, steps, warmup):
     Every timed iteration is preceded by a 256 MB write that evicts L2; the
     iterations are queued back to back (one synchronize at the end), so the
     host enqueues the op while the GPU is still busy with the flush and the
-    events time the op's kernels, not the host's launch latency."""
+    events time the op's kernels, not the host's launch latency. (The write
+    is followed by a 256 MB read, so the op does not pay for writing back
+    the flush's dirty lines.) The convs
+    run on weights packed once (vae_conv2d_pack / vae_upsample_conv_pack);
+    the packing is timed on its own, the same way, as pack_ms."""
     import torch
 
     import diffusion_vae_decoder_gb300 as pkg
@@ -581,42 +585,58 @@ def time_op(op, c, hw, steps, warmup):
     wt, b = S.make_conv_params(c, c, 3, 32)
     wt, b = torch.from_numpy(wt).cuda(), torch.from_numpy(b).cuda()
     g, be = (torch.from_numpy(a).cuda() for a in S.make_norm_params(c, 33))
+    pack_fn = None
     if op == "conv":
         out = torch.empty_like(x)
-        fn = lambda: pkg.vae_conv2d(x, wt, b, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
+        pack_fn = lambda: pkg.vae_conv2d_pack(wt, b)  # noqa: E731
+        pk = pack_fn()
+        fn = lambda: pkg.vae_conv2d_packed(x, pk, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
         work, unit = 2.0 * c * c * 9 * hw * hw, "TFLOP/s"
     elif op == "upsample_conv":
         out = torch.empty((1, 2 * hw, 2 * hw, c), device="cuda")
-        fn = lambda: pkg.vae_upsample_conv(x, wt, b, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
+        pack_fn = lambda: pkg.vae_upsample_conv_pack(wt, b)  # noqa: E731
+        pk = pack_fn()
+        fn = lambda: pkg.vae_upsample_conv_packed(x, pk, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
         # executed work: four parity 2x2 convs, 4 taps per output pixel
         work, unit = 2.0 * c * c * 4 * 4 * hw * hw, "TFLOP/s"
     else:
         out = torch.empty_like(x)
         fn = lambda: pkg.vae_groupnorm_silu(x, g, be, layout=pkg.VAE_NHWC, out=out)  # noqa: E731
         work, unit = 12.0 * c * hw * hw, "GB/s"
-    for _ in range(warmup):
-        fn()
-    torch.cuda.synchronize()
+    # L2 eviction between timed iterations: write one 256 MB buffer, then
+    # read another, so that L2 ends up holding clean lines of unrelated data
+    # (a write alone would leave it full of dirty lines whose write-back
+    # would land inside the next timed op)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    events = []
-    for _ in range(steps):
-        flush.zero_()  # evict L2 between timed iterations
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        fn()
-        e1.record()
-        events.append((e0, e1))
-    torch.cuda.synchronize()
-    times = [e0.elapsed_time(e1) for e0, e1 in events]
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+
+    def timed(f):
+        for _ in range(warmup):
+            f()
+        torch.cuda.synchronize()
+        events = []
+        for _ in range(steps):
+            flush.zero_()  # evict L2 between timed iterations
+            flush_r.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            f()
+            e1.record()
+            events.append((e0, e1))
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in events]
+
+    times = timed(fn)
+    pack_ms = statistics.median(timed(pack_fn)) if pack_fn else None
     assert pkg.vae_device_error() == 0
     ms = statistics.median(times)
     rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
     peaks, src = load_peaks()
     peak = (peaks["bf16_tflops"] * TF32_OVER_BF16 if unit == "TFLOP/s" else peaks["hbm_gbs"])
     return {"op": op, "c": c, "hw": hw, "layout": "NHWC", "ms_median": ms,
-            "ms_min": min(times), "rate": rate, "unit": unit, "peak": peak,
+            "ms_min": min(times), "pack_ms": pack_ms, "rate": rate, "unit": unit, "peak": peak,
             "frac": rate / peak, "peak_source": src + " burst",
-            "l2": "flushed between iterations"}
+            "l2": "flushed between iterations (256 MB write, then 256 MB read)"}
 
 
 def run_op(args):

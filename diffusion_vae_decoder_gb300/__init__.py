@@ -104,6 +104,12 @@ _SIGS = {
     "vae_conv2d_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "vae_conv2d": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _P, _P, _SZ,
                         _P]),
+    "vae_conv2d_pack_bytes": (_SZ, [_I, _I, _I, _I]),
+    "vae_conv2d_pack": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _P, _SZ, _P]),
+    "vae_conv2d_packed": (_I, [_P, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _I, _P, _P, _SZ, _P]),
+    "vae_upsample_conv_pack_bytes": (_SZ, [_I, _I]),
+    "vae_upsample_conv_pack": (_I, [_P, _P, _I, _I, _P, _SZ, _P]),
+    "vae_upsample_conv_packed": (_I, [_P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _SZ, _P]),
     "vae_upsample_conv_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "vae_upsample_conv": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _SZ, _P]),
     "vae_groupnorm_silu_workspace_size": (_SZ, [_I, _I, _LL, _I, _I]),
@@ -227,6 +233,89 @@ def vae_conv2d(x, weight, bias=None, residual=None, sc_x=None, sc_w=None, sc_b=N
     _check("vae_conv2d", lib.vae_conv2d(
         _ptr(x), n, cin, h, w, layout, _ptr(weight), _ptr(bias), cout, k, _ptr(residual),
         _ptr(sc_x), _ptr(sc_w), _ptr(sc_b), sc_cin, _ptr(out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+class PackedWeights:
+    """A conv's weights packed once on the device (vae_conv2d_pack /
+    vae_upsample_conv_pack): the byte buffer and the sizes it was made for."""
+
+    def __init__(self, kind, buf, cout, cin, k, sc_cin):
+        self.kind, self.buf = kind, buf
+        self.cout, self.cin, self.k, self.sc_cin = cout, cin, k, sc_cin
+
+
+def vae_conv2d_pack(weight, bias=None, sc_w=None, sc_b=None, stream=None):
+    import torch
+    lib = load_library()
+    _need(weight, "weight")
+    bias, sc_b = _opt(bias, "bias"), _opt(sc_b, "sc_b")
+    cout, cin, k, _ = weight.shape
+    sc_cin = 0
+    if sc_w is not None:
+        sc_w = _need(sc_w.reshape(sc_w.shape[0], -1).contiguous(), "sc_w")
+        sc_cin = sc_w.shape[1]
+    nbytes = lib.vae_conv2d_pack_bytes(cout, cin, k, sc_cin)
+    buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=weight.device)
+    _check("vae_conv2d_pack", lib.vae_conv2d_pack(
+        _ptr(weight), _ptr(bias), cout, cin, k, _ptr(sc_w), _ptr(sc_b), sc_cin, _ptr(buf),
+        buf.numel(), _stream(stream)))
+    return PackedWeights("conv2d", buf, cout, cin, k, sc_cin)
+
+
+def vae_conv2d_packed(x, pack, residual=None, sc_x=None, layout=VAE_NCHW, out=None, stream=None):
+    lib = load_library()
+    _need(x, "x")
+    residual, sc_x = _opt(residual, "residual"), _opt(sc_x, "sc_x")
+    if pack.kind != "conv2d":
+        raise TypeError("pack was not made by vae_conv2d_pack")
+    if layout == VAE_NCHW:
+        n, cin, h, w = x.shape
+    else:
+        n, h, w, cin = x.shape
+    cout, k = pack.cout, pack.k
+    shape = (n, cout, h, w) if layout == VAE_NCHW else (n, h, w, cout)
+    if out is None:
+        import torch
+        out = torch.empty(shape, dtype=torch.float32, device=x.device)
+    ws = _ws(lib.vae_conv2d_workspace_size(n, cin, h, w, layout, cout, k, pack.sc_cin), x.device)
+    _check("vae_conv2d_packed", lib.vae_conv2d_packed(
+        _ptr(x), n, cin, h, w, layout, _ptr(pack.buf), cout, k, _ptr(residual), _ptr(sc_x),
+        pack.sc_cin, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def vae_upsample_conv_pack(weight, bias=None, stream=None):
+    import torch
+    lib = load_library()
+    _need(weight, "weight")
+    bias = _opt(bias, "bias")
+    cout, cin = weight.shape[0], weight.shape[1]
+    nbytes = lib.vae_upsample_conv_pack_bytes(cout, cin)
+    buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=weight.device)
+    _check("vae_upsample_conv_pack", lib.vae_upsample_conv_pack(
+        _ptr(weight), _ptr(bias), cout, cin, _ptr(buf), buf.numel(), _stream(stream)))
+    return PackedWeights("upsample_conv", buf, cout, cin, 3, 0)
+
+
+def vae_upsample_conv_packed(x, pack, layout=VAE_NCHW, out=None, stream=None):
+    lib = load_library()
+    _need(x, "x")
+    if pack.kind != "upsample_conv":
+        raise TypeError("pack was not made by vae_upsample_conv_pack")
+    if layout == VAE_NCHW:
+        n, cin, h, w = x.shape
+    else:
+        n, h, w, cin = x.shape
+    cout = pack.cout
+    shape = (n, cout, 2 * h, 2 * w) if layout == VAE_NCHW else (n, 2 * h, 2 * w, cout)
+    if out is None:
+        import torch
+        out = torch.empty(shape, dtype=torch.float32, device=x.device)
+    ws = _ws(lib.vae_upsample_conv_workspace_size(n, cin, h, w, layout, cout), x.device)
+    _check("vae_upsample_conv_packed", lib.vae_upsample_conv_packed(
+        _ptr(x), n, cin, h, w, layout, _ptr(pack.buf), cout, _ptr(out), _ptr(ws), ws.numel(),
         _stream(stream)))
     return out
 

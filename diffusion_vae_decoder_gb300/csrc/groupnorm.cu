@@ -14,6 +14,9 @@
 // per-channel affine  y = x * scale[c] + shift[c].
 // Pass 2 (apply): one vectorised elementwise sweep, SiLU, optional TF32
 // rounding when the result feeds a tensor-core conv.
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -41,12 +44,13 @@ __device__ __forceinline__ Triple merge(Triple a, Triple b) {
   return {n, fmaf(d, wb, a.mean), a.m2 + b.m2 + d * d * a.n * wb};
 }
 
-// NHWC: x[n][spatial][c]. grid = (nblk, n). Partials [n][groups][nblk].
-__global__ void __launch_bounds__(kStatThreads)
-    gn_stats_nhwc(const float *__restrict__ x, int c, long long spatial, int groups, int nblk,
-                  double *__restrict__ part) {
-  extern __shared__ float sm[];  // [ppi][c] x 3
-  const int n = blockIdx.y, blk = blockIdx.x;
+// NHWC: x[n][spatial][c]. Block `blk` of `nblk` of sample n reduces its slab
+// of pixels into partials [n][groups][nblk] (count, mean, M2); sm holds
+// 3 * kStatThreads * 4 floats.
+template <class P>
+__device__ __forceinline__ void stats_slab_nhwc(const float *__restrict__ x, int c,
+                                                long long spatial, int groups, int nblk, int n,
+                                                int blk, float *sm, P *__restrict__ part) {
   const int tpp = c >> 2;
   const int ppi = kStatThreads / tpp;
   const int tid = threadIdx.x;
@@ -111,11 +115,19 @@ __global__ void __launch_bounds__(kStatThreads)
         const float *e = sm + (static_cast<long long>(l) * c + ch) * 3;
         acc = merge(acc, Triple{e[0], e[1], e[2]});
       }
-    double *o = part + ((static_cast<long long>(n) * groups + g) * nblk + blk) * 3;
+    P *o = part + ((static_cast<long long>(n) * groups + g) * nblk + blk) * 3;
     o[0] = acc.n;
     o[1] = acc.mean;
     o[2] = acc.m2;
   }
+}
+
+// grid = (nblk, n). Partials [n][groups][nblk].
+__global__ void __launch_bounds__(kStatThreads)
+    gn_stats_nhwc(const float *__restrict__ x, int c, long long spatial, int groups, int nblk,
+                  double *__restrict__ part) {
+  extern __shared__ float sm[];  // [ppi][c] x 3
+  stats_slab_nhwc(x, c, spatial, groups, nblk, blockIdx.y, blockIdx.x, sm, part);
 }
 
 // NCHW: group (n, g) is the contiguous segment of cg * spatial floats.
@@ -163,14 +175,16 @@ __global__ void __launch_bounds__(kStatThreads)
   }
 }
 
-// One CTA per (n, g): merge nblk partials, write scale/shift per channel.
+// One CTA (a power-of-two blockDim <= kFinalizeThreads) for (sample, group)
+// ng: merge its nblk partials, write scale/shift per channel.
 template <class P>
-__global__ void gn_finalize(const P *__restrict__ part, long long nblk, int c, int groups,
-                            float eps, const float *__restrict__ gamma,
-                            const float *__restrict__ beta, float *__restrict__ scale,
-                            float *__restrict__ shift) {
-  __shared__ float red[kFinalizeThreads][3];
-  const int ng = blockIdx.x;
+__device__ __forceinline__ void finalize_group(const P *__restrict__ part, long long nblk, int c,
+                                               int groups, float eps,
+                                               const float *__restrict__ gamma,
+                                               const float *__restrict__ beta,
+                                               float *__restrict__ scale,
+                                               float *__restrict__ shift, int ng,
+                                               float (*red)[3]) {
   const int n = ng / groups, g = ng % groups;
   Triple acc{0.f, 0.f, 0.f};
   for (long long b = threadIdx.x; b < nblk; b += blockDim.x) {
@@ -194,16 +208,25 @@ __global__ void gn_finalize(const P *__restrict__ part, long long nblk, int c, i
     __syncthreads();
   }
   const int cg = c / groups;
-  if (threadIdx.x < cg) {
-    const double cntv = red[0][0];
-    const double mean = red[0][1];
-    const double var = cntv > 0 ? red[0][2] / cntv : 0.0;
-    const double rstd = 1.0 / sqrt(var + static_cast<double>(eps));
-    const int ch = g * cg + threadIdx.x;
+  const double cntv = red[0][0];
+  const double mean = red[0][1];
+  const double var = cntv > 0 ? red[0][2] / cntv : 0.0;
+  const double rstd = 1.0 / sqrt(var + static_cast<double>(eps));
+  for (int j = threadIdx.x; j < cg; j += blockDim.x) {
+    const int ch = g * cg + j;
     const double a = rstd * gamma[ch];
     scale[n * c + ch] = static_cast<float>(a);
     shift[n * c + ch] = static_cast<float>(beta[ch] - mean * a);
   }
+}
+
+template <class P>
+__global__ void gn_finalize(const P *__restrict__ part, long long nblk, int c, int groups,
+                            float eps, const float *__restrict__ gamma,
+                            const float *__restrict__ beta, float *__restrict__ scale,
+                            float *__restrict__ shift) {
+  __shared__ float red[kFinalizeThreads][3];
+  finalize_group(part, nblk, c, groups, eps, gamma, beta, scale, shift, blockIdx.x, red);
 }
 
 // SiLU with the fast exponential and division: their few-ulp error sits far
@@ -362,17 +385,21 @@ __global__ void __launch_bounds__(kCompactThreads)
   if (threadIdx.x == 0) cnt[ng] = 0u;
 }
 
-// Finalize and apply in one kernel, for few partials per group: every CTA
-// merges its sample's partials into shared scale/shift, then runs the same
-// vectorised apply loop as gn_apply_nhwc.
-__global__ void __launch_bounds__(256)
-    gn_apply_fused_nhwc(const float *__restrict__ x, unsigned per_sample4, int c,
-                        const float *__restrict__ part, int slots, int groups, float eps,
-                        const float *__restrict__ gamma, const float *__restrict__ beta, int silu,
-                        int round, const float *__restrict__ res, float *__restrict__ y) {
-  __shared__ __align__(16) float ssc[1024];
-  __shared__ __align__(16) float ssh[1024];
-  const int n = blockIdx.y;
+__device__ __forceinline__ void apply_share(const float *__restrict__ x, unsigned per_sample4,
+                                            int c, int silu, int round,
+                                            const float *__restrict__ res, float *__restrict__ y,
+                                            const float *ssc, const float *ssh, int n,
+                                            unsigned blk, unsigned nblk);
+
+// Merge sample n's partials ([n][groups][slots], float) into scale/shift in
+// shared memory (ssc, ssh: c floats each), then the vectorised apply loop of
+// gn_apply_nhwc over this block's share (block blk of nblk; nblk * 1024 a
+// multiple of c).
+__device__ __forceinline__ void apply_from_partials(
+    const float *__restrict__ x, unsigned per_sample4, int c, const float *__restrict__ part,
+    int slots, int groups, float eps, const float *__restrict__ gamma,
+    const float *__restrict__ beta, int silu, int round, const float *__restrict__ res,
+    float *__restrict__ y, float *ssc, float *ssh, int n, unsigned blk, unsigned nblk) {
   const int cg = c / groups;
   // tpg lanes (a power of two <= 32) merge one group's partials: strided
   // over the slots, then a butterfly over the lanes.
@@ -404,26 +431,122 @@ __global__ void __launch_bounds__(256)
     }
   }
   __syncthreads();
+  apply_share(x, per_sample4, c, silu, round, res, y, ssc, ssh, n, blk, nblk);
+}
+
+// The vectorised apply over block blk's share (of nblk) of sample n, with the
+// affine in shared memory (ssc, ssh).
+__device__ __forceinline__ void apply_share(const float *__restrict__ x, unsigned per_sample4,
+                                            int c, int silu, int round,
+                                            const float *__restrict__ res, float *__restrict__ y,
+                                            const float *ssc, const float *ssh, int n,
+                                            unsigned blk, unsigned nblk) {
   const size_t base4 = static_cast<size_t>(n) * per_sample4;
   const float4 *xv = reinterpret_cast<const float4 *>(x) + base4;
   float4 *yv = reinterpret_cast<float4 *>(y) + base4;
   const float4 *rv = res ? reinterpret_cast<const float4 *>(res) + base4 : nullptr;
-  const unsigned i0 = blockIdx.x * 256u + threadIdx.x;
-  const unsigned stride = gridDim.x * 256u;
+  const unsigned i0 = blk * 256u + threadIdx.x;
+  const unsigned stride = nblk * 256u;
   const int ch = static_cast<int>((i0 * 4u) % static_cast<unsigned>(c));
   const float4 a = *reinterpret_cast<const float4 *>(ssc + ch);
   const float4 b = *reinterpret_cast<const float4 *>(ssh + ch);
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (unsigned i = i0; i < per_sample4; i += stride) {
-    const float4 v = __ldg(xv + i);
-    const float4 r = rv ? __ldg(rv + i) : zero;
+  auto one = [&](float4 v, float4 r) {
     float4 o;
     o.x = rnd(act(fmaf(v.x, a.x, b.x), silu) + r.x, round);
     o.y = rnd(act(fmaf(v.y, a.y, b.y), silu) + r.y, round);
     o.z = rnd(act(fmaf(v.z, a.z, b.z), silu) + r.z, round);
     o.w = rnd(act(fmaf(v.w, a.w, b.w), silu) + r.w, round);
-    yv[i] = o;
+    return o;
+  };
+  unsigned i = i0;
+  for (; i + 3 * stride < per_sample4; i += 4 * stride) {  // four loads in flight
+    float4 v[4], r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      v[u] = __ldg(xv + i + u * stride);
+      r[u] = rv ? __ldg(rv + i + u * stride) : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) yv[i + u * stride] = one(v[u], r[u]);
   }
+  for (; i < per_sample4; i += stride) yv[i] = one(__ldg(xv + i), rv ? __ldg(rv + i) : zero);
+}
+
+// Finalize and apply in one kernel, for few partials per group: every CTA
+// merges its sample's partials into shared scale/shift, then runs the same
+// vectorised apply loop as gn_apply_nhwc.
+__global__ void __launch_bounds__(256)
+    gn_apply_fused_nhwc(const float *__restrict__ x, unsigned per_sample4, int c,
+                        const float *__restrict__ part, int slots, int groups, float eps,
+                        const float *__restrict__ gamma, const float *__restrict__ beta, int silu,
+                        int round, const float *__restrict__ res, float *__restrict__ y) {
+  __shared__ __align__(16) float ssc[1024];
+  __shared__ __align__(16) float ssh[1024];
+  apply_from_partials(x, per_sample4, c, part, slots, groups, eps, gamma, beta, silu, round, res,
+                      y, ssc, ssh, blockIdx.y, blockIdx.x, gridDim.x);
+}
+
+// Arrive at a grid-wide barrier (counter zeroed before the launch; each
+// barrier adds gridDim.x * gridDim.y) and wait for `target` arrivals; the
+// wait is bounded (VAE_EDEVICE_TIMEOUT). Returns false to every thread of
+// the block when it gave up.
+__device__ __forceinline__ bool grid_barrier(unsigned *bar, unsigned target, int *err,
+                                             unsigned long long wait_ns, int *s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    const uint64_t t0 = global_timer_ns();
+    int ok = 1;
+    while (static_cast<unsigned>(ld_acquire_gpu(reinterpret_cast<const int *>(bar))) < target) {
+      __nanosleep(64);  // (hundreds of pollers share the counter's cache line)
+      if (global_timer_ns() - t0 > wait_ns) {
+        atomicCAS(err, 0, static_cast<int>(VAE_EDEVICE_TIMEOUT));
+        ok = 0;
+        break;
+      }
+    }
+    *s_ok = ok;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+// The whole GroupNorm(+SiLU) in one cooperative launch, for tensors that L2
+// holds between the two reads: every block reduces its slab of pixels into
+// per-(block, group) partials; after a grid barrier the first n * groups
+// blocks each merge one (sample, group)'s partials into the per-channel
+// affine (scale, shift); after a second barrier every block applies it to its
+// share -- the second read of x comes from L2, so HBM moves each element in
+// and out once.
+__global__ void __launch_bounds__(256)
+    gn_coop_nhwc(const float *__restrict__ x, int c, long long spatial, int groups, float eps,
+                 const float *__restrict__ gamma, const float *__restrict__ beta, int silu,
+                 int round, const float *__restrict__ res, float *__restrict__ y,
+                 float *__restrict__ part, float *__restrict__ scale, float *__restrict__ shift,
+                 unsigned *bar, int *err, unsigned long long wait_ns) {
+  __shared__ __align__(16) float ssc[1024];
+  __shared__ __align__(16) float ssh[1024];
+  __shared__ float red[256][3];
+  __shared__ int s_ok;
+  extern __shared__ float sm[];  // stats scratch [ppi][c] x 3
+  const int n = blockIdx.y;
+  const int nblk = gridDim.x;
+  const unsigned total = gridDim.x * gridDim.y;
+  stats_slab_nhwc(x, c, spatial, groups, nblk, n, blockIdx.x, sm, part);
+  if (!grid_barrier(bar, total, err, wait_ns, &s_ok)) return;
+  const int lin = blockIdx.y * gridDim.x + blockIdx.x;
+  if (lin < static_cast<int>(gridDim.y) * groups)
+    finalize_group(part, nblk, c, groups, eps, gamma, beta, scale, shift, lin, red);
+  if (!grid_barrier(bar, 2 * total, err, wait_ns, &s_ok)) return;
+  for (int ch = threadIdx.x; ch < c; ch += blockDim.x) {
+    ssc[ch] = __ldcg(scale + n * c + ch);  // (written in this launch: not through L1's
+    ssh[ch] = __ldcg(shift + n * c + ch);  //  read-only path)
+  }
+  __syncthreads();
+  apply_share(x, static_cast<unsigned>(spatial * c / 4), c, silu, round, res, y, ssc, ssh, n,
+              blockIdx.x, nblk);
 }
 
 // Blocks per sample for the apply loops: a multiple of c / gcd(c, 1024) so
@@ -483,6 +606,80 @@ size_t groupnorm_ws_bytes(int n, int c, long long spatial, int groups) {
   return cv.used;
 }
 
+namespace {
+
+// VAE_GN=multipass keeps every GroupNorm on the three-launch path
+// (comparisons).
+bool coop_gn_enabled() {
+  static const bool v = [] {
+    const char *e = std::getenv("VAE_GN");
+    return !(e && std::strcmp(e, "multipass") == 0);
+  }();
+  return v;
+}
+
+// The one-launch path (gn_coop_nhwc): NHWC tensors of at most kCoopMaxBytes
+// (L2 keeps them between the two reads), the grid co-resident. Returns
+// VAE_EUNSUPPORTED when it does not apply (the caller takes the three-launch
+// path).
+constexpr long long kCoopMaxBytes = 64ll << 20;
+
+int groupnorm_coop(const float *x, int n, int c, long long spatial, int groups, float eps,
+                   const float *gamma, const float *beta, int silu, int round_out, float *y,
+                   void *ws, cudaStream_t s, const float *residual) {
+  if (static_cast<long long>(n) * spatial * c * 4 > kCoopMaxBytes) return VAE_EUNSUPPORTED;
+  const long long per4 = spatial * c / 4;
+  if (per4 > 0xffffffffll / 2) return VAE_EUNSUPPORTED;
+  static int coop_ok = -1, per_sm = 0;
+  const int tpp = c / 4, ppi = kStatThreads / tpp;
+  const size_t sm = static_cast<size_t>(ppi) * c * 3 * sizeof(float);
+  if (coop_ok < 0) {
+    int dev = 0, attr = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&attr, cudaDevAttrCooperativeLaunch, dev);
+    coop_ok = attr;
+  }
+  if (!coop_ok) return VAE_EUNSUPPORTED;
+  // resident blocks per SM at this dynamic shared memory size
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gn_coop_nhwc, 256, sm) !=
+      cudaSuccess || per_sm <= 0)
+    return VAE_EUNSUPPORTED;
+  // blocks per sample: up to four per SM in all, a multiple of c / gcd(c, 1024)
+  long long gcd = c, b2 = 1024;
+  while (b2) {
+    const long long t = gcd % b2;
+    gcd = b2;
+    b2 = t;
+  }
+  const long long unit = c / gcd;
+  const long long resident = static_cast<long long>(per_sm) * num_sms();
+  long long bps = std::min<long long>(std::min(4ll * num_sms(), resident) / n,
+                                      (per4 + 255) / 256);
+  bps = std::min<long long>(bps, kMaxBlocksPerGroupSeg) / unit * unit;  // (fits the workspace)
+  if (bps < 1 || bps * n > resident || bps > spatial) return VAE_EUNSUPPORTED;
+  if (static_cast<long long>(n) * groups > bps * n) return VAE_EUNSUPPORTED;  // finalize blocks
+  Carver cv(ws, ~size_t(0));
+  float *part = cv.take<float>(static_cast<size_t>(n) * groups * bps * 3);
+  float *scale = cv.take<float>(static_cast<size_t>(n) * c);
+  float *shift = cv.take<float>(static_cast<size_t>(n) * c);
+  unsigned *bar = cv.take<unsigned>(1);
+  int *err = device_error_word();
+  if (!err) return VAE_ECUDA;
+  VAE_CUDA_TRY(cudaMemsetAsync(bar, 0, sizeof(unsigned), s));
+  const unsigned long long wait_ns = wait_limit_ns();
+  void *args[] = {const_cast<float **>(&x), &c, &spatial, &groups, &eps,
+                  const_cast<float **>(&gamma), const_cast<float **>(&beta), &silu, &round_out,
+                  const_cast<float **>(&residual), &y, &part, &scale, &shift, &bar, &err,
+                  const_cast<unsigned long long *>(&wait_ns)};
+  VAE_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(gn_coop_nhwc),
+                                           dim3(static_cast<unsigned>(bps), n), dim3(256), args,
+                                           sm, s));
+  count_launches(1);
+  return VAE_OK;
+}
+
+}  // namespace
+
 int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, int groups,
                    float eps, const float *gamma, const float *beta, int silu, int round_out,
                    float *y, void *ws, cudaStream_t s, const float *residual) {
@@ -493,6 +690,11 @@ int groupnorm_silu(const float *x, int n, int c, long long spatial, int nhwc, in
        reinterpret_cast<uintptr_t>(residual)) & 15)
     return VAE_EINVAL;
   if (residual && !nhwc) return VAE_EUNSUPPORTED;
+  if (nhwc && coop_gn_enabled()) {
+    const int rc = groupnorm_coop(x, n, c, spatial, groups, eps, gamma, beta, silu, round_out, y,
+                                  ws, s, residual);
+    if (rc != VAE_EUNSUPPORTED) return rc;
+  }
   Carver cv(ws, ~size_t(0));
   double *part = cv.take<double>(static_cast<size_t>(n) * groups * kMaxBlocksPerGroupSeg * 3);
   float *scale = cv.take<float>(static_cast<size_t>(n) * c);

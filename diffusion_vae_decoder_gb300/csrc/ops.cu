@@ -283,39 +283,46 @@ size_t vae_conv2d_workspace_size(int n, int cin, int h, int w, int layout, int c
   return cv.used;
 }
 
-int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout, const float *weight,
-               const float *bias, int cout, int k, const float *residual, const float *sc_x,
-               const float *sc_w, const float *sc_b, int sc_cin, float *y, void *ws,
-               size_t ws_bytes, vae_stream_t stream) {
-  auto s = reinterpret_cast<cudaStream_t>(stream);
-  if (!x || !weight || !y || !ws || n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0)
-    return VAE_EINVAL;
+namespace {
+
+// The layout of a weight pack made by vae_conv2d_pack / vae_upsample_conv_pack:
+// the GEMM-layout weights (rows x ldb floats, TF32-rounded), then the bias
+// (cout floats, the shortcut's folded in; zeros without one), each carve
+// 256-byte aligned.
+struct ConvPack {
+  float *w, *bias;
+};
+ConvPack carve_pack(Carver &cv, size_t rows, int ldb, int cout) {
+  ConvPack p{};
+  p.w = cv.take<float>(rows * static_cast<size_t>(ldb));
+  p.bias = cv.take<float>(static_cast<size_t>(cout));
+  return p;
+}
+
+int conv_args_ok(const float *x, float *y, int n, int cin, int h, int w, int layout, int cout,
+                 int k, const float *residual, const float *sc_x, int sc_cin) {
+  if (!x || !y || n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0) return VAE_EINVAL;
   if (layout != VAE_NCHW && layout != VAE_NHWC) return VAE_EINVAL;
   if (k != 1 && k != 3) return VAE_EUNSUPPORTED;
-  const bool has_sc = sc_x != nullptr || sc_w != nullptr;
-  if (has_sc && (!sc_x || !sc_w || sc_cin <= 0)) return VAE_EINVAL;
+  if (sc_x && sc_cin <= 0) return VAE_EINVAL;
   if (cin > 4096 || cout > 4096 || sc_cin > 4096 || h > 65535 || w > 65535)
     return VAE_EUNSUPPORTED;
   if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) ||
       (sc_x && !aligned16(sc_x)))
     return VAE_EINVAL;
   if (layout == VAE_NHWC && cout % 4) return VAE_EUNSUPPORTED;
-  const int scc = has_sc ? sc_cin : 0;
-  const long long spatial = static_cast<long long>(h) * w;
-  Carver cv(ws, ws_bytes);
-  ConvWs cw = carve_conv(cv, n, cin, spatial, layout, cout, k * k, scc);
-  if (!cv.ok()) return VAE_EWORKSPACE;
+  return VAE_OK;
+}
 
-  const int ldb = packed_ldb(cin, k * k, scc);
-  VAE_TRY(pack_conv_weights(weight, cout, cin, k * k, sc_w, scc, cw.packed, cout, ldb, s));
-  const float *bsum = bias;
-  if (has_sc && (bias || sc_b)) {
-    VAE_TRY(add_bias(cw.bias_sum, bias, sc_b, cout, s));
-    bsum = cw.bias_sum;
-  }
+// The conv on packed weights (cw: the call's workspace; its packed area is
+// not used when the weights come packed).
+int conv2d_run(const float *x, int n, int cin, int h, int w, int layout, const float *packed,
+               const float *bias, int cout, int k, const float *residual, const float *sc_x,
+               int scc, float *y, const ConvWs &cw, cudaStream_t s) {
+  const long long spatial = static_cast<long long>(h) * w;
   const float *xa = nullptr, *sca = nullptr;
   VAE_TRY(stage_nhwc(x, n, cin, spatial, layout, cw.xs, round_up32(cin), 1.f, 0.f, 0, &xa, s));
-  if (has_sc)
+  if (scc)
     VAE_TRY(stage_nhwc(sc_x, n, scc, spatial, layout, cw.scs, round_up32(scc), 1.f, 0.f, 0,
                        &sca, s));
   IgemmDesc d;
@@ -327,18 +334,123 @@ int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout, const f
   d.a_c = round_up32(cin);
   d.k = k;
   d.sc = sca;
-  d.sc_c = has_sc ? round_up32(scc) : 0;
-  d.b = cw.packed;
-  d.ldb = ldb;
+  d.sc_c = scc ? round_up32(scc) : 0;
+  d.b = packed;
+  d.ldb = packed_ldb(cin, k * k, scc);
   d.cout = cout;
   d.out = y;
   d.ldo = cout;
   d.out_nchw = layout == VAE_NCHW;
-  d.bias = bsum;
+  d.bias = bias;
   d.residual = residual;
   d.split_ws = cw.split;
   d.split_ws_floats = cw.split_floats;
   return igemm_launch(d, s);
+}
+
+int upsample_run(const float *x, int n, int cin, int h, int w, int layout, const float *packed,
+                 const float *bias, int cout, float *y, const ConvWs &cw, cudaStream_t s) {
+  const float *xa = nullptr;
+  VAE_TRY(stage_nhwc(x, n, cin, static_cast<long long>(h) * w, layout, cw.xs, round_up32(cin),
+                     1.f, 0.f, 0, &xa, s));
+  IgemmDesc d;
+  d.mode = AMode::Upsample;
+  d.a = xa;
+  d.imgs = n;
+  d.hin = h;
+  d.win = w;
+  d.a_c = round_up32(cin);
+  d.b = packed;
+  d.ldb = upsample_ldb(cin);
+  d.cout = cout;
+  d.out = y;
+  d.ldo = cout;
+  d.out_nchw = layout == VAE_NCHW;
+  d.bias = bias;
+  d.split_ws = cw.split;
+  d.split_ws_floats = cw.split_floats;
+  return igemm_launch(d, s);
+}
+
+int upsample_args_ok(const float *x, float *y, int n, int cin, int h, int w, int layout,
+                     int cout) {
+  if (!x || !y || n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0) return VAE_EINVAL;
+  if (layout != VAE_NCHW && layout != VAE_NHWC) return VAE_EINVAL;
+  if (cin > 4096 || cout > 4096 || h > 32767 || w > 32767) return VAE_EUNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y)) return VAE_EINVAL;
+  if (layout == VAE_NHWC && cout % 4) return VAE_EUNSUPPORTED;
+  return VAE_OK;
+}
+
+}  // namespace
+
+int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout, const float *weight,
+               const float *bias, int cout, int k, const float *residual, const float *sc_x,
+               const float *sc_w, const float *sc_b, int sc_cin, float *y, void *ws,
+               size_t ws_bytes, vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!weight || !ws) return VAE_EINVAL;
+  const bool has_sc = sc_x != nullptr || sc_w != nullptr;
+  if (has_sc && (!sc_x || !sc_w || sc_cin <= 0)) return VAE_EINVAL;
+  const int scc = has_sc ? sc_cin : 0;
+  VAE_TRY(conv_args_ok(x, y, n, cin, h, w, layout, cout, k, residual, sc_x, scc));
+  Carver cv(ws, ws_bytes);
+  ConvWs cw = carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout, k * k, scc);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  VAE_TRY(pack_conv_weights(weight, cout, cin, k * k, sc_w, scc, cw.packed, cout,
+                            packed_ldb(cin, k * k, scc), s));
+  const float *bsum = bias;
+  if (has_sc && (bias || sc_b)) {
+    VAE_TRY(add_bias(cw.bias_sum, bias, sc_b, cout, s));
+    bsum = cw.bias_sum;
+  }
+  return conv2d_run(x, n, cin, h, w, layout, cw.packed, bsum, cout, k, residual, sc_x, scc, y, cw,
+                    s);
+}
+
+size_t vae_conv2d_pack_bytes(int cout, int cin, int k, int sc_cin) {
+  if (cout <= 0 || cin <= 0 || (k != 1 && k != 3) || sc_cin < 0) return 0;
+  Carver cv(nullptr, 0);
+  carve_pack(cv, cout, packed_ldb(cin, k * k, sc_cin), cout);
+  return cv.used;
+}
+
+int vae_conv2d_pack(const float *weight, const float *bias, int cout, int cin, int k,
+                    const float *sc_w, const float *sc_b, int sc_cin, void *packed,
+                    size_t packed_bytes, vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!weight || !packed || cout <= 0 || cin <= 0 || sc_cin < 0 || (sc_w && sc_cin <= 0) ||
+      (!sc_w && (sc_b || sc_cin)))
+    return VAE_EINVAL;
+  if (k != 1 && k != 3) return VAE_EUNSUPPORTED;
+  if (cin > 4096 || cout > 4096 || sc_cin > 4096) return VAE_EUNSUPPORTED;
+  const int ldb = packed_ldb(cin, k * k, sc_cin);
+  Carver cv(packed, packed_bytes);
+  ConvPack p = carve_pack(cv, cout, ldb, cout);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  VAE_TRY(pack_conv_weights(weight, cout, cin, k * k, sc_w, sc_cin, p.w, cout, ldb, s));
+  if (bias || sc_b) {
+    VAE_TRY(add_bias(p.bias, bias, sc_b, cout, s));
+  } else {
+    VAE_CUDA_TRY(cudaMemsetAsync(p.bias, 0, static_cast<size_t>(cout) * sizeof(float), s));
+  }
+  return VAE_OK;
+}
+
+int vae_conv2d_packed(const float *x, int n, int cin, int h, int w, int layout,
+                      const void *packed, int cout, int k, const float *residual,
+                      const float *sc_x, int sc_cin, float *y, void *ws, size_t ws_bytes,
+                      vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!packed || !ws || sc_cin < 0 || (sc_cin > 0) != (sc_x != nullptr)) return VAE_EINVAL;
+  VAE_TRY(conv_args_ok(x, y, n, cin, h, w, layout, cout, k, residual, sc_x, sc_cin));
+  Carver pc(const_cast<void *>(packed), ~size_t(0));
+  const ConvPack p = carve_pack(pc, cout, packed_ldb(cin, k * k, sc_cin), cout);
+  Carver cv(ws, ws_bytes);
+  ConvWs cw = carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout, k * k, sc_cin);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  return conv2d_run(x, n, cin, h, w, layout, p.w, p.bias, cout, k, residual, sc_x, sc_cin, y, cw,
+                    s);
 }
 
 // ------------------------------------------------------------------ upsample + conv
@@ -353,37 +465,54 @@ int vae_upsample_conv(const float *x, int n, int cin, int h, int w, int layout,
                       const float *weight, const float *bias, int cout, float *y, void *ws,
                       size_t ws_bytes, vae_stream_t stream) {
   auto s = reinterpret_cast<cudaStream_t>(stream);
-  if (!x || !weight || !y || !ws || n <= 0 || cin <= 0 || h <= 0 || w <= 0 || cout <= 0)
-    return VAE_EINVAL;
-  if (layout != VAE_NCHW && layout != VAE_NHWC) return VAE_EINVAL;
-  if (cin > 4096 || cout > 4096 || h > 32767 || w > 32767) return VAE_EUNSUPPORTED;
-  if (!aligned16(x) || !aligned16(y)) return VAE_EINVAL;
-  if (layout == VAE_NHWC && cout % 4) return VAE_EUNSUPPORTED;
-  const long long spatial = static_cast<long long>(h) * w;
+  if (!weight || !ws) return VAE_EINVAL;
+  VAE_TRY(upsample_args_ok(x, y, n, cin, h, w, layout, cout));
   Carver cv(ws, ws_bytes);
-  ConvWs cw = carve_conv(cv, n, cin, spatial, layout, cout, kUpsamplePackTaps, 0, 4);
+  ConvWs cw = carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout,
+                         kUpsamplePackTaps, 0, 4);
   if (!cv.ok()) return VAE_EWORKSPACE;
-  const int ldb = upsample_ldb(cin);
   VAE_TRY(pack_upsample_weights(weight, cout, cin, cw.packed, s));
-  const float *xa = nullptr;
-  VAE_TRY(stage_nhwc(x, n, cin, spatial, layout, cw.xs, round_up32(cin), 1.f, 0.f, 0, &xa, s));
-  IgemmDesc d;
-  d.mode = AMode::Upsample;
-  d.a = xa;
-  d.imgs = n;
-  d.hin = h;
-  d.win = w;
-  d.a_c = round_up32(cin);
-  d.b = cw.packed;
-  d.ldb = ldb;
-  d.cout = cout;
-  d.out = y;
-  d.ldo = cout;
-  d.out_nchw = layout == VAE_NCHW;
-  d.bias = bias;
-  d.split_ws = cw.split;
-  d.split_ws_floats = cw.split_floats;
-  return igemm_launch(d, s);
+  return upsample_run(x, n, cin, h, w, layout, cw.packed, bias, cout, y, cw, s);
+}
+
+size_t vae_upsample_conv_pack_bytes(int cout, int cin) {
+  if (cout <= 0 || cin <= 0) return 0;
+  Carver cv(nullptr, 0);
+  carve_pack(cv, 4ull * cout, upsample_ldb(cin), cout);
+  return cv.used;
+}
+
+int vae_upsample_conv_pack(const float *weight, const float *bias, int cout, int cin,
+                           void *packed, size_t packed_bytes, vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!weight || !packed || cout <= 0 || cin <= 0) return VAE_EINVAL;
+  if (cin > 4096 || cout > 4096) return VAE_EUNSUPPORTED;
+  Carver cv(packed, packed_bytes);
+  ConvPack p = carve_pack(cv, 4ull * cout, upsample_ldb(cin), cout);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  VAE_TRY(pack_upsample_weights(weight, cout, cin, p.w, s));
+  if (bias) {
+    VAE_CUDA_TRY(cudaMemcpyAsync(p.bias, bias, static_cast<size_t>(cout) * sizeof(float),
+                                 cudaMemcpyDeviceToDevice, s));
+  } else {
+    VAE_CUDA_TRY(cudaMemsetAsync(p.bias, 0, static_cast<size_t>(cout) * sizeof(float), s));
+  }
+  return VAE_OK;
+}
+
+int vae_upsample_conv_packed(const float *x, int n, int cin, int h, int w, int layout,
+                             const void *packed, int cout, float *y, void *ws, size_t ws_bytes,
+                             vae_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (!packed || !ws) return VAE_EINVAL;
+  VAE_TRY(upsample_args_ok(x, y, n, cin, h, w, layout, cout));
+  Carver pc(const_cast<void *>(packed), ~size_t(0));
+  const ConvPack p = carve_pack(pc, 4ull * cout, upsample_ldb(cin), cout);
+  Carver cv(ws, ws_bytes);
+  ConvWs cw = carve_conv(cv, n, cin, static_cast<long long>(h) * w, layout, cout,
+                         kUpsamplePackTaps, 0, 4);
+  if (!cv.ok()) return VAE_EWORKSPACE;
+  return upsample_run(x, n, cin, h, w, layout, p.w, p.bias, cout, y, cw, s);
 }
 
 // ------------------------------------------------------------------ GroupNorm + SiLU

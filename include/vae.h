@@ -81,6 +81,32 @@ VAE_API int vae_conv2d(const float *x, int n, int cin, int h, int w, int layout,
                const float *sc_w, const float *sc_b, int sc_cin, float *y, void *ws,
                size_t ws_bytes, vae_stream_t stream);
 
+/* Weights packed once (the GEMM layout vae_conv2d builds on every call), for
+ * a conv applied many times:
+ *   vae_conv2d_pack_bytes  size of the pack for (cout, cin, k, sc_cin)
+ *   vae_conv2d_pack        weight [cout,cin,k,k], bias or NULL, and the 1x1
+ *                          shortcut's sc_w [cout,sc_cin] / sc_b or NULL (with
+ *                          sc_cin = 0 and NULLs when there is none) into the
+ *                          caller's device buffer `packed` (>= the size above,
+ *                          256-byte aligned); stream-ordered, no allocation
+ *   vae_conv2d_packed      vae_conv2d on such a pack: the same arguments and
+ *                          workspace (vae_conv2d_workspace_size), with cin, k,
+ *                          cout and sc_cin as given to vae_conv2d_pack (not
+ *                          checked against the pack: it holds only numbers);
+ *                          sc_x non-NULL exactly when sc_cin > 0.
+ * The pack is read-only for vae_conv2d_packed and may serve concurrent calls.
+ * Errors: VAE_EINVAL (NULLs, bad sizes, shortcut arguments that disagree),
+ * VAE_EUNSUPPORTED (sizes beyond the limits above), VAE_EWORKSPACE
+ * (packed_bytes or ws_bytes too small). */
+VAE_API size_t vae_conv2d_pack_bytes(int cout, int cin, int k, int sc_cin);
+VAE_API int vae_conv2d_pack(const float *weight, const float *bias, int cout, int cin, int k,
+                            const float *sc_w, const float *sc_b, int sc_cin, void *packed,
+                            size_t packed_bytes, vae_stream_t stream);
+VAE_API int vae_conv2d_packed(const float *x, int n, int cin, int h, int w, int layout,
+                              const void *packed, int cout, int k, const float *residual,
+                              const float *sc_x, int sc_cin, float *y, void *ws, size_t ws_bytes,
+                              vae_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * vae_upsample_conv -- nearest-2x upsample followed by a 3x3 stride-1 pad-1
  * convolution (cortiq-engine "Module vae", struct VaeUpRef):
@@ -95,6 +121,16 @@ VAE_API size_t vae_upsample_conv_workspace_size(int n, int cin, int h, int w, in
 VAE_API int vae_upsample_conv(const float *x, int n, int cin, int h, int w, int layout,
                       const float *weight, const float *bias, int cout, float *y, void *ws,
                       size_t ws_bytes, vae_stream_t stream);
+/* The same with the weights packed once (as for vae_conv2d_pack): the pack
+ * holds the four parity kernels and the bias; vae_upsample_conv_packed takes
+ * vae_upsample_conv's arguments and workspace with the pack in place of
+ * weight and bias. Errors as for vae_conv2d_pack / vae_conv2d_packed. */
+VAE_API size_t vae_upsample_conv_pack_bytes(int cout, int cin);
+VAE_API int vae_upsample_conv_pack(const float *weight, const float *bias, int cout, int cin,
+                                   void *packed, size_t packed_bytes, vae_stream_t stream);
+VAE_API int vae_upsample_conv_packed(const float *x, int n, int cin, int h, int w, int layout,
+                                     const void *packed, int cout, float *y, void *ws,
+                                     size_t ws_bytes, vae_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * vae_groupnorm_silu -- GroupNorm (cortiq-engine "Module vae", structs

@@ -110,6 +110,53 @@ def test_conv2d_residual_and_shortcut_exact(layout):
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
+def test_conv2d_packed_weights_exact(layout):
+    """Weights packed once (vae_conv2d_pack) serve several calls: two inputs
+    through the same pack with the 1x1 shortcut and its bias folded in, one
+    pack without bias with the in-place residual; every result exact."""
+    P = pkg()
+    n, cin, cout, h, w = 2, 64, 272, 9, 150
+    wt = S.integer_tensor((cout, cout, 3, 3), 40, -2, 2)
+    b = S.integer_tensor((cout,), 41, -4, 4)
+    sw = S.integer_tensor((cout, cin, 1, 1), 42, -2, 2)
+    sb = S.integer_tensor((cout,), 43, -4, 4)
+    pack = P.vae_conv2d_pack(dev(wt), dev(b), sc_w=dev(sw), sc_b=dev(sb))
+    for seed in (44, 45):
+        x = S.integer_tensor((n, cout, h, w), seed, -3, 3)
+        sx = S.integer_tensor((n, cin, h, w), seed + 10, -3, 3)
+        ref = O.conv2d(x, wt, b) + O.conv2d(sx, sw, sb)
+        y = sentinel_like(out_shape(ref.shape, layout))
+        P.vae_conv2d_packed(dev(to_layout(x, layout)), pack, sc_x=dev(to_layout(sx, layout)),
+                            layout=layout, out=y)
+        got = from_layout(y.cpu().numpy(), layout)
+        assert_all_written(got, "packed conv")
+        np.testing.assert_array_equal(got, ref)
+    pack2 = P.vae_conv2d_pack(dev(wt))
+    x = S.integer_tensor((n, cout, h, w), 46, -3, 3)
+    res = S.integer_tensor((n, cout, h, w), 47, -5, 5)
+    y2 = dev(to_layout(res, layout))
+    P.vae_conv2d_packed(dev(to_layout(x, layout)), pack2, residual=y2, layout=layout, out=y2)
+    np.testing.assert_array_equal(from_layout(y2.cpu().numpy(), layout), O.conv2d(x, wt) + res)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_upsample_conv_packed_weights_exact(layout):
+    P = pkg()
+    n, cin, cout, h, w = 2, 96, 160, 7, 70
+    wt = S.integer_tensor((cout, cin, 3, 3), 48, -2, 2)
+    b = S.integer_tensor((cout,), 49, -4, 4)
+    x = S.integer_tensor((n, cin, h, w), 50, -3, 3)
+    for bias in (b, None):
+        pk = P.vae_upsample_conv_pack(dev(wt), None if bias is None else dev(bias))
+        ref = O.upsample_conv(x, wt, bias)
+        y = sentinel_like(out_shape(ref.shape, layout))
+        P.vae_upsample_conv_packed(dev(to_layout(x, layout)), pk, layout=layout, out=y)
+        got = from_layout(y.cpu().numpy(), layout)
+        assert_all_written(got, "packed upsample conv")
+        np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("c,hw", [(128, 64), (256, 32), (512, 16), (512, 8)])
 def test_conv2d_float_parity(layout, c, hw):
     x = S.make_normal((1, c, hw, hw), 11)
@@ -362,6 +409,33 @@ def test_groupnorm_silu_parity(layout, n, c, h, w, silu):
     assert_all_written(got)
     m = metrics(got, ref)
     assert m["rel_l2"] < 2e-6 and m["max_abs"] < 2e-5, m
+
+
+def test_groupnorm_above_the_one_launch_size():
+    """NHWC tensors above 64 MB (L2 would not keep them between the two
+    reads) take the three-launch path: statistics, finalize, apply."""
+    x = S.make_normal((1, 128, 400, 410), 60) * 2.0 - 0.5
+    g, b = S.make_norm_params(128, 61)
+    ref = O.silu(O.group_norm(x, g, b, 32, 1e-6))
+    got = pkg().vae_groupnorm_silu(dev(np.moveaxis(x, 1, -1)), dev(g), dev(b), 32, 1e-6, True,
+                                   layout=pkg().VAE_NHWC).cpu().numpy()
+    m = metrics(np.moveaxis(got, -1, 1), ref)
+    assert m["rel_l2"] < 2e-6 and m["max_abs"] < 2e-5, m
+
+
+def test_groupnorm_three_launch_path_forced():
+    """The GroupNorm tests again with VAE_GN=multipass (child process: the
+    setting is read once), so the three-launch path stays covered at the
+    shapes the one-launch path takes by default."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, VAE_GN="multipass")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m", "gpu",
+                        "tests/test_gpu_ops.py", "-k", "groupnorm and not forced"],
+                       env=env, cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and " passed" in r.stdout, r.stdout[-3000:] + r.stderr[-2000:]
 
 
 def test_groupnorm_in_place_and_5d():
