@@ -86,7 +86,7 @@ class ProfRecord(ctypes.Structure):
 
 
 PROF_KINDS = {0: "conv3x3", 1: "upsample_conv", 2: "groupnorm", 3: "attention", 4: "layout",
-              5: "head"}
+              5: "head", 6: "groupnorm_affine"}
 
 
 class TracePoint(ctypes.Structure):

@@ -165,7 +165,13 @@ struct Chain {
   NormW norm_out;
   float *head_w = nullptr;  // conv_out packed for the fused CUDA-core head (cout <= 4)
   std::vector<void *> allocs;
+  // GroupNorm ahead (igemm_gn_ahead_ok): the current decode's row flags and
+  // per-conv row counters (zeroed at its start), and how many such convs it
+  // has launched (conv i uses counter i and flag value i + 1).
+  int *ga_flags = nullptr, *ga_next = nullptr;
+  int ga_idx = 0;
 };
+constexpr int kMaxGnAheadConvs = 64;
 
 struct Builder {
   Chain *ch;
@@ -332,6 +338,7 @@ struct Plan {
   int max_c = 0;
   int attn_c = 0, attn_l = 0;
   long long max_slots = 0;  // GroupNorm partial slots of the largest producer conv
+  long long max_rows = 0;   // n * H of the tallest activation
 };
 
 long long stat_slots_of(AMode mode, int hin, int win, int cout) {
@@ -347,6 +354,7 @@ Plan make_plan(const Chain &ch, int n, int h, int w) {
   Plan p;
   auto see = [&](long long hh, long long ww, int c) {
     p.max_elems = std::max(p.max_elems, static_cast<size_t>(n * hh * ww * c));
+    p.max_rows = std::max(p.max_rows, n * hh);
     p.max_c = std::max(p.max_c, c);
     p.max_slots = std::max(p.max_slots, stat_slots_of(AMode::Conv, static_cast<int>(hh),
                                                       static_cast<int>(ww), c));
@@ -377,6 +385,8 @@ struct DecodeWs {
   float *part;  // GroupNorm partials written by the producer conv's epilogue
   float *split; // split-K partial sums of the low-resolution convs
   unsigned *gn_cnt;  // per-(sample, group) arrival counters of the GroupNorm finalize
+  int *ga_next, *ga_flags;  // GroupNorm-ahead counters and row flags (right after gn_cnt)
+  size_t zero_bytes;        // gn_cnt .. ga_flags, zeroed at the start of a decode
   AttnScratch attn;
   void *gn;
 };
@@ -401,6 +411,10 @@ DecodeWs carve_decode(Carver &cv, const Chain &ch, const Plan &p, int n, int h, 
   // reduce may use
   d.part = cv.take<float>(static_cast<size_t>(n) * ch.groups * std::max(1024ll, p.max_slots) * 3);
   d.gn_cnt = cv.take<unsigned>(static_cast<size_t>(n) * ch.groups);
+  d.ga_next = cv.take<int>(kMaxGnAheadConvs);
+  d.ga_flags = cv.take<int>(static_cast<size_t>(std::max(1ll, p.max_rows)));
+  d.zero_bytes = static_cast<size_t>(reinterpret_cast<char *>(d.ga_flags + std::max(1ll, p.max_rows)) -
+                                     reinterpret_cast<char *>(d.gn_cnt));
   const size_t nl = static_cast<size_t>(n) * p.attn_l;
   const size_t lp = static_cast<size_t>(round_up32(p.attn_l));
   const int c = p.attn_c;
@@ -425,6 +439,15 @@ struct Step {
   ~Step() { p.close(idx, s); }
 };
 
+// How a conv gets its GroupNorm+SiLU input (run_gn_for): `act` is the
+// tensor it reads; with `fold` the kernel applies the affine (scale, shift)
+// to its halo itself, with `ahead` it makes `act` from x while it runs.
+struct GnIn {
+  const float *act = nullptr;
+  const float *scale = nullptr, *shift = nullptr, *x = nullptr;
+  bool fold = false, ahead = false;
+};
+
 double conv_flops(const ConvW &c, long long out_pixels) {
   return 2.0 * out_pixels * c.cout * (static_cast<double>(c.cin) * c.k * c.k + c.sc_cin);
 }
@@ -433,8 +456,7 @@ int run_conv(Chain &ch, const ConvW &c, const float *in, int n, int h, int w,
              const float *sc_in, const float *residual, float *out, int round_out,
              cudaStream_t s, bool upsample = false, bool nchw_out = false,
              Stats *st = nullptr, float *part = nullptr, int groups = 0,
-             float *split = nullptr, const float *gn_scale = nullptr,
-             const float *gn_shift = nullptr) {
+             float *split = nullptr, const GnIn *gin = nullptr) {
   const long long in_px = static_cast<long long>(n) * ch.frames * h * w;
   const long long out_px = in_px * (upsample ? 4 : 1);
   // algorithmic bytes: the input, the output, a residual and a shortcut
@@ -468,8 +490,19 @@ int run_conv(Chain &ch, const ConvW &c, const float *in, int n, int h, int w,
   d.round_out = ch.exact ? 0 : round_out;  // split-TF32 operands stay FP32
   d.split_ws = split;
   d.split_ws_floats = split ? kSplitWsFloats : 0;
-  d.gn_scale = gn_scale;  // the input's GroupNorm+SiLU, applied in the kernel
-  d.gn_shift = gn_shift;
+  if (gin && gin->fold) {  // the input's GroupNorm+SiLU, applied in the kernel
+    d.gn_scale = gin->scale;
+    d.gn_shift = gin->shift;
+  }
+  const bool ahead = gin && gin->ahead;
+  if (ahead) {  // `in` made by the launch itself from gin->x
+    d.ga_x = gin->x;
+    d.ga_scale = gin->scale;
+    d.ga_shift = gin->shift;
+    d.ga_flags = ch.ga_flags;
+    d.ga_next = ch.ga_next + ch.ga_idx;
+    d.ga_epoch = ch.ga_idx + 1;
+  }
   int fused = 0;
   long long slots = 0;
   if (st) {
@@ -478,7 +511,14 @@ int run_conv(Chain &ch, const ConvW &c, const float *in, int n, int h, int w,
     d.stat_ok = &fused;
     d.stat_slots = &slots;
   }
-  const int rc = igemm_launch(d, s);
+  int rc = igemm_launch(d, s);
+  if (ahead && rc == VAE_OK) ++ch.ga_idx;
+  if (ahead && rc == VAE_EUNSUPPORTED) {  // another path: the separate apply pass first
+    VAE_TRY(groupnorm_apply(gin->x, n, c.cin, in_px / n, gin->scale, gin->shift, 1, 1,
+                            const_cast<float *>(in), s));
+    d.ga_x = nullptr;
+    rc = igemm_launch(d, s);
+  }
   if (st) {
     st->ready = rc == VAE_OK && fused && slots > 0;
     st->slots = st->ready ? slots : 0;
@@ -518,38 +558,61 @@ bool gn_folds_into(const Chain &ch, const ConvW &c, int w) {
   return igemm_input_gn_ok(d);
 }
 
-// The GroupNorm+SiLU of `in` that conv `c` reads: either applied here into
-// ws.T (*act = ws.T), or reduced to its affine in ws.ss for the conv to apply
-// (*act = in; *scale / *shift set). A trace still receives the normalised
-// tensor.
+// Whether conv `c` (input rows w pixels wide) makes its GroupNorm+SiLU input
+// itself while it runs (GroupNorm ahead).
+bool gn_ahead_into(const Chain &ch, const ConvW &c, int w) {
+  if (!ch.ga_flags || ch.ga_idx >= kMaxGnAheadConvs || ch.exact || ch.frames != 1) return false;
+  IgemmDesc d;
+  d.mode = AMode::Conv;
+  d.k = c.k;
+  d.kt = c.kt;
+  d.win = w;
+  d.cout = c.cout;
+  d.sc_c = c.sc_cin;
+  d.a_c = round_up32(c.cin);
+  return igemm_gn_ahead_ok(d);
+}
+
+// The GroupNorm+SiLU of `in` that conv `c` reads: applied here into ws.T, or
+// reduced to its per-(sample, channel) affine in ws.ss for the conv to apply
+// (fold) or to make ws.T with while it runs (ahead). A trace receives the
+// normalised tensor here, or after the conv when the conv makes it.
 int run_gn_for(Chain &ch, const NormW &nw, const ConvW &c, const float *in, int n, int w,
-               long long sp, const DecodeWs &ws, const Stats &st, const float **act,
-               const float **scale, const float **shift, cudaStream_t s) {
-  *scale = *shift = nullptr;
-  *act = in;
+               long long sp, const DecodeWs &ws, const Stats &st, GnIn *g, cudaStream_t s) {
+  *g = GnIn{};
+  g->act = in;
   const size_t bytes = 4ull * n * sp * nw.c;
-  if (!gn_folds_into(ch, c, w)) {
+  const bool fold = gn_folds_into(ch, c, w);
+  const bool ahead = !fold && gn_ahead_into(ch, c, w);
+  if (!fold && !ahead) {
     VAE_TRY(run_gn(ch, nw, in, n, sp, ws.T, ws, st, s));
     if (ch.tr) ch.tr->emit(ws.T, bytes, s);
-    *act = ws.T;
+    g->act = ws.T;
     return VAE_OK;
   }
   float *sc = ws.ss, *sh = ws.ss + static_cast<size_t>(n) * nw.c;
   {
     // bytes: the statistics pass over the input when they were not fused
     // into its producer, else only the partials
-    Step step(ch.prof, VAE_PROF_GROUPNORM, 0,
+    Step step(ch.prof, VAE_PROF_GN_AFFINE, 0,
               st.ready ? 12.0 * n * ch.groups * st.slots : 4.0 * n * sp * nw.c, s);
     VAE_TRY(groupnorm_scale_shift(in, n, nw.c, sp, ch.groups, ch.eps, nw.g, nw.b,
                                   st.ready ? ws.part : nullptr, st.slots, sc, sh, ws.gn, s,
                                   ws.gn_cnt));
   }
+  g->scale = sc;
+  g->shift = sh;
+  if (ahead) {
+    g->ahead = true;
+    g->x = in;
+    g->act = ws.T;
+    return VAE_OK;
+  }
+  g->fold = true;
   if (ch.tr) {
     VAE_TRY(groupnorm_apply(in, n, nw.c, sp, sc, sh, 1, !ch.exact, ws.T, s));
     ch.tr->emit(ws.T, bytes, s);
   }
-  *scale = sc;
-  *shift = sh;
   return VAE_OK;
 }
 
@@ -559,18 +622,21 @@ int run_resnet(Chain &ch, const ResW &r, const float *in, float *out, const Deco
                int h, int w, int round_out, Stats &st, cudaStream_t s) {
   const long long sp = static_cast<long long>(h) * w * ch.frames;  // GroupNorm extent
   const size_t out_bytes = 4ull * n * sp * r.c1.cout;
-  const float *a1, *a2, *gsc, *gsh;
-  VAE_TRY(run_gn_for(ch, r.n1, r.c1, in, n, w, sp, ws, st, &a1, &gsc, &gsh, s));
-  VAE_TRY(run_conv(ch, r.c1, a1, n, h, w, nullptr, nullptr, ws.H, 0, s, false, false, &st,
-                   ws.part, ch.groups, ws.split, gsc, gsh));
+  const size_t in_bytes = 4ull * n * sp * r.c1.cin;
+  GnIn g;
+  VAE_TRY(run_gn_for(ch, r.n1, r.c1, in, n, w, sp, ws, st, &g, s));
+  VAE_TRY(run_conv(ch, r.c1, g.act, n, h, w, nullptr, nullptr, ws.H, 0, s, false, false, &st,
+                   ws.part, ch.groups, ws.split, &g));
+  if (ch.tr && g.ahead) ch.tr->emit(g.act, in_bytes, s);
   if (ch.tr) ch.tr->emit(ws.H, out_bytes, s);
-  VAE_TRY(run_gn_for(ch, r.n2, r.c2, ws.H, n, w, sp, ws, st, &a2, &gsc, &gsh, s));
+  VAE_TRY(run_gn_for(ch, r.n2, r.c2, ws.H, n, w, sp, ws, st, &g, s));
   if (r.c2.sc_cin)
-    VAE_TRY(run_conv(ch, r.c2, a2, n, h, w, in, nullptr, out, round_out, s, false, false,
-                     &st, ws.part, ch.groups, ws.split, gsc, gsh));
+    VAE_TRY(run_conv(ch, r.c2, g.act, n, h, w, in, nullptr, out, round_out, s, false, false,
+                     &st, ws.part, ch.groups, ws.split, &g));
   else
-    VAE_TRY(run_conv(ch, r.c2, a2, n, h, w, nullptr, in, out, round_out, s, false, false,
-                     &st, ws.part, ch.groups, ws.split, gsc, gsh));
+    VAE_TRY(run_conv(ch, r.c2, g.act, n, h, w, nullptr, in, out, round_out, s, false, false,
+                     &st, ws.part, ch.groups, ws.split, &g));
+  if (ch.tr && g.ahead) ch.tr->emit(g.act, out_bytes, s);
   if (ch.tr) ch.tr->emit(out, out_bytes, s);
   return VAE_OK;
 }
@@ -745,9 +811,11 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
   // The GroupNorm finalize counters start every decode at zero (each
   // finalize leaves them at zero; this also clears what an aborted decode
   // may have left).
-  if (cudaMemsetAsync(d.gn_cnt, 0, static_cast<size_t>(n) * ch->groups * sizeof(unsigned), s) !=
-      cudaSuccess)
-    return VAE_ECUDA;
+  // (with the GroupNorm-ahead counters and row flags right after them)
+  if (cudaMemsetAsync(d.gn_cnt, 0, d.zero_bytes, s) != cudaSuccess) return VAE_ECUDA;
+  ch->ga_flags = d.ga_flags;
+  ch->ga_next = d.ga_next;
+  ch->ga_idx = 0;
   // z / scaling_factor + shift_factor, NCHW -> NHWC (channels padded to 32).
   const float *lat = nullptr;
   {
@@ -915,6 +983,8 @@ int decode_causal_impl(Chain *ch, const float *z, int n, int t, int h, int w, fl
   if (cudaMemsetAsync(d.gn_cnt, 0, static_cast<size_t>(n) * ch->groups * sizeof(unsigned), s) !=
       cudaSuccess)
     return VAE_ECUDA;
+  ch->ga_flags = ch->ga_next = nullptr;  // (its convs have time taps: no GroupNorm ahead)
+  ch->ga_idx = 0;
   const long long vox = static_cast<long long>(t) * h * w;
   const float *lat = nullptr;
   {

@@ -139,6 +139,15 @@ struct IgemmDesc {
   float2 *rs_out = nullptr;
   float rs_scale = 1.0f;
   int rs_cols = 0, rs_ld = 0;
+  // GroupNorm ahead (Conv; only where igemm_gn_ahead_ok(d)): `a` is not an
+  // input but made by the launch itself, a = tf32(silu(ga_x * ga_scale[s][c]
+  // + ga_shift[s][c])) ([s][a_c] arrays, s = image / t), row by row ahead of
+  // the tiles that read it. ga_flags: imgs * hin ints, none equal to ga_epoch
+  // on entry (a row is made when its flag reads ga_epoch); ga_next: an int
+  // that is 0 on entry (the row counter).
+  const float *ga_x = nullptr, *ga_scale = nullptr, *ga_shift = nullptr;
+  int *ga_flags = nullptr, *ga_next = nullptr;
+  int ga_epoch = 0;
 };
 // Output-channel (column) tile of a launch with `cout` columns.
 int igemm_col_tile(int cout);
@@ -150,6 +159,13 @@ int igemm_col_tile(int cout);
 bool igemm_input_gn_ok(const IgemmDesc &d);
 // Whether igemm_launch takes a softmax-normalised A (sm_m) for this GEMM.
 bool igemm_softmax_a_ok(const IgemmDesc &d);
+// Whether igemm_launch can make its A operand from ga_x (GroupNorm ahead):
+// 3x3 single-frame convs on the halo (256-channel tiles, rows wider than 64,
+// no shortcut) or channel-major (65-128 output channels) paths, TF32
+// products, a_c in {32, 64, 128, 256, 512}, output NHWC; opt-in (VAE_GNA=on:
+// slower than the separate pass on GB300). A launch that ends up on another
+// path returns VAE_EUNSUPPORTED before doing anything.
+bool igemm_gn_ahead_ok(const IgemmDesc &d);
 // Split-K reduce (splitk.cu): out = alpha * sum of the partials + bias
 // (+ residual), rounded on request; GroupNorm partials [samples][groups][slots]
 // of the result when stat_part is given (*stat_slots receives slots, 0 if none).

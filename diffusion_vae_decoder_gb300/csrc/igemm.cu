@@ -128,8 +128,8 @@ int pair_setting() {
 
 // Output tiles per image of a conv / upsample conv whose tiles hold `rows`
 // pixel rows (per output parity tile for the upsample conv).
-long long tiles_per_image(const IgemmDesc &d, int rows) {
-  const int bw = std::min(128, pow2_at_least(d.win));
+long long tiles_per_image(const IgemmDesc &d, int rows, int max_bw = 128) {
+  const int bw = std::min(max_bw, pow2_at_least(d.win));
   const int bh = rows / bw;
   long long t = static_cast<long long>(ceil_div(d.win, bw)) * ceil_div(d.hin, bh);
   if (d.mode == AMode::Upsample) t *= 4;  // one tile per output parity
@@ -166,10 +166,18 @@ bool use_pair(const IgemmDesc &d) {
   return est2 <= est1;
 }
 
-long long stat_slots_for(const IgemmDesc &d, bool pair) {
+long long stat_slots_for(const IgemmDesc &d, bool pair, int max_bw) {
   if (!(d.mode == AMode::Conv || d.mode == AMode::Upsample)) return 0;
   const int ms = (pair || pick_bn(d.cout) == 128) ? 2 : 1;
-  return static_cast<long long>(d.t > 0 ? d.t : 1) * tiles_per_image(d, ms * kBM) * ms * 4;
+  return static_cast<long long>(d.t > 0 ? d.t : 1) * tiles_per_image(d, ms * kBM, max_bw) * ms * 4;
+}
+
+// Channel-major tiles (MODE 4, see igemm_launch) take bands at most 64 pixels
+// wide; this is the row width the conv's tiles get when they may run so.
+int conv_max_bw(const IgemmDesc &d, bool split) {
+  const bool swap_geom = !split && d.mode == AMode::Conv && pick_bn(d.cout) == 128 && d.k == 3 &&
+                         d.kt == 1 && !d.out_nchw && buffered_a_enabled();
+  return swap_geom ? 64 : 128;
 }
 
 }  // namespace
@@ -205,6 +213,31 @@ bool igemm_input_gn_ok(const IgemmDesc &d) {
   return operand_transforms_enabled() && halo_candidate(d, d.precise || split_forced());
 }
 
+// GroupNorm ahead runs only with VAE_GNA=on. Measured on GB300 it loses to
+// the separate apply pass (which streams at about 0.9 of HBM bandwidth): in
+// the 1024^2 decode the 1024^2 x 128-channel convs go from 0.39-0.45 ms to
+// 0.69-0.73 ms (0.79-0.83 ms with sixteen loads in flight per thread), the
+// 256^2 x 512-channel ones from 0.30 to 0.39 ms, against 0.05-0.17 ms saved
+// per GroupNorm: the four extra warps' row stream competes with the conv's
+// own copies and stores, and the first tiles wait for their rows.
+bool gn_ahead_enabled() {
+  static const bool v = [] {
+    const char *e = std::getenv("VAE_GNA");
+    return e && std::strcmp(e, "on") == 0;
+  }();
+  return v;
+}
+
+bool igemm_gn_ahead_ok(const IgemmDesc &d) {
+  if (!gn_ahead_enabled() || d.precise || split_forced() || d.mode != AMode::Conv || d.k != 3 ||
+      d.kt != 1 || d.out_nchw || !buffered_a_enabled())
+    return false;
+  if (d.a_c <= 0 || d.a_c > 512 || 128 % (d.a_c / 4) != 0 || d.a_c % 32) return false;
+  const int bn = pick_bn(d.cout);
+  if (bn == 256) return halo_candidate(d, false);
+  return bn == 128 && d.win >= 2;
+}
+
 bool igemm_softmax_a_ok(const IgemmDesc &d) {
   return operand_transforms_enabled() && d.mode == AMode::Gemm && !d.precise &&
          !split_forced() && pick_bn(d.cout) == 256;
@@ -213,7 +246,8 @@ bool igemm_softmax_a_ok(const IgemmDesc &d) {
 // Upper bound over the tile geometries a launch may take (callers size the
 // partials buffer with it; the launch reports the stride it used).
 long long igemm_stat_slots(const IgemmDesc &d) {
-  return std::max(stat_slots_for(d, false), stat_slots_for(d, true));
+  return std::max({stat_slots_for(d, false, 128), stat_slots_for(d, false, 64),
+                   stat_slots_for(d, true, 128)});
 }
 
 int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
@@ -230,8 +264,11 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   const bool split = d.precise || split_forced();
   const bool pair = !split && use_pair(d);
   // operand transforms: only on the paths that implement them
-  const int xf = d.gn_scale ? 1 : d.sm_m ? 2 : 0;
-  if (d.gn_scale && d.sm_m) return VAE_EINVAL;
+  const int xf = d.gn_scale ? 1 : d.sm_m ? 2 : d.ga_x ? 3 : 0;
+  if ((d.gn_scale != nullptr) + (d.sm_m != nullptr) + (d.ga_x != nullptr) > 1) return VAE_EINVAL;
+  if (xf == 3 && (!igemm_gn_ahead_ok(d) || !d.ga_scale || !d.ga_shift || !d.ga_flags ||
+                  !d.ga_next || d.ga_epoch == 0))
+    return VAE_EUNSUPPORTED;
   if (xf == 1 && (!igemm_input_gn_ok(d) || !d.gn_shift)) return VAE_EUNSUPPORTED;
   if (xf == 2 && (!igemm_softmax_a_ok(d) || !d.sm_inv_l || d.sm_cols <= 0)) return VAE_EUNSUPPORTED;
   if (d.rs_out && (d.mode != AMode::Gemm || d.rs_ld < ceil_div(d.cout, bn) || d.rs_cols <= 0))
@@ -266,6 +303,16 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   kp.rs_ld = d.rs_ld;
   if (xf == 1 && ((reinterpret_cast<uintptr_t>(d.gn_scale) | reinterpret_cast<uintptr_t>(d.gn_shift)) & 15))
     return VAE_EINVAL;
+  kp.ga_x = d.ga_x;
+  kp.ga_scale = d.ga_scale;
+  kp.ga_shift = d.ga_shift;
+  kp.ga_t = const_cast<float *>(d.a);
+  kp.ga_flags = d.ga_flags;
+  kp.ga_next = d.ga_next;
+  kp.ga_epoch = d.ga_epoch;
+  if (xf == 3 && ((reinterpret_cast<uintptr_t>(d.ga_scale) | reinterpret_cast<uintptr_t>(d.ga_shift) |
+                   reinterpret_cast<uintptr_t>(d.ga_x)) & 15))
+    return VAE_EINVAL;
 
   CUtensorMap ta{}, tb{}, ts{};
   int bkdim;
@@ -297,7 +344,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
       kp.hout = d.hin;
       kp.wout = d.win;
       const int rows = (bn == 128 || pair ? 2 : 1) * kBM;  // M sub-tiles (see Cfg)
-      kp.bw = std::min(128, pow2_at_least(d.win));
+      kp.bw = std::min(conv_max_bw(d, split), pow2_at_least(d.win));
       kp.bh = rows / kp.bw;
       kp.tiles_x = ceil_div(d.win, kp.bw);
       kp.tiles_y = ceil_div(d.hin, kp.bh);
@@ -434,7 +481,8 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // inside one 32-channel chunk; otherwise the caller computes them itself.
   if (d.stat_part) {
     const int cg = d.stat_groups > 0 ? d.cout / d.stat_groups : 0;
-    const long long slots = stat_slots_for(d, pair);
+    const long long slots =
+        stat_slots_for(d, pair, d.mode == AMode::Conv ? conv_max_bw(d, split) : 128);
     if (epi && d.mode != AMode::Gemm && d.cout % 32 == 0 && d.stat_groups > 0 &&
         d.cout % d.stat_groups == 0 && cg >= 1 && cg <= 32 && (cg & (cg - 1)) == 0 &&
         slots > 0 && slots < (1ll << 31)) {
@@ -461,10 +509,12 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   // channels: the MMA runs M = 128 channels x N = 256 pixels (one wide
   // instruction where the pixel-major tile needs two 128 x 128 ones that both
   // read the weights), and per 32-channel chunk one band of bh + 2 rows per
-  // kx serves the three ky taps. Needs the staged epilogue (it transposes).
+  // kx serves the three ky taps (bands at most 64 pixels wide: 4 rows + 2
+  // halo rows, three of them in flight). Needs the staged epilogue (it
+  // transposes).
   const bool swap = !split && !halo && d.mode == AMode::Conv && kp.k == 3 && kp.kt == 1 &&
-                    bn == 128 &&
-                    kp.splits == 1 && epi && kp.bw >= 2 && buffered_a_enabled();
+                    bn == 128 && kp.splits == 1 && epi && kp.bw >= 2 && kp.bw <= 64 &&
+                    (kp.bh + 2) * kp.bw * 128 <= 49152 && buffered_a_enabled();
   if (swap) {
     const uint64_t dims[4] = {static_cast<uint64_t>(d.a_c), static_cast<uint64_t>(d.win),
                               static_cast<uint64_t>(d.hin), static_cast<uint64_t>(d.imgs)};
@@ -475,6 +525,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
                              1};
     VAE_TRY(encode_tiled(&ta, d.a, 4, dims, str, box));
   }
+  if (xf == 3 && !(halo || swap)) return VAE_EUNSUPPORTED;
   if (halo) {
     const uint64_t dims[4] = {static_cast<uint64_t>(d.a_c), static_cast<uint64_t>(d.win),
                               static_cast<uint64_t>(d.hin), static_cast<uint64_t>(d.imgs)};
@@ -522,7 +573,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
   if (split) {
     rc = launch_split(static_cast<int>(d.mode), bn, ta, tb, ts, to, tr, kp, stream);
   } else if (xf) {
-    rc = launch_xf(xf, pair, ta, tb, ts, to, tr, kp, stream);
+    rc = launch_xf(xf, swap ? 4 : halo ? 3 : 2, pair, ta, tb, ts, to, tr, kp, stream);
   } else switch (d.mode) {
     case AMode::Conv:
       if (pair)

@@ -80,6 +80,16 @@ struct KParams {
   float2 *rs_out;
   float rs_scale;
   int rs_cols, rs_ld;
+  // XF = 3 (GroupNorm ahead): the conv's A source ga_t (= the tensor tmA
+  // reads) is the GroupNorm+SiLU of ga_x, made by four more warps of every
+  // CTA while the conv runs: they take image rows (units: image * hin + row)
+  // from the counter ga_next in order, write ga_t = tf32(silu(ga_x *
+  // ga_scale[s][c] + ga_shift[s][c])) for the row and set ga_flags[unit] =
+  // ga_epoch; the producer waits for the rows a tile reads before its copies.
+  const float *ga_x, *ga_scale, *ga_shift;
+  float *ga_t;
+  int *ga_flags, *ga_next;
+  int ga_epoch;
 };
 
 // One work item of a CTA: a tile and the range [k0, k1) of its reduction
@@ -146,11 +156,13 @@ struct WorkIter {
 // split it in place into TF32 parts (hi = tf32(v), lo = tf32(v - hi), lo
 // stored beside hi) and the MMA issuer forms a_hi b_hi + a_lo b_hi + a_hi
 // b_lo (three MMAs per step) into the FP32 accumulator.
-// XF: an operand transform by four more warps between the copy and the MMA
-// (1: GroupNorm+SiLU of the halo buffer, MODE 3; 2: softmax normalisation
-// of the GEMM A stage, MODE 2). Each CTA's copy lands on a barrier of its
-// own; the transforming warps of both CTAs of a pair then arrive on the
-// leader's barrier the MMA issuer waits on.
+// XF: four more warps per CTA. 1 and 2 transform each landed A buffer
+// between the copy and the MMA (1: GroupNorm+SiLU of the halo buffer, MODE
+// 3; 2: softmax normalisation of the GEMM A stage, MODE 2): each CTA's copy
+// lands on a barrier of its own, then the transforming warps of both CTAs
+// of a pair arrive on the leader's barrier the MMA issuer waits on. 3
+// (MODES 3, 4) writes the conv's A operand itself, the GroupNorm+SiLU of the
+// layer's input, a few rows ahead of the tiles that read it (see KParams).
 template <int BN, int MS, int MODE = 0, bool PAIR = false, bool SPLIT = false, int XF = 0>
 struct Cfg {
   static constexpr bool HALO = MODE == 3;
@@ -158,16 +170,19 @@ struct Cfg {
   static_assert(!PAIR || (MS == 1 && BN == 256 && MODE <= 3),
                 "paired tiles: 256 output columns, the pixel-major conv modes and GEMM");
   static_assert(!SPLIT || (!PAIR && MODE <= 2), "split products: per-step A and B stages");
-  static_assert(XF == 0 || (!SPLIT && ((XF == 1 && MODE == 3) || (XF == 2 && MODE == 2 && MS == 1))),
-                "operand transforms: GroupNorm on halo buffers, softmax on GEMM A stages");
+  static_assert(XF == 0 || (!SPLIT && ((XF == 1 && MODE == 3) || (XF == 2 && MODE == 2 && MS == 1) ||
+                                       (XF == 3 && (MODE == 3 || MODE == 4)))),
+                "operand transforms: GroupNorm on halo buffers, softmax on GEMM A stages, "
+                "GroupNorm ahead of the buffered-A conv modes");
   static constexpr int THREADS = (SPLIT || XF) ? kThreads + 128 : kThreads;
   static constexpr int NCTA = PAIR ? 2 : 1;
-  // Separately buffered A operand (MODES 3 and 4): two buffers, each serving
-  // several reduction steps. MODE 4 holds (bh + 2) rows x bw pixels with
-  // bh * bw = 256, at most 64 KB (bw <= 128).
+  // Separately buffered A operand (MODES 3 and 4), each buffer serving
+  // several reduction steps: MODE 3 two halo buffers; MODE 4 three bands of
+  // (bh + 2) rows x bw pixels with bh * bw = 256, at most 48 KB (bw <= 64),
+  // so that a band's copy has two bands' MMAs to land in.
   static constexpr uint32_t HALO_BYTES =
-      HALO ? ((MS + 2) * 130 * 128 + 1023) / 1024 * 1024 : SWAP ? 65536 : 0;
-  static constexpr int HALO_BUFS = (HALO || SWAP) ? 2 : 0;
+      HALO ? ((MS + 2) * 130 * 128 + 1023) / 1024 * 1024 : SWAP ? 49152 : 0;
+  static constexpr int HALO_BUFS = HALO ? 2 : SWAP ? 3 : 0;
   // MODE 4: appended-shortcut tiles (MS x 128 rows each) sharing one A buffer.
   static constexpr int SC_PER_BUF = SWAP ? static_cast<int>(HALO_BYTES / (MS * kABytes)) : 1;
   static constexpr uint32_t A_LOAD = (HALO || SWAP) ? 0 : MS * kABytes;  // TMA bytes per stage
@@ -182,7 +197,7 @@ struct Cfg {
   // buffers let a block's store drain (and the next block's residual land)
   // while the warp works on the current one; the halo modes keep one so that
   // their shared memory holds more weight stages (measured faster on GB300).
-  static constexpr int NSTG = HALO ? 1 : 2;
+  static constexpr int NSTG = (HALO || SWAP) ? 1 : 2;
   static constexpr uint32_t STAGING = 4 * NSTG * 4096;
   static constexpr int FIT =
       (232448 - 1024 - STAGING - 1024 - HALO_BUFS * HALO_BYTES) / STAGE_BYTES;
@@ -192,7 +207,7 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
   static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
   static constexpr size_t SMEM = 1024 + HALO_BUFS * HALO_BYTES + STAGES * STAGE_BYTES + STAGING +
-                                 (4 * STAGES + 19) * sizeof(uint64_t) + 16;
+                                 (4 * STAGES + 21) * sizeof(uint64_t) + 16;
   static_assert(STAGES >= 2, "at least double-buffered stages");
   static_assert(!(HALO || SWAP) || STAGES >= 3, "buffered-A modes need a weight ring");
   static_assert(!SWAP || (BN == 128 && MS == 2), "MODE 4 tiles are 128 channels x 256 pixels");
@@ -309,8 +324,8 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
   uint64_t *drain = acc_empty + 2;  // used only after an abort
   uint64_t *res_bar = drain + 1;    // per epilogue warp and staging buffer: residual landed
   uint64_t *a_full = res_bar + 8;   // MODES 3, 4: A buffer landed / free
-  uint64_t *a_empty = a_full + 2;
-  uint64_t *xfull = a_empty + 2;    // SPLIT / XF 2: stage transformed, ready for the MMA
+  uint64_t *a_empty = a_full + 3;  // (three of each: the deepest A-buffer ring)
+  uint64_t *xfull = a_empty + 3;    // SPLIT / XF 2: stage transformed, ready for the MMA
   uint64_t *xa_full = xfull + STAGES;  // XF 2: this CTA's A stage landed
   uint64_t *h_full = xa_full + STAGES;  // XF 1: this CTA's halo buffer landed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(h_full + 2);
@@ -335,13 +350,13 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
     }
     mbar_init(drain, 1);
     for (int q = 0; q < 8; ++q) mbar_init(&res_bar[q], 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       // XF 1: the transforming warps of every CTA of the pair arrive instead
       // of a copy completing
       mbar_init(&a_full[b], XF == 1 ? 4 * C::NCTA : 1);
       mbar_init(&a_empty[b], 1);
-      mbar_init(&h_full[b], 1);
     }
+    for (int b = 0; b < 2; ++b) mbar_init(&h_full[b], 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&xfull[s], SPLIT ? 128 : 4 * C::NCTA);  // splitting threads / transforming warps
       mbar_init(&xa_full[s], 1);
@@ -400,6 +415,21 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
       const int boff = PAIR ? static_cast<int>(rank) * (BN / 2) : 0;
       const int yoff = PAIR ? static_cast<int>(rank) * (p.bh >> 1) : 0;
       const uint32_t tx_mult = PAIR ? 2u : 1u;
+      // XF 3: wait until image rows [r0, r1] (clamped to the image) are made
+      // for this launch, then let the async proxy (the TMA) read them.
+      auto wait_rows = [&](int img, int r0, int r1) -> bool {
+        r0 = max(r0, 0);
+        r1 = min(r1, p.hin - 1);
+        for (int r = r0; r <= r1; ++r) {
+          const int *f = p.ga_flags + static_cast<long long>(img) * p.hin + r;
+          if (ld_acquire_gpu(f) == p.ga_epoch) continue;
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire_gpu(f) != p.ga_epoch)
+            if (*abort || global_timer_ns() - t0 > p.wait_ns) return false;
+        }
+        fence_proxy_async_global();
+        return true;
+      };
       WorkIter<MODE> it(p, wid, wcount);
       Work w;
       while (!failed && it.next(p, w)) {
@@ -421,6 +451,16 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
           tx = rem % p.tiles_x;
         }
         const int n_idx = img / p.t, t_idx = img % p.t;
+        if constexpr (XF == 3) {
+          // the rows this CTA's A copies of the tile read, once made
+          const int r0 = MODE == 3 ? ty * p.bh + yoff - 1 : ty * p.bh - 1;
+          const int r1 = MODE == 3 ? r0 + (PAIR ? (p.bh >> 1) : p.bh) + 1 : r0 + p.bh + 1;
+          if (!wait_rows(img, r0, r1)) {
+            raise_error(p, abort);
+            failed = true;
+            break;
+          }
+        }
         if constexpr (MODE == 3) {
           // One halo tile per 32-channel chunk, then one weight stage per tap
           // (no appended shortcut in this mode).
@@ -446,7 +486,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
             }
             a_pending |= 1u << abuf;
             a_par = (a_par & ~(1u << abuf)) | (aphase << abuf);
-            if (++abuf == 2) {
+            if (++abuf == C::HALO_BUFS) {
               abuf = 0;
               aphase ^= 1u;
             }
@@ -502,7 +542,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
               }
               a_pending |= 1u << abuf;
               a_par = (a_par & ~(1u << abuf)) | (aphase << abuf);
-              if (++abuf == 2) {
+              if (++abuf == C::HALO_BUFS) {
                 abuf = 0;
                 aphase ^= 1u;
               }
@@ -608,7 +648,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
           for (int s = 0; s < STAGES; ++s)
             if (pending & (1u << s)) mbar_wait_drain(&full[s], (pend_par >> s) & 1u, p.wait_ns);
           if (XF != 1)
-            for (int b = 0; b < 2; ++b)
+            for (int b = 0; b < C::HALO_BUFS; ++b)
               if (a_pending & (1u << b))
                 mbar_wait_drain(&a_full[b], (a_par >> b) & 1u, p.wait_ns);
         }
@@ -697,7 +737,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
             }
             if (failed) break;
             commit(&a_empty[abuf]);
-            if (++abuf == 2) {
+            if (++abuf == C::HALO_BUFS) {
               abuf = 0;
               aphase ^= 1u;
             }
@@ -747,7 +787,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
               }
               if (failed) break;
               umma_commit(&a_empty[abuf]);
-              if (++abuf == 2) {
+              if (++abuf == C::HALO_BUFS) {
                 abuf = 0;
                 aphase ^= 1u;
               }
@@ -892,7 +932,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
           const int mp0 = pc * 32;  // first pixel of the chunk within the tile
           const int bx = tx * p.bw + (mp0 & (p.bw - 1)), by = ty * p.bh + (mp0 >> lbw);
           float *sb = stg + sbuf * 1024;
-          if (lane == 0) bulk_wait_read<1>();  // the store that used sb last is done
+          if (lane == 0) bulk_wait_read<C::NSTG - 1>();  // the store that used sb last is done
           __syncwarp();
           // Pixel j is row j of the block, this lane's channel its column;
           // the 128-byte swizzle puts 16-byte chunk (lane / 4) at
@@ -911,7 +951,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
             tma_store_4d(&tmO, sb, c0, bx, by, img);
             bulk_commit();
           }
-          sbuf ^= 1;
+          if (C::NSTG == 2) sbuf ^= 1;
           if (p.stat_part) {
             // (count, mean, M2) of each group (stat_cg adjacent lanes) over
             // the chunk's in-image pixels; slot = (frame, tile, chunk).
@@ -1406,7 +1446,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
           else
             mbar_arrive_cluster(afull_c + abuf * 8);
         }
-        if (++abuf == 2) {
+        if (++abuf == C::HALO_BUFS) {
           abuf = 0;
           aphase ^= 1u;
         }
@@ -1474,6 +1514,60 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
+        }
+      }
+    }
+  }
+
+  if constexpr (XF == 3) {
+    if (warp >= 6) {
+      // ---------------------------------------------------------- GroupNorm ahead (XF 3)
+      // Rows in the order the counter hands them out (lowest first, so the
+      // first tiles' rows come first): t = tf32(silu(x * scale + shift)),
+      // the same arithmetic as the separate GroupNorm apply; then the row's
+      // flag. Thread tt keeps channel quad tt % (cin / 4) (128 is a multiple
+      // of cin / 4), loading its affine once per row; eight 16-byte loads in
+      // flight per thread.
+      __shared__ int s_unit;
+      constexpr int kU = 8;
+      const int tt = threadIdx.x - kThreads;  // 0..127
+      const int c4 = p.cin_pad >> 2;
+      const int q4 = tt % c4;
+      const int units = p.imgs * p.hin;
+      const long long row_f4 = static_cast<long long>(p.win) * c4;
+      while (true) {
+        if (tt == 0) s_unit = *abort ? units : atomicAdd(p.ga_next, 1);
+        named_barrier_sync(1, 128);
+        const int u = s_unit;
+        if (u >= units) break;
+        const int sample = (u / p.hin) / p.t;
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p.ga_scale) +
+                               static_cast<long long>(sample) * c4 + q4);
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p.ga_shift) +
+                               static_cast<long long>(sample) * c4 + q4);
+        const float4 *src = reinterpret_cast<const float4 *>(p.ga_x) + u * row_f4;
+        float4 *dst = reinterpret_cast<float4 *>(p.ga_t) + u * row_f4;
+        for (long long i0 = tt; i0 < row_f4; i0 += 128 * kU) {
+          float4 v[kU];
+#pragma unroll
+          for (int k = 0; k < kU; ++k)
+            if (i0 + 128 * k < row_f4) v[k] = __ldg(src + i0 + 128 * k);
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            float e[4] = {fmaf(v[k].x, a.x, b.x), fmaf(v[k].y, a.y, b.y),
+                          fmaf(v[k].z, a.z, b.z), fmaf(v[k].w, a.w, b.w)};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) e[j] = round_tf32(__fdividef(e[j], 1.0f + __expf(-e[j])));
+            v[k] = make_float4(e[0], e[1], e[2], e[3]);
+          }
+#pragma unroll
+          for (int k = 0; k < kU; ++k)
+            if (i0 + 128 * k < row_f4) dst[i0 + 128 * k] = v[k];
+        }
+        named_barrier_sync(1, 128);  // every store of the row issued (and s_unit read)
+        if (tt == 0) {
+          __threadfence();
+          st_release_gpu(p.ga_flags + u, p.ga_epoch);
         }
       }
     }
@@ -1549,8 +1643,9 @@ int launch_split(int mode, int bn, const CUtensorMap &ta, const CUtensorMap &tb,
                  const KParams &kp, cudaStream_t s);
 
 // Operand-transform instantiations (igemm_xf.cu): xf 1 (input GroupNorm,
-// halo conv) or 2 (softmax A, GEMM), 256-column tiles, paired or not.
-int launch_xf(int xf, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+// halo conv), 2 (softmax A, GEMM) or 3 (GroupNorm ahead; mode 3 halo or 4
+// channel-major), paired or not where the mode has pairs.
+int launch_xf(int xf, int mode, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
               const CUtensorMap &ts, const CUtensorMap &to, const CUtensorMap &tr,
               const KParams &kp, cudaStream_t s);
 

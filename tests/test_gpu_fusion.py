@@ -1,19 +1,19 @@
-"""Operand transforms inside the tensor-core kernels (cortiq-engine "Module
-vae": VaeResnetRef GroupNorm -> SiLU -> conv; VaeAttnRef softmax(q k^T /
-sqrt(c)) v), against the float64 oracle:
+"""GroupNorm and softmax work moved into the tensor-core kernels
+(cortiq-engine "Module vae": VaeResnetRef GroupNorm -> SiLU -> conv;
+VaeAttnRef softmax(q k^T / sqrt(c)) v), against the float64 oracle:
 
-* the resnets' GroupNorm+SiLU applied by the 3x3 conv that reads it, on the
-  halo rows it stages (only the per-(sample, channel) affine is computed
-  beforehand), where the conv runs 256-channel halo tiles;
-* the c = 512 attention's row softmax folded into its two GEMMs (row
-  statistics from the score GEMM's epilogue, normalisation of the P.V
-  kernel's A stages).
+* the resnets' GroupNorm+SiLU made by extra warps of the conv that reads
+  it, row by row ahead of its tiles (GroupNorm ahead: opt-in, VAE_GNA=on,
+  measured slower than the separate pass on GB300; run in a child process);
+* opt-in (VAE_FUSE=on: measured slower than the separate passes on GB300,
+  run in a child process): the resnets' GroupNorm+SiLU applied by the 3x3
+  conv that reads it, on the halo rows it stages, where the conv runs
+  256-channel halo tiles; and the c = 512 attention's row softmax folded into
+  its two GEMMs (row statistics from the score GEMM's epilogue, normalisation
+  of the P.V kernel's A stages).
 
-The transforms are opt-in (VAE_FUSE=on: measured slower than the separate
-passes on GB300), so the default run checks the separate passes here and a
-child process runs the same cases, the 256^2 decoder parity and its
-layer-by-layer trace with the transforms on (the setting is read once per
-process)."""
+Each child runs this module, the 256^2 decoder parity and its layer-by-layer
+trace (the settings are read once per process)."""
 import os
 import subprocess
 import sys
@@ -72,15 +72,16 @@ def test_ragged_batch_decode(pkg):
     assert m["cos"] >= COS_MIN and m["max_abs"] <= RGB_MAXABS, m
     for b in range(2):
         assert metrics(got[b], ref[b])["cos"] >= COS_MIN, b
-    # At 48 x 80 the five GroupNorms ahead of a 256-channel conv without a
-    # shortcut operand fold (the 512 -> 256 resnet's norm1, both norms of the
-    # other two resnets); its norm2 feeds a conv with a 1x1 shortcut.
-    act = 2 * 48 * 80 * 256 * 4
-    folded = [s for s in steps if s["kind"] == "groupnorm" and s["bytes"] < 0.05 * act]
-    if _fuse_on():
-        assert len(folded) == 5, [s for s in steps if s["kind"] == "groupnorm"]
-    else:
-        assert not folded
+    # GroupNorm steps reduced to the per-channel affine, their apply running
+    # inside the conv. At 48 x 80 (256-channel halo convs) the five ahead of
+    # a conv without a shortcut operand (the 512 -> 256 resnet's norm1, both
+    # norms of the other two resnets; its norm2 feeds a conv with a 1x1
+    # shortcut); at 96 x 160 all six (channel-major convs) with GroupNorm
+    # ahead (VAE_FUSE=on's halo transform covers only the 48 x 80 ones).
+    affine = [s for s in steps if s["kind"] == "groupnorm_affine"]
+    gna_on = os.environ.get("VAE_GNA") == "on"
+    expect = 11 if gna_on else (5 if _fuse_on() else 0)
+    assert len(affine) == expect, [s for s in steps if s["kind"].startswith("groupnorm")]
 
 
 def test_ragged_batch_layers(pkg):
@@ -108,13 +109,29 @@ def test_attention_softmax_folded_on_ragged_keys(pkg):
         assert m["cos"] >= COS_MIN and m["rel_l2"] <= REL_L2_MAX, (what, m)
 
 
+def test_groupnorm_ahead_on():
+    """The same checks, the decoder_256 parity and its layer trace with the
+    GroupNorm made ahead of the conv's tiles (VAE_GNA=on)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    if os.environ.get("VAE_GNA") == "on" or _fuse_on():
+        pytest.skip("already a child")
+    env = dict(os.environ, VAE_GNA="on")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m", "gpu",
+                        "tests/test_gpu_fusion.py", "tests/test_gpu_chain.py::test_decoder_256_parity",
+                        "tests/test_gpu_layers.py::test_layer_parity_decoder_256"],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout
+
+
 def test_operand_transforms_on():
     """The same checks, the decoder_256 parity and the layer-by-layer trace of
     the 256^2 decode with VAE_FUSE=on."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    if _fuse_on():
-        pytest.skip("already the child")
+    if _fuse_on() or os.environ.get("VAE_GNA") == "on":
+        pytest.skip("already a child")
     env = dict(os.environ, VAE_FUSE="on")
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m", "gpu",
                         "tests/test_gpu_fusion.py", "tests/test_gpu_chain.py::test_decoder_256_parity",
