@@ -510,8 +510,8 @@ def _graph_decode_stats(pkg, arch, latent, seed, steps):
 
 def run_extras(pkg, tf32_peak, gpu_index):
     """The other configured workloads, each on its own (rank 0, one GPU):
-    the 256^2 decode (Mpix/s), the tiny decoder (latency), the 3-D causal
-    conv stack [1,128,17,128,128] (conv TFLOP/s)."""
+    the 256^2 decode and the batch-4 512^2 decode (Mpix/s), the tiny decoder
+    (latency), the 3-D causal conv stack [1,128,17,128,128] (conv TFLOP/s)."""
     import torch
     out = {}
     ms, conv_tf, conv_ms = _graph_decode_stats(pkg, "flux", (1, 16, 32, 32),
@@ -520,6 +520,12 @@ def run_extras(pkg, tf32_peak, gpu_index):
                           "unit": "Mpix/s", "ms_per_step": ms, "steps": 200,
                           "conv_tflops": conv_tf, "conv_frac": conv_tf / tf32_peak,
                           "conv_ms_per_step": conv_ms}
+    lat4 = WORKLOADS["decoder_512_b4"]["latent"]
+    ms, conv_tf, conv_ms = _graph_decode_stats(pkg, "flux", lat4, WORKLOADS["decoder_512_b4"]["seed"],
+                                               20)
+    out["decoder_512_b4"] = {"value": out_pixels(lat4) / 1e6 / (ms / 1e3), "unit": "Mpix/s",
+                             "ms_per_step": ms, "steps": 20, "conv_tflops": conv_tf,
+                             "conv_frac": conv_tf / tf32_peak, "conv_ms_per_step": conv_ms}
     ms, conv_tf, _ = _graph_decode_stats(pkg, "tiny", (1, 16, 8, 8), S.seed_of("tiny_decoder"),
                                          500)
     out["tiny_decoder"] = {"latency_ms": ms, "value": out_pixels((1, 16, 8, 8)) / 1e6 / (ms / 1e3),
