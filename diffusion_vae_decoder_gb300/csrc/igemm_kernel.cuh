@@ -174,7 +174,14 @@ struct Cfg {
                                        (XF == 3 && (MODE == 3 || MODE == 4)))),
                 "operand transforms: GroupNorm on halo buffers, softmax on GEMM A stages, "
                 "GroupNorm ahead of the buffered-A conv modes");
-  static constexpr int THREADS = (SPLIT || XF) ? kThreads + 128 : kThreads;
+  // Epilogue warps: eight (two per TMEM lane quarter, each taking half of
+  // the tile's columns) on the upsample parity tiles, whose epilogue (four
+  // taps of reduction per output pixel, GroupNorm statistics of a large
+  // output) otherwise paces the tile: 0.74 -> 0.63 ms for the 1024^2
+  // upsample conv. Four elsewhere (measured no faster with eight on the
+  // channel-major and GEMM tiles).
+  static constexpr int EPW = (!SPLIT && !XF && MODE == 1 && BN >= 128) ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPW + ((SPLIT || XF) ? 128 : 0);
   static constexpr int NCTA = PAIR ? 2 : 1;
   // Separately buffered A operand (MODES 3 and 4), each buffer serving
   // several reduction steps: MODE 3 two halo buffers; MODE 4 three bands of
@@ -198,7 +205,7 @@ struct Cfg {
   // while the warp works on the current one; the halo modes keep one so that
   // their shared memory holds more weight stages (measured faster on GB300).
   static constexpr int NSTG = (HALO || SWAP) ? 1 : 2;
-  static constexpr uint32_t STAGING = 4 * NSTG * 4096;
+  static constexpr uint32_t STAGING = EPW * NSTG * 4096;
   static constexpr int FIT =
       (232448 - 1024 - STAGING - 1024 - HALO_BUFS * HALO_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
@@ -207,7 +214,7 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
   static constexpr int CH = BN < 32 ? BN : 32;  // epilogue column chunk
   static constexpr size_t SMEM = 1024 + HALO_BUFS * HALO_BYTES + STAGES * STAGE_BYTES + STAGING +
-                                 (4 * STAGES + 21) * sizeof(uint64_t) + 16;
+                                 (4 * STAGES + 29) * sizeof(uint64_t) + 16;
   static_assert(STAGES >= 2, "at least double-buffered stages");
   static_assert(!(HALO || SWAP) || STAGES >= 3, "buffered-A modes need a weight ring");
   static_assert(!SWAP || (BN == 128 && MS == 2), "MODE 4 tiles are 128 channels x 256 pixels");
@@ -323,7 +330,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
   uint64_t *acc_empty = acc_full + 2;
   uint64_t *drain = acc_empty + 2;  // used only after an abort
   uint64_t *res_bar = drain + 1;    // per epilogue warp and staging buffer: residual landed
-  uint64_t *a_full = res_bar + 8;   // MODES 3, 4: A buffer landed / free
+  uint64_t *a_full = res_bar + 16;  // MODES 3, 4: A buffer landed / free
   uint64_t *a_empty = a_full + 3;  // (three of each: the deepest A-buffer ring)
   uint64_t *xfull = a_empty + 3;    // SPLIT / XF 2: stage transformed, ready for the MMA
   uint64_t *xa_full = xfull + STAGES;  // XF 2: this CTA's A stage landed
@@ -346,10 +353,10 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], PAIR ? 8 : 4);  // every epilogue warp of the pair
+      mbar_init(&acc_empty[b], C::EPW * C::NCTA);  // every epilogue warp of the pair
     }
     mbar_init(drain, 1);
-    for (int q = 0; q < 8; ++q) mbar_init(&res_bar[q], 1);
+    for (int q = 0; q < 2 * C::EPW; ++q) mbar_init(&res_bar[q], 1);
     for (int b = 0; b < 3; ++b) {
       // XF 1: the transforming warps of every CTA of the pair arrive instead
       // of a copy completing
@@ -846,8 +853,12 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
   } else if (!(SPLIT || XF) || warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int ew = warp - 2;  // epilogue warp index
+    // with eight epilogue warps, warp ew takes column half ew / 4 of the tile
+    constexpr int kHalves = C::EPW / 4;
+    const int half = ew >> 2;
     const int m = q * 32 + lane;
-    float *stg = staging + q * C::NSTG * 1024;  // this warp's 4 KB staging buffer(s)
+    float *stg = staging + ew * C::NSTG * 1024;  // this warp's 4 KB staging buffer(s)
     int sbuf = 0;
     uint32_t res_phase = 0;    // bit b: phase of this warp's residual barrier b
     uint32_t res_pending = 0;  // bit b: a residual load into buffer b not yet waited for
@@ -913,13 +924,15 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
           }
         };
         float rnext[32], rcur[32];
-        uint32_t mnext = chunk_mask(0);
-        if (p.has_res) load_res(0, mnext, rnext);
-        for (int pc = 0; pc < 8 && c0 < p.cout; ++pc) {
+        // this warp's 32-pixel chunks of the tile's 256
+        const int pc0 = half * (8 / kHalves), pc1 = pc0 + 8 / kHalves;
+        uint32_t mnext = chunk_mask(pc0 * 32);
+        if (p.has_res) load_res(pc0 * 32, mnext, rnext);
+        for (int pc = pc0; pc < pc1 && c0 < p.cout; ++pc) {
           const uint32_t vmask = mnext;
 #pragma unroll
           for (int j = 0; j < 32; ++j) rcur[j] = rnext[j];
-          if (pc + 1 < 8) {
+          if (pc + 1 < pc1) {
             mnext = chunk_mask((pc + 1) * 32);
             if (p.has_res) load_res((pc + 1) * 32, mnext, rnext);
           }
@@ -1062,8 +1075,10 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
       const float rbias = (MODE == 2 && p.bias_per_row && p.bias && valid) ? p.bias[row] : 0.f;
       float rs_m = -INFINITY, rs_s = 0.f;  // softmax statistics of this row (rs_out)
 
+      constexpr int kChunks = BN / C::CH;  // column chunks of the tile
+      const int cb = half * (kChunks / kHalves), ce = cb + kChunks / kHalves;
 #pragma unroll 1
-      for (int c = 0; c < BN / C::CH; ++c) {
+      for (int c = cb; c < ce; ++c) {
         float v[C::CH];
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -1142,7 +1157,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
           // The residual block of channels from c0 lands in staging buffer b
           // (its 4 KB box, clipped rows and channels read as zero).
           auto load_res = [&](int b, int c0) {
-            uint64_t *bar = &res_bar[q * 2 + b];
+            uint64_t *bar = &res_bar[ew * 2 + b];
             mbar_arrive_expect_tx(bar, 4096);
             float *dst = stg + b * 1024;
             if (MODE == 2)
@@ -1160,16 +1175,16 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
                 bulk_wait_read<0>();
                 load_res(sbuf, col0);
               }
-              if (C::NSTG == 2 && c + 1 < BN / C::CH && col0 + C::CH < p.cout) {
+              if (C::NSTG == 2 && c + 1 < ce && col0 + C::CH < p.cout) {
                 bulk_wait_read<0>();  // the store from the other buffer has read it
                 load_res(sbuf ^ 1, col0 + C::CH);
               }
             }
             res_pending |= 1u << sbuf;
-            if (C::NSTG == 2 && c + 1 < BN / C::CH && col0 + C::CH < p.cout)
+            if (C::NSTG == 2 && c + 1 < ce && col0 + C::CH < p.cout)
               res_pending |= 1u << (sbuf ^ 1);
             __syncwarp();
-            bool rok = mbar_wait(&res_bar[q * 2 + sbuf], (res_phase >> sbuf) & 1u, abort,
+            bool rok = mbar_wait(&res_bar[ew * 2 + sbuf], (res_phase >> sbuf) & 1u, abort,
                                  p.wait_ns);
             rok = __all_sync(0xffffffffu, rok);
             res_phase ^= 1u << sbuf;
@@ -1317,7 +1332,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
     if (lane == 0 && p.epi_tma) bulk_wait_all();
     for (int b = 0; b < 2; ++b)
       if (lane == 0 && (res_pending & (1u << b)))
-        mbar_wait_drain(&res_bar[q * 2 + b], (res_phase >> b) & 1u, p.wait_ns);
+        mbar_wait_drain(&res_bar[ew * 2 + b], (res_phase >> b) & 1u, p.wait_ns);
   } else if constexpr (SPLIT) {
     // ------------------------------------------------------------ split (SPLIT)
     // Each landed stage, in place: v -> hi = tf32(v), and lo = tf32(v - hi)
