@@ -630,17 +630,13 @@ int groupnorm_coop(const float *x, int n, int c, long long spatial, int groups, 
   if (static_cast<long long>(n) * spatial * c * 4 > kCoopMaxBytes) return VAE_EUNSUPPORTED;
   const long long per4 = spatial * c / 4;
   if (per4 > 0xffffffffll / 2) return VAE_EUNSUPPORTED;
-  static int coop_ok = -1, per_sm = 0;
   const int tpp = c / 4, ppi = kStatThreads / tpp;
   const size_t sm = static_cast<size_t>(ppi) * c * 3 * sizeof(float);
-  if (coop_ok < 0) {
-    int dev = 0, attr = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&attr, cudaDevAttrCooperativeLaunch, dev);
-    coop_ok = attr;
-  }
-  if (!coop_ok) return VAE_EUNSUPPORTED;
-  // resident blocks per SM at this dynamic shared memory size
+  int dev = 0, coop = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
+    return VAE_EUNSUPPORTED;
+  // resident blocks per SM at this call's dynamic shared memory size
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gn_coop_nhwc, 256, sm) !=
       cudaSuccess || per_sm <= 0)
     return VAE_EUNSUPPORTED;
