@@ -1,5 +1,5 @@
 """Failure paths on the GPU, exercised without a fault, a trap or a hang
-(SURVEY's failure-detection bar; "VAE decode -> GPU handoff", section
+(bounded device waits with an error word; "VAE decode -> GPU handoff", section
 "Correctness gate": a status comes back instead of a silent fallback):
 
   * a bounded device-side wait that runs out: the conv's stream-K hand-off
