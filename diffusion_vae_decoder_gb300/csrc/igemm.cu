@@ -537,8 +537,12 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
     VAE_TRY(encode_tiled(&ta, d.a, 4, dims, str, box));
   }
 
-  // Stream-K for convs whose whole tiles would leave the last round of SMs
-  // mostly idle (e.g. 256 tiles on 152 SMs: 1.68 rounds run as 2). Not for
+  // Stream-K for convs on 1-SM tiles whose whole tiles would leave the last
+  // round of SMs mostly idle (e.g. 256 tiles on 152 SMs: 1.68 rounds run as
+  // 2). (On paired tiles -- ranges per pair, each CTA handing its rows to the
+  // same-rank CTA of the next pair, a cooperative cluster launch -- it was
+  // exact but measured slower: the 128^2 x 512-channel convs 0.100-0.109 ->
+  // 0.102-0.119 ms.) Not for
   // the attention GEMMs (measured slower): their n-tiles of one row block
   // share a large A operand through L2 only while they run side by side,
   // which the stream-K ranges undo.
@@ -551,6 +555,7 @@ int igemm_launch(const IgemmDesc &d, cudaStream_t stream) {
     const double rounds = static_cast<double>(tiles) / sms;
     const double eff = rounds / std::ceil(rounds);
     const int ms = (!halo && bn == 128) ? 2 : 1;
+    // raw partial sums of one CTA's rows of a tile: ms x 128 rows x bn
     const size_t slot = static_cast<size_t>(ms) * bn * kBM;
     const size_t need = static_cast<size_t>(sms) * slot + static_cast<size_t>(sms) * 4;
     // Only long reductions: on short ones the tail/head partials would cost

@@ -55,7 +55,8 @@ struct KParams {
   // between two CTAs: the CTA holding its later part (the tail, at the start
   // of its range) writes the raw sums to its slot of sk_part and raises its
   // flags; the CTA holding the head (at the end of its range) adds them in
-  // its epilogue. Fixed split points: deterministic.
+  // its epilogue. Fixed split points: deterministic. (1-SM tiles only; the
+  // hand-over indexes the neighbour as blockIdx + NCTA.)
   int sk;
   int sk_units;
   long long sk_total;
@@ -1007,7 +1008,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
       if (w.head) {
         bool ok = true;
         if (lane == 0) {
-          const int *f = p.sk_flag + (blockIdx.x + 1) * 4 + q;
+          const int *f = p.sk_flag + (blockIdx.x + C::NCTA) * 4 + q;
           const uint64_t t0 = global_timer_ns();
           while (ld_acquire_gpu(f) == 0) {
             if (*abort || global_timer_ns() - t0 > p.wait_ns) {
@@ -1099,7 +1100,7 @@ __global__ void __launch_bounds__(Cfg<BN, MS, MODE, PAIR, SPLIT, XF>::THREADS, 1
             continue;
           }
           const float4 *src =
-              reinterpret_cast<const float4 *>(p.sk_part) + (blockIdx.x + 1) * sk_slot_f4 + off;
+              reinterpret_cast<const float4 *>(p.sk_part) + (blockIdx.x + C::NCTA) * sk_slot_f4 + off;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float4 t = __ldcg(src + j * 128);

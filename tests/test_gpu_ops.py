@@ -297,14 +297,17 @@ def test_conv2d_channel_major_float_parity():
     assert_layer_parity(got, ref, "conv2d channel-major c=128")
 
 
-# Stream-K: 256 tiles of 128 pixels (one image row each) on a 152-SM part
-# would run as 1.68 rounds; the reduction is split at fixed points between
-# neighbouring CTAs (tail written raw and flagged, head adds it). Halo mode
-# (no shortcut) and per-tap mode (with an appended shortcut); integer data
-# keeps every partial sum exact.
+# Stream-K on 1-SM tiles: 192 tiles of 128 pixels x 64 channels on a
+# 152-SM part would run as 1.26 rounds; the reduction (256 input channels: 72
+# or 74 steps) is split at fixed points between neighbouring CTAs (tail
+# written raw and flagged, head adds it). Per-tap mode, with and without an
+# appended shortcut; integer data keeps every partial sum exact. The halo
+# shape (256 output channels) takes paired tiles by default and stream-K on
+# 1-SM tiles under VAE_PAIR=off (run by test_gpu_pairs.py).
+@pytest.mark.parametrize("shape", [(1, 256, 64, 192, 128), (1, 256, 256, 256, 128)])
 @pytest.mark.parametrize("with_sc", [False, True])
-def test_conv2d_stream_k_exact_integer(with_sc):
-    n, cin, cout, h, w = 1, 128, 256, 256, 128
+def test_conv2d_stream_k_exact_integer(with_sc, shape):
+    n, cin, cout, h, w = shape
     lay = pkg().VAE_NHWC
     x = S.integer_tensor((n, cin, h, w), 61, -3, 3)
     wt = S.integer_tensor((cout, cin, 3, 3), 62, -2, 2)

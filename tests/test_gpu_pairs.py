@@ -43,4 +43,5 @@ def test_exact_integer_convs_on_forced_pairs():
 
 
 def test_full_size_sweep_on_single_sm_tiles():
-    _child_pytest("off", ["tests/test_gpu_configs.py", "-k", "sweep"])
+    _child_pytest("off", ["tests/test_gpu_configs.py", "tests/test_gpu_ops.py", "-k",
+                          "sweep or stream_k"])
