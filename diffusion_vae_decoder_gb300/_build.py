@@ -15,7 +15,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libvae.so")
 
 SOURCES = ["igemm.cu", "igemm_split.cu", "igemm_xf.cu", "groupnorm.cu", "softmax.cu", "layout.cu", "ops.cu", "chain.cu",
-           "runtime.cu", "noalloc.cu", "head.cu", "flash.cu", "splitk.cu", "peak.cu", "tiled.cu"]
+           "runtime.cu", "noalloc.cu", "head.cu", "head_tc.cu", "flash.cu", "splitk.cu", "peak.cu", "tiled.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",

@@ -23,6 +23,8 @@
 // write with the per-group arrival counters of their finalize (zeroed at the
 // start of every decode), the split-K area and the attention scratch.
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <unordered_set>
 #include <vector>
@@ -164,6 +166,7 @@ struct Chain {
   std::vector<UpW> ups;
   NormW norm_out;
   float *head_w = nullptr;  // conv_out packed for the fused CUDA-core head (cout <= 4)
+  float *head_tc_w = nullptr;  // conv_out packed for the tensor-core head (TF32 decodes)
   std::vector<void *> allocs;
   // GroupNorm ahead (igemm_gn_ahead_ok): the current decode's row flags and
   // per-conv row counters (zeroed at its start), and how many such convs it
@@ -558,6 +561,27 @@ bool gn_folds_into(const Chain &ch, const ConvW &c, int w) {
   return igemm_input_gn_ok(d);
 }
 
+// VAE_HEAD=cuda keeps TF32 decodes on the CUDA-core head (comparisons).
+bool head_tc_enabled() {
+  static const bool v = [] {
+    const char *e = std::getenv("VAE_HEAD");
+    return !(e && std::strcmp(e, "cuda") == 0);
+  }();
+  return v;
+}
+
+// Whether a decode (exact: with split-TF32 products) runs norm_out + conv_out
+// as the fused tensor-core head, or as one of the fused heads at all.
+bool uses_tc_head(const Chain &ch, bool exact) {
+  return !exact && ch.head_tc_w && head_tc_enabled();
+}
+bool uses_fused_head(const Chain &ch, bool exact) {
+  return uses_tc_head(ch, exact) || ch.head_w != nullptr;
+}
+
+// Whether the decode of an [n, *, h, w] latent forms split-TF32 products.
+bool decode_exact(const Chain &ch, int n, int h, int w);
+
 // Whether conv `c` (input rows w pixels wide) makes its GroupNorm+SiLU input
 // itself while it runs (GroupNorm ahead).
 bool gn_ahead_into(const Chain &ch, const ConvW &c, int w) {
@@ -676,7 +700,8 @@ std::vector<vae_trace_point> trace_points(const Chain &ch, int n, int h, int w) 
       cur = add(VAE_TRACE_UPSAMPLE, u.up.cout, hh, ww, cur, -1);
     }
   }
-  if (!ch.head_w) cur = add(VAE_TRACE_GROUPNORM, ch.norm_out.c, hh, ww, cur, -1);
+  if (!uses_fused_head(ch, decode_exact(ch, n, h, w)))
+    cur = add(VAE_TRACE_GROUPNORM, ch.norm_out.c, hh, ww, cur, -1);
   add(VAE_TRACE_RGB, ch.conv_out.cout, hh, ww, cur, -1);
   return pts;
 }
@@ -735,11 +760,24 @@ int vae_chain_prepare(const vae_chain_args *a, void **handle, vae_stream_t strea
   ch->norm_out = b.norm(a->norm_out, c);
   ch->conv_out = b.conv(a->conv_out, c, a->conv_out.cout);
   if (ch->conv_out.k != 3 && b.status == VAE_OK) b.fail(VAE_EINVAL);
-  if (b.status == VAE_OK && head_supported(c, a->conv_out.cout, a->conv_out.k)) {
+  // The fused heads: TF32 decodes run norm_out + conv_out on the tensor cores,
+  // split-TF32 ones on the FP32 CUDA cores (cout <= 4); other shapes take the
+  // GroupNorm pass and the implicit-GEMM conv.
+  const bool cuda_head = head_supported(c, a->conv_out.cout, a->conv_out.k);
+  const bool tc_head = a->conv_out.k == 3 && ch->precision != VAE_PRECISION_SPLIT_TF32 &&
+                       head_tc_supported(c, a->conv_out.cout);
+  if (b.status == VAE_OK && (cuda_head || tc_head)) {
     const float *wt =
         b.upload_tmp(a->conv_out.weight, static_cast<size_t>(a->conv_out.cout) * c * 9);
-    ch->head_w = b.dev<float>(head_packed_floats(c));
-    if (b.status == VAE_OK) b.fail(head_pack_weights(wt, a->conv_out.cout, c, ch->head_w, s));
+    if (cuda_head) {
+      ch->head_w = b.dev<float>(head_packed_floats(c));
+      if (b.status == VAE_OK) b.fail(head_pack_weights(wt, a->conv_out.cout, c, ch->head_w, s));
+    }
+    if (tc_head) {
+      ch->head_tc_w = b.dev<float>(head_tc_packed_floats(c, a->conv_out.cout));
+      if (b.status == VAE_OK)
+        b.fail(head_tc_pack_weights(wt, a->conv_out.cout, c, ch->head_tc_w, s));
+    }
   }
   if (b.status == VAE_OK && cudaStreamSynchronize(s) != cudaSuccess) b.fail(VAE_ECUDA);
   cudaStreamSynchronize(s);
@@ -790,6 +828,12 @@ double decode_conv_gflops(const Chain &ch, int n, int h, int w) {
   return (f + conv(ch.conv_out, px)) / 1e9;
 }
 
+bool decode_exact(const Chain &ch, int n, int h, int w) {
+  return ch.precision == VAE_PRECISION_SPLIT_TF32 ||
+         (ch.precision == VAE_PRECISION_AUTO &&
+          decode_conv_gflops(ch, n, h, w) <= VAE_SPLIT_AUTO_GFLOP);
+}
+
 int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void *ws,
                 size_t ws_bytes, cudaStream_t s) {
   if (ch->causal) return VAE_EINVAL;  // a 3-D causal decoder: vae_decode_causal
@@ -804,9 +848,7 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
   Carver cv(ws, ws_bytes);
   DecodeWs d = carve_decode(cv, *ch, p, n, h, w);
   if (!cv.ok()) return VAE_EWORKSPACE;
-  ch->exact = ch->precision == VAE_PRECISION_SPLIT_TF32 ||
-              (ch->precision == VAE_PRECISION_AUTO &&
-               decode_conv_gflops(*ch, n, h, w) <= VAE_SPLIT_AUTO_GFLOP);
+  ch->exact = decode_exact(*ch, n, h, w);
 
   // The GroupNorm finalize counters start every decode at zero (each
   // finalize leaves them at zero; this also clears what an aborted decode
@@ -864,7 +906,7 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
     }
   }
   const long long hw = static_cast<long long>(hh) * ww;
-  if (ch->head_w) {
+  if (uses_fused_head(*ch, ch->exact)) {
     const int c = ch->norm_out.c, co = ch->conv_out.cout;
     Step step(ch->prof, VAE_PROF_HEAD, 2.0 * 9 * c * co * n * hw, (4.0 * c + 4.0 * co) * n * hw,
               s);
@@ -872,8 +914,12 @@ int decode_impl(Chain *ch, const float *z, int n, int h, int w, float *rgb, void
     VAE_TRY(groupnorm_scale_shift(cur, n, c, hw, ch->groups, ch->eps, ch->norm_out.g,
                                   ch->norm_out.b, st.ready ? d.part : nullptr, st.slots, scale,
                                   shift, d.gn, s, d.gn_cnt));
-    VAE_TRY(head_gn_silu_conv(cur, n, hh, ww, c, scale, shift, ch->head_w, ch->conv_out.b, co,
-                              rgb, s));
+    if (uses_tc_head(*ch, ch->exact))
+      VAE_TRY(head_tc_gn_silu_conv(cur, n, hh, ww, c, scale, shift, ch->head_tc_w,
+                                   ch->conv_out.b, co, rgb, s));
+    else
+      VAE_TRY(head_gn_silu_conv(cur, n, hh, ww, c, scale, shift, ch->head_w, ch->conv_out.b,
+                                co, rgb, s));
     if (ch->tr) ch->tr->emit(rgb, 4ull * n * hw * co, s);
     return VAE_OK;
   }

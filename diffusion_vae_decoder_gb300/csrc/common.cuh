@@ -250,6 +250,15 @@ int head_pack_weights(const float *w, int cout, int cin, float *dst, cudaStream_
 int head_gn_silu_conv(const float *x, int n, int h, int w, int c, const float *scale,
                       const float *shift, const float *wpk, const float *bias, int cout,
                       float *y, cudaStream_t s);
+// The same on the tensor cores with TF32 operands (head_tc.cu; cout <= 7 and
+// cin * 16 * ceil(9 * cout / 16) * 4 <= 32 KB): weights packed [NT][cin],
+// NT = 16 * ceil(9 * cout / 16), row t * cout + o = tap t of output o.
+bool head_tc_supported(int cin, int cout);
+size_t head_tc_packed_floats(int cin, int cout);
+int head_tc_pack_weights(const float *w, int cout, int cin, float *dst, cudaStream_t s);
+int head_tc_gn_silu_conv(const float *x, int n, int h, int w, int c, const float *scale,
+                         const float *shift, const float *wpk, const float *bias, int cout,
+                         float *y, cudaStream_t s);
 
 // Fused attention (flash.cu): O = softmax(Q K^T * scale) V for one head of
 // width d; q, k token-major [L][ld]; vt [d][ldv] (zero beyond L); out [L][ldo].

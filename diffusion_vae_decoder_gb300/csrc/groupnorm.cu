@@ -19,6 +19,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "silu.cuh"
 
 namespace vae {
 
@@ -257,6 +258,11 @@ __global__ void __launch_bounds__(256)
   const float4 a = *reinterpret_cast<const float4 *>(scale + n * c + ch);
   const float4 b = *reinterpret_cast<const float4 *>(shift + n * c + ch);
   auto one = [&](float4 v, float4 r) {
+    if (silu && round && !rv) {  // the decode's GroupNorm+SiLU: packed form
+      const float2 s0 = silu2_tf32(v.x, v.y, a.x, a.y, b.x, b.y);
+      const float2 s1 = silu2_tf32(v.z, v.w, a.z, a.w, b.z, b.w);
+      return make_float4(s0.x, s0.y, s1.x, s1.y);
+    }
     float4 o;
     o.x = act(fmaf(v.x, a.x, b.x), silu) + r.x;
     o.y = act(fmaf(v.y, a.y, b.y), silu) + r.y;
