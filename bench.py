@@ -349,6 +349,9 @@ def run_ours(args):
     conv_tflops = sum(r["flops"] for r in conv) / (conv_ms / 1e3) / 1e12
     gn_ms = sum(r["ms"] for r in gn)
     gn_gbs = sum(r["bytes"] for r in gn) / (gn_ms / 1e3) / 1e9
+    head = [r for r in recs if r["kind"] == "head"]
+    head_ms = sum(r["ms"] for r in head)
+    head_gbs = sum(r["bytes"] for r in head) / (head_ms / 1e3) / 1e9 if head_ms > 0 else None
     step_ms_sum = sum(r["ms"] for r in recs) / n_prof
     by_kind = {}
     for r in recs:
@@ -453,6 +456,11 @@ def run_ours(args):
                                    "bytes_per_element": "8 (read + write) where the statistics "
                                                         "come from the producing conv, 12 for "
                                                         "the two-pass GroupNorms"},
+            "roofline_head": None if head_gbs is None else {
+                "bound": "hbm", "achieved": head_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": head_gbs / peaks["hbm_gbs"],
+                "bytes_per_pixel": "4 * C_in read + 4 * C_out written (norm_out + conv_out step, "
+                                   "its GroupNorm finalize included)"},
             "steps_by_kind": by_kind, "profiled_ms_per_step": ms_profiled,
             "profiled_steps_sum_ms": step_ms_sum,
             "cpu_baseline": cpu,

@@ -458,6 +458,11 @@ __device__ __forceinline__ void apply_share(const float *__restrict__ x, unsigne
   const float4 b = *reinterpret_cast<const float4 *>(ssh + ch);
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   auto one = [&](float4 v, float4 r) {
+    if (silu && round && !rv) {  // the decode's GroupNorm+SiLU: packed form
+      const float2 s0 = silu2_tf32(v.x, v.y, a.x, a.y, b.x, b.y);
+      const float2 s1 = silu2_tf32(v.z, v.w, a.z, a.w, b.z, b.w);
+      return make_float4(s0.x, s0.y, s1.x, s1.y);
+    }
     float4 o;
     o.x = rnd(act(fmaf(v.x, a.x, b.x), silu) + r.x, round);
     o.y = rnd(act(fmaf(v.y, a.y, b.y), silu) + r.y, round);
