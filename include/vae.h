@@ -444,8 +444,9 @@ typedef enum {
                                   the producing conv supplied the statistics; 12 otherwise)    */
   VAE_PROF_ATTENTION = 3,      /* mid attention block (flops: 4*L*L*c + 8*L*c*c per image)   */
   VAE_PROF_LAYOUT = 4,         /* latent de-normalisation / layout staging (bytes)           */
-  VAE_PROF_HEAD = 5,           /* norm_out GroupNorm+SiLU fused into conv_out (CUDA cores):
-                                  flops 2*9*cin*cout, bytes 4*cin + 4*cout per output pixel */
+  VAE_PROF_HEAD = 5,           /* norm_out GroupNorm+SiLU fused into conv_out (tensor cores in
+                                  TF32 decodes, FP32 CUDA cores in split-TF32 ones): flops
+                                  2*9*cin*cout, bytes 4*cin + 4*cout per output pixel */
   VAE_PROF_GN_AFFINE = 6       /* a GroupNorm reduced to its per-channel affine, applied by the
                                   conv that reads it (bytes: the statistics read: 12 per
                                   partial, or 4 per element without fused partials)          */
